@@ -1,0 +1,417 @@
+"""Benchmark of paged decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one decode call over one batch of the Llama-style GQA workload
+(B=8 sequences, H=32, KV=8, D=128, BLOCK=16, fp16, past lengths uniform in
+[512, 4096], blocks randomly permuted in a shared pool, NQ=1): the partition
+kernel plus the log-sum-exp merge kernel.  The metric is decode-attention
+throughput in GB/s of algorithmic bytes (every visible K and V row once, q,
+the output, the table entries and lengths) divided by device time, with the
+fraction of the measured HBM copy bandwidth.
+
+Sequences are independent, so N GPUs run N independent batches (weak
+scaling, no collective on the data path); ``value`` is the bytes of all ranks
+over the slowest rank's time.
+
+The KV pools (75 MB for this workload) would fit in the 129 MB L2, so the
+bench keeps several copies of the pools (together larger than 3x L2) and
+rotates through them step by step: every step reads its K/V from HBM.
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+WORKLOAD = "gqa_fp16"
+METRIC = "decode attention HBM GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-workload table and the CPU baseline")
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Largest value over ranks (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = ROOT / "MEASURED_PEAKS.json"
+    if path.exists():
+        d = json.loads(path.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our kernels
+def rotation_copies(w, device):
+    """Enough copies of the KV pools that consecutive steps never hit in L2."""
+    pool = 2 * w.k_cache.numel() * w.k_cache.element_size()
+    n = max(1, math.ceil(3 * L2_BYTES / pool))
+    kc = [w.k_cache.to(device)]
+    vc = [w.v_cache.to(device)]
+    for _ in range(n - 1):
+        kc.append(kc[0].clone())
+        vc.append(vc[0].clone())
+    return kc, vc, n * pool
+
+
+def make_plans(w, device, partitions=None):
+    from paged_kv_cache_182_gb300 import binding
+
+    kc, vc, pool_bytes = rotation_copies(w, device)
+    q, table, lens, kn, vn = (t.to(device) for t in (w.q, w.block_table, w.seq_lens,
+                                                      w.k_new, w.v_new))
+    P = w.spec.partitions if partitions is None else partitions
+    out = torch.empty(q.shape, dtype=q.dtype, device=device)
+    ws = torch.empty(max(1, binding.workspace_bytes(w.spec.B, w.spec.H, w.spec.KV, w.spec.D,
+                                                    w.spec.NQ, P)),
+                     dtype=torch.uint8, device=device)
+    plans = []
+    for k, v in zip(kc, vc):
+        p = binding.Plan(q, k, v, table, lens, kn, vn, scale=w.spec.scale, causal=w.spec.causal,
+                         partitions=P, out=out, workspace=ws)
+        p.bind_stream(torch.cuda.current_stream(device))
+        plans.append(p)
+    return plans, pool_bytes
+
+
+def time_steps(plans, steps, warmup, world, trace=True):
+    """Times `steps` decode calls (rotating over the pool copies) on the current
+    stream.  Returns (ms per step over the whole region, mean partition-kernel
+    ms, kernels launched)."""
+    from paged_kv_cache_182_gb300 import binding
+
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if trace else []
+    for a, b in evs:  # create the events before the timed region
+        a.record(stream)
+        b.record(stream)
+    for i in range(warmup):
+        plans[i % len(plans)].set_trace()
+        plans[i % len(plans)].run_bound()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = binding.kernel_launches()
+    start.record(stream)
+    for i in range(steps):
+        p = plans[i % len(plans)]
+        if trace:
+            p.set_trace(*evs[i])
+        p.run_bound()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches = binding.kernel_launches() - launches0
+    for p in plans:
+        p.set_trace()
+    ms = start.elapsed_time(end) / steps
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs) if trace else None
+    return ms, split_ms, launches
+
+
+def e2e_steps(w, device, steps, warmup):
+    """Same metric end to end through the public host-buffer call: per step the
+    step's inputs (q, table, lengths, new rows) go host->device from pinned
+    memory and the output comes back; the KV cache stays resident in HBM."""
+    from paged_kv_cache_182_gb300 import binding
+
+    kc, vc = w.k_cache.to(device), w.v_cache.to(device)
+    host = [t.pin_memory() for t in (w.q, w.block_table, w.seq_lens, w.k_new, w.v_new)]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = w.q.numel() * w.q.element_size()
+
+    def step():
+        return binding.decode_host(*host, k_cache=kc, v_cache=vc, scale=w.spec.scale,
+                                   causal=w.spec.causal, partitions=w.spec.partitions)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) / steps * 1e3, h2d, d2h
+
+
+def cpu_baseline(w, budget_s=10.0):
+    """The float64 oracle as it stands on the host cores, on whole sequences of
+    the workload until about `budget_s` seconds have passed."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    orc = oracle.default()
+    threads = orc.max_threads()
+    args = [np.ascontiguousarray(t.to(torch.float64).numpy()) if t.is_floating_point() else
+            t.numpy() for t in w.tensors()]
+    done_bytes, t0, calls = 0, time.perf_counter(), 0
+    per = W.algorithmic_bytes(w)
+    while True:
+        orc.decode(*args, scale=w.spec.scale, causal=w.spec.causal, threads=threads)
+        calls += 1
+        done_bytes += per
+        el = time.perf_counter() - t0
+        if el >= budget_s or calls >= 2000:
+            break
+    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{calls} full decode steps of {w.spec.name} (B={w.spec.B}) in {el:.1f} s, "
+                      f"float64, OpenMP over (sequence, head, row)"}
+
+
+def per_workload_table(device, steps, warmup, peak):
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    rows = []
+    for name in W.ORDER:
+        w = W.make(name, seed=0, poison=False)
+        plans, _ = make_plans(w, device)
+        ms, split_ms, _ = time_steps(plans, steps, warmup, 1)
+        by = W.algorithmic_bytes(w)
+        gbs = by / (ms * 1e-3) / 1e9
+        rows.append({"workload": name, "us_per_step": round(ms * 1e3, 2),
+                     "partition_kernel_us": round(split_ms * 1e3, 2),
+                     "GB_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 3),
+                     "tokens_per_s": round(w.spec.B * w.spec.NQ / (ms * 1e-3), 1),
+                     "bytes_per_step": by, "partitions": w.spec.partitions or "auto"})
+        del plans
+        torch.cuda.empty_cache()
+    return rows
+
+
+def run_ours(args, rank, world, local):
+    from paged_kv_cache_182_gb300 import binding  # noqa: F401  (fails loudly if not built)
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    device = torch.device("cuda", local)
+    peak, peak_kind = measured_peaks()
+    w = W.make(args.workload, seed=rank, poison=False)
+    per_rank_bytes = W.algorithmic_bytes(w)
+    plans, pool_bytes = make_plans(w, device)
+    plans_n = list(range(len(plans)))
+    with Clocks(local) as clk:
+        ms, split_ms, launches = time_steps(plans, args.steps, args.warmup, world)
+    ms_max = reduce_max(ms, world)
+    value = world * per_rank_bytes / (ms_max * 1e-3) / 1e9
+    achieved = per_rank_bytes / (split_ms * 1e-3) / 1e9
+    del plans
+    torch.cuda.empty_cache()
+    e2e_ms, h2d, d2h = e2e_steps(w, device, max(20, args.steps // 4), 3)
+    e2e_ms = reduce_max(e2e_ms, world)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1), random block permutation)",
+        "config": {"workload": w.spec.name, "B": w.spec.B, "H": w.spec.H, "KV": w.spec.KV,
+                   "D": w.spec.D, "BLOCK": w.spec.BLOCK, "NQ": w.spec.NQ,
+                   "causal": w.spec.causal, "partitions": w.spec.partitions or "auto",
+                   "seq_lens": w.seq_lens.tolist(), "bytes_per_step": per_rank_bytes,
+                   "l2": f"inputs larger than L2: {len(plans_n)} copies of the KV pools "
+                         f"({pool_bytes // 2**20} MiB) rotated step by step",
+                   "parallelism": f"independent batches x{world}"},
+        "tokens_per_s": round(world * w.spec.B * w.spec.NQ / (ms_max * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "pa_split_kernel", "peak_kind": peak_kind},
+        "e2e": {"value": round(world * per_rank_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_extras:
+        line["per_workload"] = per_workload_table(device, 50, 5, peak)
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    w = W.make(args.workload, seed=0, poison=False)
+    s = w.spec
+    orc = oracle.default()
+    threads = orc.max_threads()
+    rows = s.B * s.H * s.NQ
+    args_np = [np.ascontiguousarray(t.to(torch.float64).numpy()) if t.is_floating_point() else
+               t.numpy() for t in w.tensors()]
+    # sample: one query head per KV head of every sequence (all keys read once
+    # per KV head, as a grouped kernel would), i.e. 1/g of the rows
+    mask = np.zeros((s.B, s.H, s.NQ), dtype=np.uint8)
+    mask[:, :: s.group, :] = 1
+    frac = float(mask.sum()) / rows
+    by = W.algorithmic_bytes(w)
+
+    def step():
+        orc.decode(*args_np, scale=s.scale, causal=s.causal, row_mask=mask, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = (time.perf_counter() - t0) / args.steps
+    # the sample computes `frac` of the rows: a full step takes el / frac
+    full = el / frac
+    value = by / full / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(full * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), random block permutation)",
+        "config": {"workload": s.name, "B": s.B, "H": s.H, "KV": s.KV, "D": s.D,
+                   "BLOCK": s.BLOCK, "NQ": s.NQ, "causal": s.causal},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"each step computes the rows of one query head per KV "
+                                   f"head ({frac:.3f} of all rows); time scaled by 1/{frac:.3f} "
+                                   f"to a full step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --impl ours needs a CUDA device")
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

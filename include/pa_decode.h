@@ -1,0 +1,131 @@
+/*
+ * pa_decode.h -- C ABI of libpadecode.so: decode-step attention over a paged
+ * KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one defined by onnxruntime-ep-mlx 0.31.1,
+ * src/ops/paged_attention.rs (VECTOR_BODY: paged gather, grouped-query map,
+ * causal bound, online softmax; VECTOR_PARTIALS / PARTIALS_REDUCE: the split
+ * into partitions and their log-sum-exp merge; fn vector: the arguments).
+ * For every sequence b, query head h and new row r:
+ *
+ *   kh    = h / (H / KV)
+ *   past  = seq_lens[b]
+ *   total = past + (causal ? r + 1 : NQ)
+ *   key i = k_cache row (block_table[b][i / BLOCK] * BLOCK + i % BLOCK, kh)
+ *           for i < past, else k_new[b][kh][i - past]   (values likewise)
+ *   out[b][h][r] = sum_i softmax_i(scale * q[b][h][r] . key_i) * value_i
+ *
+ * Layouts (row-major, element offsets, no padding):
+ *   q, out           [B][H][NQ][D]
+ *   k_cache, v_cache [num_blocks][BLOCK][KV][D]
+ *   block_table      [B][max_blocks]   int32 physical block ids
+ *   seq_lens         [B]               int32 cached tokens per sequence
+ *   k_new, v_new     [B][KV][NQ][D]    the NQ rows appended this step
+ *
+ * Ownership: every pointer argument is a caller-owned DEVICE pointer (the
+ * library allocates no memory and never synchronises); every call is
+ * asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream).
+ * Table entries are read only for blocks that hold visible keys; entries past
+ * a sequence's last block and cache slots past its length are never read.
+ *
+ * Errors: functions return PA_OK (0) or a negative PA_ERR_* code before
+ * anything is launched; pa_strerror() names what to verify.  Conditions that
+ * only the device can see (a table entry outside the pool in checked mode, a
+ * length larger than max_blocks * BLOCK) are OR-ed into *opts->status as
+ * PA_STATUS_* bits and become visible after the caller synchronises; the
+ * kernels never trap.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types of q, caches, k_new, v_new (and out) */
+#define PA_F32 0
+#define PA_F16 1
+#define PA_BF16 2
+
+/* return codes */
+#define PA_OK 0
+#define PA_ERR_NULL_POINTER (-1) /* a required pointer (or opts) is NULL */
+#define PA_ERR_BAD_DIMS (-2)     /* H % KV != 0, a size < 1, or a size too large */
+#define PA_ERR_UNSUPPORTED (-3)  /* D, BLOCK, NQ, dtype or out_dtype outside the built set */
+#define PA_ERR_ALIGNMENT (-4)    /* a data pointer is not 16-byte aligned (workspace: 256) */
+#define PA_ERR_WORKSPACE (-5)    /* workspace NULL or smaller than pa_workspace_bytes() */
+#define PA_ERR_CUDA (-6)         /* a CUDA runtime call or kernel launch failed */
+#define PA_ERR_DRIVER (-7)       /* the tensor-map encoder of the driver is unavailable */
+
+/* device status bits, OR-ed into *opts->status when it is not NULL */
+#define PA_STATUS_BAD_BLOCK 1  /* checked mode: a table entry outside [0, num_blocks) */
+#define PA_STATUS_BAD_LENGTH 2 /* seq_lens[b] < 0 or > max_blocks * BLOCK (clamped) */
+#define PA_STATUS_TIMEOUT 4    /* an internal wait gave up (the output is undefined) */
+
+/* supported sizes */
+#define PA_MAX_NQ 16
+
+typedef struct pa_opts {
+    int batch;       /* B, sequences in this call (0 = nothing to do) */
+    int max_blocks;  /* row stride of block_table (entries per sequence) */
+    int num_blocks;  /* physical blocks in each of k_cache and v_cache */
+    int dtype;       /* PA_F32, PA_F16 or PA_BF16: q, k_cache, v_cache, k_new, v_new */
+    int out_dtype;   /* -1 = same as dtype; or PA_F32 for a float32 output */
+    int partitions;  /* 0 = automatic split, 1 = one pass per sequence,
+                        P >= 2 = each sequence split into P key ranges */
+    int checked;     /* nonzero: report table entries outside the pool */
+    void *workspace; /* device scratch of >= pa_workspace_bytes() bytes, 256-aligned;
+                        may be NULL when partitions == 1 */
+    size_t workspace_bytes;
+    int *status;        /* device int32 for PA_STATUS_* bits, or NULL */
+    void *trace_begin;  /* optional cudaEvent_t recorded before the partition kernel */
+    void *trace_split;  /* optional cudaEvent_t recorded after it (before the merge) */
+} pa_opts;
+
+/*
+ * Decode attention for `opts->batch` sequences (see the definition above).
+ * Launches the partition kernel (one CTA per KV head and key range of a
+ * sequence; every CTA serves all H/KV * NQ query rows of its KV head so each
+ * K/V row is read from memory once) and, unless partitions == 1, the
+ * log-sum-exp merge kernel for sequences that were split.
+ *   scale     multiplies q . k, applied in float32 exactly as given
+ *   H, KV     query heads and KV heads, H % KV == 0
+ *   D         head size, 64 or 128
+ *   BLOCK     tokens per cache block, 8, 16, 32 or 64
+ *   NQ        new rows this step, 1 .. PA_MAX_NQ
+ *   causal    nonzero: new row r sees the past and new rows 0..r only
+ *   stream    cudaStream_t to launch on
+ * Returns PA_OK or a PA_ERR_* code.
+ */
+int pa_decode(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, const int32_t *seq_lens,
+              const void *k_new, const void *v_new, void *out, float scale,
+              int H, int KV, int D, int BLOCK, int NQ, int causal,
+              const pa_opts *opts, void *stream);
+
+/*
+ * Bytes of workspace pa_decode needs for these sizes (0 when partitions == 1).
+ * Depends only on the arguments, not on the device or the lengths: it holds
+ * a per-sequence schedule and one float32 partial state (max, sum, D
+ * accumulators) per query row for every key range the split can produce.
+ * Returns 0 for invalid arguments.
+ */
+size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions);
+
+/* A sentence naming what to verify for a PA_ERR_* code (static storage). */
+const char *pa_strerror(int code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+/* Kernels this library has launched since it was loaded (all devices). */
+uint64_t pa_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

@@ -1,0 +1,215 @@
+"""ctypes binding of ``libpadecode.so`` (C ABI in ``include/pa_decode.h``).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  If the library has not been built, importing this
+module raises -- there is no Python or CPU fallback.
+
+Tensor layouts (row-major, contiguous):
+  q, out           [B, H, NQ, D]            float32 / float16 / bfloat16
+  k_cache, v_cache [num_blocks, BLOCK, KV, D]
+  block_table      [B, max_blocks]          int32
+  seq_lens         [B]                      int32 (cached tokens per sequence)
+  k_new, v_new     [B, KV, NQ, D]
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from . import _build
+
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LENGTH, PA_STATUS_TIMEOUT = 1, 2, 4
+PA_MAX_NQ = 16
+_DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+
+LIBRARY = _build.LIBRARY
+
+
+class PaOpts(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int),
+        ("max_blocks", ctypes.c_int),
+        ("num_blocks", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("out_dtype", ctypes.c_int),
+        ("partitions", ctypes.c_int),
+        ("checked", ctypes.c_int),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("status", ctypes.c_void_p),
+        ("trace_begin", ctypes.c_void_p),
+        ("trace_split", ctypes.c_void_p),
+    ]
+
+
+def load(path: Path = LIBRARY) -> ctypes.CDLL:
+    """Load the C-ABI library and declare its signatures."""
+    if not Path(path).exists():
+        raise RuntimeError(
+            f"{path} is missing: build it with paged_kv_cache_182_gb300._build.build() "
+            "(there is no fallback path)")
+    lib = ctypes.CDLL(str(path))
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.pa_decode.restype = I
+    lib.pa_decode.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I, I, I,
+                              ctypes.POINTER(PaOpts), P]
+    lib.pa_workspace_bytes.restype = ctypes.c_size_t
+    lib.pa_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.pa_strerror.restype = ctypes.c_char_p
+    lib.pa_strerror.argtypes = [I]
+    lib.pa_version.restype = I
+    lib.pa_kernel_launches.restype = ctypes.c_uint64
+    return lib
+
+
+LIB = load()
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(f"pa_decode returned {code}: {strerror(code)}")
+
+
+def strerror(code: int) -> str:
+    return LIB.pa_strerror(int(code)).decode()
+
+
+def kernel_launches() -> int:
+    return int(LIB.pa_kernel_launches())
+
+
+def workspace_bytes(B: int, H: int, KV: int, D: int, NQ: int, partitions: int = 0) -> int:
+    return int(LIB.pa_workspace_bytes(B, H, KV, D, NQ, partitions))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """One prepared decode call on fixed device tensors.
+
+    Validates shapes once and packs the ctypes arguments, so that repeated
+    calls (a decode loop, CUDA-graph capture, the bench) cost one foreign
+    call.  The workspace is allocated once, here, with torch.
+    """
+
+    def __init__(self, q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *,
+                 scale: float, causal: bool = False, partitions: int = 0, out=None,
+                 out_dtype=None, workspace=None, status=None, checked: bool = False,
+                 trace=None):
+        B, H, NQ, D = q.shape
+        NB, BLOCK, KV, D2 = k_cache.shape
+        if (D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape)
+                or tuple(k_new.shape) != (B, KV, NQ, D) or tuple(v_new.shape) != (B, KV, NQ, D)):
+            raise ValueError("inconsistent q / cache / new-row shapes")
+        if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+            raise ValueError("block_table must be [B, max_blocks] and seq_lens [B]")
+        if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+            raise TypeError("block_table and seq_lens must be int32")
+        dt = q.dtype
+        for t in (k_cache, v_cache, k_new, v_new):
+            if t.dtype != dt:
+                raise TypeError("q, caches and new rows must share one dtype")
+        if dt not in _DT:
+            raise TypeError(f"unsupported dtype {dt}")
+        tensors = (q, k_cache, v_cache, block_table, seq_lens, k_new, v_new)
+        for t in tensors:
+            if not t.is_cuda:
+                raise ValueError("all tensors must be CUDA tensors")
+            if not t.is_contiguous():
+                raise ValueError("all tensors must be contiguous")
+        odt = dt if out_dtype is None else out_dtype
+        if out is None:
+            out = torch.empty((B, H, NQ, D), dtype=odt, device=q.device)
+        elif tuple(out.shape) != (B, H, NQ, D) or not out.is_contiguous() or out.dtype != odt:
+            raise ValueError("out must be a contiguous [B, H, NQ, D] tensor of the output dtype")
+        need = workspace_bytes(B, H, KV, D, NQ, partitions)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        self.tensors = tensors
+        self.out = out
+        self.workspace = workspace
+        self.status = status
+        self.trace = trace
+        self.device = q.device
+        self.shape = dict(B=B, H=H, KV=KV, D=D, BLOCK=BLOCK, NQ=NQ, num_blocks=NB,
+                          max_blocks=int(block_table.shape[1]))
+        self.opts = PaOpts(
+            batch=B, max_blocks=int(block_table.shape[1]), num_blocks=NB, dtype=_DT[dt],
+            out_dtype=_DT[odt], partitions=int(partitions), checked=int(bool(checked)),
+            workspace=None if workspace is None else workspace.data_ptr(),
+            workspace_bytes=0 if workspace is None else workspace.numel(),
+            status=None if status is None else status.data_ptr(),
+            trace_begin=None if trace is None else trace[0].cuda_event,
+            trace_split=None if trace is None else trace[1].cuda_event)
+        self._args = [_ptr(t) for t in tensors] + [_ptr(out), ctypes.c_float(scale), H, KV, D,
+                                                   BLOCK, NQ, int(bool(causal)),
+                                                   ctypes.byref(self.opts)]
+
+    def set_trace(self, begin=None, split=None):
+        """Events recorded around the partition kernel by the next run()."""
+        self.opts.trace_begin = None if begin is None else begin.cuda_event
+        self.opts.trace_split = None if split is None else split.cuda_event
+
+    def bind_stream(self, stream=None):
+        """Fix the stream of later run_bound() calls (default: torch's current)."""
+        self._bound = self._args + [_stream_handle(stream)]
+
+    def run_bound(self):
+        """Launch on the stream fixed by bind_stream(): one foreign call, no lookups."""
+        rc = LIB.pa_decode(*self._bound)
+        if rc != 0:
+            raise PagedAttentionError(rc)
+        return self.out
+
+    def run(self, stream=None):
+        """Launch on ``stream`` (default: torch's current stream); returns ``out``."""
+        with torch.cuda.device(self.device):
+            rc = LIB.pa_decode(*self._args, _stream_handle(stream))
+        if rc != 0:
+            raise PagedAttentionError(rc)
+        return self.out
+
+
+def decode(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *, scale: float,
+           causal: bool = False, partitions: int = 0, out=None, out_dtype=None, workspace=None,
+           status=None, checked: bool = False, stream=None):
+    """Decode attention on device tensors (see the module docstring); returns ``out``."""
+    plan = Plan(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, scale=scale,
+                causal=causal, partitions=partitions, out=out, out_dtype=out_dtype,
+                workspace=workspace, status=status, checked=checked)
+    return plan.run(stream)
+
+
+def decode_host(q, block_table, seq_lens, k_new, v_new, *, k_cache, v_cache, scale: float,
+                causal: bool = False, partitions: int = 0, out_dtype=None, stream=None):
+    """End-to-end decode step from host tensors.
+
+    The KV cache (``k_cache``, ``v_cache``) is device-resident state, as a KV
+    cache is; the step's inputs -- q, the block table, the lengths and the
+    new rows -- are host tensors (pinned for asynchronous copies).  They are
+    copied to the device, the kernels run, and the output is copied back to
+    pinned host memory.  Returns the host output tensor.
+    """
+    device = k_cache.device
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    with torch.cuda.stream(stream):
+        dev = [t.to(device, non_blocking=True) for t in (q, block_table, seq_lens, k_new, v_new)]
+        out = decode(dev[0], k_cache, v_cache, dev[1], dev[2], dev[3], dev[4], scale=scale,
+                     causal=causal, partitions=partitions, out_dtype=out_dtype, stream=stream)
+        host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        host.copy_(out, non_blocking=True)
+    stream.synchronize()
+    return host

@@ -1,0 +1,64 @@
+// pa_common.cuh -- constants and launch-parameter blocks shared by the host
+// launcher (pa_host.cu) and the kernel instantiations (pa_inst_*.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;                     // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one TMA producer warp
+constexpr int kStages = 3;                            // shared-memory ring depth
+constexpr int kSubBatch = 4;        // token steps per online-softmax update
+constexpr int kStageBytes = 32768;  // K + V bytes per pipeline stage (target)
+constexpr int kHeaderBytes = 1024;  // barriers + schedule, keeps stages 1024-aligned
+constexpr int kAutoMaxTarget = 4096;  // cap on automatic item targets
+constexpr int kMinChunk = 128;      // smallest automatic key range (tokens)
+constexpr int kTargetWaves = 2;     // automatic split: items ~ waves * resident CTAs
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct SplitParams {
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    void* out;
+    const int32_t* table;
+    const int32_t* seq_lens;
+    int2* sched;    // [B] (first chunk index, chunk count), or NULL for one pass
+    float2* ws_ml;  // [items][row_stride] (max, sum) in base-2 units
+    float* ws_o;    // [items][row_stride][D]
+    int* status;
+    float qscale;   // scale * log2(e)
+    int B, H, KV, NQ, BLOCK, maxb, num_blocks;
+    int causal, partitions, target_items, min_chunk, checked;
+    int R;             // query rows per KV head = (H / KV) * NQ
+    int rows_per_cta;  // kConsumerWarps * RG
+    int NRS;           // row groups per KV head = ceil(R / rows_per_cta)
+    int TT;            // tokens per pipeline stage, a multiple of BLOCK
+    int row_stride;    // workspace rows per item = min(R, rows_per_cta)
+};
+
+struct CombineParams {
+    const int2* sched;
+    const float2* ws_ml;
+    const float* ws_o;
+    void* out;
+    int B, KV, R, NRS, rows_per_cta, row_stride;
+};
+
+using SplitFn = void (*)(SplitParams, CUtensorMap, CUtensorMap);
+using CombineFn = void (*)(CombineParams);
+
+// Kernel tables, one per input element type (pa_inst_*.cu).
+SplitFn pick_split_f32(int D, int RG);
+SplitFn pick_split_f16(bool f32_out, int D, int RG);
+SplitFn pick_split_bf16(bool f32_out, int D, int RG);
+CombineFn pick_combine_f32(int D);
+CombineFn pick_combine_f16(int D);
+CombineFn pick_combine_bf16(int D);
+
+}  // namespace pa

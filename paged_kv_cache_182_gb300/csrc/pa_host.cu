@@ -1,0 +1,426 @@
+// pa_host.cu -- host side of libpadecode.so: argument validation, workspace
+// layout, tensor-map encoding, kernel choice and launch, and the C ABI of
+// include/pa_decode.h.
+//
+// The launch arguments mirror fn vector of onnxruntime-ep-mlx 0.31.1,
+// src/ops/paged_attention.rs (heads, kv_heads, head, block, max_blocks,
+// batch, queries, causal, scale, and a partition count); the batch, the
+// table stride and the pool size cross the boundary as values instead of
+// template constants, and the workspace is caller-owned.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_decode.h"
+
+namespace pa {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+size_t elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+// Query rows per consumer warp: 4 up to 16 rows per KV head, else 8.
+int rows_group(int R) { return R <= 16 ? 4 : 8; }
+
+int tokens_per_stage(int D, int es, int BLOCK)
+{
+    int tt = kStageBytes / (2 * D * es);
+    if (tt < BLOCK)
+        tt = BLOCK;
+    return tt;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Upper bound on the work items of one call (also the partition grid size).
+long long item_bound(int B, int KV, int NRS, int partitions)
+{
+    const long long per_seq = static_cast<long long>(KV) * NRS;
+    if (partitions == 1)
+        return B * per_seq;
+    if (partitions >= 2)
+        return B * per_seq * partitions;
+    return kAutoMaxTarget + B * per_seq;
+}
+
+struct WsLayout {
+    size_t sched, ml, o, total;
+};
+
+WsLayout ws_layout(int B, int D, int row_stride, long long items)
+{
+    WsLayout w;
+    w.sched = 0;
+    w.ml = align_up(static_cast<size_t>(B) * sizeof(int2), 256);
+    w.o = w.ml + align_up(static_cast<size_t>(items) * row_stride * sizeof(float2), 256);
+    w.total = w.o + static_cast<size_t>(items) * row_stride * D * sizeof(float);
+    return w;
+}
+
+// --- tensor maps --------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    return fn;
+}
+
+struct MapKey {
+    const void* ptr;
+    long long rows;
+    int KV, D, BLOCK, dtype;
+    bool operator==(const MapKey& o) const
+    {
+        return ptr == o.ptr && rows == o.rows && KV == o.KV && D == o.D && BLOCK == o.BLOCK &&
+               dtype == o.dtype;
+    }
+};
+
+std::mutex g_map_mutex;
+constexpr int kMapCache = 32;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_count = 0, g_map_next = 0;
+
+// Cache pool [num_blocks * BLOCK rows][KV][D] as a 3-D tensor; one box is one
+// block of one KV head: {D, 1, BLOCK}.
+int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dtype,
+              CUtensorMap* out)
+{
+    const MapKey key{base, static_cast<long long>(num_blocks) * BLOCK, KV, D, BLOCK, dtype};
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < g_map_count; ++i)
+        if (g_map_keys[i] == key) {
+            *out = g_maps[i];
+            return PA_OK;
+        }
+    auto enc = encoder();
+    if (!enc)
+        return PA_ERR_DRIVER;
+    const size_t es = elem_size(dtype);
+    const CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(KV),
+                          static_cast<cuuint64_t>(key.rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
+                             static_cast<cuuint64_t>(KV) * D * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(BLOCK)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUtensorMap map;
+    const CUresult rc = enc(&map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+    const int slot = g_map_count < kMapCache ? g_map_count++ : (g_map_next++ % kMapCache);
+    g_map_keys[slot] = key;
+    g_maps[slot] = map;
+    *out = map;
+    return PA_OK;
+}
+
+// --- kernel table -----------------------------------------------------------------
+SplitFn pick_split(int dtype, bool f32_out, int D, int RG)
+{
+    switch (dtype) {
+    case PA_F32:
+        return pick_split_f32(D, RG);
+    case PA_F16:
+        return pick_split_f16(f32_out, D, RG);
+    default:
+        return pick_split_bf16(f32_out, D, RG);
+    }
+}
+
+CombineFn pick_combine(int out_dtype, int D)
+{
+    switch (out_dtype) {
+    case PA_F32:
+        return pick_combine_f32(D);
+    case PA_F16:
+        return pick_combine_f16(D);
+    default:
+        return pick_combine_bf16(D);
+    }
+}
+
+struct FuncState {
+    const void* fn;
+    int device;
+    int smem_set;
+    int occupancy;
+    int sms;
+};
+std::mutex g_func_mutex;
+constexpr int kFuncCache = 64;
+FuncState g_funcs[kFuncCache];
+int g_func_count = 0;
+
+// Raises the dynamic shared-memory limit of `fn` on the current device when
+// needed; returns its occupancy (CTAs per SM) and the SM count.
+int prepare_func(const void* fn, int threads, int smem, int* occ, int* sms)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_func_mutex);
+    FuncState* st = nullptr;
+    for (int i = 0; i < g_func_count; ++i)
+        if (g_funcs[i].fn == fn && g_funcs[i].device == dev)
+            st = &g_funcs[i];
+    if (!st) {
+        if (g_func_count == kFuncCache)
+            g_func_count = 0;
+        st = &g_funcs[g_func_count++];
+        *st = FuncState{fn, dev, 0, 0, 0};
+        if (cudaDeviceGetAttribute(&st->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    if (smem > st->smem_set) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+        st->smem_set = smem;
+        st->occupancy = 0;
+    }
+    if (st->occupancy == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        st->occupancy = n < 1 ? 1 : n;
+    }
+    *occ = st->occupancy;
+    *sms = st->sms;
+    return PA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+uint64_t pa_kernel_launches(void) { return g_launches.load(); }
+
+const char* pa_strerror(int code)
+{
+    switch (code) {
+    case PA_OK:
+        return "success";
+    case PA_ERR_NULL_POINTER:
+        return "PagedAttention: a required pointer is NULL; verify q, caches, block table, "
+               "seq_lens, k_new, v_new, out and opts";
+    case PA_ERR_BAD_DIMS:
+        return "PagedAttention: invalid sizes; verify H % KV == 0, batch >= 0, max_blocks >= 1, "
+               "num_blocks * BLOCK < 2^31 and a finite scale";
+    case PA_ERR_UNSUPPORTED:
+        return "PagedAttention: unsupported configuration; verify D in {64,128}, BLOCK in "
+               "{8,16,32,64}, 1 <= NQ <= 16, dtype and out_dtype";
+    case PA_ERR_ALIGNMENT:
+        return "PagedAttention: misaligned pointer; verify 16-byte aligned tensors and a "
+               "256-byte aligned workspace";
+    case PA_ERR_WORKSPACE:
+        return "PagedAttention: workspace missing or too small; verify pa_workspace_bytes()";
+    case PA_ERR_CUDA:
+        return "PagedAttention: CUDA call failed; verify the device, the stream and GPU limits";
+    case PA_ERR_DRIVER:
+        return "PagedAttention: cannot reach the driver's tensor-map encoder; verify the CUDA "
+               "driver version";
+    default:
+        return "PagedAttention: unknown error code";
+    }
+}
+
+size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions)
+{
+    if (batch < 0 || H < 1 || KV < 1 || H % KV || (D != 64 && D != 128) || NQ < 1 ||
+        NQ > PA_MAX_NQ || partitions < 0)
+        return 0;
+    if (partitions == 1 || batch == 0)
+        return 0;
+    const int R = (H / KV) * NQ;
+    const int rows_per_cta = kConsumerWarps * rows_group(R);
+    const int NRS = (R + rows_per_cta - 1) / rows_per_cta;
+    const int row_stride = R < rows_per_cta ? R : rows_per_cta;
+    return ws_layout(batch, D, row_stride, item_bound(batch, KV, NRS, partitions)).total;
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+              const int32_t* seq_lens, const void* k_new, const void* v_new, void* out,
+              float scale, int H, int KV, int D, int BLOCK, int NQ, int causal,
+              const pa_opts* opts, void* stream)
+{
+    if (!opts)
+        return PA_ERR_NULL_POINTER;
+    const int B = opts->batch;
+    if (B < 0 || H < 1 || KV < 1 || H % KV != 0 || opts->max_blocks < 1 ||
+        opts->num_blocks < 1 || opts->partitions < 0)
+        return PA_ERR_BAD_DIMS;
+    if ((D != 64 && D != 128) || (BLOCK != 8 && BLOCK != 16 && BLOCK != 32 && BLOCK != 64) ||
+        NQ < 1 || NQ > PA_MAX_NQ)
+        return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(opts->num_blocks) * BLOCK >= (1ll << 31) ||
+        static_cast<long long>(opts->max_blocks) * BLOCK >= (1ll << 30))
+        return PA_ERR_BAD_DIMS;
+    const int dtype = opts->dtype;
+    if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+        return PA_ERR_UNSUPPORTED;
+    const int out_dtype = opts->out_dtype < 0 ? dtype : opts->out_dtype;
+    if (out_dtype != dtype && out_dtype != PA_F32)
+        return PA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale))
+        return PA_ERR_BAD_DIMS;
+    if (B == 0)
+        return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !k_new || !v_new || !out)
+        return PA_ERR_NULL_POINTER;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_ALIGNMENT;
+
+    const int R = (H / KV) * NQ;
+    const int RG = rows_group(R);
+    const int rows_per_cta = kConsumerWarps * RG;
+    const int NRS = (R + rows_per_cta - 1) / rows_per_cta;
+    const int partitions = opts->partitions;
+    const int row_stride = R < rows_per_cta ? R : rows_per_cta;
+    const long long items = item_bound(B, KV, NRS, partitions);
+    if (items >= (1ll << 31))
+        return PA_ERR_BAD_DIMS;
+    WsLayout ws{};
+    if (partitions != 1) {
+        ws = ws_layout(B, D, row_stride, items);
+        if (!opts->workspace || opts->workspace_bytes < ws.total)
+            return PA_ERR_WORKSPACE;
+        if (!aligned(opts->workspace, 256))
+            return PA_ERR_ALIGNMENT;
+    }
+
+    const int es = static_cast<int>(elem_size(dtype));
+    const int TT = tokens_per_stage(D, es, BLOCK);
+    const int smem = 1024 /* alignment slack */ + kHeaderBytes + 2 * kStages * TT * D * es +
+                     static_cast<int>(align_up(2 * NQ * D * es, 16));
+
+    CUtensorMap kmap, vmap;
+    int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, &kmap);
+    if (rc == PA_OK)
+        rc = cache_map(v_cache, opts->num_blocks, BLOCK, KV, D, dtype, &vmap);
+    if (rc != PA_OK)
+        return rc;
+
+    const SplitFn split = pick_split(dtype, out_dtype == PA_F32 && dtype != PA_F32, D, RG);
+    int occ = 1, sms = 1;
+    rc = prepare_func(reinterpret_cast<const void*>(split), kThreads, smem, &occ, &sms);
+    if (rc != PA_OK)
+        return rc;
+
+    SplitParams p{};
+    p.q = q;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.out = out;
+    p.table = block_table;
+    p.seq_lens = seq_lens;
+    unsigned char* wsb = static_cast<unsigned char*>(opts->workspace);
+    p.sched = partitions != 1 ? reinterpret_cast<int2*>(wsb + ws.sched) : nullptr;
+    p.ws_ml = partitions != 1 ? reinterpret_cast<float2*>(wsb + ws.ml) : nullptr;
+    p.ws_o = partitions != 1 ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;
+    p.status = opts->status;
+    p.qscale = scale * kLog2e;
+    p.B = B;
+    p.H = H;
+    p.KV = KV;
+    p.NQ = NQ;
+    p.BLOCK = BLOCK;
+    p.maxb = opts->max_blocks;
+    p.num_blocks = opts->num_blocks;
+    p.causal = causal ? 1 : 0;
+    p.partitions = partitions;
+    long long target = static_cast<long long>(sms) * occ * kTargetWaves;
+    if (target > kAutoMaxTarget)
+        target = kAutoMaxTarget;
+    p.target_items = static_cast<int>(target);
+    p.min_chunk = static_cast<int>(align_up(kMinChunk, BLOCK));
+    p.checked = opts->checked ? 1 : 0;
+    p.R = R;
+    p.rows_per_cta = rows_per_cta;
+    p.NRS = NRS;
+    p.TT = TT;
+    p.row_stride = row_stride;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (opts->trace_begin &&
+        cudaEventRecord(static_cast<cudaEvent_t>(opts->trace_begin), st) != cudaSuccess)
+        return PA_ERR_CUDA;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(items));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[3] = {&p, &kmap, &vmap};
+    if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(split), args) != cudaSuccess)
+        return PA_ERR_CUDA;
+    g_launches.fetch_add(1);
+
+    if (opts->trace_split &&
+        cudaEventRecord(static_cast<cudaEvent_t>(opts->trace_split), st) != cudaSuccess)
+        return PA_ERR_CUDA;
+
+    if (partitions != 1) {
+        CombineParams cp{};
+        cp.sched = p.sched;
+        cp.ws_ml = p.ws_ml;
+        cp.ws_o = p.ws_o;
+        cp.out = out;
+        cp.B = B;
+        cp.KV = KV;
+        cp.R = R;
+        cp.NRS = NRS;
+        cp.rows_per_cta = rows_per_cta;
+        cp.row_stride = row_stride;
+        const CombineFn comb = pick_combine(out_dtype, D);
+        cudaLaunchConfig_t cc{};
+        cc.gridDim = dim3(static_cast<unsigned>(B) * KV * NRS);
+        cc.blockDim = dim3(128);
+        cc.dynamicSmemBytes = 0;
+        cc.stream = st;
+        cc.attrs = attr;
+        cc.numAttrs = 1;
+        void* cargs[1] = {&cp};
+        if (cudaLaunchKernelExC(&cc, reinterpret_cast<const void*>(comb), cargs) != cudaSuccess)
+            return PA_ERR_CUDA;
+        g_launches.fetch_add(1);
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+"""The C-ABI library loads, exports what include/*.h declares, and rejects
+invalid arguments on the host before any CUDA call (runs without a GPU)."""
+import ctypes
+import math
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_182_gb300 import _build
+
+    _build.build()
+    from paged_kv_cache_182_gb300 import binding
+
+    return binding
+
+
+def declared_functions():
+    names = set()
+    for header in sorted((ROOT / "include").glob("*.h")):
+        text = re.sub(r"/\*.*?\*/", "", header.read_text(), flags=re.S)
+        names.update(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("pa_decode", "pa_workspace_bytes", "pa_strerror", "pa_version"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(str(lib.LIBRARY))
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+
+
+def test_version_and_messages(lib):
+    assert lib.LIB.pa_version() >= 100
+    msgs = {c: lib.strerror(c) for c in range(-7, 1)}
+    assert len(set(msgs.values())) == len(msgs)
+    for c in range(-7, 0):
+        assert "verify" in msgs[c]
+
+
+def test_workspace_bytes(lib):
+    ws = lib.workspace_bytes
+    assert ws(8, 32, 8, 128, 1, 1) == 0
+    assert ws(8, 32, 7, 128, 1, 0) == 0  # H % KV != 0
+    assert ws(8, 32, 8, 96, 1, 0) == 0   # unsupported D
+    assert ws(8, 32, 8, 128, 1, 0) > 0
+    assert ws(1, 32, 8, 128, 1, 32) < ws(1, 32, 8, 128, 1, 64)
+    # one float32 (max, sum, D accumulators) state per row and key range
+    assert ws(1, 32, 8, 128, 1, 32) >= 32 * 8 * 4 * (128 + 2) * 4
+
+
+class Fake:
+    """16-byte aligned fake device addresses: validation must fail before any use."""
+
+    q = ctypes.c_void_p(0x10000)
+    kc = ctypes.c_void_p(0x20000)
+    vc = ctypes.c_void_p(0x30000)
+    table = ctypes.c_void_p(0x40000)
+    lens = ctypes.c_void_p(0x50000)
+    kn = ctypes.c_void_p(0x60000)
+    vn = ctypes.c_void_p(0x70000)
+    out = ctypes.c_void_p(0x80000)
+
+
+def call(lib, *, H=8, KV=2, D=64, BLOCK=16, NQ=1, scale=0.125, opts=None, q=Fake.q, **ov):
+    o = lib.PaOpts(batch=2, max_blocks=4, num_blocks=8, dtype=lib.PA_F16, out_dtype=-1,
+                   partitions=1, checked=0, workspace=None, workspace_bytes=0, status=None,
+                   trace_begin=None, trace_split=None)
+    for k, v in ov.items():
+        setattr(o, k, v)
+    ref = None if opts == "null" else ctypes.byref(o)
+    return lib.LIB.pa_decode(q, Fake.kc, Fake.vc, Fake.table, Fake.lens, Fake.kn, Fake.vn,
+                             Fake.out, ctypes.c_float(scale), H, KV, D, BLOCK, NQ, 0, ref, None)
+
+
+def test_rejects_invalid_arguments(lib):
+    assert call(lib, opts="null") == -1
+    assert call(lib, H=8, KV=3) == -2
+    assert call(lib, batch=-1) == -2
+    assert call(lib, max_blocks=0) == -2
+    assert call(lib, scale=math.nan) == -2
+    assert call(lib, num_blocks=1 << 28) == -2
+    assert call(lib, D=96) == -3
+    assert call(lib, BLOCK=12) == -3
+    assert call(lib, NQ=0) == -3
+    assert call(lib, NQ=17) == -3
+    assert call(lib, dtype=7) == -3
+    assert call(lib, dtype=lib.PA_BF16, out_dtype=lib.PA_F16) == -3
+    assert call(lib, q=None) == -1
+    assert call(lib, q=ctypes.c_void_p(0x10008)) == -4
+    assert call(lib, partitions=0) == -5
+    assert call(lib, partitions=0, workspace=0x100010, workspace_bytes=1 << 30) == -4
+
+
+def test_empty_batch_is_a_no_op(lib):
+    before = lib.kernel_launches()
+    assert call(lib, batch=0) == 0
+    assert lib.kernel_launches() == before

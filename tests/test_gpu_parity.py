@@ -1,0 +1,186 @@
+"""CUDA path against the float64 oracle, element by element (needs a GPU).
+
+Inputs come from the seeded generators; unused pool blocks and cache slots
+past each length are NaN, so any stray read shows up as a non-finite output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity_util as pu
+from paged_kv_cache_182_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+FMT_OUT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def small(name, **kw):
+    """A reduced copy of a named workload: several tiles, ragged tails."""
+    s = W.SPECS[name]
+    base = dict(
+        tiny_fp32=dict(),
+        gqa_fp16=dict(B=3, past=150, past_hi=900),
+        long_bf16=dict(past=3000),
+        causal_append_fp16=dict(B=3, past=333),
+        ragged_fp16=dict(B=7, past=20, past_hi=2500),
+    )[name]
+    base.update(kw)
+    return W.shrink(s, **base)
+
+
+# ------------------------------------------------------------- full workloads
+@pytest.mark.parametrize("name", W.ORDER)
+def test_full_workload_f32_output(name):
+    w = W.make(name, seed=0)
+    got = pu.run_gpu(w, out_dtype=torch.float32)
+    want = pu.run_oracle(w)
+    pu.check(got, want, w.spec.dtype, "f32", name)
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_full_workload_native_output(name):
+    w = W.make(name, seed=1)
+    got = pu.run_gpu(w)
+    assert got.dtype == FMT_OUT[w.spec.dtype]
+    want = pu.run_oracle(w)
+    pu.check(got, want, w.spec.dtype, w.spec.dtype, name)
+
+
+# ---------------------------------------------------------- split invariance
+@pytest.mark.parametrize("name", W.ORDER)
+@pytest.mark.parametrize("P", [1, 2, 7, 32, 0])
+def test_partition_counts(name, P):
+    w = W.make(small(name), seed=2)
+    got = pu.run_gpu(w, partitions=P, out_dtype=torch.float32)
+    pu.check(got, pu.run_oracle(w), w.spec.dtype, "f32", f"{name} P={P}")
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_more_seeds_small(seed):
+    for name in W.ORDER:
+        w = W.make(small(name), seed=seed)
+        got = pu.run_gpu(w, out_dtype=torch.float32)
+        pu.check(got, pu.run_oracle(w), w.spec.dtype, "f32", f"{name} seed={seed}")
+
+
+# ---------------------------------------------------------------- shape sweep
+SWEEP = [
+    # dtype, H, KV, D, BLOCK, NQ, causal, lens
+    ("f32", 8, 2, 128, 8, 1, False, [1, 77, 300]),
+    ("bf16", 16, 2, 64, 64, 3, True, [0, 64, 129, 1000]),
+    ("f16", 12, 3, 128, 32, 16, True, [5, 40]),
+    ("f16", 12, 3, 128, 32, 16, False, [31, 33]),
+    ("f16", 40, 5, 64, 16, 2, True, [400, 17]),       # 16 rows per KV head
+    ("bf16", 64, 1, 128, 16, 1, False, [700]),        # MQA: 64 rows, two row groups
+    ("f32", 4, 4, 64, 16, 1, False, [5000]),           # no grouping, long
+    ("f16", 32, 8, 128, 8, 4, True, [2047, 2048, 2049]),
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: f"{c[0]}-H{c[1]}-KV{c[2]}-D{c[3]}-B{c[4]}-NQ{c[5]}-{'c' if c[6] else 'n'}")
+@pytest.mark.parametrize("P", [0, 1, 3])
+def test_shape_sweep(case, P):
+    dt, H, KV, D, BLOCK, NQ, causal, lens = case
+    spec = W.Spec("sweep", dt, B=len(lens), H=H, KV=KV, D=D, BLOCK=BLOCK, NQ=NQ,
+                  causal=causal, pool_blocks=0, extra_table_cols=2)
+    w = W.make(spec, seed=5, lens=lens)
+    # a few spare (poisoned) pool blocks beyond the referenced ones
+    got = pu.run_gpu(w, partitions=P, out_dtype=torch.float32)
+    pu.check(got, pu.run_oracle(w), dt, "f32", f"sweep {case} P={P}")
+
+
+# ------------------------------------------------------------- closed forms
+def test_single_key_returns_new_value_exactly():
+    spec = W.Spec("one", "f16", B=3, H=8, KV=2, D=128, BLOCK=16, NQ=1)
+    w = W.make(spec, seed=6, lens=[0, 0, 0])
+    got = pu.run_gpu(w, partitions=0)
+    g = spec.group
+    want = w.v_new[:, :, 0, :].repeat_interleave(g, dim=1)
+    assert torch.equal(got[:, :, 0, :].cpu(), want)
+
+
+def test_block_permutation_is_bitwise_invariant():
+    w = W.make(small("gqa_fp16"), seed=7)
+    a = pu.run_gpu(w, out_dtype=torch.float32).cpu()
+    g = torch.Generator().manual_seed(8)
+    perm = torch.randperm(w.num_blocks, generator=g)  # new slot of each old block
+    inv = torch.argsort(perm)
+    w2 = W.Workload(w.spec, w.seq_lens, w.block_table.clone(), w.q, w.k_cache[inv].contiguous(),
+                    w.v_cache[inv].contiguous(), w.k_new, w.v_new)
+    t = w2.block_table
+    t[t >= 0] = perm[t[t >= 0].long()].to(torch.int32)
+    b = pu.run_gpu(w2, out_dtype=torch.float32).cpu()
+    assert torch.equal(a, b)
+
+
+def test_repeat_calls_are_deterministic():
+    w = W.make(small("ragged_fp16"), seed=9)
+    a = pu.run_gpu(w, out_dtype=torch.float32).cpu()
+    b = pu.run_gpu(w, out_dtype=torch.float32).cpu()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------- streams and graphs
+def test_side_stream_and_graph_replay():
+    from paged_kv_cache_182_gb300 import binding
+
+    w = W.make(small("gqa_fp16"), seed=10)
+    dev = w.to("cuda")
+    want = pu.run_oracle(w)
+    s = torch.cuda.Stream()
+    plan = binding.Plan(*dev.tensors(), scale=w.spec.scale, partitions=0,
+                        out_dtype=torch.float32)
+    with torch.cuda.stream(s):
+        plan.run(s)
+    s.synchronize()
+    pu.check(plan.out, want, "f16", "f32", "side stream")
+    plan.out.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        plan.run()
+    graph.replay()
+    torch.cuda.synchronize()
+    pu.check(plan.out, want, "f16", "f32", "graph replay")
+
+
+# ----------------------------------------------------------- device checks
+def test_checked_mode_reports_bad_block():
+    w = W.make(small("gqa_fp16"), seed=11)
+    w.block_table[1, 2] = w.num_blocks + 3
+    w.block_table[2, 0] = -2
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pu.run_gpu(w, out_dtype=torch.float32, status=status, checked=True)
+    assert int(status.item()) & 1
+
+
+def test_length_beyond_table_is_clamped_and_reported():
+    w = W.make(small("gqa_fp16"), seed=12)
+    lens = w.seq_lens.clone()
+    w_ok = W.Workload(w.spec, lens.clone(), w.block_table, w.q, w.k_cache, w.v_cache,
+                      w.k_new, w.v_new)
+    cap = w.max_blocks * w.spec.BLOCK
+    lens[0] = cap + 100
+    w.seq_lens = lens
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pu.run_gpu(w, out_dtype=torch.float32, status=status)
+    assert int(status.item()) & 2
+    assert w_ok.seq_lens[0] <= cap
+
+
+def test_checked_mode_clean_run_has_zero_status():
+    w = W.make(small("ragged_fp16"), seed=13)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pu.run_gpu(w, out_dtype=torch.float32, status=status, checked=True)
+    assert int(status.item()) == 0
+    pu.check(got, pu.run_oracle(w), "f16", "f32", "checked clean")
+
+
+def test_kernel_launch_counter_moves():
+    from paged_kv_cache_182_gb300 import binding
+
+    before = binding.kernel_launches()
+    w = W.make(small("gqa_fp16"), seed=14)
+    pu.run_gpu(w, partitions=1)
+    pu.run_gpu(w, partitions=0)
+    assert binding.kernel_launches() - before == 3
