@@ -158,7 +158,7 @@ def make(spec: Spec | str, seed: int = 0, poison: bool = True, lens=None) -> Wor
         seq_lens = torch.as_tensor(lens, dtype=torch.int32).reshape(spec.B)
     nblk = [(int(n) + spec.BLOCK - 1) // spec.BLOCK for n in seq_lens.tolist()]
     used = sum(nblk)
-    pool = max(spec.pool_blocks, used)
+    pool = max(spec.pool_blocks, used, 1)  # the pool is never empty
     perm = torch.randperm(pool, generator=g).to(torch.int32)
     maxb = max(nblk + [1]) + spec.extra_table_cols
     table = torch.full((spec.B, maxb), -1, dtype=torch.int32)
