@@ -59,6 +59,8 @@ extern "C" {
 #define PA_ERR_WORKSPACE (-5)    /* workspace NULL or smaller than pa_workspace_bytes() */
 #define PA_ERR_CUDA (-6)         /* a CUDA runtime call or kernel launch failed */
 #define PA_ERR_DRIVER (-7)       /* the tensor-map encoder of the driver is unavailable */
+#define PA_ERR_STATIC_LIMIT (-8) /* pa_decode_static_workspace: the call needs more
+                                    scratch than PA_STATIC_WORKSPACE_BYTES */
 
 /* device status bits, OR-ed into *opts->status when it is not NULL */
 #define PA_STATUS_BAD_BLOCK 1  /* checked mode: a table entry outside [0, num_blocks) */
@@ -67,6 +69,9 @@ extern "C" {
 
 /* supported sizes */
 #define PA_MAX_NQ 16
+
+/* scratch built into the library for pa_decode_static_workspace (16 MiB) */
+#define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 
 typedef struct pa_opts {
     int batch;       /* B, sequences in this call (0 = nothing to do) */
@@ -105,6 +110,37 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
               const void *k_new, const void *v_new, void *out, float scale,
               int H, int KV, int D, int BLOCK, int NQ, int causal,
               const pa_opts *opts, void *stream);
+
+/*
+ * pa_decode for callers that cannot allocate device memory.  The paged
+ * attention page has no counterpart to this entry point; it exists for
+ * callers such as an engine plugin that is handed only its input and output
+ * buffers (the host framework owns every device allocation), a serving loop
+ * that reserved all device memory up front, or latency-critical code that
+ * must not pay the device-wide synchronisation a cudaMalloc/cudaFree brings.
+ *
+ * Same arguments and results as pa_decode, except that opts->workspace and
+ * opts->workspace_bytes are ignored: the split scratch is a fixed array
+ * inside the library, PA_STATIC_WORKSPACE_BYTES per GPU, which every GPU that
+ * loads the library holds until the process exits.  The call allocates and
+ * frees nothing.
+ *   - A call whose pa_workspace_bytes() exceeds PA_STATIC_WORKSPACE_BYTES
+ *     returns PA_ERR_STATIC_LIMIT and launches nothing (use fewer partitions,
+ *     partitions == 1, or pa_decode with your own workspace).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture
+ *     starts.
+ *   - All calls on a device share the array, which keeps whatever the last
+ *     call left in it.  Nothing in it has to start at zero (each call writes
+ *     every value it later reads), but two calls whose kernels overlap on the
+ *     GPU (different streams, or host threads racing on one device) corrupt
+ *     each other's results: issue them on one stream.
+ */
+int pa_decode_static_workspace(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_table, const int32_t *seq_lens,
+                               const void *k_new, const void *v_new, void *out, float scale,
+                               int H, int KV, int D, int BLOCK, int NQ, int causal,
+                               const pa_opts *opts, void *stream);
 
 /*
  * Bytes of workspace pa_decode needs for these sizes (0 when partitions == 1).

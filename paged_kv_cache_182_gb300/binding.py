@@ -56,6 +56,8 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_decode.restype = I
     lib.pa_decode.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I, I, I,
                               ctypes.POINTER(PaOpts), P]
+    lib.pa_decode_static_workspace.restype = I
+    lib.pa_decode_static_workspace.argtypes = lib.pa_decode.argtypes
     lib.pa_workspace_bytes.restype = ctypes.c_size_t
     lib.pa_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.pa_strerror.restype = ctypes.c_char_p

@@ -247,6 +247,10 @@ const char* pa_strerror(int code)
     case PA_ERR_DRIVER:
         return "PagedAttention: cannot reach the driver's tensor-map encoder; verify the CUDA "
                "driver version";
+    case PA_ERR_STATIC_LIMIT:
+        return "PagedAttention: the call needs more scratch than the library's built-in "
+               "PA_STATIC_WORKSPACE_BYTES; verify pa_workspace_bytes(), use fewer partitions, "
+               "or call pa_decode with a workspace of your own";
     default:
         return "PagedAttention: unknown error code";
     }
