@@ -9,15 +9,16 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;                     // compute warps per CTA
+constexpr int kConsumerWarps = 8;                     // compute warps per CTA
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one TMA producer warp
-constexpr int kStages = 3;                            // shared-memory ring depth
+constexpr int kMaxStages = 8;                         // shared-memory ring depth limit
 constexpr int kSubBatch = 4;        // token steps per online-softmax update
-constexpr int kStageBytes = 32768;  // K + V bytes per pipeline stage (target)
-constexpr int kHeaderBytes = 1024;  // barriers + schedule, keeps stages 1024-aligned
+constexpr int kStageBytes = 32768;  // K + V tile bytes per pipeline stage (target)
+constexpr int kHeaderBytes = 1024;  // barriers and broadcast scalars
+constexpr int kMaxBatch = 4096;     // sequences per call (the schedule lives in smem)
 constexpr int kAutoMaxTarget = 4096;  // cap on automatic item targets
 constexpr int kMinChunk = 128;      // smallest automatic key range (tokens)
-constexpr int kTargetWaves = 2;     // automatic split: items ~ waves * resident CTAs
+constexpr int kTargetWaves = 4;     // automatic split: items ~ waves * resident CTAs
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -35,11 +36,21 @@ struct SplitParams {
     float qscale;   // scale * log2(e)
     int B, H, KV, NQ, BLOCK, maxb, num_blocks;
     int causal, partitions, target_items, min_chunk, checked;
+    int chunk_align;   // automatic key ranges are multiples of this (a stage's tokens)
     int R;             // query rows per KV head = (H / KV) * NQ
     int rows_per_cta;  // kConsumerWarps * RG
     int NRS;           // row groups per KV head = ceil(R / rows_per_cta)
     int TT;            // tokens per pipeline stage, a multiple of BLOCK
     int row_stride;    // workspace rows per item = min(R, rows_per_cta)
+    int stages;        // ring depth (<= kMaxStages)
+    int stage_bytes;   // bytes of one stage: K tile | K new rows | V tile | V new rows
+    int knew_off;      // byte offsets of the parts within a stage (1024-aligned)
+    int v_off;
+    int vnew_off;
+    int lens_off;      // shared-memory byte offsets from the 1024-aligned base
+    int prefix_off;
+    int merge_off;
+    int stage_off;
 };
 
 struct CombineParams {
@@ -53,10 +64,13 @@ struct CombineParams {
 using SplitFn = void (*)(SplitParams, CUtensorMap, CUtensorMap);
 using CombineFn = void (*)(CombineParams);
 
-// Kernel tables, one per input element type (pa_inst_*.cu).
+// Kernel tables, one per input element type (pa_inst_*.cu).  float32 inputs
+// use the CUDA-core kernel (RG query rows per warp); 16-bit inputs use the
+// tensor-core kernel (16 * MT query rows per CTA pass).
+constexpr int kMmaTokens = 16 * kConsumerWarps;  // tokens per stage of the tensor-core kernel
 SplitFn pick_split_f32(int D, int RG);
-SplitFn pick_split_f16(bool f32_out, int D, int RG);
-SplitFn pick_split_bf16(bool f32_out, int D, int RG);
+SplitFn pick_split_f16(bool f32_out, int D, int MT);
+SplitFn pick_split_bf16(bool f32_out, int D, int MT);
 CombineFn pick_combine_f32(int D);
 CombineFn pick_combine_f16(int D);
 CombineFn pick_combine_bf16(int D);

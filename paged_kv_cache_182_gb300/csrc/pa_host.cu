@@ -27,8 +27,17 @@ std::atomic<uint64_t> g_launches{0};
 
 size_t elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 
-// Query rows per consumer warp: 4 up to 16 rows per KV head, else 8.
-int rows_group(int R) { return R <= 16 ? 4 : 8; }
+// CUDA-core path (float32): query rows per consumer warp, 4 up to 32 rows
+// per KV head, else 8; a CTA pass covers kConsumerWarps * RG rows.
+int rows_group(int R) { return R <= 32 ? 4 : 8; }
+
+// Tensor-core path (16-bit): 16-row MMA tiles per CTA pass.
+int mma_tiles(int R) { return R <= 16 ? 1 : 2; }
+
+int rows_per_pass(int dtype, int R)
+{
+    return dtype == PA_F32 ? kConsumerWarps * rows_group(R) : 16 * mma_tiles(R);
+}
 
 int tokens_per_stage(int D, int es, int BLOCK)
 {
@@ -102,6 +111,8 @@ int g_map_count = 0, g_map_next = 0;
 int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dtype,
               CUtensorMap* out)
 {
+    // 16-bit caches feed the tensor-core kernel: 64-column boxes, 128-byte swizzle.
+    const bool swz = dtype != PA_F32;
     const MapKey key{base, static_cast<long long>(num_blocks) * BLOCK, KV, D, BLOCK, dtype};
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_map_count; ++i)
@@ -120,11 +131,13 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
                           static_cast<cuuint64_t>(key.rows)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
                              static_cast<cuuint64_t>(KV) * D * es};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(BLOCK)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(swz ? 64 : D), 1u,
+                         static_cast<cuuint32_t>(BLOCK)};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUtensorMap map;
     const CUresult rc = enc(&map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (rc != CUDA_SUCCESS)
         return PA_ERR_CUDA;
@@ -236,7 +249,7 @@ const char* pa_strerror(int code)
                "num_blocks * BLOCK < 2^31 and a finite scale";
     case PA_ERR_UNSUPPORTED:
         return "PagedAttention: unsupported configuration; verify D in {64,128}, BLOCK in "
-               "{8,16,32,64}, 1 <= NQ <= 16, dtype and out_dtype";
+               "{8,16,32,64}, 1 <= NQ <= 16, batch <= 4096, dtype and out_dtype";
     case PA_ERR_ALIGNMENT:
         return "PagedAttention: misaligned pointer; verify 16-byte aligned tensors and a "
                "256-byte aligned workspace";
@@ -264,10 +277,16 @@ size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partition
     if (partitions == 1 || batch == 0)
         return 0;
     const int R = (H / KV) * NQ;
-    const int rows_per_cta = kConsumerWarps * rows_group(R);
-    const int NRS = (R + rows_per_cta - 1) / rows_per_cta;
-    const int row_stride = R < rows_per_cta ? R : rows_per_cta;
-    return ws_layout(batch, D, row_stride, item_bound(batch, KV, NRS, partitions)).total;
+    // the larger of the two paths' needs, so that the size does not depend on the dtype
+    size_t need = 0;
+    for (int dtype : {PA_F32, PA_F16}) {
+        const int rpc = rows_per_pass(dtype, R);
+        const int NRS = (R + rpc - 1) / rpc;
+        const int row_stride = R < rpc ? R : rpc;
+        const size_t t = ws_layout(batch, D, row_stride, item_bound(batch, KV, NRS, partitions)).total;
+        need = t > need ? t : need;
+    }
+    return need;
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
@@ -297,6 +316,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         return PA_ERR_BAD_DIMS;
     if (B == 0)
         return PA_OK;
+    if (B > kMaxBatch)
+        return PA_ERR_UNSUPPORTED;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !k_new || !v_new || !out)
         return PA_ERR_NULL_POINTER;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
@@ -305,8 +326,10 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         return PA_ERR_ALIGNMENT;
 
     const int R = (H / KV) * NQ;
+    const bool mma = dtype != PA_F32;
     const int RG = rows_group(R);
-    const int rows_per_cta = kConsumerWarps * RG;
+    const int MT = mma_tiles(R);
+    const int rows_per_cta = rows_per_pass(dtype, R);
     const int NRS = (R + rows_per_cta - 1) / rows_per_cta;
     const int partitions = opts->partitions;
     const int row_stride = R < rows_per_cta ? R : rows_per_cta;
@@ -323,9 +346,31 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     }
 
     const int es = static_cast<int>(elem_size(dtype));
-    const int TT = tokens_per_stage(D, es, BLOCK);
-    const int smem = 1024 /* alignment slack */ + kHeaderBytes + 2 * kStages * TT * D * es +
-                     static_cast<int>(align_up(2 * NQ * D * es, 16));
+    const int TT = mma ? kMmaTokens : tokens_per_stage(D, es, BLOCK);
+    // shared memory: header | lens[B] | prefix[B+1] | consumer scratch | ring
+    const int lens_off = kHeaderBytes;
+    const int prefix_off = static_cast<int>(align_up(lens_off + 4 * B, 16));
+    const int merge_off = static_cast<int>(align_up(prefix_off + 4 * (B + 1), 128));
+    const int merge_bytes =
+        mma ? 2 * (16 * MT) * (kMmaTokens + 8) * 2 + 2 * kConsumerWarps * (16 * MT) * 4
+            : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4;
+    const int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));
+    const int knew_off = TT * D * es;
+    const int v_off = static_cast<int>(align_up(knew_off + NQ * D * es, 1024));
+    const int vnew_off = v_off + TT * D * es;
+    const int stage_bytes = static_cast<int>(align_up(vnew_off + NQ * D * es, 1024));
+    int dev = 0, smem_optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+        return PA_ERR_CUDA;
+    const int slack = 1024;  // alignment of the dynamic shared-memory base
+    int stages = (smem_optin - slack - stage_off) / stage_bytes;
+    if (stages > kMaxStages)
+        stages = kMaxStages;
+    if (stages < 2)
+        return PA_ERR_UNSUPPORTED;
+    const int smem = slack + stage_off + stages * stage_bytes;
 
     CUtensorMap kmap, vmap;
     int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, &kmap);
@@ -334,7 +379,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     if (rc != PA_OK)
         return rc;
 
-    const SplitFn split = pick_split(dtype, out_dtype == PA_F32 && dtype != PA_F32, D, RG);
+    const SplitFn split =
+        pick_split(dtype, out_dtype == PA_F32 && dtype != PA_F32, D, mma ? MT : RG);
     int occ = 1, sms = 1;
     rc = prepare_func(reinterpret_cast<const void*>(split), kThreads, smem, &occ, &sms);
     if (rc != PA_OK)
@@ -362,17 +408,30 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.num_blocks = opts->num_blocks;
     p.causal = causal ? 1 : 0;
     p.partitions = partitions;
-    long long target = static_cast<long long>(sms) * occ * kTargetWaves;
+    long long grid = static_cast<long long>(sms) * occ;  // persistent CTAs
+    if (grid > items)
+        grid = items;
+    long long target = grid * kTargetWaves;
     if (target > kAutoMaxTarget)
         target = kAutoMaxTarget;
     p.target_items = static_cast<int>(target);
-    p.min_chunk = static_cast<int>(align_up(kMinChunk, BLOCK));
+    p.min_chunk = static_cast<int>(align_up(kMinChunk > TT ? kMinChunk : TT, TT));
+    p.chunk_align = TT;
     p.checked = opts->checked ? 1 : 0;
     p.R = R;
     p.rows_per_cta = rows_per_cta;
     p.NRS = NRS;
     p.TT = TT;
     p.row_stride = row_stride;
+    p.stages = stages;
+    p.stage_bytes = stage_bytes;
+    p.knew_off = knew_off;
+    p.v_off = v_off;
+    p.vnew_off = vnew_off;
+    p.lens_off = lens_off;
+    p.prefix_off = prefix_off;
+    p.merge_off = merge_off;
+    p.stage_off = stage_off;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (opts->trace_begin &&
@@ -384,7 +443,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
 
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(items));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
