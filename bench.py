@@ -175,9 +175,7 @@ def make_plans(w, device, partitions=None):
                                                       w.k_new, w.v_new))
     P = w.spec.partitions if partitions is None else partitions
     out = torch.empty(q.shape, dtype=q.dtype, device=device)
-    ws = torch.empty(max(1, binding.workspace_bytes(w.spec.B, w.spec.H, w.spec.KV, w.spec.D,
-                                                    w.spec.NQ, P)),
-                     dtype=torch.uint8, device=device)
+    ws = binding.new_workspace(w.spec.B, w.spec.H, w.spec.KV, w.spec.D, w.spec.NQ, P, device)
     plans = []
     for k, v in zip(kc, vc):
         p = binding.Plan(q, k, v, table, lens, kn, vn, scale=w.spec.scale, causal=w.spec.causal,

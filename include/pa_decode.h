@@ -83,11 +83,18 @@ typedef struct pa_opts {
                         P >= 2 = each sequence split into P key ranges */
     int checked;     /* nonzero: report table entries outside the pool */
     void *workspace; /* device scratch of >= pa_workspace_bytes() bytes, 256-aligned;
-                        may be NULL when partitions == 1 */
+                        may be NULL when partitions == 1.  Unless merge_kernel is
+                        set, its first pa_workspace_zero_bytes() bytes (split
+                        counters) must be zero before its first use; every call
+                        that completes leaves them zero again (after a call that
+                        reports PA_STATUS_TIMEOUT, zero them once more) */
     size_t workspace_bytes;
     int *status;        /* device int32 for PA_STATUS_* bits, or NULL */
     void *trace_begin;  /* optional cudaEvent_t recorded before the partition kernel */
     void *trace_split;  /* optional cudaEvent_t recorded after it (before the merge) */
+    int merge_kernel;   /* 0 (default): the partition kernel's last CTA to finish a
+                           split sequence merges its partial states; 1: a separate
+                           log-sum-exp merge kernel does (no counters needed) */
 } pa_opts;
 
 /*
@@ -131,10 +138,11 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
  *     that device current; make that first call before any stream capture
  *     starts.
  *   - All calls on a device share the array, which keeps whatever the last
- *     call left in it.  Nothing in it has to start at zero (each call writes
- *     every value it later reads), but two calls whose kernels overlap on the
- *     GPU (different streams, or host threads racing on one device) corrupt
- *     each other's results: issue them on one stream.
+ *     call left in it.  Nothing in it has to start at zero (this entry point
+ *     always merges split sequences with the separate merge kernel, and each
+ *     call writes every value it later reads), but two calls whose kernels
+ *     overlap on the GPU (different streams, or host threads racing on one
+ *     device) corrupt each other's results: issue them on one stream.
  */
 int pa_decode_static_workspace(const void *q, const void *k_cache, const void *v_cache,
                                const int32_t *block_table, const int32_t *seq_lens,
@@ -150,6 +158,13 @@ int pa_decode_static_workspace(const void *q, const void *k_cache, const void *v
  * Returns 0 for invalid arguments.
  */
 size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions);
+
+/*
+ * Leading bytes of the workspace that must be zero before its first use with
+ * the in-kernel merge (per-sequence split counters; see pa_opts.workspace).
+ * 0 when partitions == 1.  Returns 0 for invalid arguments.
+ */
+size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions);
 
 /* A sentence naming what to verify for a PA_ERR_* code (static storage). */
 const char *pa_strerror(int code);

@@ -42,6 +42,7 @@ class PaOpts(ctypes.Structure):
         ("status", ctypes.c_void_p),
         ("trace_begin", ctypes.c_void_p),
         ("trace_split", ctypes.c_void_p),
+        ("merge_kernel", ctypes.c_int),
     ]
 
 
@@ -60,6 +61,8 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_decode_static_workspace.argtypes = lib.pa_decode.argtypes
     lib.pa_workspace_bytes.restype = ctypes.c_size_t
     lib.pa_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.pa_workspace_zero_bytes.restype = ctypes.c_size_t
+    lib.pa_workspace_zero_bytes.argtypes = [I, I, I, I, I, I]
     lib.pa_strerror.restype = ctypes.c_char_p
     lib.pa_strerror.argtypes = [I]
     lib.pa_version.restype = I
@@ -88,6 +91,17 @@ def workspace_bytes(B: int, H: int, KV: int, D: int, NQ: int, partitions: int = 
     return int(LIB.pa_workspace_bytes(B, H, KV, D, NQ, partitions))
 
 
+def workspace_zero_bytes(B: int, H: int, KV: int, D: int, NQ: int, partitions: int = 0) -> int:
+    """Leading workspace bytes that must be zero before first use (in-kernel merge)."""
+    return int(LIB.pa_workspace_zero_bytes(B, H, KV, D, NQ, partitions))
+
+
+def new_workspace(B, H, KV, D, NQ, partitions=0, device="cuda"):
+    """A zero-filled workspace of the size pa_decode needs (None when none is needed)."""
+    need = workspace_bytes(B, H, KV, D, NQ, partitions)
+    return torch.zeros(need, dtype=torch.uint8, device=device) if need > 0 else None
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -109,7 +123,7 @@ class Plan:
     def __init__(self, q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *,
                  scale: float, causal: bool = False, partitions: int = 0, out=None,
                  out_dtype=None, workspace=None, status=None, checked: bool = False,
-                 trace=None):
+                 trace=None, merge_kernel: bool = False):
         B, H, NQ, D = q.shape
         NB, BLOCK, KV, D2 = k_cache.shape
         if (D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape)
@@ -136,9 +150,8 @@ class Plan:
             out = torch.empty((B, H, NQ, D), dtype=odt, device=q.device)
         elif tuple(out.shape) != (B, H, NQ, D) or not out.is_contiguous() or out.dtype != odt:
             raise ValueError("out must be a contiguous [B, H, NQ, D] tensor of the output dtype")
-        need = workspace_bytes(B, H, KV, D, NQ, partitions)
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is None:
+            workspace = new_workspace(B, H, KV, D, NQ, partitions, q.device)
         self.tensors = tensors
         self.out = out
         self.workspace = workspace
@@ -154,7 +167,8 @@ class Plan:
             workspace_bytes=0 if workspace is None else workspace.numel(),
             status=None if status is None else status.data_ptr(),
             trace_begin=None if trace is None else trace[0].cuda_event,
-            trace_split=None if trace is None else trace[1].cuda_event)
+            trace_split=None if trace is None else trace[1].cuda_event,
+            merge_kernel=int(bool(merge_kernel)))
         self._args = [_ptr(t) for t in tensors] + [_ptr(out), ctypes.c_float(scale), H, KV, D,
                                                    BLOCK, NQ, int(bool(causal)),
                                                    ctypes.byref(self.opts)]
@@ -186,11 +200,14 @@ class Plan:
 
 def decode(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *, scale: float,
            causal: bool = False, partitions: int = 0, out=None, out_dtype=None, workspace=None,
-           status=None, checked: bool = False, stream=None):
-    """Decode attention on device tensors (see the module docstring); returns ``out``."""
+           status=None, checked: bool = False, stream=None, merge_kernel: bool = False):
+    """Decode attention on device tensors (see the module docstring); returns ``out``.
+
+    A caller-provided ``workspace`` must be zero-filled before its first use
+    (see pa_opts.workspace); ``new_workspace`` makes one."""
     plan = Plan(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, scale=scale,
                 causal=causal, partitions=partitions, out=out, out_dtype=out_dtype,
-                workspace=workspace, status=status, checked=checked)
+                workspace=workspace, status=status, checked=checked, merge_kernel=merge_kernel)
     return plan.run(stream)
 
 

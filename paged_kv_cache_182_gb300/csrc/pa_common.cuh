@@ -11,14 +11,14 @@ namespace pa {
 
 constexpr int kConsumerWarps = 8;                     // compute warps per CTA
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one TMA producer warp
-constexpr int kMaxStages = 8;                         // shared-memory ring depth limit
+constexpr int kMaxStages = 32;                        // shared-memory ring depth limit
+constexpr int kMinRing = 3;                           // stages kept before widening scratch
 constexpr int kSubBatch = 4;        // token steps per online-softmax update
-constexpr int kStageBytes = 32768;  // K + V tile bytes per pipeline stage (target)
-constexpr int kHeaderBytes = 1024;  // barriers and broadcast scalars
+constexpr int kStageBytes = 32768;     // CUDA-core path: K + V tile bytes per stage (target)
+constexpr int kMmaStageBytes = 65536;  // tensor-core path: K + V tile bytes per stage (target)
+constexpr int kHeaderBytes = 2048;  // barriers, broadcast scalars, zero row, table-entry slots
 constexpr int kMaxBatch = 4096;     // sequences per call (the schedule lives in smem)
-constexpr int kAutoMaxTarget = 4096;  // cap on automatic item targets
-constexpr int kMinChunk = 128;      // smallest automatic key range (tokens)
-constexpr int kTargetWaves = 4;     // automatic split: items ~ waves * resident CTAs
+constexpr int kMaxGrid = 1024;      // partition-kernel CTAs at most (sizes the workspace)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -29,14 +29,17 @@ struct SplitParams {
     void* out;
     const int32_t* table;
     const int32_t* seq_lens;
-    int2* sched;    // [B] (first chunk index, chunk count), or NULL for one pass
+    int2* sched;    // [B] (prefix, count) for the merge kernel, or NULL for one pass
+    int* counters;  // [B * NRS * KV] finished pieces per split segment (in-kernel merge), or NULL
     float2* ws_ml;  // [items][row_stride] (max, sum) in base-2 units
     float* ws_o;    // [items][row_stride][D]
     int* status;
     float qscale;   // scale * log2(e)
     int B, H, KV, NQ, BLOCK, maxb, num_blocks;
-    int causal, partitions, target_items, min_chunk, checked;
-    int chunk_align;   // automatic key ranges are multiples of this (a stage's tokens)
+    int causal, partitions, checked;
+    int qbuf_off;      // tensor-core kernel: scratch offset of the two query-row buffers
+    int box_rows;      // rows of one TMA box (cache tokens); divides BLOCK and TT
+    int empty_count;   // consumer warps that release each stage
     int R;             // query rows per KV head = (H / KV) * NQ
     int rows_per_cta;  // kConsumerWarps * RG
     int NRS;           // row groups per KV head = ceil(R / rows_per_cta)
@@ -59,6 +62,8 @@ struct CombineParams {
     const float* ws_o;
     void* out;
     int B, KV, R, NRS, rows_per_cta, row_stride;
+    int stream;  // automatic (balanced) schedule: records are per partition-kernel CTA
+    int grid;    // partition-kernel CTAs (automatic schedule)
 };
 
 using SplitFn = void (*)(SplitParams, CUtensorMap, CUtensorMap);
@@ -67,7 +72,8 @@ using CombineFn = void (*)(CombineParams);
 // Kernel tables, one per input element type (pa_inst_*.cu).  float32 inputs
 // use the CUDA-core kernel (RG query rows per warp); 16-bit inputs use the
 // tensor-core kernel (16 * MT query rows per CTA pass).
-constexpr int kMmaTokens = 16 * kConsumerWarps;  // tokens per stage of the tensor-core kernel
+constexpr int kMmaTokens = 16;  // tokens per stage of the tensor-core kernel (one warp's MMA group)
+constexpr int kMergeDR = 32;  // tensor-core kernel: output columns merged per round
 SplitFn pick_split_f32(int D, int RG);
 SplitFn pick_split_f16(bool f32_out, int D, int MT);
 SplitFn pick_split_bf16(bool f32_out, int D, int MT);

@@ -49,28 +49,30 @@ int tokens_per_stage(int D, int es, int BLOCK)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Upper bound on the work items of one call (also the partition grid size).
-long long item_bound(int B, int KV, int NRS, int partitions)
+// Workspace records of one call: automatic schedule, two per partition-kernel
+// CTA (its first and last piece); fixed partitions, one per item.
+long long record_bound(int B, int KV, int NRS, int partitions)
 {
     const long long per_seq = static_cast<long long>(KV) * NRS;
-    if (partitions == 1)
-        return B * per_seq;
-    if (partitions >= 2)
-        return B * per_seq * partitions;
-    return kAutoMaxTarget + B * per_seq;
+    if (partitions == 0)
+        return 2ll * kMaxGrid;
+    return B * per_seq * partitions;
 }
 
+// Workspace: split counters (in-kernel merge) | per-sequence schedule |
+// (max, sum) of every partial record | accumulators of every partial record.
 struct WsLayout {
-    size_t sched, ml, o, total;
+    size_t counters, sched, ml, o, total;
 };
 
-WsLayout ws_layout(int B, int D, int row_stride, long long items)
+WsLayout ws_layout(int B, int D, int segments, int row_stride, long long records)
 {
     WsLayout w;
-    w.sched = 0;
-    w.ml = align_up(static_cast<size_t>(B) * sizeof(int2), 256);
-    w.o = w.ml + align_up(static_cast<size_t>(items) * row_stride * sizeof(float2), 256);
-    w.total = w.o + static_cast<size_t>(items) * row_stride * D * sizeof(float);
+    w.counters = 0;
+    w.sched = align_up(static_cast<size_t>(segments) * sizeof(int), 256);
+    w.ml = w.sched + align_up(static_cast<size_t>(B) * sizeof(int2), 256);
+    w.o = w.ml + align_up(static_cast<size_t>(records) * row_stride * sizeof(float2), 256);
+    w.total = w.o + static_cast<size_t>(records) * row_stride * D * sizeof(float);
     return w;
 }
 
@@ -108,12 +110,12 @@ int g_map_count = 0, g_map_next = 0;
 
 // Cache pool [num_blocks * BLOCK rows][KV][D] as a 3-D tensor; one box is one
 // block of one KV head: {D, 1, BLOCK}.
-int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dtype,
+int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dtype, int box_rows,
               CUtensorMap* out)
 {
     // 16-bit caches feed the tensor-core kernel: 64-column boxes, 128-byte swizzle.
     const bool swz = dtype != PA_F32;
-    const MapKey key{base, static_cast<long long>(num_blocks) * BLOCK, KV, D, BLOCK, dtype};
+    const MapKey key{base, static_cast<long long>(num_blocks) * BLOCK, KV, D, box_rows, dtype};
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_map_count; ++i)
         if (g_map_keys[i] == key) {
@@ -127,18 +129,33 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
     const CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(KV),
-                          static_cast<cuuint64_t>(key.rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
-                             static_cast<cuuint64_t>(KV) * D * es};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(swz ? 64 : D), 1u,
-                         static_cast<cuuint32_t>(BLOCK)};
-    cuuint32_t estr[3] = {1u, 1u, 1u};
+    // float32 (CUDA-core path): 3-D {D, KV, rows}, box {D, 1, box_rows}, no swizzle.
+    // 16-bit (tensor-core path): 4-D {64, D/64, KV, rows}, box {64, D/64, 1,
+    // box_rows} -- one box brings both 64-column halves of box_rows token rows.
     CUtensorMap map;
-    const CUresult rc = enc(&map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult rc;
+    if (swz) {
+        cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(KV),
+                              static_cast<cuuint64_t>(key.rows)};
+        cuuint64_t strides[3] = {128u, static_cast<cuuint64_t>(D) * es,
+                                 static_cast<cuuint64_t>(KV) * D * es};
+        cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(D / 64), 1u,
+                             static_cast<cuuint32_t>(box_rows)};
+        cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+        rc = enc(&map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(KV),
+                              static_cast<cuuint64_t>(key.rows)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
+                                 static_cast<cuuint64_t>(KV) * D * es};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1u, static_cast<cuuint32_t>(box_rows)};
+        cuuint32_t estr[3] = {1u, 1u, 1u};
+        rc = enc(&map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (rc != CUDA_SUCCESS)
         return PA_ERR_CUDA;
     const int slot = g_map_count < kMapCache ? g_map_count++ : (g_map_next++ % kMapCache);
@@ -269,24 +286,44 @@ const char* pa_strerror(int code)
     }
 }
 
-size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions)
+// Largest layout over the two paths (the row grouping differs by dtype), so
+// that the sizes do not depend on the dtype.
+static WsLayout ws_bound(int batch, int H, int KV, int D, int NQ, int partitions)
 {
-    if (batch < 0 || H < 1 || KV < 1 || H % KV || (D != 64 && D != 128) || NQ < 1 ||
-        NQ > PA_MAX_NQ || partitions < 0)
-        return 0;
-    if (partitions == 1 || batch == 0)
-        return 0;
     const int R = (H / KV) * NQ;
-    // the larger of the two paths' needs, so that the size does not depend on the dtype
-    size_t need = 0;
+    WsLayout best{};
     for (int dtype : {PA_F32, PA_F16}) {
         const int rpc = rows_per_pass(dtype, R);
         const int NRS = (R + rpc - 1) / rpc;
         const int row_stride = R < rpc ? R : rpc;
-        const size_t t = ws_layout(batch, D, row_stride, item_bound(batch, KV, NRS, partitions)).total;
-        need = t > need ? t : need;
+        const WsLayout w = ws_layout(batch, D, batch * NRS * KV, row_stride,
+                                     record_bound(batch, KV, NRS, partitions));
+        if (w.total > best.total)
+            best.total = w.total;
+        if (w.sched > best.sched)
+            best.sched = w.sched;  // = bytes of the counters region
     }
-    return need;
+    return best;
+}
+
+static bool ws_args_ok(int batch, int H, int KV, int D, int NQ, int partitions)
+{
+    return batch >= 0 && H >= 1 && KV >= 1 && H % KV == 0 && (D == 64 || D == 128) && NQ >= 1 &&
+           NQ <= PA_MAX_NQ && partitions >= 0;
+}
+
+size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions)
+{
+    if (!ws_args_ok(batch, H, KV, D, NQ, partitions) || partitions == 1 || batch == 0)
+        return 0;
+    return ws_bound(batch, H, KV, D, NQ, partitions).total;
+}
+
+size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions)
+{
+    if (!ws_args_ok(batch, H, KV, D, NQ, partitions) || partitions == 1 || batch == 0)
+        return 0;
+    return ws_bound(batch, H, KV, D, NQ, partitions).sched;
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
@@ -333,12 +370,17 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     const int NRS = (R + rows_per_cta - 1) / rows_per_cta;
     const int partitions = opts->partitions;
     const int row_stride = R < rows_per_cta ? R : rows_per_cta;
-    const long long items = item_bound(B, KV, NRS, partitions);
-    if (items >= (1ll << 31))
+    const long long records = record_bound(B, KV, NRS, partitions);
+    if (records >= (1ll << 31))
+        return PA_ERR_BAD_DIMS;
+    // the automatic schedule counts BLOCK-token units of all segments in int32
+    const long long units = static_cast<long long>(B) * (opts->max_blocks + 1 + NQ / BLOCK + 1) *
+                            NRS * KV;
+    if (partitions == 0 && units >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
     WsLayout ws{};
     if (partitions != 1) {
-        ws = ws_layout(B, D, row_stride, items);
+        ws = ws_layout(B, D, B * NRS * KV, row_stride, records);
         if (!opts->workspace || opts->workspace_bytes < ws.total)
             return PA_ERR_WORKSPACE;
         if (!aligned(opts->workspace, 256))
@@ -346,25 +388,46 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     }
 
     const int es = static_cast<int>(elem_size(dtype));
-    const int TT = mma ? kMmaTokens : tokens_per_stage(D, es, BLOCK);
+    // tensor-core path: up to 64 KB stages, at most 8 warps (16-token groups x
+    // row groups) per stage: 128 tokens (64 with 32 rows per pass)
+    int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
+    if (mma && (TT / kMmaTokens) * MT > kConsumerWarps)
+        TT = kConsumerWarps / MT * kMmaTokens;
+    const int box_rows = mma ? (BLOCK < kMmaTokens ? BLOCK : kMmaTokens) : BLOCK;
+    const int ROWS = 16 * MT;
     // shared memory: header | lens[B] | prefix[B+1] | consumer scratch | ring
     const int lens_off = kHeaderBytes;
     const int prefix_off = static_cast<int>(align_up(lens_off + 4 * B, 16));
     const int merge_off = static_cast<int>(align_up(prefix_off + 4 * (B + 1), 128));
-    const int merge_bytes =
-        mma ? 2 * (16 * MT) * (kMmaTokens + 8) * 2 + 2 * kConsumerWarps * (16 * MT) * 4
-            : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4;
-    const int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));
-    const int knew_off = TT * D * es;
-    const int v_off = static_cast<int>(align_up(knew_off + NQ * D * es, 1024));
-    const int vnew_off = v_off + TT * D * es;
-    const int stage_bytes = static_cast<int>(align_up(vnew_off + NQ * D * es, 1024));
+    // stage: tensor-core path K tile | V tile | K new rows | V new rows (tiles
+    // 1024-aligned for the swizzle); CUDA-core path K tile | K new | V tile | V new
+    int v_off, knew_off, vnew_off, stage_end;
+    if (mma) {
+        v_off = TT * D * es;
+        knew_off = 2 * TT * D * es;
+        vnew_off = knew_off + NQ * D * es;
+        stage_end = vnew_off + NQ * D * es;
+    } else {
+        knew_off = TT * D * es;
+        v_off = static_cast<int>(align_up(knew_off + NQ * D * es, 1024));
+        vnew_off = v_off + TT * D * es;
+        stage_end = vnew_off + NQ * D * es;
+    }
+    const int stage_bytes = static_cast<int>(align_up(stage_end, 1024));
     int dev = 0, smem_optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess)
         return PA_ERR_CUDA;
     const int slack = 1024;  // alignment of the dynamic shared-memory base
+    // consumer scratch: tensor-core path, (max, sum) tables, one merge round of
+    // [warps][16 rows][kMergeDR] floats and two query-row buffers; CUDA-core
+    // path, per-warp states
+    const int qbuf_off = 2048 + kConsumerWarps * 16 * kMergeDR * 4;
+    const int merge_bytes = mma ? qbuf_off + 2 * ROWS * D * es
+                                : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4 +
+                                      kConsumerWarps * RG * 8;
+    const int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));
     int stages = (smem_optin - slack - stage_off) / stage_bytes;
     if (stages > kMaxStages)
         stages = kMaxStages;
@@ -373,9 +436,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     const int smem = slack + stage_off + stages * stage_bytes;
 
     CUtensorMap kmap, vmap;
-    int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, &kmap);
+    int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, &kmap);
     if (rc == PA_OK)
-        rc = cache_map(v_cache, opts->num_blocks, BLOCK, KV, D, dtype, &vmap);
+        rc = cache_map(v_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, &vmap);
     if (rc != PA_OK)
         return rc;
 
@@ -395,6 +458,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.seq_lens = seq_lens;
     unsigned char* wsb = static_cast<unsigned char*>(opts->workspace);
     p.sched = partitions != 1 ? reinterpret_cast<int2*>(wsb + ws.sched) : nullptr;
+    p.counters = partitions != 1 && !opts->merge_kernel ? reinterpret_cast<int*>(wsb + ws.counters)
+                                                         : nullptr;
     p.ws_ml = partitions != 1 ? reinterpret_cast<float2*>(wsb + ws.ml) : nullptr;
     p.ws_o = partitions != 1 ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;
     p.status = opts->status;
@@ -409,14 +474,13 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.causal = causal ? 1 : 0;
     p.partitions = partitions;
     long long grid = static_cast<long long>(sms) * occ;  // persistent CTAs
-    if (grid > items)
-        grid = items;
-    long long target = grid * kTargetWaves;
-    if (target > kAutoMaxTarget)
-        target = kAutoMaxTarget;
-    p.target_items = static_cast<int>(target);
-    p.min_chunk = static_cast<int>(align_up(kMinChunk > TT ? kMinChunk : TT, TT));
-    p.chunk_align = TT;
+    if (grid > kMaxGrid)
+        grid = kMaxGrid;
+    if (partitions != 0 && grid > records)  // fixed partitions: no more CTAs than items
+        grid = records;
+    p.qbuf_off = qbuf_off;
+    p.box_rows = box_rows;
+    p.empty_count = mma ? (TT / kMmaTokens) * MT : kConsumerWarps;
     p.checked = opts->checked ? 1 : 0;
     p.R = R;
     p.rows_per_cta = rows_per_cta;
@@ -458,7 +522,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         cudaEventRecord(static_cast<cudaEvent_t>(opts->trace_split), st) != cudaSuccess)
         return PA_ERR_CUDA;
 
-    if (partitions != 1) {
+    if (partitions != 1 && opts->merge_kernel) {
         CombineParams cp{};
         cp.sched = p.sched;
         cp.ws_ml = p.ws_ml;
@@ -470,6 +534,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         cp.NRS = NRS;
         cp.rows_per_cta = rows_per_cta;
         cp.row_stride = row_stride;
+        cp.stream = partitions == 0 ? 1 : 0;
+        cp.grid = static_cast<int>(grid);
         const CombineFn comb = pick_combine(out_dtype, D);
         cudaLaunchConfig_t cc{};
         cc.gridDim = dim3(static_cast<unsigned>(B) * KV * NRS);

@@ -37,6 +37,7 @@
 #include <cuda_fp16.h>
 
 #include <cfloat>
+#include <climits>
 #include <cstring>
 #include <type_traits>
 
@@ -105,59 +106,65 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x)
 }
 
 // ---------------------------------------------------------------- schedule
+// A segment is the key range [0, past + NQ) of one (sequence b, row group rsg,
+// KV head kh).  A piece is a contiguous part [start, end) of one segment that
+// one CTA processes; `whole` pieces write the normalised output, the others a
+// partial (max, sum, accumulator) record `rec` of the workspace.
+//
+// Automatic mode (partitions == 0): the segments, cut into BLOCK-token units,
+// are laid end to end (sequence, then row group, then KV head) and CTA k takes
+// units [k*W/G, (k+1)*W/G) of the W units (G = min(CTAs, W), so no range is
+// empty) -- every CTA streams the same number
+// of cache blocks whatever the length mix, and only the pieces cut at CTA
+// boundaries need merging (records 2k and 2k+1: the CTA's first and last
+// piece).
+// Fixed partitions (P >= 1): each segment is split into P ranges of whole
+// blocks (P == 1: no split); the ranges are items dealt to CTAs round-robin;
+// record = item index.
 struct Item {
-    int b, c, kh, rsg, n, past, start, end;  // key range [start, end)
+    int b, rsg, kh, past, start, end;
+    int whole;  // the piece is its whole segment
+    int rec;    // workspace record of a partial piece
+    int units;  // automatic mode: units of the piece
 };
 
-__device__ __forceinline__ int chunk_of(const SplitParams& p, int total, int auto_chunk)
+__device__ __forceinline__ int chunk_of(const SplitParams& p, int total)
 {
-    if (p.partitions == 0)
-        return auto_chunk;
     const int per = p.partitions == 1 ? total : (total + p.partitions - 1) / p.partitions;
     return ((per + p.BLOCK - 1) / p.BLOCK) * p.BLOCK;
 }
 
-// Shared-memory schedule built once per CTA: clamped lengths, the automatic
-// key-range length, and the prefix sum of key ranges per sequence.
+// Shared-memory schedule built once per CTA.
 struct Sched {
-    const int* lens;    // [B]
-    const int* prefix;  // [B + 1] key ranges before sequence b
-    int auto_chunk;
-    int total_items;
+    const int* lens;    // [B] clamped cached lengths
+    const int* prefix;  // [B + 1] automatic: units before sequence b (all its segments);
+                        //         fixed: ranges before sequence b (one segment's worth)
+    int total;          // automatic: W units; fixed: number of items
 };
 
-// Executed by one full warp after `lens` is in shared memory.  CTA 0 also
-// records every sequence's (first range, range count) for the merge kernel.
-__device__ __forceinline__ void build_schedule(const SplitParams& p, const int* lens, int* prefix, int* info,
-                               int lane)
+__device__ __forceinline__ long long range_start(long long k, long long W, long long G)
 {
-    int C = 0;
-    if (p.partitions == 0) {
-        long long sum = 0;
-        for (int b = lane; b < p.B; b += 32)
-            sum += lens[b] + p.NQ;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            sum += __shfl_xor_sync(kFull, sum, o);
-        const long long units = sum * p.KV * p.NRS;
-        long long per = (units + p.target_items - 1) / p.target_items;
-        per = ((per + p.chunk_align - 1) / p.chunk_align) * p.chunk_align;
-        if (per < p.min_chunk)
-            per = p.min_chunk;
-        if (per > (1 << 30))
-            per = 1 << 30;
-        C = static_cast<int>(per);
-    }
+    return k * W / G;
+}
+
+// Executed by one full warp after `lens` is in shared memory.  CTA 0 also
+// records every sequence's (prefix, count) for the merge kernel.
+__device__ __forceinline__ void build_schedule(const SplitParams& p, const int* lens, int* prefix,
+                                               int* info, int lane)
+{
+    const int U = p.NRS * p.KV;
+    const bool stream = p.partitions == 0;
     int run = 0;
     for (int base = 0; base < p.B; base += 32) {
         const int b = base + lane;
         int n = 0;
         if (b < p.B) {
             const int total = lens[b] + p.NQ;
-            const int chunk = chunk_of(p, total, C);
+            const int chunk = stream ? p.BLOCK : chunk_of(p, total);
             n = (total + chunk - 1) / chunk;
         }
-        int incl = n;
+        const int w = stream ? n * U : n;
+        int incl = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(kFull, incl, o);
@@ -165,46 +172,142 @@ __device__ __forceinline__ void build_schedule(const SplitParams& p, const int* 
                 incl += y;
         }
         if (b < p.B) {
-            prefix[b] = run + incl - n;
+            prefix[b] = run + incl - w;
             if (blockIdx.x == 0 && p.sched)
-                p.sched[b] = make_int2(run + incl - n, n);
+                p.sched[b] = make_int2(run + incl - w, n);
         }
         run += __shfl_sync(kFull, incl, 31);
     }
     if (lane == 0) {
         prefix[p.B] = run;
-        info[0] = C;
-        info[1] = run * p.NRS * p.KV;
+        info[1] = stream ? run : run * U;
     }
 }
 
-// Work item `item`: items are ordered by sequence, key range, row group, KV
-// head (adjacent KV heads read interleaved rows of the same cache blocks).
-__device__ __forceinline__ Item decode_item(const SplitParams& p, const Sched& s, int item)
+__device__ __forceinline__ int last_le(const int* prefix, int B, long long x)
 {
-    const int U = p.NRS * p.KV;
-    const int g = item / U;
-    const int rem = item - g * U;
-    Item it;
-    it.rsg = rem / p.KV;
-    it.kh = rem - it.rsg * p.KV;
-    int lo = 0, hi = p.B - 1;  // last b with prefix[b] <= g
+    int lo = 0, hi = B - 1;  // last b with prefix[b] <= x
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (s.prefix[mid] <= g)
+        if (prefix[mid] <= x)
             lo = mid;
         else
             hi = mid - 1;
     }
-    it.b = lo;
-    it.c = g - s.prefix[lo];
-    it.n = s.prefix[lo + 1] - s.prefix[lo];
-    it.past = s.lens[lo];
-    const int total = it.past + p.NQ;
-    const int chunk = chunk_of(p, total, s.auto_chunk);
-    it.start = it.c * chunk;
-    it.end = min(it.start + chunk, total);
-    return it;
+    return lo;
+}
+
+// Iterates this CTA's pieces in order (identically in every warp).
+struct PieceIter {
+    long long pos, stop, first_pos;
+    bool ok;
+    Item it;
+
+    __device__ __forceinline__ void first(const SplitParams& p, const Sched& sc)
+    {
+        if (p.partitions == 0) {
+            // with fewer units than CTAs only the first W CTAs take work, so
+            // that every range is non-empty (the merge kernel counts on it)
+            const long long G = min(static_cast<long long>(gridDim.x), static_cast<long long>(sc.total));
+            pos = blockIdx.x < G ? range_start(blockIdx.x, sc.total, G) : 0;
+            stop = blockIdx.x < G ? range_start(blockIdx.x + 1, sc.total, G) : 0;
+        } else {
+            pos = blockIdx.x;
+            stop = sc.total;
+        }
+        first_pos = pos;
+        load(p, sc);
+    }
+
+    __device__ __forceinline__ void next(const SplitParams& p, const Sched& sc)
+    {
+        pos += p.partitions == 0 ? it.units : gridDim.x;
+        load(p, sc);
+    }
+
+    __device__ __forceinline__ void load(const SplitParams& p, const Sched& sc)
+    {
+        ok = pos < stop;
+        if (!ok)
+            return;
+        if (p.partitions == 0) {
+            const int b = last_le(sc.prefix, p.B, pos);
+            const int total = sc.lens[b] + p.NQ;
+            const int n = (total + p.BLOCK - 1) / p.BLOCK;
+            const int local = static_cast<int>(pos - sc.prefix[b]);
+            const int seg = local / n;
+            const int uu = local - seg * n;
+            const int len = static_cast<int>(min(static_cast<long long>(n - uu), stop - pos));
+            it.b = b;
+            it.rsg = seg / p.KV;
+            it.kh = seg - it.rsg * p.KV;
+            it.past = sc.lens[b];
+            it.start = uu * p.BLOCK;
+            it.end = min((uu + len) * p.BLOCK, total);
+            it.whole = uu == 0 && len == n;
+            it.rec = 2 * blockIdx.x + (pos == first_pos ? 0 : 1);
+            it.units = len;
+        } else {
+            const int U = p.NRS * p.KV;
+            const int item = static_cast<int>(pos);
+            const int g = item / U;
+            const int rem = item - g * U;
+            const int b = last_le(sc.prefix, p.B, g);
+            const int c = g - sc.prefix[b];
+            const int total = sc.lens[b] + p.NQ;
+            const int chunk = chunk_of(p, total);
+            it.b = b;
+            it.rsg = rem / p.KV;
+            it.kh = rem - it.rsg * p.KV;
+            it.past = sc.lens[b];
+            it.start = c * chunk;
+            it.end = min(it.start + chunk, total);
+            it.whole = sc.prefix[b + 1] - sc.prefix[b] == 1;
+            it.rec = item;
+            it.units = 0;
+        }
+    }
+};
+
+// Pieces of segment (b, rsg, kh) and the workspace record of piece c, as the
+// partition kernel laid them out (see the schedule comment above).
+struct SegPieces {
+    int n;          // pieces of the segment
+    int k0;         // automatic mode: CTA of the first piece
+    int rec_first;  // automatic mode: record of the first piece
+    int item0;      // fixed partitions: first key range of the sequence
+};
+
+__device__ __forceinline__ SegPieces seg_pieces(const SplitParams& p, const Sched& sc, int b, int rsg,
+                                                int kh)
+{
+    SegPieces sp;
+    if (p.partitions == 0) {
+        const long long W = sc.total;
+        const long long G = min(static_cast<long long>(gridDim.x), W);
+        const int units = (sc.lens[b] + p.NQ + p.BLOCK - 1) / p.BLOCK;
+        const long long s0 = sc.prefix[b] + static_cast<long long>(rsg * p.KV + kh) * units;
+        const long long s1 = s0 + units;
+        sp.k0 = static_cast<int>(((s0 + 1) * G - 1) / W);
+        const int k1 = static_cast<int>((s1 * G - 1) / W);
+        sp.n = k1 - sp.k0 + 1;
+        sp.rec_first = 2 * sp.k0 + (range_start(sp.k0, W, G) == s0 ? 0 : 1);
+        sp.item0 = 0;
+    } else {
+        sp.n = sc.prefix[b + 1] - sc.prefix[b];
+        sp.item0 = sc.prefix[b];
+        sp.k0 = 0;
+        sp.rec_first = 0;
+    }
+    return sp;
+}
+
+__device__ __forceinline__ size_t seg_record(const SplitParams& p, const SegPieces& sp, int c, int rsg,
+                                             int kh)
+{
+    if (p.partitions == 0)
+        return c == 0 ? static_cast<size_t>(sp.rec_first) : static_cast<size_t>(2 * (sp.k0 + c));
+    return (static_cast<size_t>(sp.item0 + c) * p.NRS + rsg) * p.KV + kh;
 }
 
 __device__ __forceinline__ void consumer_bar_sync()
@@ -402,12 +505,16 @@ struct SimtMath {
 
 // ------------------------------------------------------- CTA set-up, producer
 // Shared memory of the partition kernels, carved from a 1024-aligned base:
-//   [0, 64)      full barriers     [64, 128)  empty barriers
-//   [128, 192)   broadcast scalars [256, 272) a zeroed 16-byte row (mma path)
+//   [0, 256)     full barriers      [256, 512)  empty barriers
+//   [512, 576)   broadcast scalars  [576, 608)  query-buffer barriers (full, free)
+//   [640, 896)   a zeroed 256-byte row (tensor-core path)
+//   [1024, 2048) producer table-entry slots
 //   lens[B] | prefix[B+1] | consumer scratch | ring of `stages` stages.
 struct Smem {
     uint64_t* full;
     uint64_t* empty;
+    uint64_t* q_full;  // [2]
+    uint64_t* q_free;  // [2]
     int* info;
     volatile int* abort_flag;
     const void* zero16;
@@ -415,6 +522,7 @@ struct Smem {
     int* prefix;
     unsigned char* scratch;
     unsigned char* ring;
+    int* entries;  // producer's table-entry slots [kTableSlots][kSlotInts]
 };
 
 __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
@@ -423,9 +531,12 @@ __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
     Smem sm;
     sm.full = reinterpret_cast<uint64_t*>(base);
     sm.empty = sm.full + kMaxStages;
-    sm.info = reinterpret_cast<int*>(base + 128);
+    sm.info = reinterpret_cast<int*>(base + 512);
     sm.abort_flag = sm.info + 15;
-    sm.zero16 = base + 256;
+    sm.q_full = reinterpret_cast<uint64_t*>(base + 576);
+    sm.q_free = sm.q_full + 2;
+    sm.zero16 = base + 640;
+    sm.entries = reinterpret_cast<int*>(base + 1024);
     sm.lens = reinterpret_cast<int*>(base + p.lens_off);
     sm.prefix = reinterpret_cast<int*>(base + p.prefix_off);
     sm.scratch = base + p.merge_off;
@@ -440,10 +551,15 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kConsumerWarps);
+            mbar_init(&sm.empty[s], p.empty_count);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_free[i], kConsumerWarps);
         }
         sm.info[15] = 0;
-        *reinterpret_cast<uint4*>(const_cast<void*>(sm.zero16)) = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i)
+            reinterpret_cast<uint4*>(const_cast<void*>(sm.zero16))[i] = make_uint4(0, 0, 0, 0);
         fence_mbar_init();
     }
     const int cap = p.maxb * p.BLOCK;
@@ -463,17 +579,63 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
     Sched sc;
     sc.lens = sm.lens;
     sc.prefix = sm.prefix;
-    sc.auto_chunk = sm.info[0];
-    sc.total_items = sm.info[1];
+    sc.total = sm.info[1];
     return sc;
 }
 
+// Walks the tiles of this CTA's pieces in order.
+struct TileIter {
+    PieceIter pc;
+    int j, ntiles;
+    __device__ __forceinline__ void start(const SplitParams& p, const Sched& sc)
+    {
+        pc.first(p, sc);
+        j = 0;
+        ntiles = pc.ok ? (pc.it.end - pc.it.start + p.TT - 1) / p.TT : 0;
+    }
+    __device__ __forceinline__ bool valid() const { return pc.ok; }
+    __device__ __forceinline__ void next(const SplitParams& p, const Sched& sc)
+    {
+        if (++j == ntiles) {
+            pc.next(p, sc);
+            j = 0;
+            ntiles = pc.ok ? (pc.it.end - pc.it.start + p.TT - 1) / p.TT : 0;
+        }
+    }
+};
+
+constexpr int kTableAhead = 8;   // tiles whose table entries are in flight ahead of use
+constexpr int kTableSlots = 16;  // entry slots (> kTableAhead)
+constexpr int kSlotInts = 16;    // entries per slot (boxes per tile at most)
+
+// Starts a non-blocking copy of the table entries of the tile at `t` into
+// entry slot `slot` (lane i copies entry i), as one cp.async group.
+__device__ __forceinline__ void fetch_entries(const SplitParams& p, const Sched& sc, const TileIter& t,
+                                              int* slot, int lane)
+{
+    if (t.valid()) {
+        const Item& it = t.pc.it;
+        const int t0 = it.start + t.j * p.TT;
+        const int cache_end = min(min(t0 + p.TT, it.end), it.past);
+        const int nb = cache_end > t0 ? (cache_end - t0 + p.box_rows - 1) / p.box_rows : 0;
+        if (lane < nb) {
+            const int32_t* src =
+                p.table + static_cast<size_t>(it.b) * p.maxb + (t0 + lane * p.box_rows) / p.BLOCK;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(slot + lane)),
+                         "l"(src)
+                         : "memory");
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // The producer warp: for every tile of every item of this CTA, wait for a
-// free stage, read the table entries of the tile (one per lane), and issue
-// one TMA box per cache block for K and for V (two 64-column boxes per block
-// with the 128-byte swizzle when kSwizzled), plus a bulk copy of the new rows
-// when the tile reaches them.  Completion is counted on the stage's full
-// barrier.
+// free stage and issue one TMA box per cache block for K and for V (two
+// 64-column boxes per block with the 128-byte swizzle when kSwizzled), plus a
+// bulk copy of the new rows when the tile reaches them.  Completion is
+// counted on the stage's full barrier.  Table entries are fetched
+// kTableAhead tiles ahead with cp.async, so no dependent global load sits on
+// the issue path.
 template <typename T, int D, bool kSwizzled>
 __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, const CUtensorMap* kmap,
                         const CUtensorMap* vmap, int lane)
@@ -483,18 +645,46 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
         tma_prefetch_desc(vmap);
     }
     const int S = p.stages, TT = p.TT;
-    const uint32_t block_bytes = static_cast<uint32_t>(p.BLOCK * D * sizeof(T));
+    const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows * D * sizeof(T));
     const uint32_t new_bytes = static_cast<uint32_t>(p.NQ * D * sizeof(T));
+    int* entries = sm.entries;  // [kTableSlots][kSlotInts]
+
+    TileIter cur, ahead;
+    cur.start(p, sc);
+    ahead.start(p, sc);
+    for (int k = 0; k < kTableAhead; ++k) {
+        fetch_entries(p, sc, ahead, entries + (k % kTableSlots) * kSlotInts, lane);
+        if (ahead.valid())
+            ahead.next(p, sc);
+    }
+    const int HB = p.box_rows;
     uint32_t gt = 0;  // tiles issued by this CTA
-    bool ok = true;
-    for (int item = blockIdx.x; item < sc.total_items && ok; item += gridDim.x) {
-        const Item it = decode_item(p, sc, item);
-        const int ntiles = (it.end - it.start + TT - 1) / TT;
-        for (int j = 0; j < ntiles; ++j, ++gt) {
-            const int s = gt % S;
-            if (gt >= static_cast<uint32_t>(S)) {
-                ok = !*sm.abort_flag &&
-                     mbar_wait_bounded(&sm.empty[s], ((gt / S) - 1) & 1, kWaitLimitNs);
+    int piece = -1;   // pieces begun by this CTA
+    for (; cur.valid(); cur.next(p, sc), ++gt) {
+        fetch_entries(p, sc, ahead, entries + ((gt + kTableAhead) % kTableSlots) * kSlotInts, lane);
+        if (ahead.valid())
+            ahead.next(p, sc);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
+        const int s = gt % S;
+        if (gt >= static_cast<uint32_t>(S)) {
+            bool ok = !*sm.abort_flag &&
+                      mbar_wait_bounded(&sm.empty[s], ((gt / S) - 1) & 1, kWaitLimitNs);
+            ok = __all_sync(kFull, ok);
+            if (!ok) {
+                if (lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+                break;
+            }
+        }
+        const Item& it = cur.pc.it;
+        if (kSwizzled && cur.j == 0) {
+            // the piece's query rows go to buffer piece & 1 once every
+            // consumer warp has finished the tiles of the piece two back
+            ++piece;
+            const int par = piece & 1;
+            if (piece >= 2) {
+                bool ok = !*sm.abort_flag &&
+                          mbar_wait_bounded(&sm.q_free[par], ((piece >> 1) - 1) & 1, kWaitLimitNs);
                 ok = __all_sync(kFull, ok);
                 if (!ok) {
                     if (lane == 0)
@@ -502,57 +692,118 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
                     break;
                 }
             }
-            const int t0 = it.start + j * TT;
-            const int t1 = min(t0 + TT, it.end);
-            const int cache_end = min(t1, it.past);
-            const int nb = cache_end > t0 ? (cache_end - t0 + p.BLOCK - 1) / p.BLOCK : 0;
-            const bool has_new = t1 > it.past;
-            int phys = 0;
-            if (lane < nb) {
-                phys = p.table[static_cast<size_t>(it.b) * p.maxb + t0 / p.BLOCK + lane];
-                if (p.checked && (phys < 0 || phys >= p.num_blocks) && p.status)
-                    atomicOr(p.status, PA_STATUS_BAD_BLOCK);
-            }
-            unsigned char* st = sm.ring + static_cast<size_t>(s) * p.stage_bytes;
-            unsigned char* ks = st;
-            unsigned char* vs = st + p.v_off;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&sm.full[s],
-                                      2u * nb * block_bytes + (has_new ? 2u * new_bytes : 0u));
-            __syncwarp();
-            if (lane < nb) {
-                // Out-of-pool coordinates read as zeros: the copy never faults.
-                const int z = phys * p.BLOCK;
-                if constexpr (kSwizzled) {
-                    // [D/64 halves][TT rows][64 columns], 128-byte swizzle
-#pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        const size_t off = static_cast<size_t>(h) * TT * 128 + lane * p.BLOCK * 128;
-                        tma_load_3d(ks + off, kmap, 64 * h, it.kh, z, &sm.full[s]);
-                        tma_load_3d(vs + off, vmap, 64 * h, it.kh, z, &sm.full[s]);
-                    }
-                } else {
-                    const size_t off = static_cast<size_t>(lane) * p.BLOCK * D * sizeof(T);
-                    tma_load_3d(ks + off, kmap, 0, it.kh, z, &sm.full[s]);
-                    tma_load_3d(vs + off, vmap, 0, it.kh, z, &sm.full[s]);
-                }
-            }
-            if (has_new && lane == 0) {
-                const size_t off = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.NQ * D;
-                bulk_load(st + p.knew_off, static_cast<const T*>(p.k_new) + off, new_bytes,
-                          &sm.full[s]);
-                bulk_load(st + p.vnew_off, static_cast<const T*>(p.v_new) + off, new_bytes,
-                          &sm.full[s]);
+            if (lane == 0) {
+                const int rows = min(p.rows_per_cta, p.R - it.rsg * p.rows_per_cta);
+                const uint32_t qb = static_cast<uint32_t>(rows * D * sizeof(T));
+                const size_t off =
+                    ((static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta) * D;
+                unsigned char* dst = sm.scratch + p.qbuf_off + par * p.rows_per_cta * D * sizeof(T);
+                mbar_arrive_expect_tx(&sm.q_full[par], qb);
+                bulk_load(dst, static_cast<const T*>(p.q) + off, qb, &sm.q_full[par]);
             }
         }
+        const int t0 = it.start + cur.j * TT;
+        const int t1 = min(t0 + TT, it.end);
+        const int cache_end = min(t1, it.past);
+        const int nb = cache_end > t0 ? (cache_end - t0 + HB - 1) / HB : 0;
+        const bool has_new = t1 > it.past;
+        if (lane < nb && p.checked) {
+            const int phys = entries[(gt % kTableSlots) * kSlotInts + lane];  // own cp.async
+            if ((phys < 0 || phys >= p.num_blocks) && p.status)
+                atomicOr(p.status, PA_STATUS_BAD_BLOCK);
+        }
+        unsigned char* st = sm.ring + static_cast<size_t>(s) * p.stage_bytes;
+        unsigned char* ks = st;
+        unsigned char* vs = st + p.v_off;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&sm.full[s],
+                                  2u * nb * box_bytes + (has_new ? 2u * new_bytes : 0u));
+        __syncwarp();
+        // One warp instruction issues every box of the stage: lane 2i loads
+        // the K rows of box i, lane 2i+1 its V rows (the issue cost of a TMA
+        // instruction is per instruction, not per lane).
+        __syncwarp();  // entries written by other lanes' cp.async are visible
+        if (lane < 2 * nb) {
+            const int bi = lane >> 1;
+            const bool is_v = lane & 1;
+            const int ph = entries[(gt % kTableSlots) * kSlotInts + bi];
+            // Out-of-pool coordinates read as zeros: the copy never faults.
+            const int z = ph * p.BLOCK + (t0 + bi * HB) % p.BLOCK;
+            const size_t off = static_cast<size_t>(bi) * HB * D * sizeof(T);
+            if constexpr (kSwizzled) {
+                // box [HB rows][D/64 halves][64 columns], 128-byte swizzle
+                tma_load_4d((is_v ? vs : ks) + off, is_v ? vmap : kmap, 0, 0, it.kh, z, &sm.full[s]);
+            } else {
+                tma_load_3d((is_v ? vs : ks) + off, is_v ? vmap : kmap, 0, it.kh, z, &sm.full[s]);
+            }
+        }
+        if (has_new && lane == 0) {
+            const size_t off = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.NQ * D;
+            bulk_load(st + p.knew_off, static_cast<const T*>(p.k_new) + off, new_bytes, &sm.full[s]);
+            bulk_load(st + p.vnew_off, static_cast<const T*>(p.v_new) + off, new_bytes, &sm.full[s]);
+        }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     // Leave no copy in flight if the pipeline was abandoned.
     __syncwarp();
     if (*sm.abort_flag && lane == 0) {
         const uint32_t first = gt > static_cast<uint32_t>(S) ? gt - S : 0u;
         for (uint32_t g = first; g < gt; ++g)
             mbar_wait_bounded(&sm.full[g % S], (g / S) & 1, kWaitLimitNs);
+        for (int pc = max(0, piece - 1); pc <= piece; ++pc)
+            mbar_wait_bounded(&sm.q_full[pc & 1], (pc >> 1) & 1, kWaitLimitNs);
     }
+}
+
+// ---------------------------------------------------------- in-kernel merge
+// Called by all consumer threads after this CTA wrote the partial record of
+// piece `it` (not a whole segment).  Counts the finished pieces of the
+// segment; the CTA that finishes the last one merges every record of the
+// segment (M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
+// out = L == 0 ? O : O / L) and resets the counter for the next call.
+// `tot` is shared scratch for rows_per_cta (max, sum) pairs; `flag` a shared int.
+template <int D, typename TO>
+__device__ void finish_split_piece(const SplitParams& p, const Sched& sc, const Item& it, int R_cta,
+                                   float2* tot, volatile int* flag)
+{
+    const int tid = threadIdx.x;  // consumer threads only: 0 .. kConsumerWarps*32-1
+    const int seg = (it.b * p.NRS + it.rsg) * p.KV + it.kh;
+    __threadfence();  // this thread's record stores before the count
+    consumer_bar_sync();
+    const SegPieces sp = seg_pieces(p, sc, it.b, it.rsg, it.kh);
+    if (tid == 0)
+        *flag = atomicAdd(&p.counters[seg], 1) == sp.n - 1;
+    consumer_bar_sync();
+    if (!*flag)
+        return;
+    __threadfence();  // the other CTAs' records are visible (read them through L2)
+    for (int rl = tid; rl < R_cta; rl += kConsumerWarps * 32) {
+        float M = -FLT_MAX, L = 0.f;
+        for (int c = 0; c < sp.n; ++c)
+            M = fmaxf(M, __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]).x);
+        for (int c = 0; c < sp.n; ++c) {
+            const float2 ml = __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]);
+            L = fmaf(ml.y, fast_exp2(ml.x - M), L);
+        }
+        tot[rl] = make_float2(M, L);
+    }
+    consumer_bar_sync();
+    const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta;
+    for (int idx = tid; idx < R_cta * D; idx += kConsumerWarps * 32) {
+        const int rl = idx / D, d = idx - rl * D;
+        const float2 ml = tot[rl];
+        float O = 0.f;
+        for (int c = 0; c < sp.n; ++c) {
+            const size_t wrow = seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl;
+            const float f = fast_exp2(__ldcg(&p.ws_ml[wrow]).x - ml.x);
+            O = fmaf(f, __ldcg(&p.ws_o[wrow * D + d]), O);
+        }
+        const float val = ml.y == 0.f ? O : O / ml.y;
+        static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
+    }
+    if (tid == 0)
+        p.counters[seg] = 0;  // every piece has arrived: ready for the next call
+    consumer_bar_sync();      // `tot` and `flag` are free again
 }
 
 // ------------------------------------------- float32 CUDA-core partition kernel
@@ -568,6 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* mb_o = reinterpret_cast<float*>(sm.scratch);  // [kConsumerWarps*RG][D]
     float* mb_m = mb_o + kConsumerWarps * RG * D;
     float* mb_l = mb_m + kConsumerWarps * RG;
+    float2* merge_tot = reinterpret_cast<float2*>(mb_l + kConsumerWarps * RG);  // [rows per pass]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -587,8 +839,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Math = SimtMath<T, D, RG>;
     uint32_t gt = 0;
     const int tid = threadIdx.x;  // 0 .. kConsumerWarps*32-1
-    for (int item = blockIdx.x; item < sc.total_items; item += gridDim.x) {
-        const Item it = decode_item(p, sc, item);
+    PieceIter pi;
+    for (pi.first(p, sc); pi.ok; pi.next(p, sc)) {
+        const Item& it = pi.it;
         const int ntiles = (it.end - it.start + TT - 1) / TT;
         const int R_cta = min(p.rows_per_cta, p.R - it.rsg * p.rows_per_cta);
         const int nrg_raw = (R_cta + RG - 1) / RG;
@@ -643,16 +896,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 L = fmaf(mb_l[slot], f, L);
                 O = fmaf(mb_o[slot * D + d], f, O);
             }
-            if (it.n == 1) {
+            if (it.whole) {
                 const float val = L == 0.f ? O : O / L;
                 static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
             } else {
-                const size_t wrow = static_cast<size_t>(item) * p.row_stride + rl;
+                const size_t wrow = static_cast<size_t>(it.rec) * p.row_stride + rl;
                 p.ws_o[wrow * D + d] = O;
                 if (d == 0)
                     p.ws_ml[wrow] = make_float2(M, L);
             }
         }
+        if (!it.whole && p.counters)
+            finish_split_piece<D, TO>(p, sc, it, R_cta, merge_tot, &sm.info[14]);
     }
 }
 
@@ -683,65 +938,79 @@ struct Pack<__nv_bfloat16> {
     }
 };
 
-// Stage of the tensor-core kernel: K and V tiles of kMmaTokens tokens stored
-// [D/64 halves][tokens][64 columns] with the TMA 128-byte swizzle (16-byte
-// chunk c of token row t sits at chunk c ^ (t % 8)); the new rows unswizzled.
-template <int D>
-__device__ __forceinline__ uint32_t tile_chunk_addr(uint32_t tile, int tok, int chunk)
-{
-    const int h = chunk >> 3, c = chunk & 7;
-    return tile + h * (kMmaTokens * 128) + tok * 128 + ((c ^ (tok & 7)) << 4);
-}
+// Stage of the tensor-core kernel: K and V tiles of kMmaTokens (16) tokens
+// stored [16 tokens][D/64 halves][64 columns]: 128-byte lines, line
+// L = token * (D/64) + half, with the TMA 128-byte swizzle (16-byte chunk c of
+// line L sits at chunk c ^ (L % 8)); the new rows unswizzled [NQ][D]; a
+// 256-byte zero row stands in for tokens past the tile.
+struct RowAddr {
+    uint32_t base;  // address of the row's first 128-byte line
+    uint32_t swz;   // XOR of the first line (the second line's is swz ^ hx)
+    uint32_t hx;    // 1 for swizzled rows of two lines, else 0
+    __device__ __forceinline__ uint32_t at(int chunk) const
+    {
+        const uint32_t h = static_cast<uint32_t>(chunk) >> 3;
+        return base + h * 128 + ((static_cast<uint32_t>(chunk & 7) ^ swz ^ (h * hx)) << 4);
+    }
+};
 
-// Shared-memory address of 16-byte chunk `chunk` of token `tok` of the tile
-// starting at key t0: a cache row, a new row, or the zero row past the tile.
 template <int D>
-__device__ __forceinline__ uint32_t row_chunk(uint32_t tile, uint32_t fresh, uint32_t zero, int tok,
-                                              int n_tile, int t0, int past, int chunk)
+__device__ __forceinline__ RowAddr row_addr(uint32_t tile, uint32_t fresh, uint32_t zero, int tok,
+                                            int n_tile, int t0, int past)
 {
-    if (tok >= n_tile)
-        return zero;
+    constexpr int NH = D / 64;
+    RowAddr r;
     const int ta = t0 + tok;
-    if (ta < past)
-        return tile_chunk_addr<D>(tile, tok, chunk);
-    return fresh + (ta - past) * (D * 2) + chunk * 16;
+    if (tok >= n_tile) {
+        r.base = zero;
+        r.swz = 0;
+        r.hx = 0;
+    } else if (ta < past) {
+        r.base = tile + tok * (D * 2);
+        r.swz = (tok * NH) & 7;
+        r.hx = NH - 1;
+    } else {
+        r.base = fresh + (ta - past) * (D * 2);
+        r.swz = 0;
+        r.hx = 0;
+    }
+    return r;
 }
 
-// T: __half or __nv_bfloat16; D: head size; MT: 16-row tiles per CTA pass;
+// T: __half or __nv_bfloat16; D: head size; MT: 16-row groups per CTA pass;
 // TO: output element type.  One CTA per SM (persistent).
 //
-// Per stage of kMmaTokens tokens: warp w computes S = Q K^T for tokens
-// [16w, 16w+16) with m16n8k16 MMAs (float32 accumulators), scales and masks
-// them, and publishes its row maxima; after a barrier every warp forms the
-// common running maximum, writes its probabilities P (split into a 16-bit
-// high part and a 16-bit remainder so that P V keeps about 22 bits) to shared
-// memory; after a second barrier warp w accumulates O[:, its D/8 columns] +=
-// P V over all tokens of the stage.  Every warp therefore owns distinct output
-// columns and no cross-warp merge of O is needed; the row sums are added at
-// the end of the item.
+// The ring holds stages of TT tokens (32 KB of K and V).  Stage g of the CTA
+// belongs to warp set g % nsets: each warp of the set takes one 16-token
+// group and one 16-row group and computes S = Q K^T with m16n8k16 MMAs
+// (float32 accumulators),
+// scale and mask S, update their running row maxima (rescaling their
+// accumulators only when a maximum grew), and accumulate O += P V with P kept
+// in registers as a 16-bit high part plus a 16-bit remainder (P V keeps about
+// 22 bits of P).  Warps never wait for one another inside a piece; at the end
+// of a piece their (max, sum, O) states are merged through shared memory in
+// rounds of kMergeDR columns.  The query rows of each piece arrive in one of
+// two shared buffers filled by the producer.
 template <typename T, int D, int MT, typename TO>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap)
 {
     constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
-    constexpr int KS = D / 16;                     // k-steps of Q K^T
-    constexpr int NTW = D / 8 / kConsumerWarps;    // 8-column tiles of O per warp
+    constexpr int KS = D / 16;  // k-steps of Q K^T
+    constexpr int NT = D / 8;   // 8-column tiles of O
     constexpr int ROWS = 16 * MT;
-    constexpr int PP = kMmaTokens + 8;             // P row pitch (halves), breaks bank conflicts
-    static_assert(NTW == 1 || NTW == 2, "D must be 64 or 128");
+    constexpr int TS = kConsumerWarps / MT;  // warps per row group
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const Smem sm = carve(p, smem_raw);
-    uint16_t* Phi = reinterpret_cast<uint16_t*>(sm.scratch);  // [ROWS][PP]
-    uint16_t* Plo = Phi + ROWS * PP;
-    float* red_max = reinterpret_cast<float*>(Plo + ROWS * PP);  // [warps][ROWS]
-    float* red_l = red_max + kConsumerWarps * ROWS;
+    float2* ml_buf = reinterpret_cast<float2*>(sm.scratch);         // [warps][16] (max, sum)
+    float2* tot = reinterpret_cast<float2*>(sm.scratch + 1024);     // [ROWS] merged (max, sum)
+    float* obuf = reinterpret_cast<float*>(sm.scratch + 2048);      // [warps][16][kMergeDR]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
-    const int TT = kMmaTokens;
 
     grid_dependency_wait();
     grid_dependents_launch();
@@ -753,247 +1022,280 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     const int g = lane >> 2, qd = lane & 3;
+    const int rg = warp % MT, ts = warp / MT;
+    // A stage of TT tokens is consumed by a set of WS = (TT/16)*MT warps (one
+    // per 16-token group and row group); the nsets sets take stages in turn.
+    const int TT = p.TT;
+    const int WS = (TT / kMmaTokens) * MT;
+    const int nsets = kConsumerWarps / WS;
+    const int my_set = warp / WS;
+    const int tb = ((warp % WS) / MT) * kMmaTokens;  // this warp's tokens in a stage
     const uint32_t zero = smem_u32(sm.zero16);
-    const uint32_t phi_base = smem_u32(Phi), plo_base = smem_u32(Plo);
-    const int tb = 16 * warp;  // this warp's tokens of every stage
+    const uint32_t qbuf = smem_u32(sm.scratch + p.qbuf_off);
     uint32_t gt = 0;
+    int piece = 0;
+    bool alive = true;
 
-    for (int item = blockIdx.x; item < sc.total_items; item += gridDim.x) {
-        const Item it = decode_item(p, sc, item);
+    PieceIter pi;
+    for (pi.first(p, sc); pi.ok; pi.next(p, sc), ++piece) {
+        const Item& it = pi.it;
         const int ntiles = (it.end - it.start + TT - 1) / TT;
         const int R_cta = min(ROWS, p.R - it.rsg * ROWS);
-        const T* qbase = static_cast<const T*>(p.q) +
-                         ((static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * ROWS) * D;
+        const int row0 = rg * 16;  // first row of this warp's group within the CTA pass
 
-        // Q fragments (row-major A of m16n8k16), zero for padding rows.
-        uint32_t qa[MT][KS][4];
-        int lim[MT][2];
+        // causal / length limits of this thread's two rows (0 for padding rows)
+        int lim[2];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int r0 = mt * 16 + g, r1 = r0 + 8;
+        for (int h = 0; h < 2; ++h) {
+            const int rl = row0 + g + 8 * h;
+            const int rho = it.rsg * ROWS + rl;
+            lim[h] = rl < R_cta ? it.past + (p.causal ? (rho % p.NQ) + 1 : p.NQ) : 0;
+        }
+        const int lim_min = __reduce_min_sync(kFull, min(lim[0] > 0 ? lim[0] : INT_MAX,
+                                                         lim[1] > 0 ? lim[1] : INT_MAX));
+
+        // Q fragments (row-major A of m16n8k16) from this piece's query buffer
+        uint32_t qa[KS][4];
+        {
+            const int par = piece & 1;
+            if (alive) {
+                alive = !*sm.abort_flag &&
+                        mbar_wait_bounded(&sm.q_full[par], (piece >> 1) & 1, kWaitLimitNs);
+                alive = __all_sync(kFull, alive);
+                if (!alive && lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+            }
+            const int qrow = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const uint32_t qaddr = qbuf + (par * ROWS + qrow) * (D * 2) + ((lane >> 4) << 4);
+            const bool r0ok = row0 + g < R_cta, r1ok = row0 + g + 8 < R_cta;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const int d0 = ks * 16 + 2 * qd;
-                qa[mt][ks][0] = r0 < R_cta ? *reinterpret_cast<const uint32_t*>(qbase + r0 * D + d0) : 0u;
-                qa[mt][ks][1] = r1 < R_cta ? *reinterpret_cast<const uint32_t*>(qbase + r1 * D + d0) : 0u;
-                qa[mt][ks][2] = r0 < R_cta ? *reinterpret_cast<const uint32_t*>(qbase + r0 * D + d0 + 8) : 0u;
-                qa[mt][ks][3] = r1 < R_cta ? *reinterpret_cast<const uint32_t*>(qbase + r1 * D + d0 + 8) : 0u;
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rl = mt * 16 + g + 8 * h;
-                const int rho = it.rsg * ROWS + rl;
-                lim[mt][h] = rl < R_cta ? it.past + (p.causal ? (rho % p.NQ) + 1 : p.NQ) : 0;
+                ldsm_x4(qaddr + ks * 32, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+                if (!r0ok) {  // rows past the pass hold stale shared memory
+                    qa[ks][0] = 0u;
+                    qa[ks][2] = 0u;
+                }
+                if (!r1ok) {
+                    qa[ks][1] = 0u;
+                    qa[ks][3] = 0u;
+                }
             }
         }
 
-        float m[MT][2], lp[MT][2], o[MT][NTW][4];
+        float m[2] = {-FLT_MAX, -FLT_MAX}, lp[2] = {0.f, 0.f};
+        float o[NT][4];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+        for (int i = 0; i < NT; ++i)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                m[mt][h] = -FLT_MAX;
-                lp[mt][h] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < NTW; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o[mt][i][e] = 0.f;
-        }
+            for (int e = 0; e < 4; ++e)
+                o[i][e] = 0.f;
 
-        bool failed = false;
         for (int j = 0; j < ntiles; ++j, ++gt) {
+            if (static_cast<int>(gt % nsets) != my_set)
+                continue;  // another warp set's stage
             const int s = gt % S;
-            bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.full[s], (gt / S) & 1, kWaitLimitNs);
-            ok = __all_sync(kFull, ok);
+            if (alive) {
+                alive = !*sm.abort_flag &&
+                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, kWaitLimitNs);
+                alive = __all_sync(kFull, alive);
+                if (!alive && lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+            }
+            if (!alive)
+                continue;
             const uint32_t st = smem_u32(sm.ring) + s * p.stage_bytes;
-            const uint32_t k_tile = st, k_new = st + p.knew_off;
-            const uint32_t v_tile = st + p.v_off, v_new = st + p.vnew_off;
+            const uint32_t k_tile = st, v_tile = st + p.v_off;
+            const uint32_t k_new = st + p.knew_off, v_new = st + p.vnew_off;
             const int t0 = it.start + j * TT;
             const int n_tile = min(TT, it.end - t0);
+            if (tb >= n_tile) {  // the stage ends before this warp's tokens
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty[s]);
+                continue;
+            }
+            // every token of this warp's group is visible to every row of the warp
+            const bool full_tile = tb + kMmaTokens <= n_tile && t0 + tb + kMmaTokens <= lim_min;
 
-            // ---- S = Q K^T for tokens [tb, tb + 16)
-            float sa[MT][2][4];
+            // ---- S = Q K^T (two accumulator sets per 8-token tile: shorter chains)
+            float sa[2][2][4];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int a = 0; a < 2; ++a)
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        sa[mt][nt][e] = 0.f;
-            if (ok) {
-                const int tok = tb + (lane & 7) + ((lane >> 4) << 3);
+                        sa[a][nt][e] = 0.f;
+            const RowAddr kr = row_addr<D>(k_tile, k_new, zero,
+                                           tb + (lane & 7) + ((lane >> 4) << 3), n_tile, t0,
+                                           it.past);
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int chunk = 2 * ks + ((lane >> 3) & 1);
-                    uint32_t b00, b01, b10, b11;
-                    ldsm_x4(row_chunk<D>(k_tile, k_new, zero, tok, n_tile, t0, it.past, chunk), b00,
-                            b01, b10, b11);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        mma_16816<kBf>(sa[mt][0], qa[mt][ks], b00, b01);
-                        mma_16816<kBf>(sa[mt][1], qa[mt][ks], b10, b11);
-                    }
-                }
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(kr.at(2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
+                mma_16816<kBf>(sa[ks & 1][0], qa[ks], b00, b01);
+                mma_16816<kBf>(sa[ks & 1][1], qa[ks], b10, b11);
             }
-            // scale, mask, partial row maxima over this warp's 16 tokens
+            // scale, mask, row maxima of the stage
+            float sv[2][4];
+            float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = e >> 1;
+                    const int tk = tb + nt * 8 + 2 * qd + (e & 1);
+                    const float v = (sa[0][nt][e] + sa[1][nt][e]) * p.qscale;
+                    const bool valid = full_tile || (tk < n_tile && t0 + tk < lim[h]);
+                    sv[nt][e] = valid ? v : -INFINITY;
+                    mx[h] = fmaxf(mx[h], sv[nt][e]);
+                }
+            bool grow = false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 2));
+                grow |= mx[h] > m[h];
+            }
+            if (__any_sync(kFull, grow)) {  // rescale only when a row maximum grew
+                float f[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int tk = tb + nt * 8 + 2 * qd + e;
-                            const float v = sa[mt][nt][2 * h + e] * p.qscale;
-                            const bool valid = tk < n_tile && t0 + tk < lim[mt][h];
-                            sa[mt][nt][2 * h + e] = valid ? v : -INFINITY;
-                            mx = fmaxf(mx, sa[mt][nt][2 * h + e]);
-                        }
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-                    if (qd == 0)
-                        red_max[warp * ROWS + mt * 16 + g + 8 * h] = mx;
-                }
-            }
-            if (consumer_bar_or(!ok)) {  // (A) uniform stop if any wait failed
-                if (threadIdx.x == 0)
-                    flag_timeout(p, sm.abort_flag);
-                failed = true;
-                break;
-            }
-            // common running maximum, probabilities, row-sum partials
-            float f[MT][2];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int row = mt * 16 + g + 8 * h;
-                    float tmax = red_max[row];
-#pragma unroll
-                    for (int w = 1; w < kConsumerWarps; ++w)
-                        tmax = fmaxf(tmax, red_max[w * ROWS + row]);
-                    const float mn = fmaxf(m[mt][h], tmax);
-                    f[mt][h] = fast_exp2(m[mt][h] - mn);
-                    m[mt][h] = mn;
-                    lp[mt][h] *= f[mt][h];
+                    const float mn = fmaxf(m[h], mx[h]);
+                    f[h] = fast_exp2(m[h] - mn);
+                    m[h] = mn;
+                    lp[h] *= f[h];
                 }
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float p0 = fast_exp2(sa[mt][nt][2 * h] - m[mt][h]);
-                        const float p1 = fast_exp2(sa[mt][nt][2 * h + 1] - m[mt][h]);
-                        lp[mt][h] += p0 + p1;
-                        uint32_t hi, lo;
-                        Pack<T>::split(p0, p1, hi, lo);
-                        const int row = mt * 16 + g + 8 * h;
-                        const int col = tb + nt * 8 + 2 * qd;
-                        *reinterpret_cast<uint32_t*>(&Phi[row * PP + col]) = hi;
-                        *reinterpret_cast<uint32_t*>(&Plo[row * PP + col]) = lo;
-                    }
-                }
-            }
-            consumer_bar_sync();  // (B) P of all warps is in shared memory
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int i = 0; i < NTW; ++i)
+                for (int i = 0; i < NT; ++i)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[mt][i][e] *= f[mt][e >> 1];
-
-            // ---- O[:, this warp's columns] += P V over the tokens of the stage
-            const int nk = (n_tile + 15) >> 4;
-            for (int kk = 0; kk < nk; ++kk) {
-                uint32_t ahi[MT][4], alo[MT][4];
+                        o[i][e] *= f[e >> 1];
+            }
+            // P as A fragments (high part and remainder)
+            uint32_t ahi[4], alo[4];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int row = mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int col = kk * 16 + ((lane >> 4) << 3);
-                    const uint32_t off = (row * PP + col) * 2;
-                    ldsm_x4(phi_base + off, ahi[mt][0], ahi[mt][1], ahi[mt][2], ahi[mt][3]);
-                    ldsm_x4(plo_base + off, alo[mt][0], alo[mt][1], alo[mt][2], alo[mt][3]);
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float p0 = fast_exp2(sv[nt][2 * h] - m[h]);
+                    const float p1 = fast_exp2(sv[nt][2 * h + 1] - m[h]);
+                    lp[h] += p0 + p1;
+                    Pack<T>::split(p0, p1, ahi[2 * nt + h], alo[2 * nt + h]);
                 }
-                const int tok = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                uint32_t vb[NTW][2];
-                if constexpr (NTW == 2) {
-                    const int chunk = warp * 2 + (lane >> 4);
-                    ldsm_x4_t(row_chunk<D>(v_tile, v_new, zero, tok, n_tile, t0, it.past, chunk),
-                              vb[0][0], vb[0][1], vb[1][0], vb[1][1]);
-                } else {
-                    ldsm_x2_t(row_chunk<D>(v_tile, v_new, zero, tok, n_tile, t0, it.past, warp),
-                              vb[0][0], vb[0][1]);
-                }
+            // ---- O += P V
+            const RowAddr vr = row_addr<D>(v_tile, v_new, zero,
+                                           tb + (lane & 7) + (((lane >> 3) & 1) << 3), n_tile, t0,
+                                           it.past);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int i = 0; i < NTW; ++i) {
-                        mma_16816<kBf>(o[mt][i], ahi[mt], vb[i][0], vb[i][1]);
-                        mma_16816<kBf>(o[mt][i], alo[mt], vb[i][0], vb[i][1]);
-                    }
+            for (int pp = 0; pp < NT / 2; ++pp) {
+                uint32_t v00, v01, v10, v11;
+                ldsm_x4_t(vr.at(2 * pp + (lane >> 4)), v00, v01, v10, v11);
+                mma_16816<kBf>(o[2 * pp], ahi, v00, v01);
+                mma_16816<kBf>(o[2 * pp + 1], ahi, v10, v11);
+                mma_16816<kBf>(o[2 * pp], alo, v00, v01);
+                mma_16816<kBf>(o[2 * pp + 1], alo, v10, v11);
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.empty[s]);
         }
-        if (failed)
-            break;
+        // Release the query buffer only now.  ldmatrix completes asynchronously
+        // and the fragments are first consumed by the MMAs of the tile loop: a
+        // release right after the load let the producer's copy of the piece two
+        // ahead land before the read had been performed.  Every MMA reading qa
+        // has issued here (a warp that computed no tile never uses qa).
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.q_free[piece & 1]);
 
-        // ---- item end: row sums over all warps, then each warp writes its columns
+        // ---- piece end: merge the TS warps of each row group
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float l = lp[mt][h];
-                l += __shfl_xor_sync(kFull, l, 1);
-                l += __shfl_xor_sync(kFull, l, 2);
-                if (qd == 0)
-                    red_l[warp * ROWS + mt * 16 + g + 8 * h] = l;
-            }
+        for (int h = 0; h < 2; ++h) {
+            lp[h] += __shfl_xor_sync(kFull, lp[h], 1);
+            lp[h] += __shfl_xor_sync(kFull, lp[h], 2);
+        }
+        consumer_bar_sync();  // the previous piece's readers are done with the buffers
+        if (qd == 0) {
+            ml_buf[warp * 16 + g] = make_float2(m[0], lp[0]);
+            ml_buf[warp * 16 + g + 8] = make_float2(m[1], lp[1]);
+        }
         if (consumer_bar_or(*sm.abort_flag != 0))
             break;
+        // rescale to the group's common maximum; one thread per row records (M, L)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = g + 8 * h;
+            float Mr = -FLT_MAX;
+            for (int t = 0; t < TS; ++t)
+                Mr = fmaxf(Mr, ml_buf[(t * MT + rg) * 16 + r].x);
+            const float f = fast_exp2(m[h] - Mr);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                o[i][2 * h] *= f;
+                o[i][2 * h + 1] *= f;
+            }
+            if (ts == 0 && qd == 0 && row0 + r < R_cta) {
+                float Lr = 0.f;
+                for (int t = 0; t < TS; ++t) {
+                    const float2 v = ml_buf[(t * MT + rg) * 16 + r];
+                    Lr = fmaf(v.y, fast_exp2(v.x - Mr), Lr);
+                }
+                tot[row0 + r] = make_float2(Mr, Lr);
+            }
+        }
+        const int rows_used = min(16, max(0, R_cta - row0));
         const size_t out_row0 =
             (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * ROWS;
+        const int tid = threadIdx.x;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int r8 = 0; r8 < D / kMergeDR; ++r8) {
+            if (r8 > 0)
+                consumer_bar_sync();  // readers of the previous round are done
+            // each warp writes its scaled accumulators of columns [r8*DR, (r8+1)*DR)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rl = mt * 16 + g + 8 * h;
-                if (rl >= R_cta)
-                    continue;
-                float L = 0.f;
+            for (int i = r8 * (kMergeDR / 8); i < (r8 + 1) * (kMergeDR / 8); ++i) {
+                const int dd = (i - r8 * (kMergeDR / 8)) * 8 + 2 * qd;
+                if (g < rows_used)
+                    *reinterpret_cast<float2*>(&obuf[(warp * 16 + g) * kMergeDR + dd]) =
+                        make_float2(o[i][0], o[i][1]);
+                if (g + 8 < rows_used)
+                    *reinterpret_cast<float2*>(&obuf[(warp * 16 + g + 8) * kMergeDR + dd]) =
+                        make_float2(o[i][2], o[i][3]);
+            }
+            consumer_bar_sync();
+            for (int idx = tid; idx < R_cta * kMergeDR; idx += kConsumerWarps * 32) {
+                const int rl = idx / kMergeDR, dd = idx - rl * kMergeDR;
+                const int grp = rl >> 4, r = rl & 15;
+                float acc = 0.f;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    L += red_l[w * ROWS + rl];
-#pragma unroll
-                for (int i = 0; i < NTW; ++i) {
-                    const int d = (warp * NTW + i) * 8 + 2 * qd;
-                    const float ox = o[mt][i][2 * h], oy = o[mt][i][2 * h + 1];
-                    if (it.n == 1) {
-                        const float sx = L == 0.f ? ox : ox / L;
-                        const float sy = L == 0.f ? oy : oy / L;
-                        TO* dst = static_cast<TO*>(p.out) + (out_row0 + rl) * D + d;
-                        dst[0] = from_float<TO>(sx);
-                        dst[1] = from_float<TO>(sy);
-                    } else {
-                        const size_t wrow = static_cast<size_t>(item) * p.row_stride + rl;
-                        *reinterpret_cast<float2*>(&p.ws_o[wrow * D + d]) = make_float2(ox, oy);
-                        if (warp == 0 && i == 0 && qd == 0)
-                            p.ws_ml[wrow] = make_float2(m[mt][h], L);
-                    }
+                for (int t = 0; t < TS; ++t)
+                    acc += obuf[((t * MT + grp) * 16 + r) * kMergeDR + dd];
+                const float2 ml = tot[rl];
+                const int d = r8 * kMergeDR + dd;
+                if (it.whole) {
+                    const float val = ml.y == 0.f ? acc : acc / ml.y;
+                    static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
+                } else {
+                    const size_t wrow = static_cast<size_t>(it.rec) * p.row_stride + rl;
+                    p.ws_o[wrow * D + d] = acc;
+                    if (d == 0)
+                        p.ws_ml[wrow] = ml;
                 }
             }
+        }
+        if (!it.whole && p.counters)
+            finish_split_piece<D, TO>(p, sc, it, R_cta, tot, &sm.info[14]);
     }
 }
 
 // -------------------------------------------------------------- merge kernel
-// One CTA per (sequence, row group, KV head); one warp per query row; lanes
-// split D.  Sequences covered by a single item were finished by the
-// partition kernel and are skipped.
+// One CTA per segment (sequence, row group, KV head); one warp per query row;
+// lanes split D.  It finds the partial records of the segment (automatic mode:
+// the CTAs whose unit ranges overlap the segment; fixed partitions: the
+// segment's items) and merges them: M = max m, L = sum l 2^(m - M),
+// O = sum o 2^(m - M), out = L == 0 ? O : O / L.  Whole segments were
+// finished by the partition kernel and are skipped.
 template <int D, typename TO>
 __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__ CombineParams p)
 {
@@ -1003,26 +1305,43 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
     const int kh = idx % p.KV;
     const int rsg = (idx / p.KV) % p.NRS;
     const int b = idx / (p.KV * p.NRS);
+    const int U = p.NRS * p.KV;
     const int2 sc = p.sched[b];
-    const int n = sc.y;
+    int n, k0 = 0, rec_first = 0;
+    if (p.stream) {
+        const int2 last = p.sched[p.B - 1];
+        const long long W = static_cast<long long>(last.x) + static_cast<long long>(last.y) * U;
+        const long long G = min(static_cast<long long>(p.grid), W);  // CTAs that took work
+        const long long s0 = sc.x + static_cast<long long>(rsg * p.KV + kh) * sc.y;
+        const long long s1 = s0 + sc.y;
+        k0 = static_cast<int>(((s0 + 1) * G - 1) / W);
+        const int k1 = static_cast<int>((s1 * G - 1) / W);
+        n = k1 - k0 + 1;
+        rec_first = 2 * k0 + (range_start(k0, W, G) == s0 ? 0 : 1);
+    } else {
+        n = sc.y;
+    }
     if (n <= 1)
         return;
+    // record of piece c (c = 0 .. n-1)
+    auto rec_of = [&](int c) -> size_t {
+        if (p.stream)
+            return c == 0 ? static_cast<size_t>(rec_first) : static_cast<size_t>(2 * (k0 + c));
+        return (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
+    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R_cta = min(p.rows_per_cta, p.R - rsg * p.rows_per_cta);
     constexpr int PER = D / 32;
     for (int rl = warp; rl < R_cta; rl += 4) {
         float M = -FLT_MAX;
-        for (int c = lane; c < n; c += 32) {
-            const size_t item = (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
-            M = fmaxf(M, p.ws_ml[item * p.row_stride + rl].x);
-        }
+        for (int c = lane; c < n; c += 32)
+            M = fmaxf(M, p.ws_ml[rec_of(c) * p.row_stride + rl].x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
         float L = 0.f;
         for (int c = lane; c < n; c += 32) {
-            const size_t item = (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
-            const float2 ml = p.ws_ml[item * p.row_stride + rl];
+            const float2 ml = p.ws_ml[rec_of(c) * p.row_stride + rl];
             L = fmaf(ml.y, fast_exp2(ml.x - M), L);
         }
 #pragma unroll
@@ -1034,8 +1353,7 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
             O[k] = 0.f;
 #pragma unroll 4
         for (int c = 0; c < n; ++c) {
-            const size_t item = (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
-            const size_t wrow = item * p.row_stride + rl;
+            const size_t wrow = rec_of(c) * p.row_stride + rl;
             const float f = fast_exp2(p.ws_ml[wrow].x - M);
 #pragma unroll
             for (int k = 0; k < PER; ++k)

@@ -56,6 +56,7 @@ extern "C" int pa_decode_static_workspace(const void* q, const void* k_cache, co
     pa_opts local = *opts;
     local.workspace = nullptr;
     local.workspace_bytes = 0;
+    local.merge_kernel = 1;  // no split counters: nothing in the array must start at zero
     if (need > 0) {
         void* addr = nullptr;
         const int rc = static_workspace_address(&addr);

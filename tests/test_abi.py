@@ -57,6 +57,10 @@ def test_workspace_bytes(lib):
     assert ws(1, 32, 8, 128, 1, 32) < ws(1, 32, 8, 128, 1, 64)
     # one float32 (max, sum, D accumulators) state per row and key range
     assert ws(1, 32, 8, 128, 1, 32) >= 32 * 8 * 4 * (128 + 2) * 4
+    zb = lib.workspace_zero_bytes
+    assert zb(8, 32, 8, 128, 1, 1) == 0
+    assert 0 < zb(8, 32, 8, 128, 1, 0) < ws(8, 32, 8, 128, 1, 0)
+    assert zb(8, 32, 8, 128, 1, 0) >= 8 * 8 * 4  # one counter per (sequence, KV head)
 
 
 class Fake:

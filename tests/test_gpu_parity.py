@@ -183,4 +183,52 @@ def test_kernel_launch_counter_moves():
     w = W.make(small("gqa_fp16"), seed=14)
     pu.run_gpu(w, partitions=1)
     pu.run_gpu(w, partitions=0)
-    assert binding.kernel_launches() - before == 3
+    pu.run_gpu(w, partitions=0, merge_kernel=True)
+    assert binding.kernel_launches() - before == 4  # 1 + 1 (merge in kernel) + 2
+
+
+# ------------------------------------------------ workspace hygiene
+@pytest.mark.parametrize("name", W.ORDER)
+@pytest.mark.parametrize("P", [0, 3])
+def test_workspace_garbage_is_never_read(name, P):
+    """A workspace full of NaN bytes must not leak into the output: every
+    partial record the merge reads was written in the same call."""
+    from paged_kv_cache_182_gb300 import binding
+
+    w = W.make(small(name), seed=15)
+    s = w.spec
+    want = pu.run_oracle(w)
+    for merge_kernel in (False, True):
+        ws = torch.full((binding.workspace_bytes(s.B, s.H, s.KV, s.D, s.NQ, P),), 0xFF,
+                        dtype=torch.uint8, device="cuda")
+        zb = binding.workspace_zero_bytes(s.B, s.H, s.KV, s.D, s.NQ, P)
+        ws[:zb] = 0  # the split counters of the in-kernel merge start at zero
+        for rep in range(2):  # the second call reuses the counters the first left
+            got = pu.run_gpu(w, partitions=P, out_dtype=torch.float32, workspace=ws,
+                             merge_kernel=merge_kernel)
+            pu.check(got, want, s.dtype, "f32",
+                     f"{name} P={P} merge_kernel={merge_kernel} call {rep} garbage workspace")
+        assert int(ws[:zb].count_nonzero()) == 0, "counters must be left at zero"
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+@pytest.mark.parametrize("P", [0, 2, 7])
+def test_separate_merge_kernel(name, P):
+    w = W.make(small(name), seed=16)
+    got = pu.run_gpu(w, partitions=P, out_dtype=torch.float32, merge_kernel=True)
+    pu.check(got, pu.run_oracle(w), w.spec.dtype, "f32", f"{name} P={P} merge kernel")
+
+
+def test_repeated_calls_full_ragged_are_stable():
+    """Many short pieces per CTA keep the producer several pieces ahead of
+    the consumers: the query-buffer and stage hand-offs are exercised on every
+    call.  Twenty calls in a row must all equal the first, which matches the
+    oracle."""
+    w = W.make("ragged_fp16", seed=17)
+    want = pu.run_oracle(w)
+    first = pu.run_gpu(w, out_dtype=torch.float32)
+    pu.check(first, want, "f16", "f32", "ragged repeated, call 0")
+    first = first.cpu()
+    for rep in range(1, 20):
+        got = pu.run_gpu(w, out_dtype=torch.float32).cpu()
+        assert torch.equal(got, first), f"call {rep} differs from call 0"
