@@ -10,13 +10,14 @@
 namespace pa {
 
 constexpr int kConsumerWarps = 8;                     // compute warps per CTA
-constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one TMA producer warp
+constexpr int kProducerWarps = 2;                     // TMA issue: K (+ query, new rows), V
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kMaxStages = 32;                        // shared-memory ring depth limit
 constexpr int kMinRing = 3;                           // stages kept before widening scratch
 constexpr int kSubBatch = 4;        // token steps per online-softmax update
 constexpr int kStageBytes = 32768;     // CUDA-core path: K + V tile bytes per stage (target)
 constexpr int kMmaStageBytes = 65536;  // tensor-core path: K + V tile bytes per stage (target)
-constexpr int kHeaderBytes = 2048;  // barriers, broadcast scalars, zero row, table-entry slots
+constexpr int kHeaderBytes = 3072;  // barriers, broadcast scalars, zero row, table-entry slots
 constexpr int kMaxBatch = 4096;     // sequences per call (the schedule lives in smem)
 constexpr int kMaxGrid = 1024;      // partition-kernel CTAs at most (sizes the workspace)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -44,6 +45,7 @@ struct SplitParams {
     int rows_per_cta;  // kConsumerWarps * RG
     int NRS;           // row groups per KV head = ceil(R / rows_per_cta)
     int TT;            // tokens per pipeline stage, a multiple of BLOCK
+    int lg_block, lg_box, lg_tt;  // log2 of BLOCK, box_rows and TT (all powers of two)
     int row_stride;    // workspace rows per item = min(R, rows_per_cta)
     int stages;        // ring depth (<= kMaxStages)
     int stage_bytes;   // bytes of one stage: K tile | K new rows | V tile | V new rows
@@ -73,7 +75,7 @@ using CombineFn = void (*)(CombineParams);
 // use the CUDA-core kernel (RG query rows per warp); 16-bit inputs use the
 // tensor-core kernel (16 * MT query rows per CTA pass).
 constexpr int kMmaTokens = 16;  // tokens per stage of the tensor-core kernel (one warp's MMA group)
-constexpr int kMergeDR = 32;  // tensor-core kernel: output columns merged per round
+constexpr int kObufFloats = 4096;  // tensor-core kernel: floats of the piece-end merge buffer
 SplitFn pick_split_f32(int D, int RG);
 SplitFn pick_split_f16(bool f32_out, int D, int MT);
 SplitFn pick_split_bf16(bool f32_out, int D, int MT);

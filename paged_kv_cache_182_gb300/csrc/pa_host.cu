@@ -49,6 +49,14 @@ int tokens_per_stage(int D, int es, int BLOCK)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+int ilog2(int x)  // x is a power of two
+{
+    int l = 0;
+    while ((1 << l) < x)
+        ++l;
+    return l;
+}
+
 // Workspace records of one call: automatic schedule, two per partition-kernel
 // CTA (its first and last piece); fixed partitions, one per item.
 long long record_bound(int B, int KV, int NRS, int partitions)
@@ -393,7 +401,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
     if (mma && (TT / kMmaTokens) * MT > kConsumerWarps)
         TT = kConsumerWarps / MT * kMmaTokens;
-    const int box_rows = mma ? (BLOCK < kMmaTokens ? BLOCK : kMmaTokens) : BLOCK;
+    // one TMA box per cache block (per tile when a block spans several tiles):
+    // the issue cost of a box is fixed, so fewer, larger boxes stream faster
+    const int box_rows = mma ? (BLOCK < TT ? BLOCK : TT) : BLOCK;
     const int ROWS = 16 * MT;
     // shared memory: header | lens[B] | prefix[B+1] | consumer scratch | ring
     const int lens_off = kHeaderBytes;
@@ -421,9 +431,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         return PA_ERR_CUDA;
     const int slack = 1024;  // alignment of the dynamic shared-memory base
     // consumer scratch: tensor-core path, (max, sum) tables, one merge round of
-    // [warps][16 rows][kMergeDR] floats and two query-row buffers; CUDA-core
+    // kObufFloats floats of merge rounds and two query-row buffers; CUDA-core
     // path, per-warp states
-    const int qbuf_off = 2048 + kConsumerWarps * 16 * kMergeDR * 4;
+    const int qbuf_off = 2048 + kObufFloats * 4;
     const int merge_bytes = mma ? qbuf_off + 2 * ROWS * D * es
                                 : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4 +
                                       kConsumerWarps * RG * 8;
@@ -486,6 +496,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.rows_per_cta = rows_per_cta;
     p.NRS = NRS;
     p.TT = TT;
+    p.lg_block = ilog2(BLOCK);
+    p.lg_box = ilog2(box_rows);
+    p.lg_tt = ilog2(TT);
     p.row_stride = row_stride;
     p.stages = stages;
     p.stage_bytes = stage_bytes;

@@ -197,11 +197,15 @@ __device__ __forceinline__ int last_le(const int* prefix, int B, long long x)
     return lo;
 }
 
-// Iterates this CTA's pieces in order (identically in every warp).
+// Iterates this CTA's pieces in order (identically in every warp).  In the
+// automatic mode only first() searches the schedule; next() steps to the
+// following segment, since every piece but the CTA's last ends where its
+// segment ends and every segment holds at least one unit.
 struct PieceIter {
-    long long pos, stop, first_pos;
+    long long pos, stop;
     bool ok;
     Item it;
+    int seg_units;  // automatic mode: units of each segment of sequence it.b
 
     __device__ __forceinline__ void first(const SplitParams& p, const Sched& sc)
     {
@@ -211,61 +215,85 @@ struct PieceIter {
             const long long G = min(static_cast<long long>(gridDim.x), static_cast<long long>(sc.total));
             pos = blockIdx.x < G ? range_start(blockIdx.x, sc.total, G) : 0;
             stop = blockIdx.x < G ? range_start(blockIdx.x + 1, sc.total, G) : 0;
-        } else {
-            pos = blockIdx.x;
-            stop = sc.total;
-        }
-        first_pos = pos;
-        load(p, sc);
-    }
-
-    __device__ __forceinline__ void next(const SplitParams& p, const Sched& sc)
-    {
-        pos += p.partitions == 0 ? it.units : gridDim.x;
-        load(p, sc);
-    }
-
-    __device__ __forceinline__ void load(const SplitParams& p, const Sched& sc)
-    {
-        ok = pos < stop;
-        if (!ok)
-            return;
-        if (p.partitions == 0) {
+            ok = pos < stop;
+            if (!ok)
+                return;
             const int b = last_le(sc.prefix, p.B, pos);
             const int total = sc.lens[b] + p.NQ;
-            const int n = (total + p.BLOCK - 1) / p.BLOCK;
+            seg_units = (total + p.BLOCK - 1) >> p.lg_block;
             const int local = static_cast<int>(pos - sc.prefix[b]);
-            const int seg = local / n;
-            const int uu = local - seg * n;
-            const int len = static_cast<int>(min(static_cast<long long>(n - uu), stop - pos));
+            const int seg = local / seg_units;
+            const int uu = local - seg * seg_units;
             it.b = b;
             it.rsg = seg / p.KV;
             it.kh = seg - it.rsg * p.KV;
             it.past = sc.lens[b];
-            it.start = uu * p.BLOCK;
-            it.end = min((uu + len) * p.BLOCK, total);
-            it.whole = uu == 0 && len == n;
-            it.rec = 2 * blockIdx.x + (pos == first_pos ? 0 : 1);
-            it.units = len;
+            it.start = uu << p.lg_block;
+            set_len(p, seg_units - uu, uu == 0);
+            it.rec = 2 * blockIdx.x;
         } else {
-            const int U = p.NRS * p.KV;
-            const int item = static_cast<int>(pos);
-            const int g = item / U;
-            const int rem = item - g * U;
-            const int b = last_le(sc.prefix, p.B, g);
-            const int c = g - sc.prefix[b];
-            const int total = sc.lens[b] + p.NQ;
-            const int chunk = chunk_of(p, total);
-            it.b = b;
-            it.rsg = rem / p.KV;
-            it.kh = rem - it.rsg * p.KV;
-            it.past = sc.lens[b];
-            it.start = c * chunk;
-            it.end = min(it.start + chunk, total);
-            it.whole = sc.prefix[b + 1] - sc.prefix[b] == 1;
-            it.rec = item;
-            it.units = 0;
+            pos = blockIdx.x;
+            stop = sc.total;
+            load_fixed(p, sc);
         }
+    }
+
+    __device__ __forceinline__ void next(const SplitParams& p, const Sched& sc)
+    {
+        if (p.partitions == 0) {
+            pos += it.units;
+            ok = pos < stop;
+            if (!ok)
+                return;
+            if (++it.kh == p.KV) {
+                it.kh = 0;
+                if (++it.rsg == p.NRS) {
+                    it.rsg = 0;
+                    ++it.b;
+                    it.past = sc.lens[it.b];
+                    seg_units = (it.past + p.NQ + p.BLOCK - 1) >> p.lg_block;
+                }
+            }
+            it.start = 0;
+            set_len(p, seg_units, true);
+            it.rec = 2 * blockIdx.x + 1;
+        } else {
+            pos += gridDim.x;
+            load_fixed(p, sc);
+        }
+    }
+
+    // automatic mode: the piece takes min(left, stop - pos) units of its segment
+    __device__ __forceinline__ void set_len(const SplitParams& p, int left, bool at_start)
+    {
+        const int len = static_cast<int>(min(static_cast<long long>(left), stop - pos));
+        it.end = min(it.start + (len << p.lg_block), it.past + p.NQ);
+        it.whole = at_start && len == seg_units;
+        it.units = len;
+    }
+
+    __device__ __forceinline__ void load_fixed(const SplitParams& p, const Sched& sc)
+    {
+        ok = pos < stop;
+        if (!ok)
+            return;
+        const int U = p.NRS * p.KV;
+        const int item = static_cast<int>(pos);
+        const int g = item / U;
+        const int rem = item - g * U;
+        const int b = last_le(sc.prefix, p.B, g);
+        const int c = g - sc.prefix[b];
+        const int total = sc.lens[b] + p.NQ;
+        const int chunk = chunk_of(p, total);
+        it.b = b;
+        it.rsg = rem / p.KV;
+        it.kh = rem - it.rsg * p.KV;
+        it.past = sc.lens[b];
+        it.start = c * chunk;
+        it.end = min(it.start + chunk, total);
+        it.whole = sc.prefix[b + 1] - sc.prefix[b] == 1;
+        it.rec = item;
+        it.units = 0;
     }
 };
 
@@ -308,6 +336,20 @@ __device__ __forceinline__ size_t seg_record(const SplitParams& p, const SegPiec
     if (p.partitions == 0)
         return c == 0 ? static_cast<size_t>(sp.rec_first) : static_cast<size_t>(2 * (sp.k0 + c));
     return (static_cast<size_t>(sp.item0 + c) * p.NRS + rsg) * p.KV + kh;
+}
+
+// Reads one word of every 32 bytes of a kernel parameter, so that its
+// constant-cache lines are fetched together at entry instead of one by one at
+// their first use on the issue path.
+template <typename Tp>
+__device__ __forceinline__ void warm_param(const Tp& x)
+{
+    constexpr int kWords = static_cast<int>(sizeof(Tp) / 4);
+    const int i = static_cast<int>(threadIdx.x) * 8;
+    if (i < kWords) {
+        const int v = reinterpret_cast<const int*>(&x)[i];
+        asm volatile("" ::"r"(v));
+    }
 }
 
 __device__ __forceinline__ void consumer_bar_sync()
@@ -508,7 +550,7 @@ struct SimtMath {
 //   [0, 256)     full barriers      [256, 512)  empty barriers
 //   [512, 576)   broadcast scalars  [576, 608)  query-buffer barriers (full, free)
 //   [640, 896)   a zeroed 256-byte row (tensor-core path)
-//   [1024, 2048) producer table-entry slots
+//   [1024, 3072) table-entry slots of the two producer warps
 //   lens[B] | prefix[B+1] | consumer scratch | ring of `stages` stages.
 struct Smem {
     uint64_t* full;
@@ -522,7 +564,7 @@ struct Smem {
     int* prefix;
     unsigned char* scratch;
     unsigned char* ring;
-    int* entries;  // producer's table-entry slots [kTableSlots][kSlotInts]
+    int* entries;  // producer warps' table-entry slots [2][kTableSlots][kSlotInts]
 };
 
 __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
@@ -550,7 +592,7 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.full[s], kProducerWarps);
             mbar_init(&sm.empty[s], p.empty_count);
         }
         for (int i = 0; i < 2; ++i) {
@@ -591,7 +633,7 @@ struct TileIter {
     {
         pc.first(p, sc);
         j = 0;
-        ntiles = pc.ok ? (pc.it.end - pc.it.start + p.TT - 1) / p.TT : 0;
+        ntiles = pc.ok ? (pc.it.end - pc.it.start + p.TT - 1) >> p.lg_tt : 0;
     }
     __device__ __forceinline__ bool valid() const { return pc.ok; }
     __device__ __forceinline__ void next(const SplitParams& p, const Sched& sc)
@@ -599,7 +641,7 @@ struct TileIter {
         if (++j == ntiles) {
             pc.next(p, sc);
             j = 0;
-            ntiles = pc.ok ? (pc.it.end - pc.it.start + p.TT - 1) / p.TT : 0;
+            ntiles = pc.ok ? (pc.it.end - pc.it.start + p.TT - 1) >> p.lg_tt : 0;
         }
     }
 };
@@ -610,17 +652,17 @@ constexpr int kSlotInts = 16;    // entries per slot (boxes per tile at most)
 
 // Starts a non-blocking copy of the table entries of the tile at `t` into
 // entry slot `slot` (lane i copies entry i), as one cp.async group.
-__device__ __forceinline__ void fetch_entries(const SplitParams& p, const Sched& sc, const TileIter& t,
-                                              int* slot, int lane)
+__device__ __forceinline__ void fetch_entries(const SplitParams& p, const TileIter& t, int* slot,
+                                              int lane)
 {
     if (t.valid()) {
         const Item& it = t.pc.it;
-        const int t0 = it.start + t.j * p.TT;
+        const int t0 = it.start + (t.j << p.lg_tt);
         const int cache_end = min(min(t0 + p.TT, it.end), it.past);
-        const int nb = cache_end > t0 ? (cache_end - t0 + p.box_rows - 1) / p.box_rows : 0;
+        const int nb = cache_end > t0 ? (cache_end - t0 + p.box_rows - 1) >> p.lg_box : 0;
         if (lane < nb) {
-            const int32_t* src =
-                p.table + static_cast<size_t>(it.b) * p.maxb + (t0 + lane * p.box_rows) / p.BLOCK;
+            const int32_t* src = p.table + static_cast<size_t>(it.b) * p.maxb +
+                                 ((t0 + (lane << p.lg_box)) >> p.lg_block);
             asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(slot + lane)),
                          "l"(src)
                          : "memory");
@@ -629,46 +671,46 @@ __device__ __forceinline__ void fetch_entries(const SplitParams& p, const Sched&
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// The producer warp: for every tile of every item of this CTA, wait for a
-// free stage and issue one TMA box per cache block for K and for V (two
-// 64-column boxes per block with the 128-byte swizzle when kSwizzled), plus a
-// bulk copy of the new rows when the tile reaches them.  Completion is
-// counted on the stage's full barrier.  Table entries are fetched
-// kTableAhead tiles ahead with cp.async, so no dependent global load sits on
-// the issue path.
+// A producer warp: for every tile of every item of this CTA, wait for a free
+// stage and issue one TMA box per cache block (or per tile when a block spans
+// several tiles).  Role 0 issues the K boxes, the query rows of each piece
+// (tensor-core path) and the new rows; role 1 the V boxes.  The issue cost of
+// a box is paid serially by the issuing warp, so two warps halve it.  Each
+// role counts its bytes on the stage's full barrier (two arrivals).  Table
+// entries are fetched kTableAhead tiles ahead with cp.async, so no dependent
+// global load sits on the issue path.
 template <typename T, int D, bool kSwizzled>
 __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, const CUtensorMap* kmap,
-                        const CUtensorMap* vmap, int lane)
+                        const CUtensorMap* vmap, int role, int lane)
 {
-    if (lane == 0) {
-        tma_prefetch_desc(kmap);
-        tma_prefetch_desc(vmap);
-    }
-    const int S = p.stages, TT = p.TT;
+    const CUtensorMap* map = role == 0 ? kmap : vmap;
+    if (lane == 0)
+        tma_prefetch_desc(map);
+    const int S = p.stages;
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows * D * sizeof(T));
     const uint32_t new_bytes = static_cast<uint32_t>(p.NQ * D * sizeof(T));
-    int* entries = sm.entries;  // [kTableSlots][kSlotInts]
+    int* entries = sm.entries + role * (kTableSlots * kSlotInts);  // this role's slots
 
     TileIter cur, ahead;
     cur.start(p, sc);
-    ahead.start(p, sc);
+    ahead = cur;
     for (int k = 0; k < kTableAhead; ++k) {
-        fetch_entries(p, sc, ahead, entries + (k % kTableSlots) * kSlotInts, lane);
+        fetch_entries(p, ahead, entries + (k % kTableSlots) * kSlotInts, lane);
         if (ahead.valid())
             ahead.next(p, sc);
     }
     const int HB = p.box_rows;
     uint32_t gt = 0;  // tiles issued by this CTA
+    int s = 0;        // ring slot of tile gt
+    uint32_t ph = 0;  // completed passes over the ring
     int piece = -1;   // pieces begun by this CTA
     for (; cur.valid(); cur.next(p, sc), ++gt) {
-        fetch_entries(p, sc, ahead, entries + ((gt + kTableAhead) % kTableSlots) * kSlotInts, lane);
+        fetch_entries(p, ahead, entries + ((gt + kTableAhead) % kTableSlots) * kSlotInts, lane);
         if (ahead.valid())
             ahead.next(p, sc);
         asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
-        const int s = gt % S;
-        if (gt >= static_cast<uint32_t>(S)) {
-            bool ok = !*sm.abort_flag &&
-                      mbar_wait_bounded(&sm.empty[s], ((gt / S) - 1) & 1, kWaitLimitNs);
+        if (ph > 0) {
+            bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.empty[s], (ph - 1) & 1, kWaitLimitNs);
             ok = __all_sync(kFull, ok);
             if (!ok) {
                 if (lane == 0)
@@ -678,11 +720,11 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
         }
         const Item& it = cur.pc.it;
         if (kSwizzled && cur.j == 0) {
+            ++piece;
             // the piece's query rows go to buffer piece & 1 once every
             // consumer warp has finished the tiles of the piece two back
-            ++piece;
             const int par = piece & 1;
-            if (piece >= 2) {
+            if (role == 0 && piece >= 2) {
                 bool ok = !*sm.abort_flag &&
                           mbar_wait_bounded(&sm.q_free[par], ((piece >> 1) - 1) & 1, kWaitLimitNs);
                 ok = __all_sync(kFull, ok);
@@ -692,7 +734,7 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
                     break;
                 }
             }
-            if (lane == 0) {
+            if (role == 0 && lane == 0) {
                 const int rows = min(p.rows_per_cta, p.R - it.rsg * p.rows_per_cta);
                 const uint32_t qb = static_cast<uint32_t>(rows * D * sizeof(T));
                 const size_t off =
@@ -702,39 +744,32 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
                 bulk_load(dst, static_cast<const T*>(p.q) + off, qb, &sm.q_full[par]);
             }
         }
-        const int t0 = it.start + cur.j * TT;
-        const int t1 = min(t0 + TT, it.end);
+        const int t0 = it.start + (cur.j << p.lg_tt);
+        const int t1 = min(t0 + p.TT, it.end);
         const int cache_end = min(t1, it.past);
-        const int nb = cache_end > t0 ? (cache_end - t0 + HB - 1) / HB : 0;
-        const bool has_new = t1 > it.past;
-        if (lane < nb && p.checked) {
-            const int phys = entries[(gt % kTableSlots) * kSlotInts + lane];  // own cp.async
+        const int nb = cache_end > t0 ? (cache_end - t0 + HB - 1) >> p.lg_box : 0;
+        const bool has_new = role == 0 && t1 > it.past;
+        const int* ent = entries + (gt % kTableSlots) * kSlotInts;
+        if (role == 0 && lane < nb && p.checked) {
+            const int phys = ent[lane];  // own cp.async
             if ((phys < 0 || phys >= p.num_blocks) && p.status)
                 atomicOr(p.status, PA_STATUS_BAD_BLOCK);
         }
         unsigned char* st = sm.ring + static_cast<size_t>(s) * p.stage_bytes;
-        unsigned char* ks = st;
-        unsigned char* vs = st + p.v_off;
         if (lane == 0)
-            mbar_arrive_expect_tx(&sm.full[s],
-                                  2u * nb * box_bytes + (has_new ? 2u * new_bytes : 0u));
-        __syncwarp();
-        // One warp instruction issues every box of the stage: lane 2i loads
-        // the K rows of box i, lane 2i+1 its V rows (the issue cost of a TMA
-        // instruction is per instruction, not per lane).
+            mbar_arrive_expect_tx(&sm.full[s], nb * box_bytes + (has_new ? 2u * new_bytes : 0u));
         __syncwarp();  // entries written by other lanes' cp.async are visible
-        if (lane < 2 * nb) {
-            const int bi = lane >> 1;
-            const bool is_v = lane & 1;
-            const int ph = entries[(gt % kTableSlots) * kSlotInts + bi];
+        // One warp instruction issues every box of the stage (lane i: box i).
+        if (lane < nb) {
+            const int phys = ent[lane];
             // Out-of-pool coordinates read as zeros: the copy never faults.
-            const int z = ph * p.BLOCK + (t0 + bi * HB) % p.BLOCK;
-            const size_t off = static_cast<size_t>(bi) * HB * D * sizeof(T);
+            const int z = (phys << p.lg_block) + ((t0 + (lane << p.lg_box)) & (p.BLOCK - 1));
+            unsigned char* dst = st + (role == 0 ? 0 : p.v_off) + static_cast<size_t>(lane) * HB * D * sizeof(T);
             if constexpr (kSwizzled) {
                 // box [HB rows][D/64 halves][64 columns], 128-byte swizzle
-                tma_load_4d((is_v ? vs : ks) + off, is_v ? vmap : kmap, 0, 0, it.kh, z, &sm.full[s]);
+                tma_load_4d(dst, map, 0, 0, it.kh, z, &sm.full[s]);
             } else {
-                tma_load_3d((is_v ? vs : ks) + off, is_v ? vmap : kmap, 0, it.kh, z, &sm.full[s]);
+                tma_load_3d(dst, map, 0, it.kh, z, &sm.full[s]);
             }
         }
         if (has_new && lane == 0) {
@@ -742,68 +777,189 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
             bulk_load(st + p.knew_off, static_cast<const T*>(p.k_new) + off, new_bytes, &sm.full[s]);
             bulk_load(st + p.vnew_off, static_cast<const T*>(p.v_new) + off, new_bytes, &sm.full[s]);
         }
+        if (++s == S) {
+            s = 0;
+            ++ph;
+        }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    // Leave no copy in flight if the pipeline was abandoned.
+    // Leave no copy in flight if the pipeline was abandoned (a stage whose
+    // other role never arrived gives up after the wait limit).
     __syncwarp();
     if (*sm.abort_flag && lane == 0) {
         const uint32_t first = gt > static_cast<uint32_t>(S) ? gt - S : 0u;
         for (uint32_t g = first; g < gt; ++g)
             mbar_wait_bounded(&sm.full[g % S], (g / S) & 1, kWaitLimitNs);
-        for (int pc = max(0, piece - 1); pc <= piece; ++pc)
-            mbar_wait_bounded(&sm.q_full[pc & 1], (pc >> 1) & 1, kWaitLimitNs);
+        if (role == 0)
+            for (int pc = max(0, piece - 1); pc <= piece; ++pc)
+                mbar_wait_bounded(&sm.q_full[pc & 1], (pc >> 1) & 1, kWaitLimitNs);
     }
 }
 
 // ---------------------------------------------------------- in-kernel merge
-// Called by all consumer threads after this CTA wrote the partial record of
-// piece `it` (not a whole segment).  Counts the finished pieces of the
-// segment; the CTA that finishes the last one merges every record of the
-// segment (M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
-// out = L == 0 ? O : O / L) and resets the counter for the next call.
-// `tot` is shared scratch for rows_per_cta (max, sum) pairs; `flag` a shared int.
+// Merges every partial record of segment (it.b, it.rsg, it.kh) into the
+// output: M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
+// out = L == 0 ? O : O / L.  All consumer threads; `tot` holds rows_per_cta
+// (M, L) pairs and `fac` fac_cap floats of shared scratch.  Records written by
+// other CTAs are read through L2 (ld.global.cg).
 template <int D, typename TO>
-__device__ void finish_split_piece(const SplitParams& p, const Sched& sc, const Item& it, int R_cta,
-                                   float2* tot, volatile int* flag)
+__device__ void merge_segment(const SplitParams& p, const Sched& sc, const Item& it, float2* tot,
+                              float* fac, int fac_cap)
 {
-    const int tid = threadIdx.x;  // consumer threads only: 0 .. kConsumerWarps*32-1
-    const int seg = (it.b * p.NRS + it.rsg) * p.KV + it.kh;
-    __threadfence();  // this thread's record stores before the count
-    consumer_bar_sync();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R_cta = min(p.rows_per_cta, p.R - it.rsg * p.rows_per_cta);
     const SegPieces sp = seg_pieces(p, sc, it.b, it.rsg, it.kh);
-    if (tid == 0)
-        *flag = atomicAdd(&p.counters[seg], 1) == sp.n - 1;
-    consumer_bar_sync();
-    if (!*flag)
-        return;
-    __threadfence();  // the other CTAs' records are visible (read them through L2)
-    for (int rl = tid; rl < R_cta; rl += kConsumerWarps * 32) {
-        float M = -FLT_MAX, L = 0.f;
-        for (int c = 0; c < sp.n; ++c)
-            M = fmaxf(M, __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]).x);
-        for (int c = 0; c < sp.n; ++c) {
+    const int n = sp.n;
+    const bool fac_smem = n * R_cta <= fac_cap;
+    // (M, L) of each row: warp w takes rows w, w + 8, ...; lanes split the records
+    for (int rl = warp; rl < R_cta; rl += kConsumerWarps) {
+        float2 first = make_float2(-FLT_MAX, 0.f);
+        float M = -FLT_MAX;
+        for (int c = lane; c < n; c += 32) {
             const float2 ml = __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]);
-            L = fmaf(ml.y, fast_exp2(ml.x - M), L);
+            if (c == lane)
+                first = ml;
+            M = fmaxf(M, ml.x);
         }
-        tot[rl] = make_float2(M, L);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        float L = 0.f;
+        for (int c = lane; c < n; c += 32) {
+            const float2 ml = c == lane ? first
+                                        : __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) *
+                                                              p.row_stride + rl]);
+            const float f = fast_exp2(ml.x - M);
+            L = fmaf(ml.y, f, L);
+            if (fac_smem)
+                fac[c * R_cta + rl] = f;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            L += __shfl_xor_sync(kFull, L, o);
+        if (lane == 0)
+            tot[rl] = make_float2(M, L);
     }
     consumer_bar_sync();
+    // O: items of 4 columns of one row; TPI threads (adjacent lanes) split the
+    // records of an item, eight loads in flight per thread
+    constexpr int D4 = D / 4;
+    const int NI = R_cta * D4;
+    int TPI = (kConsumerWarps * 32) / NI;
+    TPI = TPI >= 8 ? 8 : TPI >= 4 ? 4 : TPI >= 2 ? 2 : 1;
+    const int sub = tid % TPI;
     const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta;
-    for (int idx = tid; idx < R_cta * D; idx += kConsumerWarps * 32) {
-        const int rl = idx / D, d = idx - rl * D;
+    for (int item0 = 0; item0 < NI; item0 += (kConsumerWarps * 32) / TPI) {
+        const int item = item0 + tid / TPI;
+        const bool act = item < NI;
+        const int rl = act ? item / D4 : 0, d4 = act ? item % D4 : 0;
         const float2 ml = tot[rl];
-        float O = 0.f;
-        for (int c = 0; c < sp.n; ++c) {
-            const size_t wrow = seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl;
-            const float f = fast_exp2(__ldcg(&p.ws_ml[wrow]).x - ml.x);
-            O = fmaf(f, __ldcg(&p.ws_o[wrow * D + d]), O);
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (act) {
+            int c = sub;
+            for (; c + 7 * TPI < n; c += 8 * TPI) {
+                float4 v[8];
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const size_t wrow = seg_record(p, sp, c + u * TPI, it.rsg, it.kh) * p.row_stride + rl;
+                    v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4);
+                    f[u] = fac_smem ? fac[(c + u * TPI) * R_cta + rl]
+                                    : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - ml.x);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    O.x = fmaf(f[u], v[u].x, O.x);
+                    O.y = fmaf(f[u], v[u].y, O.y);
+                    O.z = fmaf(f[u], v[u].z, O.z);
+                    O.w = fmaf(f[u], v[u].w, O.w);
+                }
+            }
+            for (; c < n; c += TPI) {
+                const size_t wrow = seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl;
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4);
+                const float f = fac_smem ? fac[c * R_cta + rl] : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - ml.x);
+                O.x = fmaf(f, v.x, O.x);
+                O.y = fmaf(f, v.y, O.y);
+                O.z = fmaf(f, v.z, O.z);
+                O.w = fmaf(f, v.w, O.w);
+            }
         }
-        const float val = ml.y == 0.f ? O : O / ml.y;
-        static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
+        for (int o = 1; o < TPI; o <<= 1) {
+            O.x += __shfl_xor_sync(kFull, O.x, o);
+            O.y += __shfl_xor_sync(kFull, O.y, o);
+            O.z += __shfl_xor_sync(kFull, O.z, o);
+            O.w += __shfl_xor_sync(kFull, O.w, o);
+        }
+        if (act && sub == 0) {
+            const float inv = ml.y == 0.f ? 1.f : 1.f / ml.y;
+            TO* dst = static_cast<TO*>(p.out) + (out_row0 + rl) * D + 4 * d4;
+            dst[0] = from_float<TO>(O.x * inv);
+            dst[1] = from_float<TO>(O.y * inv);
+            dst[2] = from_float<TO>(O.z * inv);
+            dst[3] = from_float<TO>(O.w * inv);
+        }
     }
-    if (tid == 0)
-        p.counters[seg] = 0;  // every piece has arrived: ready for the next call
-    consumer_bar_sync();      // `tot` and `flag` are free again
+}
+
+constexpr int kFlagRound = 32;  // split pieces counted per round
+
+// Called by all consumer threads after the CTA has written the partial
+// records of all its pieces.  Each piece that is not a whole segment is
+// counted finished on its segment's counter (32 pieces per round, one lane
+// each, all atomics in flight together); the CTA that finishes the last piece
+// of a segment merges the segment's records and resets its counter for the
+// next call.  Deferring the counts to the end keeps merges out of the middle
+// of a CTA's stream.  `flags`: kFlagRound ints of shared scratch.
+template <int D, typename TO>
+__device__ void finish_split_pieces(const SplitParams& p, const Sched& sc, float2* tot, float* fac,
+                                    int fac_cap, int* flags)
+{
+    const int tid = threadIdx.x;
+    int nsplit = 0;
+    PieceIter pi;
+    for (pi.first(p, sc); pi.ok; pi.next(p, sc))
+        nsplit += pi.it.whole ? 0 : 1;
+    if (nsplit == 0)
+        return;
+    __threadfence();  // this thread's record stores before the counts
+    consumer_bar_sync();
+    for (int r0 = 0; r0 < nsplit; r0 += kFlagRound) {
+        int k = 0;
+        for (pi.first(p, sc); pi.ok; pi.next(p, sc)) {
+            const Item& it = pi.it;
+            if (it.whole)
+                continue;
+            if (k >= r0 && tid == k - r0) {  // k - r0 < 32: warp 0
+                const int seg = (it.b * p.NRS + it.rsg) * p.KV + it.kh;
+                const SegPieces sp = seg_pieces(p, sc, it.b, it.rsg, it.kh);
+                const bool last = atomicAdd(&p.counters[seg], 1) == sp.n - 1;
+                if (last)
+                    p.counters[seg] = 0;  // every piece has arrived: ready for the next call
+                flags[k - r0] = last;
+            }
+            if (++k == r0 + kFlagRound)
+                break;
+        }
+        consumer_bar_sync();
+        k = 0;
+        bool any = false;
+        for (pi.first(p, sc); pi.ok; pi.next(p, sc)) {
+            const Item& it = pi.it;
+            if (it.whole)
+                continue;
+            if (k >= r0 && flags[k - r0]) {
+                if (!any)
+                    __threadfence();  // the other CTAs' records are visible
+                any = true;
+                merge_segment<D, TO>(p, sc, it, tot, fac, fac_cap);
+                consumer_bar_sync();  // `tot` and `fac` are free again
+            }
+            if (++k == r0 + kFlagRound)
+                break;
+        }
+        consumer_bar_sync();  // `flags` is free again
+    }
 }
 
 // ------------------------------------------- float32 CUDA-core partition kernel
@@ -826,13 +982,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = p.stages;
     const int TT = p.TT;
 
+    warm_param(p);
+    warm_param(kmap);
+    warm_param(vmap);
     // Inputs may be produced by the previous kernel on the stream.
     grid_dependency_wait();
     grid_dependents_launch();
     const Sched sc = setup_cta(p, sm);
 
-    if (warp == kConsumerWarps) {
-        produce<T, D, false>(p, sc, sm, &kmap, &vmap, lane);
+    if (warp >= kConsumerWarps) {
+        produce<T, D, false>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
 
@@ -906,9 +1065,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.ws_ml[wrow] = make_float2(M, L);
             }
         }
-        if (!it.whole && p.counters)
-            finish_split_piece<D, TO>(p, sc, it, R_cta, merge_tot, &sm.info[14]);
     }
+    // uniform over the consumer warps (a late abort flag must not split them)
+    if (p.counters && !consumer_bar_or(*sm.abort_flag != 0))
+        finish_split_pieces<D, TO>(p, sc, merge_tot, mb_o, kConsumerWarps * RG * D,
+                                   reinterpret_cast<int*>(mb_m));
 }
 
 // ------------------------------------------- 16-bit tensor-core partition kernel
@@ -980,17 +1141,17 @@ __device__ __forceinline__ RowAddr row_addr(uint32_t tile, uint32_t fresh, uint3
 // T: __half or __nv_bfloat16; D: head size; MT: 16-row groups per CTA pass;
 // TO: output element type.  One CTA per SM (persistent).
 //
-// The ring holds stages of TT tokens (32 KB of K and V).  Stage g of the CTA
-// belongs to warp set g % nsets: each warp of the set takes one 16-token
+// The ring holds stages of TT tokens (up to 64 KB of K and V).  Stage g of the
+// CTA belongs to warp set g % nsets: each warp of the set takes one 16-token
 // group and one 16-row group and computes S = Q K^T with m16n8k16 MMAs
-// (float32 accumulators),
-// scale and mask S, update their running row maxima (rescaling their
-// accumulators only when a maximum grew), and accumulate O += P V with P kept
-// in registers as a 16-bit high part plus a 16-bit remainder (P V keeps about
-// 22 bits of P).  Warps never wait for one another inside a piece; at the end
-// of a piece their (max, sum, O) states are merged through shared memory in
-// rounds of kMergeDR columns.  The query rows of each piece arrive in one of
-// two shared buffers filled by the producer.
+// (float32 accumulators), scales and masks S, updates its running row maxima
+// (rescaling its accumulators only when a maximum grew), and accumulates
+// O += P V with P kept in registers as a 16-bit high part plus a 16-bit
+// remainder (P V keeps about 22 bits of P).  Warps never wait for one another
+// inside a piece; at the end of a piece their (max, sum, O) states are merged
+// through shared memory in column rounds (one when the rows are few).  The
+// query rows of each piece arrive in one of two shared buffers filled by the
+// producer.
 template <typename T, int D, int MT, typename TO>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap kmap,
@@ -1006,18 +1167,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Smem sm = carve(p, smem_raw);
     float2* ml_buf = reinterpret_cast<float2*>(sm.scratch);         // [warps][16] (max, sum)
     float2* tot = reinterpret_cast<float2*>(sm.scratch + 1024);     // [ROWS] merged (max, sum)
-    float* obuf = reinterpret_cast<float*>(sm.scratch + 2048);      // [warps][16][kMergeDR]
+    float* obuf = reinterpret_cast<float*>(sm.scratch + 2048);      // kObufFloats merge rounds
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
 
+    warm_param(p);
+    warm_param(kmap);
+    warm_param(vmap);
     grid_dependency_wait();
     grid_dependents_launch();
     const Sched sc = setup_cta(p, sm);
 
-    if (warp == kConsumerWarps) {
-        produce<T, D, true>(p, sc, sm, &kmap, &vmap, lane);
+    if (warp >= kConsumerWarps) {
+        produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
 
@@ -1248,31 +1412,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t out_row0 =
             (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * ROWS;
         const int tid = threadIdx.x;
-#pragma unroll
-        for (int r8 = 0; r8 < D / kMergeDR; ++r8) {
-            if (r8 > 0)
+        // Rounds of DRr columns: each warp writes its rows (at most RU) of the
+        // round's columns to obuf, then all threads sum the TS warps of each
+        // row.  With few rows per segment one round covers all D columns.
+        const int RU = min(16, R_cta);
+        int lg = 31 - __clz(D);  // log2 of the round width
+        while (lg > 3 && kConsumerWarps * RU * (1 << lg) > kObufFloats)
+            --lg;
+        const int DRr = 1 << lg, TPR = DRr / 8, rounds = D >> lg;
+        for (int r = 0; r < rounds; ++r) {
+            if (r > 0)
                 consumer_bar_sync();  // readers of the previous round are done
-            // each warp writes its scaled accumulators of columns [r8*DR, (r8+1)*DR)
 #pragma unroll
-            for (int i = r8 * (kMergeDR / 8); i < (r8 + 1) * (kMergeDR / 8); ++i) {
-                const int dd = (i - r8 * (kMergeDR / 8)) * 8 + 2 * qd;
+            for (int i = 0; i < NT; ++i) {
+                if (i < r * TPR || i >= (r + 1) * TPR)
+                    continue;
+                const int dd = (i - r * TPR) * 8 + 2 * qd;
                 if (g < rows_used)
-                    *reinterpret_cast<float2*>(&obuf[(warp * 16 + g) * kMergeDR + dd]) =
+                    *reinterpret_cast<float2*>(&obuf[((warp * RU + g) << lg) + dd]) =
                         make_float2(o[i][0], o[i][1]);
                 if (g + 8 < rows_used)
-                    *reinterpret_cast<float2*>(&obuf[(warp * 16 + g + 8) * kMergeDR + dd]) =
+                    *reinterpret_cast<float2*>(&obuf[((warp * RU + g + 8) << lg) + dd]) =
                         make_float2(o[i][2], o[i][3]);
             }
             consumer_bar_sync();
-            for (int idx = tid; idx < R_cta * kMergeDR; idx += kConsumerWarps * 32) {
-                const int rl = idx / kMergeDR, dd = idx - rl * kMergeDR;
-                const int grp = rl >> 4, r = rl & 15;
+            for (int idx = tid; idx < (R_cta << lg); idx += kConsumerWarps * 32) {
+                const int rl = idx >> lg, dd = idx & (DRr - 1);
+                const int grp = rl >> 4, rr = rl & 15;
                 float acc = 0.f;
 #pragma unroll
                 for (int t = 0; t < TS; ++t)
-                    acc += obuf[((t * MT + grp) * 16 + r) * kMergeDR + dd];
+                    acc += obuf[(((t * MT + grp) * RU + rr) << lg) + dd];
                 const float2 ml = tot[rl];
-                const int d = r8 * kMergeDR + dd;
+                const int d = (r << lg) + dd;
                 if (it.whole) {
                     const float val = ml.y == 0.f ? acc : acc / ml.y;
                     static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
@@ -1284,9 +1456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (!it.whole && p.counters)
-            finish_split_piece<D, TO>(p, sc, it, R_cta, tot, &sm.info[14]);
     }
+    // uniform over the consumer warps (a late abort flag must not split them)
+    if (p.counters && !consumer_bar_or(*sm.abort_flag != 0))
+        finish_split_pieces<D, TO>(p, sc, tot, obuf, kObufFloats,
+                                   reinterpret_cast<int*>(ml_buf));
 }
 
 // -------------------------------------------------------------- merge kernel
