@@ -83,18 +83,21 @@ typedef struct pa_opts {
                         P >= 2 = each sequence split into P key ranges */
     int checked;     /* nonzero: report table entries outside the pool */
     void *workspace; /* device scratch of >= pa_workspace_bytes() bytes, 256-aligned;
-                        may be NULL when partitions == 1.  Unless merge_kernel is
-                        set, its first pa_workspace_zero_bytes() bytes (split
-                        counters) must be zero before its first use; every call
-                        that completes leaves them zero again (after a call that
-                        reports PA_STATUS_TIMEOUT, zero them once more) */
+                        may be NULL when partitions == 1.  With partitions == 0
+                        and merge_kernel == 0 its first pa_workspace_zero_bytes()
+                        bytes (split counters) must be zero before its first
+                        use; every call that completes leaves them zero again
+                        (after a call that reports PA_STATUS_TIMEOUT, zero them
+                        once more) */
     size_t workspace_bytes;
     int *status;        /* device int32 for PA_STATUS_* bits, or NULL */
     void *trace_begin;  /* optional cudaEvent_t recorded before the partition kernel */
     void *trace_split;  /* optional cudaEvent_t recorded after it (before the merge) */
-    int merge_kernel;   /* 0 (default): the partition kernel's last CTA to finish a
-                           split sequence merges its partial states; 1: a separate
-                           log-sum-exp merge kernel does (no counters needed) */
+    int merge_kernel;   /* automatic split (partitions == 0): 0 (default), the
+                           partition kernel's last CTA to finish a split segment
+                           merges its partial states; 1, a separate log-sum-exp
+                           merge kernel does (no counters needed).  Fixed
+                           partitions (P >= 2) always use the merge kernel */
 } pa_opts;
 
 /*
@@ -161,8 +164,8 @@ size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partition
 
 /*
  * Leading bytes of the workspace that must be zero before its first use with
- * the in-kernel merge (per-sequence split counters; see pa_opts.workspace).
- * 0 when partitions == 1.  Returns 0 for invalid arguments.
+ * the in-kernel merge (per-segment split counters; see pa_opts.workspace).
+ * 0 unless partitions == 0.  Returns 0 for invalid arguments.
  */
 size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions);
 

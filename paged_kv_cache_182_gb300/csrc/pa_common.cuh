@@ -17,9 +17,10 @@ constexpr int kMinRing = 3;                           // stages kept before wide
 constexpr int kSubBatch = 4;        // token steps per online-softmax update
 constexpr int kStageBytes = 32768;     // CUDA-core path: K + V tile bytes per stage (target)
 constexpr int kMmaStageBytes = 65536;  // tensor-core path: K + V tile bytes per stage (target)
-constexpr int kHeaderBytes = 3072;  // barriers, broadcast scalars, zero row, table-entry slots
+constexpr int kHeaderBytes = 3584;  // barriers, scalars, zero row, table entries, split list
 constexpr int kMaxBatch = 4096;     // sequences per call (the schedule lives in smem)
 constexpr int kMaxGrid = 1024;      // partition-kernel CTAs at most (sizes the workspace)
+constexpr int kPieceBytes = 131072;  // streaming-time equivalent of a piece's fixed cost
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -46,6 +47,7 @@ struct SplitParams {
     int NRS;           // row groups per KV head = ceil(R / rows_per_cta)
     int TT;            // tokens per pipeline stage, a multiple of BLOCK
     int lg_block, lg_box, lg_tt;  // log2 of BLOCK, box_rows and TT (all powers of two)
+    int vunits;        // automatic schedule: virtual units charged per segment
     int row_stride;    // workspace rows per item = min(R, rows_per_cta)
     int stages;        // ring depth (<= kMaxStages)
     int stage_bytes;   // bytes of one stage: K tile | K new rows | V tile | V new rows
@@ -66,6 +68,7 @@ struct CombineParams {
     int B, KV, R, NRS, rows_per_cta, row_stride;
     int stream;  // automatic (balanced) schedule: records are per partition-kernel CTA
     int grid;    // partition-kernel CTAs (automatic schedule)
+    int vunits;  // automatic schedule: virtual units charged per segment
 };
 
 using SplitFn = void (*)(SplitParams, CUtensorMap, CUtensorMap);

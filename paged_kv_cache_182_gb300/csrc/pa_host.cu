@@ -329,7 +329,7 @@ size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partition
 
 size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions)
 {
-    if (!ws_args_ok(batch, H, KV, D, NQ, partitions) || partitions == 1 || batch == 0)
+    if (!ws_args_ok(batch, H, KV, D, NQ, partitions) || partitions != 0 || batch == 0)
         return 0;
     return ws_bound(batch, H, KV, D, NQ, partitions).sched;
 }
@@ -382,8 +382,14 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     if (records >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
     // the automatic schedule counts BLOCK-token units of all segments in int32
-    const long long units = static_cast<long long>(B) * (opts->max_blocks + 1 + NQ / BLOCK + 1) *
-                            NRS * KV;
+    const int es = static_cast<int>(elem_size(dtype));
+    // automatic schedule: a piece costs about as much as streaming kPieceBytes
+    // more (the merge of the consumer warps' states, the partial last stage),
+    // so each segment is charged that many virtual units when units are dealt
+    const int unit_bytes = 2 * BLOCK * D * es;
+    const int vunits = (kPieceBytes + unit_bytes / 2) / unit_bytes;
+    const long long units = static_cast<long long>(B) *
+                            (opts->max_blocks + 1 + NQ / BLOCK + 1 + vunits) * NRS * KV;
     if (partitions == 0 && units >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
     WsLayout ws{};
@@ -395,7 +401,6 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
             return PA_ERR_ALIGNMENT;
     }
 
-    const int es = static_cast<int>(elem_size(dtype));
     // tensor-core path: up to 64 KB stages, at most 8 warps (16-token groups x
     // row groups) per stage: 128 tokens (64 with 32 rows per pass)
     int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
@@ -468,8 +473,10 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.seq_lens = seq_lens;
     unsigned char* wsb = static_cast<unsigned char*>(opts->workspace);
     p.sched = partitions != 1 ? reinterpret_cast<int2*>(wsb + ws.sched) : nullptr;
-    p.counters = partitions != 1 && !opts->merge_kernel ? reinterpret_cast<int*>(wsb + ws.counters)
-                                                         : nullptr;
+    // the in-kernel merge serves the automatic schedule; fixed partitions
+    // always use the merge kernel
+    const bool merge_in_kernel = partitions == 0 && !opts->merge_kernel;
+    p.counters = merge_in_kernel ? reinterpret_cast<int*>(wsb + ws.counters) : nullptr;
     p.ws_ml = partitions != 1 ? reinterpret_cast<float2*>(wsb + ws.ml) : nullptr;
     p.ws_o = partitions != 1 ? reinterpret_cast<float*>(wsb + ws.o) : nullptr;
     p.status = opts->status;
@@ -499,6 +506,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.lg_block = ilog2(BLOCK);
     p.lg_box = ilog2(box_rows);
     p.lg_tt = ilog2(TT);
+    p.vunits = vunits;
     p.row_stride = row_stride;
     p.stages = stages;
     p.stage_bytes = stage_bytes;
@@ -535,7 +543,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         cudaEventRecord(static_cast<cudaEvent_t>(opts->trace_split), st) != cudaSuccess)
         return PA_ERR_CUDA;
 
-    if (partitions != 1 && opts->merge_kernel) {
+    if (partitions != 1 && !merge_in_kernel) {
         CombineParams cp{};
         cp.sched = p.sched;
         cp.ws_ml = p.ws_ml;
@@ -549,6 +557,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         cp.row_stride = row_stride;
         cp.stream = partitions == 0 ? 1 : 0;
         cp.grid = static_cast<int>(grid);
+        cp.vunits = vunits;
         const CombineFn comb = pick_combine(out_dtype, D);
         cudaLaunchConfig_t cc{};
         cc.gridDim = dim3(static_cast<unsigned>(B) * KV * NRS);

@@ -140,11 +140,34 @@ struct Sched {
     const int* prefix;  // [B + 1] automatic: units before sequence b (all its segments);
                         //         fixed: ranges before sequence b (one segment's worth)
     int total;          // automatic: W units; fixed: number of items
+    long long cost;     // automatic: C = W + vunits * (number of segments)
 };
 
-__device__ __forceinline__ long long range_start(long long k, long long W, long long G)
+// Automatic mode deals cost, not units: segment g (in stream order) costs
+// vunits + its units, the virtual units charged ahead of its first real unit,
+// so that a CTA holding many short pieces (each with a fixed overhead) gets
+// fewer units.  Real unit x of segment g sits at cost position
+// c(x) = x + vunits * (g + 1); CTA k of G owns the units whose c * G / C
+// rounds down to k, a contiguous and, for the CTAs inside a segment, non-empty
+// range (G <= C).
+
+// CTAs holding segment g = its units [x0, x0 + nu): the first (k0), how many,
+// and the workspace record of the segment's piece in CTA k0 (2 k0 when the
+// segment starts that CTA's range, else 2 k0 + 1).
+struct SegSpan {
+    int k0, n, rec_first;
+};
+__device__ __forceinline__ SegSpan seg_span(long long x0, int nu, long long g, int V, long long C,
+                                            long long G)
 {
-    return k * W / G;
+    const long long c0 = x0 + static_cast<long long>(V) * (g + 1);
+    SegSpan r;
+    r.k0 = static_cast<int>(c0 * G / C);
+    r.n = static_cast<int>((c0 + nu - 1) * G / C) - r.k0 + 1;
+    const bool cont =
+        x0 > 0 && static_cast<int>((x0 - 1 + static_cast<long long>(V) * g) * G / C) == r.k0;
+    r.rec_first = 2 * r.k0 + (cont ? 1 : 0);
+    return r;
 }
 
 // Executed by one full warp after `lens` is in shared memory.  CTA 0 also
@@ -197,6 +220,31 @@ __device__ __forceinline__ int last_le(const int* prefix, int B, long long x)
     return lo;
 }
 
+// First real unit of CTA k of G (automatic mode): the smallest x with
+// c(x) >= ceil(k C / G), or W when there is none.
+__device__ __forceinline__ long long cost_start(const SplitParams& p, const Sched& sc, long long k,
+                                                long long G)
+{
+    const long long T = (k * sc.cost + G - 1) / G;
+    if (T >= sc.cost)
+        return sc.total;
+    const long long VU = static_cast<long long>(p.vunits) * p.NRS * p.KV;  // cost of a sequence's virtual units
+    int lo = 0, hi = p.B - 1;  // last b whose cost prefix is <= T
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sc.prefix[mid] + VU * mid <= T)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int nb = (sc.lens[lo] + p.NQ + p.BLOCK - 1) >> p.lg_block;
+    const long long local = T - (sc.prefix[lo] + VU * lo);
+    const long long per = nb + p.vunits;
+    const long long s = local / per;
+    const long long r = local - s * per - p.vunits;
+    return sc.prefix[lo] + s * nb + (r > 0 ? r : 0);
+}
+
 // Iterates this CTA's pieces in order (identically in every warp).  In the
 // automatic mode only first() searches the schedule; next() steps to the
 // following segment, since every piece but the CTA's last ends where its
@@ -210,11 +258,10 @@ struct PieceIter {
     __device__ __forceinline__ void first(const SplitParams& p, const Sched& sc)
     {
         if (p.partitions == 0) {
-            // with fewer units than CTAs only the first W CTAs take work, so
-            // that every range is non-empty (the merge kernel counts on it)
-            const long long G = min(static_cast<long long>(gridDim.x), static_cast<long long>(sc.total));
-            pos = blockIdx.x < G ? range_start(blockIdx.x, sc.total, G) : 0;
-            stop = blockIdx.x < G ? range_start(blockIdx.x + 1, sc.total, G) : 0;
+            // G = min(CTAs, C): every CTA inside a segment then holds a unit
+            const long long G = min(static_cast<long long>(gridDim.x), sc.cost);
+            pos = blockIdx.x < G ? cost_start(p, sc, blockIdx.x, G) : 0;
+            stop = blockIdx.x < G ? cost_start(p, sc, blockIdx.x + 1, G) : 0;
             ok = pos < stop;
             if (!ok)
                 return;
@@ -311,15 +358,14 @@ __device__ __forceinline__ SegPieces seg_pieces(const SplitParams& p, const Sche
 {
     SegPieces sp;
     if (p.partitions == 0) {
-        const long long W = sc.total;
-        const long long G = min(static_cast<long long>(gridDim.x), W);
-        const int units = (sc.lens[b] + p.NQ + p.BLOCK - 1) / p.BLOCK;
-        const long long s0 = sc.prefix[b] + static_cast<long long>(rsg * p.KV + kh) * units;
-        const long long s1 = s0 + units;
-        sp.k0 = static_cast<int>(((s0 + 1) * G - 1) / W);
-        const int k1 = static_cast<int>((s1 * G - 1) / W);
-        sp.n = k1 - sp.k0 + 1;
-        sp.rec_first = 2 * sp.k0 + (range_start(sp.k0, W, G) == s0 ? 0 : 1);
+        const long long G = min(static_cast<long long>(gridDim.x), sc.cost);
+        const int units = (sc.lens[b] + p.NQ + p.BLOCK - 1) >> p.lg_block;
+        const int gl = rsg * p.KV + kh;
+        const SegSpan ss = seg_span(sc.prefix[b] + static_cast<long long>(gl) * units, units,
+                                    static_cast<long long>(b) * p.NRS * p.KV + gl, p.vunits, sc.cost, G);
+        sp.k0 = ss.k0;
+        sp.n = ss.n;
+        sp.rec_first = ss.rec_first;
         sp.item0 = 0;
     } else {
         sp.n = sc.prefix[b + 1] - sc.prefix[b];
@@ -551,6 +597,7 @@ struct SimtMath {
 //   [512, 576)   broadcast scalars  [576, 608)  query-buffer barriers (full, free)
 //   [640, 896)   a zeroed 256-byte row (tensor-core path)
 //   [1024, 3072) table-entry slots of the two producer warps
+//   [3072, 3584) split pieces awaiting their counts
 //   lens[B] | prefix[B+1] | consumer scratch | ring of `stages` stages.
 struct Smem {
     uint64_t* full;
@@ -565,6 +612,7 @@ struct Smem {
     unsigned char* scratch;
     unsigned char* ring;
     int* entries;  // producer warps' table-entry slots [2][kTableSlots][kSlotInts]
+    int4* split_list;  // [kSplitList] split pieces awaiting their counts (b, rsg, kh, flag)
 };
 
 __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
@@ -579,6 +627,7 @@ __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
     sm.q_free = sm.q_full + 2;
     sm.zero16 = base + 640;
     sm.entries = reinterpret_cast<int*>(base + 1024);
+    sm.split_list = reinterpret_cast<int4*>(base + 3072);
     sm.lens = reinterpret_cast<int*>(base + p.lens_off);
     sm.prefix = reinterpret_cast<int*>(base + p.prefix_off);
     sm.scratch = base + p.merge_off;
@@ -622,6 +671,7 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
     sc.lens = sm.lens;
     sc.prefix = sm.prefix;
     sc.total = sm.info[1];
+    sc.cost = sc.total + static_cast<long long>(p.vunits) * p.B * p.NRS * p.KV;
     return sc;
 }
 
@@ -797,16 +847,31 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
 }
 
 // ---------------------------------------------------------- in-kernel merge
+// Counter increment with acquire-release semantics at GPU scope: after a CTA
+// barrier, the release publishes every record store of the CTA's threads
+// (cumulativity through the barrier); the acquire makes the records of the
+// CTAs that counted before visible to this CTA after its next barrier.
+__device__ __forceinline__ int count_piece(int* counter)
+{
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
 // Merges every partial record of segment (it.b, it.rsg, it.kh) into the
 // output: M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
 // out = L == 0 ? O : O / L.  All consumer threads; `tot` holds rows_per_cta
 // (M, L) pairs and `fac` fac_cap floats of shared scratch.  Records written by
 // other CTAs are read through L2 (ld.global.cg).
 template <int D, typename TO>
-__device__ void merge_segment(const SplitParams& p, const Sched& sc, const Item& it, float2* tot,
+__device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 seg, float2* tot,
                               float* fac, int fac_cap)
 {
+    constexpr int kT = kConsumerWarps * 32;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    struct {
+        int b, rsg, kh;
+    } it{seg.x, seg.y, seg.z};
     const int R_cta = min(p.rows_per_cta, p.R - it.rsg * p.rows_per_cta);
     const SegPieces sp = seg_pieces(p, sc, it.b, it.rsg, it.kh);
     const int n = sp.n;
@@ -841,124 +906,142 @@ __device__ void merge_segment(const SplitParams& p, const Sched& sc, const Item&
             tot[rl] = make_float2(M, L);
     }
     consumer_bar_sync();
-    // O: items of 4 columns of one row; TPI threads (adjacent lanes) split the
-    // records of an item, eight loads in flight per thread
+    // O: items of 4 columns of one row (at most 32 rows x D/4 = 1024 items,
+    // four per thread); TPI adjacent lanes split the records of an item when
+    // the items are few.  A thread keeps the loads of all its items for two
+    // records in flight.
     constexpr int D4 = D / 4;
+    constexpr int LG4 = D4 == 16 ? 4 : 5;
     const int NI = R_cta * D4;
-    int TPI = (kConsumerWarps * 32) / NI;
+    int TPI = kT / NI;
     TPI = TPI >= 8 ? 8 : TPI >= 4 ? 4 : TPI >= 2 ? 2 : 1;
-    const int sub = tid % TPI;
+    const int per_pass = kT / TPI;
+    const int sub = tid % TPI, i0 = tid / TPI;
+    float4 O[4];
+    int rl_of[4];
+    bool act[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        O[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int item = i0 + j * per_pass;
+        act[j] = item < NI;
+        rl_of[j] = act[j] ? item >> LG4 : 0;
+    }
+    auto add_record = [&](int c, float4* v, float* f) {
+        const size_t rec = seg_record(p, sp, c, it.rsg, it.kh);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!act[j])
+                continue;
+            const int item = i0 + j * per_pass;
+            const size_t wrow = rec * p.row_stride + rl_of[j];
+            v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + (item & (D4 - 1)));
+            f[j] = fac_smem ? fac[c * R_cta + rl_of[j]]
+                            : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - tot[rl_of[j]].x);
+        }
+    };
+    auto fma4 = [](float4& a, float f, const float4& v) {
+        a.x = fmaf(f, v.x, a.x);
+        a.y = fmaf(f, v.y, a.y);
+        a.z = fmaf(f, v.z, a.z);
+        a.w = fmaf(f, v.w, a.w);
+    };
+    int c = sub;
+    if (NI <= per_pass) {
+        // one item per thread: eight records in flight
+        const int rl = rl_of[0];
+        const int d4 = (i0 & (D4 - 1));
+        for (; c + 7 * TPI < n; c += 8 * TPI) {
+            float4 v[8];
+            float f[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const size_t wrow = seg_record(p, sp, c + u * TPI, it.rsg, it.kh) * p.row_stride + rl;
+                v[u] = act[0] ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                f[u] = fac_smem ? fac[(c + u * TPI) * R_cta + rl]
+                                : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - tot[rl].x);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                fma4(O[0], f[u], v[u]);
+        }
+    }
+    for (; c + TPI < n; c += 2 * TPI) {
+        float4 va[4], vb[4];
+        float fa[4], fb[4];
+        add_record(c, va, fa);
+        add_record(c + TPI, vb, fb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (act[j]) {
+                fma4(O[j], fa[j], va[j]);
+                fma4(O[j], fb[j], vb[j]);
+            }
+    }
+    if (c < n) {
+        float4 va[4];
+        float fa[4];
+        add_record(c, va, fa);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (act[j])
+                fma4(O[j], fa[j], va[j]);
+    }
     const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta;
-    for (int item0 = 0; item0 < NI; item0 += (kConsumerWarps * 32) / TPI) {
-        const int item = item0 + tid / TPI;
-        const bool act = item < NI;
-        const int rl = act ? item / D4 : 0, d4 = act ? item % D4 : 0;
-        const float2 ml = tot[rl];
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (act) {
-            int c = sub;
-            for (; c + 7 * TPI < n; c += 8 * TPI) {
-                float4 v[8];
-                float f[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const size_t wrow = seg_record(p, sp, c + u * TPI, it.rsg, it.kh) * p.row_stride + rl;
-                    v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4);
-                    f[u] = fac_smem ? fac[(c + u * TPI) * R_cta + rl]
-                                    : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - ml.x);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    O.x = fmaf(f[u], v[u].x, O.x);
-                    O.y = fmaf(f[u], v[u].y, O.y);
-                    O.z = fmaf(f[u], v[u].z, O.z);
-                    O.w = fmaf(f[u], v[u].w, O.w);
-                }
-            }
-            for (; c < n; c += TPI) {
-                const size_t wrow = seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl;
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4);
-                const float f = fac_smem ? fac[c * R_cta + rl] : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - ml.x);
-                O.x = fmaf(f, v.x, O.x);
-                O.y = fmaf(f, v.y, O.y);
-                O.z = fmaf(f, v.z, O.z);
-                O.w = fmaf(f, v.w, O.w);
-            }
-        }
+    for (int j = 0; j < 4; ++j) {
         for (int o = 1; o < TPI; o <<= 1) {
-            O.x += __shfl_xor_sync(kFull, O.x, o);
-            O.y += __shfl_xor_sync(kFull, O.y, o);
-            O.z += __shfl_xor_sync(kFull, O.z, o);
-            O.w += __shfl_xor_sync(kFull, O.w, o);
+            O[j].x += __shfl_xor_sync(kFull, O[j].x, o);
+            O[j].y += __shfl_xor_sync(kFull, O[j].y, o);
+            O[j].z += __shfl_xor_sync(kFull, O[j].z, o);
+            O[j].w += __shfl_xor_sync(kFull, O[j].w, o);
         }
-        if (act && sub == 0) {
+        if (act[j] && sub == 0) {
+            const float2 ml = tot[rl_of[j]];
             const float inv = ml.y == 0.f ? 1.f : 1.f / ml.y;
-            TO* dst = static_cast<TO*>(p.out) + (out_row0 + rl) * D + 4 * d4;
-            dst[0] = from_float<TO>(O.x * inv);
-            dst[1] = from_float<TO>(O.y * inv);
-            dst[2] = from_float<TO>(O.z * inv);
-            dst[3] = from_float<TO>(O.w * inv);
+            const int item = i0 + j * per_pass;
+            TO* dst = static_cast<TO*>(p.out) + (out_row0 + rl_of[j]) * D + 4 * (item & (D4 - 1));
+            dst[0] = from_float<TO>(O[j].x * inv);
+            dst[1] = from_float<TO>(O[j].y * inv);
+            dst[2] = from_float<TO>(O[j].z * inv);
+            dst[3] = from_float<TO>(O[j].w * inv);
         }
     }
 }
 
-constexpr int kFlagRound = 32;  // split pieces counted per round
+constexpr int kSplitList = 32;  // list capacity (the automatic schedule needs two)
 
-// Called by all consumer threads after the CTA has written the partial
-// records of all its pieces.  Each piece that is not a whole segment is
-// counted finished on its segment's counter (32 pieces per round, one lane
-// each, all atomics in flight together); the CTA that finishes the last piece
-// of a segment merges the segment's records and resets its counter for the
-// next call.  Deferring the counts to the end keeps merges out of the middle
-// of a CTA's stream.  `flags`: kFlagRound ints of shared scratch.
+// Called by all consumer threads at the end of the CTA's stream, once the
+// partial records of the `n` split pieces in `list` ((b, rsg, kh, -) each) are
+// written (automatic schedule only: a CTA's first and last pieces).  Each
+// piece is counted finished on its segment's counter (one lane each, the
+// atomics in flight together); the CTA that finishes the last piece of a
+// segment merges the segment's records and resets its counter for the next
+// call.  Counting at the end keeps merges out of the CTA's stream.
 template <int D, typename TO>
-__device__ void finish_split_pieces(const SplitParams& p, const Sched& sc, float2* tot, float* fac,
-                                    int fac_cap, int* flags)
+__device__ void flush_split_pieces(const SplitParams& p, const Sched& sc, int4* list, int n, float2* tot,
+                                   float* fac, int fac_cap)
 {
     const int tid = threadIdx.x;
-    int nsplit = 0;
-    PieceIter pi;
-    for (pi.first(p, sc); pi.ok; pi.next(p, sc))
-        nsplit += pi.it.whole ? 0 : 1;
-    if (nsplit == 0)
-        return;
-    __threadfence();  // this thread's record stores before the counts
+    consumer_bar_sync();  // every thread's record stores (and the list) precede the counts
+    if (tid < n) {
+        int4 e = list[tid];
+        const int seg = (e.x * p.NRS + e.y) * p.KV + e.z;
+        const SegPieces sp = seg_pieces(p, sc, e.x, e.y, e.z);
+        const bool last = count_piece(&p.counters[seg]) == sp.n - 1;
+        if (last)
+            p.counters[seg] = 0;  // every piece has arrived: ready for the next call
+        e.w = last;
+        list[tid] = e;
+    }
     consumer_bar_sync();
-    for (int r0 = 0; r0 < nsplit; r0 += kFlagRound) {
-        int k = 0;
-        for (pi.first(p, sc); pi.ok; pi.next(p, sc)) {
-            const Item& it = pi.it;
-            if (it.whole)
-                continue;
-            if (k >= r0 && tid == k - r0) {  // k - r0 < 32: warp 0
-                const int seg = (it.b * p.NRS + it.rsg) * p.KV + it.kh;
-                const SegPieces sp = seg_pieces(p, sc, it.b, it.rsg, it.kh);
-                const bool last = atomicAdd(&p.counters[seg], 1) == sp.n - 1;
-                if (last)
-                    p.counters[seg] = 0;  // every piece has arrived: ready for the next call
-                flags[k - r0] = last;
-            }
-            if (++k == r0 + kFlagRound)
-                break;
+    for (int i = 0; i < n; ++i) {
+        const int4 e = list[i];
+        if (e.w) {
+            merge_segment<D, TO>(p, sc, e, tot, fac, fac_cap);
+            consumer_bar_sync();  // `tot` and `fac` are free again
         }
-        consumer_bar_sync();
-        k = 0;
-        bool any = false;
-        for (pi.first(p, sc); pi.ok; pi.next(p, sc)) {
-            const Item& it = pi.it;
-            if (it.whole)
-                continue;
-            if (k >= r0 && flags[k - r0]) {
-                if (!any)
-                    __threadfence();  // the other CTAs' records are visible
-                any = true;
-                merge_segment<D, TO>(p, sc, it, tot, fac, fac_cap);
-                consumer_bar_sync();  // `tot` and `fac` are free again
-            }
-            if (++k == r0 + kFlagRound)
-                break;
-        }
-        consumer_bar_sync();  // `flags` is free again
     }
 }
 
@@ -997,6 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     using Math = SimtMath<T, D, RG>;
     uint32_t gt = 0;
+    int nsplit = 0;  // split pieces listed since the last flush (uniform)
     const int tid = threadIdx.x;  // 0 .. kConsumerWarps*32-1
     PieceIter pi;
     for (pi.first(p, sc); pi.ok; pi.next(p, sc)) {
@@ -1065,11 +1149,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.ws_ml[wrow] = make_float2(M, L);
             }
         }
+        // automatic schedule: the CTA's first and last pieces at most
+        if (!it.whole && p.counters && nsplit < kSplitList) {
+            if (tid == 0)
+                sm.split_list[nsplit] = make_int4(it.b, it.rsg, it.kh, 0);
+            ++nsplit;
+        }
     }
     // uniform over the consumer warps (a late abort flag must not split them)
-    if (p.counters && !consumer_bar_or(*sm.abort_flag != 0))
-        finish_split_pieces<D, TO>(p, sc, merge_tot, mb_o, kConsumerWarps * RG * D,
-                                   reinterpret_cast<int*>(mb_m));
+    if (nsplit > 0 && !consumer_bar_or(*sm.abort_flag != 0))
+        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, merge_tot, mb_o,
+                                  kConsumerWarps * RG * D);
 }
 
 // ------------------------------------------- 16-bit tensor-core partition kernel
@@ -1198,6 +1288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t qbuf = smem_u32(sm.scratch + p.qbuf_off);
     uint32_t gt = 0;
     int piece = 0;
+    int nsplit = 0;  // split pieces listed since the last flush (uniform)
     bool alive = true;
 
     PieceIter pi;
@@ -1456,11 +1547,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        // automatic schedule: the CTA's first and last pieces at most
+        if (!it.whole && p.counters && nsplit < kSplitList) {
+            if (tid == 0)
+                sm.split_list[nsplit] = make_int4(it.b, it.rsg, it.kh, 0);
+            ++nsplit;
+        }
     }
     // uniform over the consumer warps (a late abort flag must not split them)
-    if (p.counters && !consumer_bar_or(*sm.abort_flag != 0))
-        finish_split_pieces<D, TO>(p, sc, tot, obuf, kObufFloats,
-                                   reinterpret_cast<int*>(ml_buf));
+    if (nsplit > 0 && !consumer_bar_or(*sm.abort_flag != 0))
+        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, tot, obuf, kObufFloats);
 }
 
 // -------------------------------------------------------------- merge kernel
@@ -1485,13 +1581,14 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
     if (p.stream) {
         const int2 last = p.sched[p.B - 1];
         const long long W = static_cast<long long>(last.x) + static_cast<long long>(last.y) * U;
-        const long long G = min(static_cast<long long>(p.grid), W);  // CTAs that took work
-        const long long s0 = sc.x + static_cast<long long>(rsg * p.KV + kh) * sc.y;
-        const long long s1 = s0 + sc.y;
-        k0 = static_cast<int>(((s0 + 1) * G - 1) / W);
-        const int k1 = static_cast<int>((s1 * G - 1) / W);
-        n = k1 - k0 + 1;
-        rec_first = 2 * k0 + (range_start(k0, W, G) == s0 ? 0 : 1);
+        const long long C = W + static_cast<long long>(p.vunits) * p.B * U;
+        const long long G = min(static_cast<long long>(p.grid), C);
+        const int gl = rsg * p.KV + kh;
+        const SegSpan ss = seg_span(sc.x + static_cast<long long>(gl) * sc.y, sc.y,
+                                    static_cast<long long>(b) * U + gl, p.vunits, C, G);
+        k0 = ss.k0;
+        n = ss.n;
+        rec_first = ss.rec_first;
     } else {
         n = sc.y;
     }

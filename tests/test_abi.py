@@ -59,6 +59,7 @@ def test_workspace_bytes(lib):
     assert ws(1, 32, 8, 128, 1, 32) >= 32 * 8 * 4 * (128 + 2) * 4
     zb = lib.workspace_zero_bytes
     assert zb(8, 32, 8, 128, 1, 1) == 0
+    assert zb(8, 32, 8, 128, 1, 4) == 0  # fixed partitions: the merge kernel, no counters
     assert 0 < zb(8, 32, 8, 128, 1, 0) < ws(8, 32, 8, 128, 1, 0)
     assert zb(8, 32, 8, 128, 1, 0) >= 8 * 8 * 4  # one counter per (sequence, KV head)
 

@@ -184,7 +184,9 @@ def test_kernel_launch_counter_moves():
     pu.run_gpu(w, partitions=1)
     pu.run_gpu(w, partitions=0)
     pu.run_gpu(w, partitions=0, merge_kernel=True)
-    assert binding.kernel_launches() - before == 4  # 1 + 1 (merge in kernel) + 2
+    pu.run_gpu(w, partitions=3)
+    # 1 + 1 (merge in the kernel) + 2 + 2 (fixed partitions: merge kernel)
+    assert binding.kernel_launches() - before == 6
 
 
 # ------------------------------------------------ workspace hygiene
