@@ -141,6 +141,8 @@ struct Sched {
                         //         fixed: ranges before sequence b (one segment's worth)
     int total;          // automatic: W units; fixed: number of items
     long long cost;     // automatic: C = W + vunits * (number of segments)
+    int pos0, stop0;    // automatic: this CTA's units [pos0, stop0)
+    int b0, seg0, uu0;  // automatic: where unit pos0 lies (sequence, segment, unit)
 };
 
 // Automatic mode deals cost, not units: segment g (in stream order) costs
@@ -151,21 +153,34 @@ struct Sched {
 // rounds down to k, a contiguous and, for the CTAs inside a segment, non-empty
 // range (G <= C).
 
+// CTA of G owning cost position c: the k with T(k) <= c < T(k + 1), where
+// T(k) = ceil(k C / G) (all in int32: C < 2^31, G <= kMaxGrid).
+__device__ __forceinline__ int cost_owner(int c, int C, int G)
+{
+    const int q = C / G, r = C - q * G;
+    auto T = [&](int k) { return k * q + (k * r + G - 1) / G; };
+    int k = min(static_cast<int>(static_cast<float>(c) * static_cast<float>(G) / static_cast<float>(C)),
+                G - 1);
+    while (k + 1 < G && T(k + 1) <= c)
+        ++k;
+    while (k > 0 && T(k) > c)
+        --k;
+    return k;
+}
+
 // CTAs holding segment g = its units [x0, x0 + nu): the first (k0), how many,
 // and the workspace record of the segment's piece in CTA k0 (2 k0 when the
 // segment starts that CTA's range, else 2 k0 + 1).
 struct SegSpan {
     int k0, n, rec_first;
 };
-__device__ __forceinline__ SegSpan seg_span(long long x0, int nu, long long g, int V, long long C,
-                                            long long G)
+__device__ __forceinline__ SegSpan seg_span(int x0, int nu, int g, int V, int C, int G)
 {
-    const long long c0 = x0 + static_cast<long long>(V) * (g + 1);
+    const int c0 = x0 + V * (g + 1);
     SegSpan r;
-    r.k0 = static_cast<int>(c0 * G / C);
-    r.n = static_cast<int>((c0 + nu - 1) * G / C) - r.k0 + 1;
-    const bool cont =
-        x0 > 0 && static_cast<int>((x0 - 1 + static_cast<long long>(V) * g) * G / C) == r.k0;
+    r.k0 = cost_owner(c0, C, G);
+    r.n = cost_owner(c0 + nu - 1, C, G) - r.k0 + 1;
+    const bool cont = x0 > 0 && cost_owner(x0 - 1 + V * g, C, G) == r.k0;
     r.rec_first = 2 * r.k0 + (cont ? 1 : 0);
     return r;
 }
@@ -221,14 +236,19 @@ __device__ __forceinline__ int last_le(const int* prefix, int B, long long x)
 }
 
 // First real unit of CTA k of G (automatic mode): the smallest x with
-// c(x) >= ceil(k C / G), or W when there is none.
-__device__ __forceinline__ long long cost_start(const SplitParams& p, const Sched& sc, long long k,
-                                                long long G)
+// c(x) >= ceil(k C / G), or W when there is none, with its sequence, segment
+// and unit within the segment.  C < 2^31 and G <= kMaxGrid keep it in int32.
+struct CostPos {
+    int x, b, seg, uu;
+};
+__device__ __forceinline__ CostPos cost_start(const SplitParams& p, const Sched& sc, int k, int G)
 {
-    const long long T = (k * sc.cost + G - 1) / G;
-    if (T >= sc.cost)
-        return sc.total;
-    const long long VU = static_cast<long long>(p.vunits) * p.NRS * p.KV;  // cost of a sequence's virtual units
+    const int C = static_cast<int>(sc.cost);
+    const int q = C / G, r = C - q * G;
+    const int T = k * q + (k * r + G - 1) / G;
+    if (T >= C)
+        return CostPos{sc.total, p.B, 0, 0};
+    const int VU = p.vunits * p.NRS * p.KV;  // cost of one sequence's virtual units
     int lo = 0, hi = p.B - 1;  // last b whose cost prefix is <= T
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -238,11 +258,11 @@ __device__ __forceinline__ long long cost_start(const SplitParams& p, const Sche
             hi = mid - 1;
     }
     const int nb = (sc.lens[lo] + p.NQ + p.BLOCK - 1) >> p.lg_block;
-    const long long local = T - (sc.prefix[lo] + VU * lo);
-    const long long per = nb + p.vunits;
-    const long long s = local / per;
-    const long long r = local - s * per - p.vunits;
-    return sc.prefix[lo] + s * nb + (r > 0 ? r : 0);
+    const int local = T - (sc.prefix[lo] + VU * lo);
+    const int per = nb + p.vunits;
+    const int s = local / per;
+    const int uu = max(local - s * per - p.vunits, 0);
+    return CostPos{sc.prefix[lo] + s * nb + uu, lo, s, uu};
 }
 
 // Iterates this CTA's pieces in order (identically in every warp).  In the
@@ -258,19 +278,14 @@ struct PieceIter {
     __device__ __forceinline__ void first(const SplitParams& p, const Sched& sc)
     {
         if (p.partitions == 0) {
-            // G = min(CTAs, C): every CTA inside a segment then holds a unit
-            const long long G = min(static_cast<long long>(gridDim.x), sc.cost);
-            pos = blockIdx.x < G ? cost_start(p, sc, blockIdx.x, G) : 0;
-            stop = blockIdx.x < G ? cost_start(p, sc, blockIdx.x + 1, G) : 0;
+            // the CTA's range and first piece, located once in setup_cta
+            pos = sc.pos0;
+            stop = sc.stop0;
             ok = pos < stop;
             if (!ok)
                 return;
-            const int b = last_le(sc.prefix, p.B, pos);
-            const int total = sc.lens[b] + p.NQ;
-            seg_units = (total + p.BLOCK - 1) >> p.lg_block;
-            const int local = static_cast<int>(pos - sc.prefix[b]);
-            const int seg = local / seg_units;
-            const int uu = local - seg * seg_units;
+            const int b = sc.b0, seg = sc.seg0, uu = sc.uu0;
+            seg_units = (sc.lens[b] + p.NQ + p.BLOCK - 1) >> p.lg_block;
             it.b = b;
             it.rsg = seg / p.KV;
             it.kh = seg - it.rsg * p.KV;
@@ -358,11 +373,11 @@ __device__ __forceinline__ SegPieces seg_pieces(const SplitParams& p, const Sche
 {
     SegPieces sp;
     if (p.partitions == 0) {
-        const long long G = min(static_cast<long long>(gridDim.x), sc.cost);
+        const int C = static_cast<int>(sc.cost);
+        const int G = min(static_cast<int>(gridDim.x), C);
         const int units = (sc.lens[b] + p.NQ + p.BLOCK - 1) >> p.lg_block;
         const int gl = rsg * p.KV + kh;
-        const SegSpan ss = seg_span(sc.prefix[b] + static_cast<long long>(gl) * units, units,
-                                    static_cast<long long>(b) * p.NRS * p.KV + gl, p.vunits, sc.cost, G);
+        const SegSpan ss = seg_span(sc.prefix[b] + gl * units, units, b * p.NRS * p.KV + gl, p.vunits, C, G);
         sp.k0 = ss.k0;
         sp.n = ss.n;
         sp.rec_first = ss.rec_first;
@@ -672,6 +687,26 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
     sc.prefix = sm.prefix;
     sc.total = sm.info[1];
     sc.cost = sc.total + static_cast<long long>(p.vunits) * p.B * p.NRS * p.KV;
+    if (p.partitions == 0) {
+        // G = min(CTAs, C): every CTA inside a segment then holds a unit.
+        // Lanes 0 and 1 locate the starts of this CTA's range and the next's.
+        const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), sc.cost));
+        if (warp == 0 && lane < 2) {
+            const CostPos c = static_cast<int>(blockIdx.x) < G
+                                  ? cost_start(p, sc, blockIdx.x + lane, G)
+                                  : CostPos{0, 0, 0, 0};
+            sm.info[2 + 4 * lane] = c.x;
+            sm.info[3 + 4 * lane] = c.b;
+            sm.info[4 + 4 * lane] = c.seg;
+            sm.info[5 + 4 * lane] = c.uu;
+        }
+        __syncthreads();
+        sc.pos0 = sm.info[2];
+        sc.b0 = sm.info[3];
+        sc.seg0 = sm.info[4];
+        sc.uu0 = sm.info[5];
+        sc.stop0 = sm.info[6];
+    }
     return sc;
 }
 
@@ -744,21 +779,26 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
     TileIter cur, ahead;
     cur.start(p, sc);
     ahead = cur;
-    for (int k = 0; k < kTableAhead; ++k) {
-        fetch_entries(p, ahead, entries + (k % kTableSlots) * kSlotInts, lane);
-        if (ahead.valid())
-            ahead.next(p, sc);
-    }
+    // tile 0's entries first: its boxes go out before the rest of the
+    // look-ahead window is fetched (tiles 1 .. kTableAhead, after its issue)
+    fetch_entries(p, ahead, entries, lane);
+    if (ahead.valid())
+        ahead.next(p, sc);
     const int HB = p.box_rows;
     uint32_t gt = 0;  // tiles issued by this CTA
     int s = 0;        // ring slot of tile gt
     uint32_t ph = 0;  // completed passes over the ring
     int piece = -1;   // pieces begun by this CTA
     for (; cur.valid(); cur.next(p, sc), ++gt) {
-        fetch_entries(p, ahead, entries + ((gt + kTableAhead) % kTableSlots) * kSlotInts, lane);
-        if (ahead.valid())
-            ahead.next(p, sc);
-        asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
+        if (gt == 0) {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        } else {
+            // one group per tile: tile gt's group is the oldest of kTableAhead + 1
+            fetch_entries(p, ahead, entries + ((gt + kTableAhead) % kTableSlots) * kSlotInts, lane);
+            if (ahead.valid())
+                ahead.next(p, sc);
+            asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
+        }
         if (ph > 0) {
             bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.empty[s], (ph - 1) & 1, kWaitLimitNs);
             ok = __all_sync(kFull, ok);
@@ -831,6 +871,12 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
             s = 0;
             ++ph;
         }
+        if (gt == 0)
+            for (int k = 1; k <= kTableAhead; ++k) {
+                fetch_entries(p, ahead, entries + (k % kTableSlots) * kSlotInts, lane);
+                if (ahead.valid())
+                    ahead.next(p, sc);
+            }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     // Leave no copy in flight if the pipeline was abandoned (a stage whose
@@ -865,10 +911,10 @@ __device__ __forceinline__ int count_piece(int* counter)
 // other CTAs are read through L2 (ld.global.cg).
 template <int D, typename TO>
 __device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 seg, float2* tot,
-                              float* fac, int fac_cap)
+                              float* fac, int fac_cap, int t0, int kT, int bar_id)
 {
-    constexpr int kT = kConsumerWarps * 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x - t0, warp = tid >> 5, lane = tid & 31;
+    const int nwarps = kT >> 5;
     struct {
         int b, rsg, kh;
     } it{seg.x, seg.y, seg.z};
@@ -876,44 +922,14 @@ __device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 
     const SegPieces sp = seg_pieces(p, sc, it.b, it.rsg, it.kh);
     const int n = sp.n;
     const bool fac_smem = n * R_cta <= fac_cap;
-    // (M, L) of each row: warp w takes rows w, w + 8, ...; lanes split the records
-    for (int rl = warp; rl < R_cta; rl += kConsumerWarps) {
-        float2 first = make_float2(-FLT_MAX, 0.f);
-        float M = -FLT_MAX;
-        for (int c = lane; c < n; c += 32) {
-            const float2 ml = __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]);
-            if (c == lane)
-                first = ml;
-            M = fmaxf(M, ml.x);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float L = 0.f;
-        for (int c = lane; c < n; c += 32) {
-            const float2 ml = c == lane ? first
-                                        : __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) *
-                                                              p.row_stride + rl]);
-            const float f = fast_exp2(ml.x - M);
-            L = fmaf(ml.y, f, L);
-            if (fac_smem)
-                fac[c * R_cta + rl] = f;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            L += __shfl_xor_sync(kFull, L, o);
-        if (lane == 0)
-            tot[rl] = make_float2(M, L);
-    }
-    consumer_bar_sync();
-    // O: items of 4 columns of one row (at most 32 rows x D/4 = 1024 items,
-    // four per thread); TPI adjacent lanes split the records of an item when
-    // the items are few.  A thread keeps the loads of all its items for two
-    // records in flight.
+    // O is computed in items of 4 columns of one row (at most 4 per thread);
+    // TPI adjacent lanes split the records of an item when the items are
+    // few.  TPI depends on the item count only, so the sums are formed in the
+    // same order whether a whole or a half CTA merges the segment.
     constexpr int D4 = D / 4;
     constexpr int LG4 = D4 == 16 ? 4 : 5;
     const int NI = R_cta * D4;
-    int TPI = kT / NI;
+    int TPI = (kConsumerWarps * 32) / NI;
     TPI = TPI >= 8 ? 8 : TPI >= 4 ? 4 : TPI >= 2 ? 2 : 1;
     const int per_pass = kT / TPI;
     const int sub = tid % TPI, i0 = tid / TPI;
@@ -927,66 +943,125 @@ __device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 
         act[j] = item < NI;
         rl_of[j] = act[j] ? item >> LG4 : 0;
     }
-    auto add_record = [&](int c, float4* v, float* f) {
-        const size_t rec = seg_record(p, sp, c, it.rsg, it.kh);
+    // (M, L) of each row: warp w takes rows w, w + nwarps, ...; lanes split
+    // the records.  With at most 32 records, four rows' loads are in flight.
+    if (n <= 32) {
+        for (int rl0 = warp; rl0 < R_cta; rl0 += 4 * nwarps) {
+            float2 ml[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (!act[j])
-                continue;
-            const int item = i0 + j * per_pass;
-            const size_t wrow = rec * p.row_stride + rl_of[j];
-            v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + (item & (D4 - 1)));
-            f[j] = fac_smem ? fac[c * R_cta + rl_of[j]]
-                            : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - tot[rl_of[j]].x);
+            for (int i = 0; i < 4; ++i) {
+                const int rl = rl0 + i * nwarps;
+                ml[i] = rl < R_cta && lane < n
+                            ? __ldcg(&p.ws_ml[seg_record(p, sp, lane, it.rsg, it.kh) * p.row_stride + rl])
+                            : make_float2(-FLT_MAX, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rl = rl0 + i * nwarps;
+                float M = ml[i].x;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+                const float f = lane < n ? fast_exp2(ml[i].x - M) : 0.f;
+                float L = ml[i].y * f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    L += __shfl_xor_sync(kFull, L, o);
+                if (rl < R_cta) {
+                    if (fac_smem && lane < n)
+                        fac[lane * R_cta + rl] = f;
+                    if (lane == 0)
+                        tot[rl] = make_float2(M, L);
+                }
+            }
         }
-    };
+    } else {
+        for (int rl = warp; rl < R_cta; rl += nwarps) {
+            float M = -FLT_MAX;
+            for (int c = lane; c < n; c += 32)
+                M = fmaxf(M, __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]).x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+            float L = 0.f;
+            for (int c = lane; c < n; c += 32) {
+                const float2 ml = __ldcg(&p.ws_ml[seg_record(p, sp, c, it.rsg, it.kh) * p.row_stride + rl]);
+                const float f = fast_exp2(ml.x - M);
+                L = fmaf(ml.y, f, L);
+                if (fac_smem)
+                    fac[c * R_cta + rl] = f;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                L += __shfl_xor_sync(kFull, L, o);
+            if (lane == 0)
+                tot[rl] = make_float2(M, L);
+        }
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kT) : "memory");
     auto fma4 = [](float4& a, float f, const float4& v) {
         a.x = fmaf(f, v.x, a.x);
         a.y = fmaf(f, v.y, a.y);
         a.z = fmaf(f, v.z, a.z);
         a.w = fmaf(f, v.w, a.w);
     };
-    int c = sub;
-    if (NI <= per_pass) {
-        // one item per thread: eight records in flight
-        const int rl = rl_of[0];
-        const int d4 = (i0 & (D4 - 1));
-        for (; c + 7 * TPI < n; c += 8 * TPI) {
-            float4 v[8];
-            float f[8];
+    {
+        auto add_record = [&](int c, float4* v, float* f) {
+            const size_t rec = seg_record(p, sp, c, it.rsg, it.kh);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const size_t wrow = seg_record(p, sp, c + u * TPI, it.rsg, it.kh) * p.row_stride + rl;
-                v[u] = act[0] ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                f[u] = fac_smem ? fac[(c + u * TPI) * R_cta + rl]
-                                : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - tot[rl].x);
+            for (int j = 0; j < 4; ++j) {
+                if (!act[j])
+                    continue;
+                const int item = i0 + j * per_pass;
+                const size_t wrow = rec * p.row_stride + rl_of[j];
+                v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + (item & (D4 - 1)));
+                f[j] = fac_smem ? fac[c * R_cta + rl_of[j]]
+                                : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - tot[rl_of[j]].x);
             }
+        };
+        int c = sub;
+        if (NI <= per_pass) {
+            // one item per thread: eight records in flight
+            const int rl = rl_of[0];
+            const int d4 = i0 & (D4 - 1);
+            for (; c + 7 * TPI < n; c += 8 * TPI) {
+                float4 v[8];
+                float f[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                fma4(O[0], f[u], v[u]);
+                for (int u = 0; u < 8; ++u) {
+                    const size_t wrow = seg_record(p, sp, c + u * TPI, it.rsg, it.kh) * p.row_stride + rl;
+                    v[u] = act[0] ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    f[u] = fac_smem ? fac[(c + u * TPI) * R_cta + rl]
+                                    : fast_exp2(__ldcg(&p.ws_ml[wrow]).x - tot[rl].x);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    fma4(O[0], f[u], v[u]);
+            }
         }
-    }
-    for (; c + TPI < n; c += 2 * TPI) {
-        float4 va[4], vb[4];
-        float fa[4], fb[4];
-        add_record(c, va, fa);
-        add_record(c + TPI, vb, fb);
+        // items of up to four rows per thread: two records in flight per item
+        for (; c + TPI < n; c += 2 * TPI) {
+            float4 va[4], vb[4];
+            float fa[4], fb[4];
+            add_record(c, va, fa);
+            add_record(c + TPI, vb, fb);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (act[j]) {
-                fma4(O[j], fa[j], va[j]);
-                fma4(O[j], fb[j], vb[j]);
-            }
-    }
-    if (c < n) {
-        float4 va[4];
-        float fa[4];
-        add_record(c, va, fa);
+            for (int j = 0; j < 4; ++j)
+                if (act[j]) {
+                    fma4(O[j], fa[j], va[j]);
+                    fma4(O[j], fb[j], vb[j]);
+                }
+        }
+        if (c < n) {
+            float4 va[4];
+            float fa[4];
+            add_record(c, va, fa);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (act[j])
-                fma4(O[j], fa[j], va[j]);
+            for (int j = 0; j < 4; ++j)
+                if (act[j])
+                    fma4(O[j], fa[j], va[j]);
+        }
     }
     const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta;
 #pragma unroll
@@ -1021,7 +1096,7 @@ constexpr int kSplitList = 32;  // list capacity (the automatic schedule needs t
 // call.  Counting at the end keeps merges out of the CTA's stream.
 template <int D, typename TO>
 __device__ void flush_split_pieces(const SplitParams& p, const Sched& sc, int4* list, int n, float2* tot,
-                                   float* fac, int fac_cap)
+                                   int tot_cap, float* fac, int fac_cap)
 {
     const int tid = threadIdx.x;
     consumer_bar_sync();  // every thread's record stores (and the list) precede the counts
@@ -1036,12 +1111,29 @@ __device__ void flush_split_pieces(const SplitParams& p, const Sched& sc, int4* 
         list[tid] = e;
     }
     consumer_bar_sync();
-    for (int i = 0; i < n; ++i) {
-        const int4 e = list[i];
-        if (e.w) {
-            merge_segment<D, TO>(p, sc, e, tot, fac, fac_cap);
-            consumer_bar_sync();  // `tot` and `fac` are free again
-        }
+    // Segments to merge go two at a time, one per half of the consumer warps
+    // (named barriers 2 and 3), when each fits four items per thread of a half.
+    constexpr int kHalf = kConsumerWarps * 16;
+    auto fits_half = [&](int4 e) {
+        const int R_cta = min(p.rows_per_cta, p.R - e.y * p.rows_per_cta);
+        return R_cta * (D / 4) <= 4 * kHalf && 2 * p.rows_per_cta <= tot_cap;
+    };
+    int i = 0;
+    while (true) {
+        while (i < n && !list[i].w)
+            ++i;
+        if (i == n)
+            break;
+        int j = i + 1;
+        while (j < n && !list[j].w)
+            ++j;
+        const bool pair = j < n && fits_half(list[i]) && fits_half(list[j]);
+        const bool upper = pair && tid >= kHalf;
+        merge_segment<D, TO>(p, sc, list[upper ? j : i], tot + (upper ? p.rows_per_cta : 0),
+                             fac + (upper ? fac_cap / 2 : 0), pair ? fac_cap / 2 : fac_cap,
+                             upper ? kHalf : 0, pair ? kHalf : 2 * kHalf, pair ? (upper ? 3 : 2) : 1);
+        i = pair ? j + 1 : i + 1;
+        consumer_bar_sync();  // `tot` and `fac` are free again
     }
 }
 
@@ -1158,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // uniform over the consumer warps (a late abort flag must not split them)
     if (nsplit > 0 && !consumer_bar_or(*sm.abort_flag != 0))
-        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, merge_tot, mb_o,
+        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, merge_tot, p.rows_per_cta, mb_o,
                                   kConsumerWarps * RG * D);
 }
 
@@ -1556,7 +1648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // uniform over the consumer warps (a late abort flag must not split them)
     if (nsplit > 0 && !consumer_bar_or(*sm.abort_flag != 0))
-        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, tot, obuf, kObufFloats);
+        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, tot, 2 * ROWS, obuf, kObufFloats);
 }
 
 // -------------------------------------------------------------- merge kernel
@@ -1581,11 +1673,10 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
     if (p.stream) {
         const int2 last = p.sched[p.B - 1];
         const long long W = static_cast<long long>(last.x) + static_cast<long long>(last.y) * U;
-        const long long C = W + static_cast<long long>(p.vunits) * p.B * U;
-        const long long G = min(static_cast<long long>(p.grid), C);
+        const int C = static_cast<int>(W + static_cast<long long>(p.vunits) * p.B * U);
+        const int G = min(p.grid, C);
         const int gl = rsg * p.KV + kh;
-        const SegSpan ss = seg_span(sc.x + static_cast<long long>(gl) * sc.y, sc.y,
-                                    static_cast<long long>(b) * U + gl, p.vunits, C, G);
+        const SegSpan ss = seg_span(sc.x + gl * sc.y, sc.y, b * U + gl, p.vunits, C, G);
         k0 = ss.k0;
         n = ss.n;
         rec_first = ss.rec_first;
