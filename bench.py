@@ -5,7 +5,8 @@
 One step = one decode call over one batch of the Llama-style GQA workload
 (B=8 sequences, H=32, KV=8, D=128, BLOCK=16, fp16, past lengths uniform in
 [512, 4096], blocks randomly permuted in a shared pool, NQ=1): the partition
-kernel plus the log-sum-exp merge kernel.  The metric is decode-attention
+kernel, whose last CTA on each split segment also merges its partial states
+(the automatic split; fixed partitions add the log-sum-exp merge kernel).  The metric is decode-attention
 throughput in GB/s of algorithmic bytes (every visible K and V row once, q,
 the output, the table entries and lengths) divided by device time, with the
 fraction of the measured HBM copy bandwidth.
@@ -88,6 +89,35 @@ def reduce_max(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+
+    files = sorted((ROOT / "paged_kv_cache_182_gb300" / "csrc").glob("*.cu*"))
+    files.append(ROOT / "include" / "pa_decode.h")
+    h = hashlib.sha256()
+    for f in files:
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel sources changed since."""
+    path = ROOT / "profiles" / f"{kernel}_{workload}.md"
+    if not path.exists():
+        return None
+    fields = {}
+    for line in path.read_text().splitlines():
+        key, sep, val = line.strip().partition(": ")
+        if sep and key in ("csrc_sha256", "traffic_bytes_per_launch"):
+            fields[key] = val.strip()
+    if fields.get("csrc_sha256") != kernel_sources_sha256():
+        return None
+    v = fields.get("traffic_bytes_per_launch")
+    return int(v) if v else None
 
 
 def measured_peaks():
@@ -310,6 +340,8 @@ def run_ours(args, rank, world, local):
     ms_max = reduce_max(ms, world)
     value = world * per_rank_bytes / (ms_max * 1e-3) / 1e9
     achieved = per_rank_bytes / (split_ms * 1e-3) / 1e9
+    kernel = "pa_split_kernel" if w.spec.dtype == "f32" else "pa_mma_kernel"
+    traffic = captured_traffic(kernel, w.spec.name)
     del plans
     torch.cuda.empty_cache()
     e2e_ms, h2d, d2h = e2e_steps(w, device, max(20, args.steps // 4), 3)
@@ -328,8 +360,9 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"independent batches x{world}"},
         "tokens_per_s": round(world * w.spec.B * w.spec.NQ / (ms_max * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "pa_split_kernel", "peak_kind": peak_kind},
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": kernel, "peak_kind": peak_kind,
+                     "algorithmic_bytes": per_rank_bytes},
         "e2e": {"value": round(world * per_rank_bytes / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
