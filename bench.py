@@ -79,16 +79,33 @@ def barrier(world):
         dist.barrier()
 
 
-def reduce_max(x: float, world: int) -> float:
-    """Largest value over ranks (the slowest rank's time)."""
+def _all_reduce(x: float, world: int, op: str) -> float:
     if world == 1:
         return x
     import torch.distributed as dist
 
     dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
     t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Largest value over ranks (the slowest rank's time)."""
+    return _all_reduce(x, world, "max")
+
+
+def reduce_sum(x: float, world: int) -> float:
+    """Sum over ranks (the bytes of all ranks' batches)."""
+    return _all_reduce(x, world, "sum")
+
+
+def aggregate(rank_bytes: int, rank_ms: float, world: int):
+    """Weak scaling: every rank runs its own batch.  Returns (GB/s of all
+    ranks' bytes over the slowest rank's time, that time in ms, total bytes)."""
+    ms_max = reduce_max(rank_ms, world)
+    total = reduce_sum(float(rank_bytes), world)
+    return total / (ms_max * 1e-3) / 1e9, ms_max, int(total)
 
 
 def kernel_sources_sha256() -> str:
@@ -337,15 +354,14 @@ def run_ours(args, rank, world, local):
     plans_n = list(range(len(plans)))
     with Clocks(local) as clk:
         ms, split_ms, launches = time_steps(plans, args.steps, args.warmup, world)
-    ms_max = reduce_max(ms, world)
-    value = world * per_rank_bytes / (ms_max * 1e-3) / 1e9
+    value, ms_max, total_bytes = aggregate(per_rank_bytes, ms, world)
     achieved = per_rank_bytes / (split_ms * 1e-3) / 1e9
     kernel = "pa_split_kernel" if w.spec.dtype == "f32" else "pa_mma_kernel"
     traffic = captured_traffic(kernel, w.spec.name)
     del plans
     torch.cuda.empty_cache()
     e2e_ms, h2d, d2h = e2e_steps(w, device, max(20, args.steps // 4), 3)
-    e2e_ms = reduce_max(e2e_ms, world)
+    e2e_value, e2e_ms, _ = aggregate(per_rank_bytes, e2e_ms, world)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
@@ -355,15 +371,16 @@ def run_ours(args, rank, world, local):
                    "D": w.spec.D, "BLOCK": w.spec.BLOCK, "NQ": w.spec.NQ,
                    "causal": w.spec.causal, "partitions": w.spec.partitions or "auto",
                    "seq_lens": w.seq_lens.tolist(), "bytes_per_step": per_rank_bytes,
+                   "bytes_per_step_all_ranks": total_bytes,
                    "l2": f"inputs larger than L2: {len(plans_n)} copies of the KV pools "
                          f"({pool_bytes // 2**20} MiB) rotated step by step",
                    "parallelism": f"independent batches x{world}"},
-        "tokens_per_s": round(world * w.spec.B * w.spec.NQ / (ms_max * 1e-3), 1),
+        "tokens_per_s": round(reduce_sum(w.spec.B * w.spec.NQ, world) / (ms_max * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel, "peak_kind": peak_kind,
                      "algorithmic_bytes": per_rank_bytes},
-        "e2e": {"value": round(world * per_rank_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+        "e2e": {"value": round(e2e_value, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
