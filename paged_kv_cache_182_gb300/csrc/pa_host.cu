@@ -560,7 +560,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         cp.vunits = vunits;
         const CombineFn comb = pick_combine(out_dtype, D);
         cudaLaunchConfig_t cc{};
-        cc.gridDim = dim3(static_cast<unsigned>(B) * KV * NRS);
+        cc.gridDim = dim3(static_cast<unsigned>(B) * KV * NRS, static_cast<unsigned>(row_stride));
         cc.blockDim = dim3(128);
         cc.dynamicSmemBytes = 0;
         cc.stream = st;

@@ -1652,22 +1652,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------- merge kernel
-// One CTA per segment (sequence, row group, KV head); one warp per query row;
-// lanes split D.  It finds the partial records of the segment (automatic mode:
-// the CTAs whose unit ranges overlap the segment; fixed partitions: the
-// segment's items) and merges them: M = max m, L = sum l 2^(m - M),
-// O = sum o 2^(m - M), out = L == 0 ? O : O / L.  Whole segments were
-// finished by the partition kernel and are skipped.
+// One CTA of 128 threads per (segment = sequence, row group, KV head; row).
+// It finds the partial records of the segment (automatic mode: the CTAs whose
+// unit ranges overlap the segment; fixed partitions: the segment's items) and
+// merges them: M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
+// out = L == 0 ? O : O / L.  The accumulator loads of up to eight records per
+// thread are issued before the (max, sum) loads, so a merge of up to 32
+// (D = 128) or 64 (D = 64) records costs about one L2 round trip.  Whole
+// segments were finished by the partition kernel and are skipped.
+constexpr int kCombineFac = 1024;  // records whose factors are kept in shared memory
+
 template <int D, typename TO>
 __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__ CombineParams p)
 {
     grid_dependency_wait();
     grid_dependents_launch();
-    const int idx = blockIdx.x;
+    const int idx = blockIdx.x, rl = blockIdx.y;
     const int kh = idx % p.KV;
     const int rsg = (idx / p.KV) % p.NRS;
     const int b = idx / (p.KV * p.NRS);
     const int U = p.NRS * p.KV;
+    const int R_cta = min(p.rows_per_cta, p.R - rsg * p.rows_per_cta);
+    if (rl >= R_cta)
+        return;
     const int2 sc = p.sched[b];
     int n, k0 = 0, rec_first = 0;
     if (p.stream) {
@@ -1685,49 +1692,102 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
     }
     if (n <= 1)
         return;
-    // record of piece c (c = 0 .. n-1)
-    auto rec_of = [&](int c) -> size_t {
-        if (p.stream)
-            return c == 0 ? static_cast<size_t>(rec_first) : static_cast<size_t>(2 * (k0 + c));
-        return (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
+    auto row_of = [&](int c) -> size_t {  // workspace row of record c
+        const size_t rec = p.stream ? (c == 0 ? static_cast<size_t>(rec_first)
+                                              : static_cast<size_t>(2 * (k0 + c)))
+                                    : (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
+        return rec * p.row_stride + rl;
     };
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int R_cta = min(p.rows_per_cta, p.R - rsg * p.rows_per_cta);
-    constexpr int PER = D / 32;
-    for (int rl = warp; rl < R_cta; rl += 4) {
-        float M = -FLT_MAX;
-        for (int c = lane; c < n; c += 32)
-            M = fmaxf(M, p.ws_ml[rec_of(c) * p.row_stride + rl].x);
+    __shared__ float fac[kCombineFac];
+    __shared__ float red[4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int D4 = D / 4;
+    constexpr int TPI = 128 / D4;  // threads per 4-column item
+    const int d4 = tid / TPI, sub = tid % TPI;
+    float4 v[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float L = 0.f;
-        for (int c = lane; c < n; c += 32) {
-            const float2 ml = p.ws_ml[rec_of(c) * p.row_stride + rl];
-            L = fmaf(ml.y, fast_exp2(ml.x - M), L);
+    for (int u = 0; u < 8; ++u) {
+        const int c = sub + u * TPI;
+        if (c < n)
+            v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + row_of(c) * D) + d4);
+    }
+    // M and L over the records (threads split them; block reductions)
+    float2 first = make_float2(-FLT_MAX, 0.f);
+    float M = -FLT_MAX;
+    for (int c = tid; c < n; c += 128) {
+        const float2 ml = __ldcg(&p.ws_ml[row_of(c)]);
+        if (c == tid)
+            first = ml;
+        M = fmaxf(M, ml.x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (lane == 0)
+        red[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    float L = 0.f;
+    for (int c = tid; c < n; c += 128) {
+        const float2 ml = c == tid ? first : __ldcg(&p.ws_ml[row_of(c)]);
+        const float f = fast_exp2(ml.x - M);
+        L = fmaf(ml.y, f, L);
+        if (c < kCombineFac)
+            fac[c] = f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        L += __shfl_xor_sync(kFull, L, o);
+    if (lane == 0)
+        red[warp] = L;
+    __syncthreads();
+    L = (red[0] + red[1]) + (red[2] + red[3]);
+    auto factor = [&](int c) {
+        return c < kCombineFac ? fac[c] : fast_exp2(__ldcg(&p.ws_ml[row_of(c)]).x - M);
+    };
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto fma4 = [&](float f, const float4& x) {
+        O.x = fmaf(f, x.x, O.x);
+        O.y = fmaf(f, x.y, O.y);
+        O.z = fmaf(f, x.z, O.z);
+        O.w = fmaf(f, x.w, O.w);
+    };
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int c = sub + u * TPI;
+        if (c < n)
+            fma4(factor(c), v[u]);
+    }
+    for (int c0 = sub + 8 * TPI; c0 < n; c0 += 8 * TPI) {  // more than 8 records per thread
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * TPI;
+            if (c < n)
+                v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + row_of(c) * D) + d4);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            L += __shfl_xor_sync(kFull, L, o);
-        float O[PER];
-#pragma unroll
-        for (int k = 0; k < PER; ++k)
-            O[k] = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < n; ++c) {
-            const size_t wrow = rec_of(c) * p.row_stride + rl;
-            const float f = fast_exp2(p.ws_ml[wrow].x - M);
-#pragma unroll
-            for (int k = 0; k < PER; ++k)
-                O[k] = fmaf(f, p.ws_o[wrow * D + lane + 32 * k], O[k]);
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * TPI;
+            if (c < n)
+                fma4(factor(c), v[u]);
         }
-        const size_t orow =
-            (static_cast<size_t>(b) * p.KV + kh) * p.R + rsg * p.rows_per_cta + rl;
+    }
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const float val = L == 0.f ? O[k] : O[k] / L;
-            static_cast<TO*>(p.out)[orow * D + lane + 32 * k] = from_float<TO>(val);
-        }
+    for (int o = 1; o < TPI; o <<= 1) {
+        O.x += __shfl_xor_sync(kFull, O.x, o);
+        O.y += __shfl_xor_sync(kFull, O.y, o);
+        O.z += __shfl_xor_sync(kFull, O.z, o);
+        O.w += __shfl_xor_sync(kFull, O.w, o);
+    }
+    if (sub == 0) {
+        const float inv = L == 0.f ? 1.f : 1.f / L;
+        const size_t orow = (static_cast<size_t>(b) * p.KV + kh) * p.R + rsg * p.rows_per_cta + rl;
+        TO* dst = static_cast<TO*>(p.out) + orow * D + 4 * d4;
+        dst[0] = from_float<TO>(O.x * inv);
+        dst[1] = from_float<TO>(O.y * inv);
+        dst[2] = from_float<TO>(O.z * inv);
+        dst[3] = from_float<TO>(O.w * inv);
     }
 }
 
