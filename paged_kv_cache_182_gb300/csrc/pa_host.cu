@@ -383,11 +383,16 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         return PA_ERR_BAD_DIMS;
     // the automatic schedule counts BLOCK-token units of all segments in int32
     const int es = static_cast<int>(elem_size(dtype));
-    // automatic schedule: a piece costs about as much as streaming kPieceBytes
-    // more (the merge of the consumer warps' states, the partial last stage),
-    // so each segment is charged that many virtual units when units are dealt
-    const int unit_bytes = 2 * BLOCK * D * es;
-    const int vunits = (kPieceBytes + unit_bytes / 2) / unit_bytes;
+    // tensor-core path: up to 64 KB stages, at most 8 warps (16-token groups x
+    // row groups) per stage: 128 tokens (64 with 32 rows per pass)
+    int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
+    if (mma && (TT / kMmaTokens) * MT > kConsumerWarps)
+        TT = kConsumerWarps / MT * kMmaTokens;
+    // automatic schedule: units of one stage.  Each segment is charged the
+    // measured cost of a piece in stages (the consumer warps' merge and the
+    // start of the next piece): about two, six with two row groups per pass
+    // (four merge rounds)
+    const int vunits = MT > 1 ? kPieceStages2 : kPieceStages;
     const long long units = static_cast<long long>(B) *
                             (opts->max_blocks + 1 + NQ / BLOCK + 1 + vunits) * NRS * KV;
     if (partitions == 0 && units >= (1ll << 31))
@@ -401,11 +406,6 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
             return PA_ERR_ALIGNMENT;
     }
 
-    // tensor-core path: up to 64 KB stages, at most 8 warps (16-token groups x
-    // row groups) per stage: 128 tokens (64 with 32 rows per pass)
-    int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
-    if (mma && (TT / kMmaTokens) * MT > kConsumerWarps)
-        TT = kConsumerWarps / MT * kMmaTokens;
     // one TMA box per cache block (per tile when a block spans several tiles):
     // the issue cost of a box is fixed, so fewer, larger boxes stream faster
     const int box_rows = mma ? (BLOCK < TT ? BLOCK : TT) : BLOCK;

@@ -111,13 +111,13 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x)
 // one CTA processes; `whole` pieces write the normalised output, the others a
 // partial (max, sum, accumulator) record `rec` of the workspace.
 //
-// Automatic mode (partitions == 0): the segments, cut into BLOCK-token units,
-// are laid end to end (sequence, then row group, then KV head) and CTA k takes
-// units [k*W/G, (k+1)*W/G) of the W units (G = min(CTAs, W), so no range is
-// empty) -- every CTA streams the same number
-// of cache blocks whatever the length mix, and only the pieces cut at CTA
-// boundaries need merging (records 2k and 2k+1: the CTA's first and last
-// piece).
+// Automatic mode (partitions == 0): the segments, cut into units of one
+// pipeline stage (TT tokens), are laid end to end (sequence, then row group,
+// then KV head) and each persistent CTA takes a contiguous range of units
+// (cost-balanced, below).  A stage costs about the same whether full or not, so
+// CTA boundaries fall on stage boundaries and only a segment's last stage is
+// partial.  Only the pieces cut at CTA boundaries need merging (records 2k and
+// 2k+1: the CTA's first and last piece).
 // Fixed partitions (P >= 1): each segment is split into P ranges of whole
 // blocks (P == 1: no split); the ranges are items dealt to CTAs round-robin;
 // record = item index.
@@ -198,7 +198,7 @@ __device__ __forceinline__ void build_schedule(const SplitParams& p, const int* 
         int n = 0;
         if (b < p.B) {
             const int total = lens[b] + p.NQ;
-            const int chunk = stream ? p.BLOCK : chunk_of(p, total);
+            const int chunk = stream ? p.TT : chunk_of(p, total);
             n = (total + chunk - 1) / chunk;
         }
         const int w = stream ? n * U : n;
@@ -257,7 +257,7 @@ __device__ __forceinline__ CostPos cost_start(const SplitParams& p, const Sched&
         else
             hi = mid - 1;
     }
-    const int nb = (sc.lens[lo] + p.NQ + p.BLOCK - 1) >> p.lg_block;
+    const int nb = (sc.lens[lo] + p.NQ + p.TT - 1) >> p.lg_tt;
     const int local = T - (sc.prefix[lo] + VU * lo);
     const int per = nb + p.vunits;
     const int s = local / per;
@@ -285,12 +285,12 @@ struct PieceIter {
             if (!ok)
                 return;
             const int b = sc.b0, seg = sc.seg0, uu = sc.uu0;
-            seg_units = (sc.lens[b] + p.NQ + p.BLOCK - 1) >> p.lg_block;
+            seg_units = (sc.lens[b] + p.NQ + p.TT - 1) >> p.lg_tt;
             it.b = b;
             it.rsg = seg / p.KV;
             it.kh = seg - it.rsg * p.KV;
             it.past = sc.lens[b];
-            it.start = uu << p.lg_block;
+            it.start = uu << p.lg_tt;
             set_len(p, seg_units - uu, uu == 0);
             it.rec = 2 * blockIdx.x;
         } else {
@@ -313,7 +313,7 @@ struct PieceIter {
                     it.rsg = 0;
                     ++it.b;
                     it.past = sc.lens[it.b];
-                    seg_units = (it.past + p.NQ + p.BLOCK - 1) >> p.lg_block;
+                    seg_units = (it.past + p.NQ + p.TT - 1) >> p.lg_tt;
                 }
             }
             it.start = 0;
@@ -329,7 +329,7 @@ struct PieceIter {
     __device__ __forceinline__ void set_len(const SplitParams& p, int left, bool at_start)
     {
         const int len = static_cast<int>(min(static_cast<long long>(left), stop - pos));
-        it.end = min(it.start + (len << p.lg_block), it.past + p.NQ);
+        it.end = min(it.start + (len << p.lg_tt), it.past + p.NQ);
         it.whole = at_start && len == seg_units;
         it.units = len;
     }
@@ -375,7 +375,7 @@ __device__ __forceinline__ SegPieces seg_pieces(const SplitParams& p, const Sche
     if (p.partitions == 0) {
         const int C = static_cast<int>(sc.cost);
         const int G = min(static_cast<int>(gridDim.x), C);
-        const int units = (sc.lens[b] + p.NQ + p.BLOCK - 1) >> p.lg_block;
+        const int units = (sc.lens[b] + p.NQ + p.TT - 1) >> p.lg_tt;
         const int gl = rsg * p.KV + kh;
         const SegSpan ss = seg_span(sc.prefix[b] + gl * units, units, b * p.NRS * p.KV + gl, p.vunits, C, G);
         sp.k0 = ss.k0;
