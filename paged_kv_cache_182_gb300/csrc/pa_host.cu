@@ -381,18 +381,22 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     const long long records = record_bound(B, KV, NRS, partitions);
     if (records >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
-    // the automatic schedule counts BLOCK-token units of all segments in int32
     const int es = static_cast<int>(elem_size(dtype));
-    // tensor-core path: up to 64 KB stages, at most 8 warps (16-token groups x
-    // row groups) per stage: 128 tokens (64 with 32 rows per pass)
+    // tensor-core path: up to 64 KB stages, at most 8 warps (TPW tokens x row
+    // groups) per stage: 128 tokens at D = 128 (64 with 32 rows per pass), 256
+    // at D = 64 (128); at most 16 cache blocks per stage
     int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
-    if (mma && (TT / kMmaTokens) * MT > kConsumerWarps)
-        TT = kConsumerWarps / MT * kMmaTokens;
+    const int TPW = kMmaTokens * mma_token_groups(D);  // tokens per consumer warp and stage
+    if (mma && (TT / TPW) * MT > kConsumerWarps)
+        TT = kConsumerWarps / MT * TPW;
+    if (mma && TT > 16 * BLOCK)  // at most 16 boxes (one per block) per stage and role
+        TT = 16 * BLOCK;
     // automatic schedule: units of one stage.  Each segment is charged the
     // measured cost of a piece in stages (the consumer warps' merge and the
     // start of the next piece): about two, six with two row groups per pass
     // (four merge rounds)
     const int vunits = MT > 1 ? kPieceStages2 : kPieceStages;
+    // (the units of all segments are counted in int32)
     const long long units = static_cast<long long>(B) *
                             (opts->max_blocks + 1 + NQ / BLOCK + 1 + vunits) * NRS * KV;
     if (partitions == 0 && units >= (1ll << 31))
@@ -497,7 +501,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         grid = records;
     p.qbuf_off = qbuf_off;
     p.box_rows = box_rows;
-    p.empty_count = mma ? (TT / kMmaTokens) * MT : kConsumerWarps;
+    p.empty_count = mma ? (TT / TPW) * MT : kConsumerWarps;
     p.checked = opts->checked ? 1 : 0;
     p.R = R;
     p.rows_per_cta = rows_per_cta;

@@ -1344,6 +1344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NT = D / 8;   // 8-column tiles of O
     constexpr int ROWS = 16 * MT;
     constexpr int TS = kConsumerWarps / MT;  // warps per row group
+    constexpr int TG = mma_token_groups(D);  // 16-token groups per warp and stage
+    constexpr int TPW = kMmaTokens * TG;     // tokens per warp and stage
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const Smem sm = carve(p, smem_raw);
@@ -1369,13 +1371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int g = lane >> 2, qd = lane & 3;
     const int rg = warp % MT, ts = warp / MT;
-    // A stage of TT tokens is consumed by a set of WS = (TT/16)*MT warps (one
-    // per 16-token group and row group); the nsets sets take stages in turn.
+    // A stage of TT tokens is consumed by a set of WS = (TT/TPW)*MT warps (one
+    // per TPW tokens and row group); the nsets sets take stages in turn.
     const int TT = p.TT;
-    const int WS = (TT / kMmaTokens) * MT;
+    const int WS = (TT / TPW) * MT;
     const int nsets = kConsumerWarps / WS;
     const int my_set = warp / WS;
-    const int tb = ((warp % WS) / MT) * kMmaTokens;  // this warp's tokens in a stage
+    const int tb = ((warp % WS) / MT) * TPW;  // this warp's first token in a stage
     const uint32_t zero = smem_u32(sm.zero16);
     const uint32_t qbuf = smem_u32(sm.scratch + p.qbuf_off);
     uint32_t gt = 0;
@@ -1461,42 +1463,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&sm.empty[s]);
                 continue;
             }
-            // every token of this warp's group is visible to every row of the warp
-            const bool full_tile = tb + kMmaTokens <= n_tile && t0 + tb + kMmaTokens <= lim_min;
-
-            // ---- S = Q K^T (two accumulator sets per 8-token tile: shorter chains)
-            float sa[2][2][4];
+            // a group whose every token is visible to every row of the warp
+            bool full_tile[TG];
 #pragma unroll
-            for (int a = 0; a < 2; ++a)
+            for (int u = 0; u < TG; ++u) {
+                const int tu = tb + u * kMmaTokens;
+                full_tile[u] = tu + kMmaTokens <= n_tile && t0 + tu + kMmaTokens <= lim_min;
+            }
+
+            // ---- S = Q K^T (per group, two accumulator sets per 8-token tile:
+            // shorter chains; the groups' MMAs interleave)
+            float sa[TG][2][2][4];
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            sa[u][a][nt][e] = 0.f;
+            RowAddr kr[TG];
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
+                kr[u] = row_addr<D>(k_tile, k_new, zero,
+                                    tb + u * kMmaTokens + (lane & 7) + ((lane >> 4) << 3), n_tile,
+                                    t0, it.past);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int u = 0; u < TG; ++u) {
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4(kr[u].at(2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
+                    mma_16816<kBf>(sa[u][ks & 1][0], qa[ks], b00, b01);
+                    mma_16816<kBf>(sa[u][ks & 1][1], qa[ks], b10, b11);
+                }
+            // scale, mask, row maxima of the stage
+            float sv[TG][2][4];
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sa[a][nt][e] = 0.f;
-            const RowAddr kr = row_addr<D>(k_tile, k_new, zero,
-                                           tb + (lane & 7) + ((lane >> 4) << 3), n_tile, t0,
-                                           it.past);
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t b00, b01, b10, b11;
-                ldsm_x4(kr.at(2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
-                mma_16816<kBf>(sa[ks & 1][0], qa[ks], b00, b01);
-                mma_16816<kBf>(sa[ks & 1][1], qa[ks], b10, b11);
-            }
-            // scale, mask, row maxima of the stage
-            float sv[2][4];
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = e >> 1;
-                    const int tk = tb + nt * 8 + 2 * qd + (e & 1);
-                    const float v = (sa[0][nt][e] + sa[1][nt][e]) * p.qscale;
-                    const bool valid = full_tile || (tk < n_tile && t0 + tk < lim[h]);
-                    sv[nt][e] = valid ? v : -INFINITY;
-                    mx[h] = fmaxf(mx[h], sv[nt][e]);
-                }
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const int tk = tb + u * kMmaTokens + nt * 8 + 2 * qd + (e & 1);
+                        const float v = (sa[u][0][nt][e] + sa[u][1][nt][e]) * p.qscale;
+                        const bool valid = full_tile[u] || (tk < n_tile && t0 + tk < lim[h]);
+                        sv[u][nt][e] = valid ? v : -INFINITY;
+                        mx[h] = fmaxf(mx[h], sv[u][nt][e]);
+                    }
             bool grow = false;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -1520,29 +1537,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o[i][e] *= f[e >> 1];
             }
             // P as A fragments (high part and remainder)
-            uint32_t ahi[4], alo[4];
+            uint32_t ahi[TG][4], alo[TG][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int u = 0; u < TG; ++u)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float p0 = fast_exp2(sv[nt][2 * h] - m[h]);
-                    const float p1 = fast_exp2(sv[nt][2 * h + 1] - m[h]);
-                    lp[h] += p0 + p1;
-                    Pack<T>::split(p0, p1, ahi[2 * nt + h], alo[2 * nt + h]);
-                }
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float p0 = fast_exp2(sv[u][nt][2 * h] - m[h]);
+                        const float p1 = fast_exp2(sv[u][nt][2 * h + 1] - m[h]);
+                        lp[h] += p0 + p1;
+                        Pack<T>::split(p0, p1, ahi[u][2 * nt + h], alo[u][2 * nt + h]);
+                    }
             // ---- O += P V
-            const RowAddr vr = row_addr<D>(v_tile, v_new, zero,
-                                           tb + (lane & 7) + (((lane >> 3) & 1) << 3), n_tile, t0,
-                                           it.past);
+            RowAddr vr[TG];
 #pragma unroll
-            for (int pp = 0; pp < NT / 2; ++pp) {
-                uint32_t v00, v01, v10, v11;
-                ldsm_x4_t(vr.at(2 * pp + (lane >> 4)), v00, v01, v10, v11);
-                mma_16816<kBf>(o[2 * pp], ahi, v00, v01);
-                mma_16816<kBf>(o[2 * pp + 1], ahi, v10, v11);
-                mma_16816<kBf>(o[2 * pp], alo, v00, v01);
-                mma_16816<kBf>(o[2 * pp + 1], alo, v10, v11);
-            }
+            for (int u = 0; u < TG; ++u)
+                vr[u] = row_addr<D>(v_tile, v_new, zero,
+                                    tb + u * kMmaTokens + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                    n_tile, t0, it.past);
+#pragma unroll
+            for (int pp = 0; pp < NT / 2; ++pp)
+#pragma unroll
+                for (int u = 0; u < TG; ++u) {
+                    uint32_t v00, v01, v10, v11;
+                    ldsm_x4_t(vr[u].at(2 * pp + (lane >> 4)), v00, v01, v10, v11);
+                    mma_16816<kBf>(o[2 * pp], ahi[u], v00, v01);
+                    mma_16816<kBf>(o[2 * pp + 1], ahi[u], v10, v11);
+                    mma_16816<kBf>(o[2 * pp], alo[u], v00, v01);
+                    mma_16816<kBf>(o[2 * pp + 1], alo[u], v10, v11);
+                }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.empty[s]);
