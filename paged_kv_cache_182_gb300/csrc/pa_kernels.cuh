@@ -1370,7 +1370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     const int g = lane >> 2, qd = lane & 3;
-    const int rg = warp % MT, ts = warp / MT;
+    const int rg = warp % MT;
     // A stage of TT tokens is consumed by a set of WS = (TT/TPW)*MT warps (one
     // per TPW tokens and row group); the nsets sets take stages in turn.
     const int TT = p.TT;
@@ -1580,40 +1580,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
             mbar_arrive(&sm.q_free[piece & 1]);
 
-        // ---- piece end: merge the TS warps of each row group
+        // ---- piece end: merge the TS warps of each row group.  Each warp
+        // leaves its running (max, sum) and its unscaled accumulators in
+        // shared memory; the summing threads apply the factors 2^(m_t - M).
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             lp[h] += __shfl_xor_sync(kFull, lp[h], 1);
             lp[h] += __shfl_xor_sync(kFull, lp[h], 2);
         }
-        consumer_bar_sync();  // the previous piece's readers are done with the buffers
+        // the previous piece's readers are done with the buffers; uniform abort
+        if (consumer_bar_or(*sm.abort_flag != 0))
+            break;
         if (qd == 0) {
             ml_buf[warp * 16 + g] = make_float2(m[0], lp[0]);
             ml_buf[warp * 16 + g + 8] = make_float2(m[1], lp[1]);
-        }
-        if (consumer_bar_or(*sm.abort_flag != 0))
-            break;
-        // rescale to the group's common maximum; one thread per row records (M, L)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = g + 8 * h;
-            float Mr = -FLT_MAX;
-            for (int t = 0; t < TS; ++t)
-                Mr = fmaxf(Mr, ml_buf[(t * MT + rg) * 16 + r].x);
-            const float f = fast_exp2(m[h] - Mr);
-#pragma unroll
-            for (int i = 0; i < NT; ++i) {
-                o[i][2 * h] *= f;
-                o[i][2 * h + 1] *= f;
-            }
-            if (ts == 0 && qd == 0 && row0 + r < R_cta) {
-                float Lr = 0.f;
-                for (int t = 0; t < TS; ++t) {
-                    const float2 v = ml_buf[(t * MT + rg) * 16 + r];
-                    Lr = fmaf(v.y, fast_exp2(v.x - Mr), Lr);
-                }
-                tot[row0 + r] = make_float2(Mr, Lr);
-            }
         }
         const int rows_used = min(16, max(0, R_cta - row0));
         const size_t out_row0 =
@@ -1622,11 +1602,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Rounds of DRr columns: each warp writes its rows (at most RU) of the
         // round's columns to obuf, then all threads sum the TS warps of each
         // row.  With few rows per segment one round covers all D columns.
+        // Columns are XOR-swizzled by row (8 floats per row step) so that the
+        // rows a warp writes at once fall in different banks.
         const int RU = min(16, R_cta);
         int lg = 31 - __clz(D);  // log2 of the round width
         while (lg > 3 && kConsumerWarps * RU * (1 << lg) > kObufFloats)
             --lg;
         const int DRr = 1 << lg, TPR = DRr / 8, rounds = D >> lg;
+        const int swz_mask = DRr - 1;
         for (int r = 0; r < rounds; ++r) {
             if (r > 0)
                 consumer_bar_sync();  // readers of the previous round are done
@@ -1636,30 +1619,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 const int dd = (i - r * TPR) * 8 + 2 * qd;
                 if (g < rows_used)
-                    *reinterpret_cast<float2*>(&obuf[((warp * RU + g) << lg) + dd]) =
+                    *reinterpret_cast<float2*>(
+                        &obuf[((warp * RU + g) << lg) + ((dd ^ ((g & 3) << 3)) & swz_mask)]) =
                         make_float2(o[i][0], o[i][1]);
                 if (g + 8 < rows_used)
-                    *reinterpret_cast<float2*>(&obuf[((warp * RU + g + 8) << lg) + dd]) =
+                    *reinterpret_cast<float2*>(
+                        &obuf[((warp * RU + g + 8) << lg) + ((dd ^ ((g & 3) << 3)) & swz_mask)]) =
                         make_float2(o[i][2], o[i][3]);
             }
             consumer_bar_sync();
             for (int idx = tid; idx < (R_cta << lg); idx += kConsumerWarps * 32) {
                 const int rl = idx >> lg, dd = idx & (DRr - 1);
                 const int grp = rl >> 4, rr = rl & 15;
-                float acc = 0.f;
+                float M = -FLT_MAX;
 #pragma unroll
                 for (int t = 0; t < TS; ++t)
-                    acc += obuf[(((t * MT + grp) * RU + rr) << lg) + dd];
-                const float2 ml = tot[rl];
+                    M = fmaxf(M, ml_buf[(t * MT + grp) * 16 + rr].x);
+                float L = 0.f, acc = 0.f;
+                const int col = (dd ^ ((rr & 3) << 3)) & swz_mask;
+#pragma unroll
+                for (int t = 0; t < TS; ++t) {
+                    const float2 ml = ml_buf[(t * MT + grp) * 16 + rr];
+                    const float f = fast_exp2(ml.x - M);
+                    L = fmaf(ml.y, f, L);
+                    acc = fmaf(f, obuf[(((t * MT + grp) * RU + rr) << lg) + col], acc);
+                }
                 const int d = (r << lg) + dd;
                 if (it.whole) {
-                    const float val = ml.y == 0.f ? acc : acc / ml.y;
+                    const float val = L == 0.f ? acc : acc / L;
                     static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
                 } else {
                     const size_t wrow = static_cast<size_t>(it.rec) * p.row_stride + rl;
                     p.ws_o[wrow * D + d] = acc;
                     if (d == 0)
-                        p.ws_ml[wrow] = ml;
+                        p.ws_ml[wrow] = make_float2(M, L);
                 }
             }
         }
