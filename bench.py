@@ -271,27 +271,32 @@ def time_steps(plans, steps, warmup, world, trace=True):
 
 
 def e2e_steps(w, device, steps, warmup):
-    """Same metric end to end through the public host-buffer call: per step the
-    step's inputs (q, table, lengths, new rows) go host->device from pinned
-    memory and the output comes back; the KV cache stays resident in HBM."""
+    """Same metric end to end through the public host-buffer call
+    (binding.HostPlan -> pa_decode_host): per step the step's inputs (q, table,
+    lengths, new rows) go host->device from pinned memory, the kernels run, the
+    output comes back to pinned host memory and the host waits for it; the KV
+    cache stays resident in HBM."""
     from paged_kv_cache_182_gb300 import binding
 
     kc, vc = w.k_cache.to(device), w.v_cache.to(device)
     host = [t.pin_memory() for t in (w.q, w.block_table, w.seq_lens, w.k_new, w.v_new)]
+    out = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host)
-    d2h = w.q.numel() * w.q.element_size()
+    d2h = out.numel() * out.element_size()
+    s = w.spec
+    plan = binding.HostPlan(kc, vc, B=s.B, H=s.H, NQ=s.NQ, max_blocks=int(w.block_table.shape[1]),
+                            scale=s.scale, causal=s.causal, partitions=s.partitions)
+    stream = torch.cuda.current_stream(device)
 
     def step():
-        return binding.decode_host(*host, k_cache=kc, v_cache=vc, scale=w.spec.scale,
-                                   causal=w.spec.causal, partitions=w.spec.partitions)
+        plan.run(*host, out, stream)
+        stream.synchronize()
 
     for _ in range(warmup):
         step()
-    torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
-    torch.cuda.synchronize()
     return (time.perf_counter() - t0) / steps * 1e3, h2d, d2h
 
 

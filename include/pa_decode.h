@@ -154,6 +154,40 @@ int pa_decode_static_workspace(const void *q, const void *k_cache, const void *v
                                const pa_opts *opts, void *stream);
 
 /*
+ * pa_decode for a step whose inputs and output live in host memory, as in a
+ * serving loop that assembles each step's queries, block table and lengths on
+ * the CPU.  The paged attention page passes its arrays through the host
+ * framework; this entry point keeps that shape without allocating.
+ *
+ * q, block_table, seq_lens, k_new, v_new (read) and out (written) are HOST
+ * pointers with the layouts of pa_decode; pinned (page-locked) memory makes
+ * the copies asynchronous.  k_cache and v_cache are device pointers (the cache
+ * stays resident).  opts->workspace is a device buffer of at least
+ * pa_host_workspace_bytes() bytes, 256-byte aligned: it holds the split
+ * workspace of pa_decode first (its leading pa_workspace_zero_bytes() bytes
+ * follow the same zero rule), then the device copies of the inputs and of the
+ * output.
+ *
+ * Enqueues on `stream`: one host-to-device copy per input, the decode, and the
+ * device-to-host copy of the output.  Returns without waiting: `out` holds the
+ * result once the stream has passed that copy (synchronise the stream before
+ * reading it, and do not modify the inputs before then).  Errors as pa_decode;
+ * PA_ERR_WORKSPACE when the workspace is too small.
+ */
+int pa_decode_host(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_table, const int32_t *seq_lens, const void *k_new,
+                   const void *v_new, void *out, float scale, int H, int KV, int D, int BLOCK,
+                   int NQ, int causal, const pa_opts *opts, void *stream);
+
+/*
+ * Device workspace bytes of pa_decode_host for these sizes (opts->max_blocks,
+ * opts->dtype and opts->out_dtype as in the call; -1 = same as dtype).
+ * Returns 0 for invalid arguments.
+ */
+size_t pa_host_workspace_bytes(int batch, int max_blocks, int H, int KV, int D, int NQ,
+                               int partitions, int dtype, int out_dtype);
+
+/*
  * Bytes of workspace pa_decode needs for these sizes (0 when partitions == 1).
  * Depends only on the arguments, not on the device or the lengths: it holds
  * a per-sequence schedule and one float32 partial state (max, sum, D

@@ -63,6 +63,10 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.pa_workspace_zero_bytes.restype = ctypes.c_size_t
     lib.pa_workspace_zero_bytes.argtypes = [I, I, I, I, I, I]
+    lib.pa_decode_host.restype = I
+    lib.pa_decode_host.argtypes = lib.pa_decode.argtypes
+    lib.pa_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.pa_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
     lib.pa_strerror.restype = ctypes.c_char_p
     lib.pa_strerror.argtypes = [I]
     lib.pa_version.restype = I
@@ -211,24 +215,97 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *, scale: f
     return plan.run(stream)
 
 
+class HostPlan:
+    """A prepared host-buffer decode (pa_decode_host) for fixed sizes.
+
+    The device-resident KV cache and a device workspace (the split workspace
+    plus staging for the step's inputs and output, zero-filled once here) are
+    fixed; each ``run`` takes the step's host tensors (pinned for asynchronous
+    copies) and enqueues their copies, the decode and the copy of the output
+    into ``out`` (host)."""
+
+    def __init__(self, k_cache, v_cache, *, B: int, H: int, NQ: int, max_blocks: int,
+                 scale: float, causal: bool = False, partitions: int = 0, out_dtype=None):
+        NB, BLOCK, KV, D = k_cache.shape
+        dt = k_cache.dtype
+        if dt not in _DT or v_cache.dtype != dt or tuple(v_cache.shape) != tuple(k_cache.shape):
+            raise TypeError("k_cache and v_cache must share one supported dtype and shape")
+        if not (k_cache.is_cuda and k_cache.is_contiguous() and v_cache.is_contiguous()):
+            raise ValueError("the caches must be contiguous CUDA tensors")
+        odt = dt if out_dtype is None else out_dtype
+        need = int(LIB.pa_host_workspace_bytes(B, max_blocks, H, KV, D, NQ, int(partitions),
+                                               _DT[dt], _DT[odt]))
+        if need == 0 and B > 0:
+            raise ValueError("unsupported sizes")
+        self.workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=k_cache.device)
+        self.caches = (k_cache, v_cache)
+        self.device = k_cache.device
+        self.shape = dict(B=B, H=H, KV=KV, D=D, NQ=NQ, max_blocks=max_blocks)
+        self.dtype, self.out_dtype = dt, odt
+        self.opts = PaOpts(batch=B, max_blocks=max_blocks, num_blocks=NB, dtype=_DT[dt],
+                           out_dtype=_DT[odt], partitions=int(partitions), checked=0,
+                           workspace=self.workspace.data_ptr(), workspace_bytes=need,
+                           status=None, trace_begin=None, trace_split=None, merge_kernel=0)
+        self._fixed = (ctypes.c_float(scale), H, KV, D, BLOCK, NQ, int(bool(causal)),
+                       ctypes.byref(self.opts))
+
+    def run(self, q, block_table, seq_lens, k_new, v_new, out, stream=None):
+        """Enqueue one step on ``stream`` (default: torch's current stream).  All
+        six tensors are host tensors; ``out`` holds the result once the stream
+        has been synchronised."""
+        s = self.shape
+        if (tuple(q.shape) != (s["B"], s["H"], s["NQ"], s["D"]) or
+                tuple(block_table.shape) != (s["B"], s["max_blocks"]) or
+                tuple(seq_lens.shape) != (s["B"],) or tuple(out.shape) != tuple(q.shape) or
+                tuple(k_new.shape) != (s["B"], s["KV"], s["NQ"], s["D"]) or
+                tuple(v_new.shape) != tuple(k_new.shape)):
+            raise ValueError("step tensors do not match the plan's sizes")
+        for x in (q, block_table, seq_lens, k_new, v_new, out):
+            if x.is_cuda or not x.is_contiguous():
+                raise ValueError("step tensors must be contiguous host tensors")
+        if q.dtype != self.dtype or k_new.dtype != self.dtype or v_new.dtype != self.dtype:
+            raise TypeError("q and the new rows must have the caches' dtype")
+        if out.dtype != self.out_dtype:
+            raise TypeError("out must have the plan's output dtype")
+        if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+            raise TypeError("block_table and seq_lens must be int32")
+        k_cache, v_cache = self.caches
+        with torch.cuda.device(self.device):
+            rc = LIB.pa_decode_host(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                    _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                    *self._fixed, _stream_handle(stream))
+        if rc != 0:
+            raise PagedAttentionError(rc)
+        return out
+
+
+_host_plans = {}
+
+
 def decode_host(q, block_table, seq_lens, k_new, v_new, *, k_cache, v_cache, scale: float,
                 causal: bool = False, partitions: int = 0, out_dtype=None, stream=None):
-    """End-to-end decode step from host tensors.
+    """End-to-end decode step from host tensors through pa_decode_host.
 
     The KV cache (``k_cache``, ``v_cache``) is device-resident state, as a KV
     cache is; the step's inputs -- q, the block table, the lengths and the
-    new rows -- are host tensors (pinned for asynchronous copies).  They are
-    copied to the device, the kernels run, and the output is copied back to
-    pinned host memory.  Returns the host output tensor.
+    new rows -- are host tensors (pinned for asynchronous copies).  The copies,
+    the kernels and the copy of the output back to pinned host memory are
+    enqueued by one library call; the device workspace is kept per size.
+    Returns the host output tensor after synchronising the stream.
     """
-    device = k_cache.device
+    B, H, NQ, _ = q.shape
+    odt = q.dtype if out_dtype is None else out_dtype
+    key = (k_cache.data_ptr(), v_cache.data_ptr(), tuple(k_cache.shape), B, H, NQ,
+           int(block_table.shape[1]), float(scale), bool(causal), int(partitions), odt)
+    plan = _host_plans.get(key)
+    if plan is None:
+        plan = HostPlan(k_cache, v_cache, B=B, H=H, NQ=NQ, max_blocks=int(block_table.shape[1]),
+                        scale=scale, causal=causal, partitions=partitions, out_dtype=out_dtype)
+        _host_plans.clear()  # one plan at a time: it owns a device workspace
+        _host_plans[key] = plan
     if stream is None:
-        stream = torch.cuda.current_stream(device)
-    with torch.cuda.stream(stream):
-        dev = [t.to(device, non_blocking=True) for t in (q, block_table, seq_lens, k_new, v_new)]
-        out = decode(dev[0], k_cache, v_cache, dev[1], dev[2], dev[3], dev[4], scale=scale,
-                     causal=causal, partitions=partitions, out_dtype=out_dtype, stream=stream)
-        host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        host.copy_(out, non_blocking=True)
+        stream = torch.cuda.current_stream(k_cache.device)
+    out = torch.empty(q.shape, dtype=odt, pin_memory=True)
+    plan.run(q, block_table, seq_lens, k_new, v_new, out, stream)
     stream.synchronize()
-    return host
+    return out

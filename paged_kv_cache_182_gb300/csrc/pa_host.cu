@@ -578,4 +578,103 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     return PA_OK;
 }
 
+// ------------------------------------------------------- host-buffer entry
+// Device workspace of pa_decode_host: the split workspace first (so that its
+// leading zero bytes stay at offset 0), then 256-aligned staging for q, the
+// table, the lengths, k_new, v_new and the output.
+struct HostLayout {
+    size_t q, table, lens, knew, vnew, out, total;
+};
+
+static HostLayout host_layout(size_t split_bytes, int batch, int max_blocks, int H, int KV, int D,
+                              int NQ, int dtype, int out_dtype)
+{
+    const size_t es = elem_size(dtype), eo = elem_size(out_dtype < 0 ? dtype : out_dtype);
+    HostLayout l{};
+    size_t off = align_up(split_bytes, 256);
+    l.q = off;
+    off = align_up(off + static_cast<size_t>(batch) * H * NQ * D * es, 256);
+    l.table = off;
+    off = align_up(off + static_cast<size_t>(batch) * max_blocks * 4, 256);
+    l.lens = off;
+    off = align_up(off + static_cast<size_t>(batch) * 4, 256);
+    l.knew = off;
+    off = align_up(off + static_cast<size_t>(batch) * KV * NQ * D * es, 256);
+    l.vnew = off;
+    off = align_up(off + static_cast<size_t>(batch) * KV * NQ * D * es, 256);
+    l.out = off;
+    off = align_up(off + static_cast<size_t>(batch) * H * NQ * D * eo, 256);
+    l.total = off;
+    return l;
+}
+
+size_t pa_host_workspace_bytes(int batch, int max_blocks, int H, int KV, int D, int NQ,
+                               int partitions, int dtype, int out_dtype)
+{
+    if (!ws_args_ok(batch, H, KV, D, NQ, partitions) || max_blocks < 1 || batch == 0 ||
+        (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16))
+        return 0;
+    return host_layout(pa_workspace_bytes(batch, H, KV, D, NQ, partitions), batch, max_blocks, H,
+                       KV, D, NQ, dtype, out_dtype)
+        .total;
+}
+
+int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const void* k_new,
+                   const void* v_new, void* out, float scale, int H, int KV, int D, int BLOCK,
+                   int NQ, int causal, const pa_opts* opts, void* stream)
+{
+    if (!opts)
+        return PA_ERR_NULL_POINTER;
+    const int B = opts->batch;
+    if (B < 0 || H < 1 || KV < 1 || H % KV != 0 || opts->max_blocks < 1 || NQ < 1 ||
+        NQ > PA_MAX_NQ || opts->partitions < 0)
+        return PA_ERR_BAD_DIMS;
+    if (B == 0)
+        return PA_OK;
+    if (!q || !block_table || !seq_lens || !k_new || !v_new || !out || !opts->workspace)
+        return PA_ERR_NULL_POINTER;
+    if (opts->dtype != PA_F32 && opts->dtype != PA_F16 && opts->dtype != PA_BF16)
+        return PA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128)
+        return PA_ERR_UNSUPPORTED;
+    const size_t split = pa_workspace_bytes(B, H, KV, D, NQ, opts->partitions);
+    const HostLayout l = host_layout(split, B, opts->max_blocks, H, KV, D, NQ, opts->dtype,
+                                     opts->out_dtype);
+    if (opts->workspace_bytes < l.total)
+        return PA_ERR_WORKSPACE;
+    if (!aligned(opts->workspace, 256))
+        return PA_ERR_ALIGNMENT;
+    const size_t es = elem_size(opts->dtype);
+    const size_t eo = elem_size(opts->out_dtype < 0 ? opts->dtype : opts->out_dtype);
+    unsigned char* ws = static_cast<unsigned char*>(opts->workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qb = static_cast<size_t>(B) * H * NQ * D * es;
+    const size_t nb = static_cast<size_t>(B) * KV * NQ * D * es;
+    struct {
+        void* dst;
+        const void* src;
+        size_t bytes;
+    } in[5] = {{ws + l.q, q, qb},
+               {ws + l.table, block_table, static_cast<size_t>(B) * opts->max_blocks * 4},
+               {ws + l.lens, seq_lens, static_cast<size_t>(B) * 4},
+               {ws + l.knew, k_new, nb},
+               {ws + l.vnew, v_new, nb}};
+    for (const auto& c : in)
+        if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return PA_ERR_CUDA;
+    pa_opts dev = *opts;
+    dev.workspace = split ? ws : nullptr;
+    dev.workspace_bytes = split;
+    const int rc = pa_decode(ws + l.q, k_cache, v_cache, reinterpret_cast<const int32_t*>(ws + l.table),
+                             reinterpret_cast<const int32_t*>(ws + l.lens), ws + l.knew, ws + l.vnew,
+                             ws + l.out, scale, H, KV, D, BLOCK, NQ, causal, &dev, stream);
+    if (rc != PA_OK)
+        return rc;
+    if (cudaMemcpyAsync(out, ws + l.out, static_cast<size_t>(B) * H * NQ * D * eo,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
 }  // extern "C"

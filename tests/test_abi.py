@@ -111,3 +111,45 @@ def test_empty_batch_is_a_no_op(lib):
     before = lib.kernel_launches()
     assert call(lib, batch=0) == 0
     assert lib.kernel_launches() == before
+
+
+def test_host_workspace_bytes_covers_split_workspace_and_staging(lib):
+    hw = lib.LIB.pa_host_workspace_bytes
+    split = lib.workspace_bytes(8, 32, 8, 128, 1, 0)
+    # q + out (8*32*128*2 B each), table (8*257*4), lengths, new rows (2 * 8*8*128*2)
+    staging = 2 * 8 * 32 * 128 * 2 + 8 * 257 * 4 + 8 * 4 + 2 * 8 * 8 * 128 * 2
+    need = hw(8, 257, 32, 8, 128, 1, 0, lib.PA_F16, -1)
+    assert need >= split + staging
+    assert need < split + staging + 7 * 256  # six staging regions, 256-byte aligned
+    assert hw(8, 257, 32, 8, 128, 1, 0, lib.PA_F16, lib.PA_F32) > need  # float32 output
+    assert hw(8, 0, 32, 8, 128, 1, 0, lib.PA_F16, -1) == 0
+    assert hw(8, 257, 32, 8, 96, 1, 0, lib.PA_F16, -1) == 0
+
+
+def test_host_entry_point_rejects_before_copying(lib):
+    """Argument checks of pa_decode_host return before any copy is enqueued
+    (these calls run without a GPU)."""
+    f = lib.LIB.pa_decode_host
+    host = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+
+    def go(opts, **kw):
+        a = dict(zip(("q", "kc", "vc", "table", "lens", "kn", "vn", "out"), host))
+        a.update(kw)
+        return f(a["q"], a["kc"], a["vc"], a["table"], a["lens"], a["kn"], a["vn"], a["out"],
+                 ctypes.c_float(0.1), 32, 8, 128, 16, 1, 0, opts, None)
+
+    def opts(**kw):
+        o = dict(batch=8, max_blocks=257, num_blocks=2048, dtype=lib.PA_F16, out_dtype=-1,
+                 partitions=0, checked=0, workspace=None, workspace_bytes=0, status=None,
+                 trace_begin=None, trace_split=None, merge_kernel=0)
+        o.update(kw)
+        return ctypes.byref(lib.PaOpts(**o))
+
+    need = lib.LIB.pa_host_workspace_bytes(8, 257, 32, 8, 128, 1, 0, lib.PA_F16, -1)
+    assert f(*host, ctypes.c_float(0.1), 32, 8, 128, 16, 1, 0, None, None) == -1
+    assert go(opts(batch=0)) == 0
+    assert go(opts(workspace=0x100000, workspace_bytes=need), q=None) == -1
+    assert go(opts()) == -1  # no workspace
+    assert go(opts(workspace=0x100000, workspace_bytes=need - 1)) == -5
+    assert go(opts(workspace=0x100010, workspace_bytes=need)) == -4
+    assert go(opts(workspace=0x100000, workspace_bytes=need, dtype=9)) == -3

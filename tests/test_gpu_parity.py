@@ -234,3 +234,33 @@ def test_repeated_calls_full_ragged_are_stable():
     for rep in range(1, 20):
         got = pu.run_gpu(w, out_dtype=torch.float32).cpu()
         assert torch.equal(got, first), f"call {rep} differs from call 0"
+
+
+@pytest.mark.parametrize("name", ["gqa_fp16", "ragged_fp16", "long_bf16", "tiny_fp32"])
+@pytest.mark.parametrize("P", [0, 3])
+def test_host_entry_point_matches_device_call(name, P):
+    """pa_decode_host (inputs and output in pinned host memory, two steps in a
+    row on one plan: same cache and table, new queries and new rows) gives
+    exactly pa_decode's output, which matches the oracle."""
+    from paged_kv_cache_182_gb300 import binding
+
+    w0 = W.make(small(name), seed=20)
+    s = w0.spec
+    plan = binding.HostPlan(w0.k_cache.cuda(), w0.v_cache.cuda(), B=s.B, H=s.H, NQ=s.NQ,
+                            max_blocks=int(w0.block_table.shape[1]), scale=s.scale,
+                            causal=s.causal, partitions=P, out_dtype=torch.float32)
+    g = torch.Generator().manual_seed(21)
+    for rep in range(2):
+        if rep == 0:
+            w = w0
+        else:
+            fresh = [torch.randn(t.shape, generator=g).to(t.dtype) for t in (w0.q, w0.k_new, w0.v_new)]
+            w = W.Workload(s, w0.seq_lens, w0.block_table, fresh[0], w0.k_cache, w0.v_cache,
+                           fresh[1], fresh[2])
+        host = [t.pin_memory() for t in (w.q, w.block_table, w.seq_lens, w.k_new, w.v_new)]
+        out = torch.full(w.q.shape, float("nan"), dtype=torch.float32).pin_memory()
+        plan.run(*host, out)
+        torch.cuda.synchronize()
+        want_dev = pu.run_gpu(w, partitions=P, out_dtype=torch.float32).cpu()
+        assert torch.equal(out, want_dev), f"{name} P={P} step {rep}"
+        pu.check(out, pu.run_oracle(w), s.dtype, "f32", f"{name} P={P} host step {rep}")
