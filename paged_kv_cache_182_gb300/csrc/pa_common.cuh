@@ -79,9 +79,9 @@ using CombineFn = void (*)(CombineParams);
 // use the CUDA-core kernel (RG query rows per warp); 16-bit inputs use the
 // tensor-core kernel (16 * MT query rows per CTA pass).
 constexpr int kMmaTokens = 16;  // tokens of one MMA group of the tensor-core kernel
-// 16-token groups a consumer warp takes per stage (two at D = 64: 64 KB stages
-// and two independent MMA chains per warp)
-__host__ __device__ constexpr int mma_token_groups(int D) { return D == 64 ? 2 : 1; }
+// 16-token groups a consumer warp takes per stage (two at D = 64 or with two
+// 16-row groups per pass: 64 KB stages and two independent MMA chains per warp)
+__host__ __device__ constexpr int mma_token_groups(int D, int MT) { return D == 64 || MT == 2 ? 2 : 1; }
 constexpr int kObufFloats = 4096;  // tensor-core kernel: floats of the piece-end merge buffer
 SplitFn pick_split_f32(int D, int RG);
 SplitFn pick_split_f16(bool f32_out, int D, int MT);

@@ -383,10 +383,10 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         return PA_ERR_BAD_DIMS;
     const int es = static_cast<int>(elem_size(dtype));
     // tensor-core path: up to 64 KB stages, at most 8 warps (TPW tokens x row
-    // groups) per stage: 128 tokens at D = 128 (64 with 32 rows per pass), 256
-    // at D = 64 (128); at most 16 cache blocks per stage
+    // groups) per stage: 128 tokens at D = 128, 256 at D = 64 (128 with 32 rows
+    // per pass); at most 16 cache blocks per stage
     int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
-    const int TPW = kMmaTokens * mma_token_groups(D);  // tokens per consumer warp and stage
+    const int TPW = kMmaTokens * mma_token_groups(D, MT);  // tokens per consumer warp and stage
     if (mma && (TT / TPW) * MT > kConsumerWarps)
         TT = kConsumerWarps / MT * TPW;
     if (mma && TT > 16 * BLOCK)  // at most 16 boxes (one per block) per stage and role

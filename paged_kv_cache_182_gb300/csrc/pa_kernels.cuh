@@ -1344,7 +1344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NT = D / 8;   // 8-column tiles of O
     constexpr int ROWS = 16 * MT;
     constexpr int TS = kConsumerWarps / MT;  // warps per row group
-    constexpr int TG = mma_token_groups(D);  // 16-token groups per warp and stage
+    constexpr int TG = mma_token_groups(D, MT);  // 16-token groups per warp and stage
     constexpr int TPW = kMmaTokens * TG;     // tokens per warp and stage
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
