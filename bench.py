@@ -120,6 +120,15 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
+def partition_kernel_name(spec):
+    """Which partition kernel runs a workload: float32 caches take the
+    CUDA-core kernel; 16-bit caches the transposed tensor-core kernel at 8 or
+    fewer query rows per KV head, else the 16-row one."""
+    if spec.dtype == "f32":
+        return "pa_split_kernel"
+    return "pa_mmat_kernel" if spec.group * spec.NQ <= 8 else "pa_mma_kernel"
+
+
 def captured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, or None when there is none or the kernel sources changed since."""
@@ -368,7 +377,7 @@ def run_ours(args, rank, world, local):
     _, split_ms, _ = time_steps(plans, max(20, args.steps // 4), args.warmup, world)
     value, ms_max, total_bytes = aggregate(per_rank_bytes, ms, world)
     achieved = per_rank_bytes / (split_ms * 1e-3) / 1e9
-    kernel = "pa_split_kernel" if w.spec.dtype == "f32" else "pa_mma_kernel"
+    kernel = partition_kernel_name(w.spec)
     traffic = captured_traffic(kernel, w.spec.name)
     del plans
     torch.cuda.empty_cache()

@@ -31,12 +31,19 @@ size_t elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 // per KV head, else 8; a CTA pass covers kConsumerWarps * RG rows.
 int rows_group(int R) { return R <= 32 ? 4 : 8; }
 
-// Tensor-core path (16-bit): 16-row MMA tiles per CTA pass.
-int mma_tiles(int R) { return R <= 16 ? 1 : 2; }
+// Tensor-core path (16-bit): 0 = the transposed kernel (at most 8 rows per
+// pass, the MMA's 16-row side on the tokens), else 16-row MMA tiles per pass.
+int mma_tiles(int R) { return R <= 8 ? 0 : R <= 16 ? 1 : 2; }
+
+// 16-row groups of the warps of a stage (the transposed kernel has one)
+int row_groups(int MT) { return MT > 1 ? MT : 1; }
 
 int rows_per_pass(int dtype, int R)
 {
-    return dtype == PA_F32 ? kConsumerWarps * rows_group(R) : 16 * mma_tiles(R);
+    if (dtype == PA_F32)
+        return kConsumerWarps * rows_group(R);
+    const int MT = mma_tiles(R);
+    return MT == 0 ? 8 : 16 * MT;
 }
 
 int tokens_per_stage(int D, int es, int BLOCK)
@@ -387,8 +394,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     // per pass); at most 16 cache blocks per stage
     int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
     const int TPW = kMmaTokens * mma_token_groups(D, MT);  // tokens per consumer warp and stage
-    if (mma && (TT / TPW) * MT > kConsumerWarps)
-        TT = kConsumerWarps / MT * TPW;
+    if (mma && (TT / TPW) * row_groups(MT) > kConsumerWarps)
+        TT = kConsumerWarps / row_groups(MT) * TPW;
     if (mma && TT > 16 * BLOCK)  // at most 16 boxes (one per block) per stage and role
         TT = 16 * BLOCK;
     // automatic schedule: units of one stage.  Each segment is charged the
@@ -413,7 +420,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     // one TMA box per cache block (per tile when a block spans several tiles):
     // the issue cost of a box is fixed, so fewer, larger boxes stream faster
     const int box_rows = mma ? (BLOCK < TT ? BLOCK : TT) : BLOCK;
-    const int ROWS = 16 * MT;
+    const int ROWS = rows_per_cta;  // tensor-core path: query-row buffer rows
     // shared memory: header | lens[B] | prefix[B+1] | consumer scratch | ring
     const int lens_off = kHeaderBytes;
     const int prefix_off = static_cast<int>(align_up(lens_off + 4 * B, 16));
@@ -501,7 +508,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         grid = records;
     p.qbuf_off = qbuf_off;
     p.box_rows = box_rows;
-    p.empty_count = mma ? (TT / TPW) * MT : kConsumerWarps;
+    p.empty_count = mma ? (TT / TPW) * row_groups(MT) : kConsumerWarps;
     p.checked = opts->checked ? 1 : 0;
     p.R = R;
     p.rows_per_cta = rows_per_cta;

@@ -1320,6 +1320,64 @@ __device__ __forceinline__ RowAddr row_addr(uint32_t tile, uint32_t fresh, uint3
     return r;
 }
 
+// ---- piece-end merge of the consumer warps (both tensor-core kernels).
+// Each warp leaves its running (max, sum) per row in a [warp][16] table and
+// its unscaled accumulators in obuf, [warp][RU rows][DRr columns] per round of
+// DRr = 2^lg columns; columns are XOR-swizzled by row in groups of 8 floats so
+// that the rows a warp stores at once fall in different banks.
+__device__ __forceinline__ int obuf_swz(int row) { return ((row >> 1) & 3) << 3; }
+
+// log2 of the round width: the widest power of two <= D whose round of RU
+// rows from every consumer warp fits kObufFloats.
+__device__ __forceinline__ int obuf_lg(int D, int RU)
+{
+    int lg = 31 - __clz(D);
+    while (lg > 3 && kConsumerWarps * RU * (1 << lg) > kObufFloats)
+        --lg;
+    return lg;
+}
+
+// Sums round r of the stashed states of the TS = kConsumerWarps / MT warps of
+// every row: M = max m_t, L = sum l_t 2^(m_t - M), acc = sum o_t 2^(m_t - M);
+// writes out = acc / L for a whole segment, else the partial record
+// (acc, (M, L)).  Warp w holds rows of row group w % MT.  All consumer threads.
+template <int D, int MT, typename TO>
+__device__ __forceinline__ void sum_warps(const SplitParams& p, const Item& it, int R_cta, int RU, int lg,
+                                          int r, const float2* ml_buf, const float* obuf)
+{
+    constexpr int TS = kConsumerWarps / MT;
+    const int DRr = 1 << lg;
+    const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R +
+                            static_cast<size_t>(it.rsg) * p.rows_per_cta;
+    for (int idx = threadIdx.x; idx < (R_cta << lg); idx += kConsumerWarps * 32) {
+        const int rl = idx >> lg, dd = idx & (DRr - 1);
+        const int grp = rl >> 4, rr = rl & 15;
+        float M = -FLT_MAX;
+#pragma unroll
+        for (int t = 0; t < TS; ++t)
+            M = fmaxf(M, ml_buf[(t * MT + grp) * 16 + rr].x);
+        float L = 0.f, acc = 0.f;
+        const int col = (dd ^ obuf_swz(rr)) & (DRr - 1);
+#pragma unroll
+        for (int t = 0; t < TS; ++t) {
+            const float2 ml = ml_buf[(t * MT + grp) * 16 + rr];
+            const float f = fast_exp2(ml.x - M);
+            L = fmaf(ml.y, f, L);
+            acc = fmaf(f, obuf[(((t * MT + grp) * RU + rr) << lg) + col], acc);
+        }
+        const int d = (r << lg) + dd;
+        if (it.whole) {
+            const float val = L == 0.f ? acc : acc / L;
+            static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
+        } else {
+            const size_t wrow = static_cast<size_t>(it.rec) * p.row_stride + rl;
+            p.ws_o[wrow * D + d] = acc;
+            if (d == 0)
+                p.ws_ml[wrow] = make_float2(M, L);
+        }
+    }
+}
+
 // T: __half or __nv_bfloat16; D: head size; MT: 16-row groups per CTA pass;
 // TO: output element type.  One CTA per SM (persistent).
 //
@@ -1596,20 +1654,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ml_buf[warp * 16 + g + 8] = make_float2(m[1], lp[1]);
         }
         const int rows_used = min(16, max(0, R_cta - row0));
-        const size_t out_row0 =
-            (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * ROWS;
-        const int tid = threadIdx.x;
         // Rounds of DRr columns: each warp writes its rows (at most RU) of the
         // round's columns to obuf, then all threads sum the TS warps of each
         // row.  With few rows per segment one round covers all D columns.
-        // Columns are XOR-swizzled by row (8 floats per row step) so that the
-        // rows a warp writes at once fall in different banks.
         const int RU = min(16, R_cta);
-        int lg = 31 - __clz(D);  // log2 of the round width
-        while (lg > 3 && kConsumerWarps * RU * (1 << lg) > kObufFloats)
-            --lg;
+        const int lg = obuf_lg(D, RU);
         const int DRr = 1 << lg, TPR = DRr / 8, rounds = D >> lg;
-        const int swz_mask = DRr - 1;
         for (int r = 0; r < rounds; ++r) {
             if (r > 0)
                 consumer_bar_sync();  // readers of the previous round are done
@@ -1620,45 +1670,325 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int dd = (i - r * TPR) * 8 + 2 * qd;
                 if (g < rows_used)
                     *reinterpret_cast<float2*>(
-                        &obuf[((warp * RU + g) << lg) + ((dd ^ ((g & 3) << 3)) & swz_mask)]) =
+                        &obuf[((warp * RU + g) << lg) + ((dd ^ obuf_swz(g)) & (DRr - 1))]) =
                         make_float2(o[i][0], o[i][1]);
                 if (g + 8 < rows_used)
                     *reinterpret_cast<float2*>(
-                        &obuf[((warp * RU + g + 8) << lg) + ((dd ^ ((g & 3) << 3)) & swz_mask)]) =
+                        &obuf[((warp * RU + g + 8) << lg) + ((dd ^ obuf_swz(g + 8)) & (DRr - 1))]) =
                         make_float2(o[i][2], o[i][3]);
             }
             consumer_bar_sync();
-            for (int idx = tid; idx < (R_cta << lg); idx += kConsumerWarps * 32) {
-                const int rl = idx >> lg, dd = idx & (DRr - 1);
-                const int grp = rl >> 4, rr = rl & 15;
-                float M = -FLT_MAX;
-#pragma unroll
-                for (int t = 0; t < TS; ++t)
-                    M = fmaxf(M, ml_buf[(t * MT + grp) * 16 + rr].x);
-                float L = 0.f, acc = 0.f;
-                const int col = (dd ^ ((rr & 3) << 3)) & swz_mask;
-#pragma unroll
-                for (int t = 0; t < TS; ++t) {
-                    const float2 ml = ml_buf[(t * MT + grp) * 16 + rr];
-                    const float f = fast_exp2(ml.x - M);
-                    L = fmaf(ml.y, f, L);
-                    acc = fmaf(f, obuf[(((t * MT + grp) * RU + rr) << lg) + col], acc);
-                }
-                const int d = (r << lg) + dd;
-                if (it.whole) {
-                    const float val = L == 0.f ? acc : acc / L;
-                    static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
-                } else {
-                    const size_t wrow = static_cast<size_t>(it.rec) * p.row_stride + rl;
-                    p.ws_o[wrow * D + d] = acc;
-                    if (d == 0)
-                        p.ws_ml[wrow] = make_float2(M, L);
-                }
-            }
+            sum_warps<D, MT, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf);
         }
         // automatic schedule: the CTA's first and last pieces at most
         if (!it.whole && p.counters && nsplit < kSplitList) {
-            if (tid == 0)
+            if (threadIdx.x == 0)
+                sm.split_list[nsplit] = make_int4(it.b, it.rsg, it.kh, 0);
+            ++nsplit;
+        }
+    }
+    // uniform over the consumer warps (a late abort flag must not split them)
+    if (nsplit > 0 && !consumer_bar_or(*sm.abort_flag != 0))
+        flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, tot, 2 * ROWS, obuf, kObufFloats);
+}
+
+// T: __half or __nv_bfloat16; D: head size; TO: output element type.  The
+// tensor-core kernel for at most 8 query rows per KV head and pass (GQA
+// decode): with rows this few, the 16-row side of the m16n8k16 MMA is put on
+// the tokens and the 8-column side on the rows.  Each warp takes TPW tokens of
+// a stage and computes S^T = K Q^T (tokens x 8 rows), its running row maxima
+// and sums (reduced over the lanes of a row), and O^T += V^T P^T (D x 8 rows),
+// the P fragments moved from the accumulator layout into the operand layout by
+// movmatrix transposes.  Half the MMAs and half the accumulator registers of
+// the 16-row kernel; pipeline, schedule, piece-end and split merges are the
+// same.
+template <typename T, int D, typename TO>
+__global__ void __launch_bounds__(kThreads, 1)
+    pa_mmat_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap)
+{
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int KS = D / 16;  // k-steps of K Q^T; also 16-column tiles of O^T
+    constexpr int ROWS = 8;     // query rows per CTA pass
+    constexpr int TG = mma_token_groups(D, 0);  // 16-token groups per warp and stage
+    constexpr int TPW = kMmaTokens * TG;        // tokens per warp and stage
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const Smem sm = carve(p, smem_raw);
+    float2* ml_buf = reinterpret_cast<float2*>(sm.scratch);      // [warps][16] (max, sum)
+    float2* tot = reinterpret_cast<float2*>(sm.scratch + 1024);  // split merges: (max, sum)
+    float* obuf = reinterpret_cast<float*>(sm.scratch + 2048);   // kObufFloats merge rounds
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.stages;
+
+    warm_param(p);
+    warm_param(kmap);
+    warm_param(vmap);
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const Sched sc = setup_cta(p, sm);
+
+    if (warp >= kConsumerWarps) {
+        produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
+        return;
+    }
+
+    // MMA fragment coordinates: g = lane / 4 (accumulator row: token; operand
+    // column: query row), qd = lane % 4 (accumulator columns 2 qd, 2 qd + 1:
+    // this thread's two query rows)
+    const int g = lane >> 2, qd = lane & 3;
+    const int TT = p.TT;
+    const int WS = TT / TPW;  // warps per stage
+    const int nsets = kConsumerWarps / WS;
+    const int my_set = warp / WS;
+    const int tb = (warp % WS) * TPW;  // this warp's first token in a stage
+    const uint32_t zero = smem_u32(sm.zero16);
+    const uint32_t qbuf = smem_u32(sm.scratch + p.qbuf_off);
+    uint32_t gt = 0;
+    int piece = 0;
+    int nsplit = 0;  // split pieces listed since the last flush (uniform)
+    bool alive = true;
+
+    PieceIter pi;
+    for (pi.first(p, sc); pi.ok; pi.next(p, sc), ++piece) {
+        const Item& it = pi.it;
+        const int ntiles = (it.end - it.start + TT - 1) / TT;
+        const int R_cta = min(ROWS, p.R - it.rsg * ROWS);
+
+        // causal / length limits of this thread's rows 2 qd + e (0 for padding rows)
+        int lim[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int rl = 2 * qd + e;
+            const int rho = it.rsg * ROWS + rl;
+            lim[e] = rl < R_cta ? it.past + (p.causal ? (rho % p.NQ) + 1 : p.NQ) : 0;
+        }
+        const int lim_min = __reduce_min_sync(kFull, min(lim[0] > 0 ? lim[0] : INT_MAX,
+                                                         lim[1] > 0 ? lim[1] : INT_MAX));
+
+        // Q^T fragments (operand B: k = head columns, n = query row g) from this
+        // piece's query buffer, [8 rows][D] row-major
+        uint32_t qb[KS][2];
+        {
+            const int par = piece & 1;
+            if (alive) {
+                alive = !*sm.abort_flag &&
+                        mbar_wait_bounded(&sm.q_full[par], (piece >> 1) & 1, kWaitLimitNs);
+                alive = __all_sync(kFull, alive);
+                if (!alive && lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+            }
+            const uint32_t qaddr = qbuf + (par * ROWS + (lane & 7)) * (D * 2) + ((lane >> 3) << 4);
+            const bool rok = g < R_cta;  // rows past the pass hold stale shared memory
+#pragma unroll
+            for (int kk = 0; kk < KS / 2; ++kk) {
+                ldsm_x4(qaddr + kk * 64, qb[2 * kk][0], qb[2 * kk][1], qb[2 * kk + 1][0],
+                        qb[2 * kk + 1][1]);
+                if (!rok) {
+                    qb[2 * kk][0] = 0u;
+                    qb[2 * kk][1] = 0u;
+                    qb[2 * kk + 1][0] = 0u;
+                    qb[2 * kk + 1][1] = 0u;
+                }
+            }
+        }
+
+        float m[2] = {-FLT_MAX, -FLT_MAX}, lp[2] = {0.f, 0.f};
+        float o[KS][4];  // O^T tile mt: (column 16 mt + g (+8), rows 2 qd, 2 qd + 1)
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[i][e] = 0.f;
+
+        for (int j = 0; j < ntiles; ++j, ++gt) {
+            if (static_cast<int>(gt % nsets) != my_set)
+                continue;  // another warp set's stage
+            const int s = gt % S;
+            if (alive) {
+                alive = !*sm.abort_flag &&
+                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, kWaitLimitNs);
+                alive = __all_sync(kFull, alive);
+                if (!alive && lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+            }
+            if (!alive)
+                continue;
+            const uint32_t st = smem_u32(sm.ring) + s * p.stage_bytes;
+            const uint32_t k_tile = st, v_tile = st + p.v_off;
+            const uint32_t k_new = st + p.knew_off, v_new = st + p.vnew_off;
+            const int t0 = it.start + j * TT;
+            const int n_tile = min(TT, it.end - t0);
+            if (tb >= n_tile) {  // the stage ends before this warp's tokens
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty[s]);
+                continue;
+            }
+            // a group whose every token is visible to every row of the pass
+            bool full_tile[TG];
+#pragma unroll
+            for (int u = 0; u < TG; ++u) {
+                const int tu = tb + u * kMmaTokens;
+                full_tile[u] = tu + kMmaTokens <= n_tile && t0 + tu + kMmaTokens <= lim_min;
+            }
+
+            // ---- S^T = K Q^T: operand A = 16 token rows of K (ldmatrix gives
+            // (tokens 0-7 | 8-15) x (columns 0-7 | 8-15) as a0 a2 a1 a3); two
+            // accumulator sets per group (even / odd k-steps) for shorter chains
+            float sa[TG][2][4];
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        sa[u][a][e] = 0.f;
+            RowAddr kr[TG];
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
+                kr[u] = row_addr<D>(k_tile, k_new, zero,
+                                    tb + u * kMmaTokens + (lane & 7) + ((lane >> 4) << 3), n_tile,
+                                    t0, it.past);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int u = 0; u < TG; ++u) {
+                    uint32_t a[4];
+                    ldsm_x4(kr[u].at(2 * ks + ((lane >> 3) & 1)), a[0], a[2], a[1], a[3]);
+                    mma_16816<kBf>(sa[u][ks & 1], a, qb[ks][0], qb[ks][1]);
+                }
+            // scale, mask, row maxima of the stage: element e of group u is
+            // token tb + 16 u + g + 8 (e / 2), row 2 qd + e % 2
+            float sv[TG][4];
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = e & 1;
+                    const int tk = tb + u * kMmaTokens + g + ((e >> 1) << 3);
+                    const float v = (sa[u][0][e] + sa[u][1][e]) * p.qscale;
+                    const bool valid = full_tile[u] || (tk < n_tile && t0 + tk < lim[h]);
+                    sv[u][e] = valid ? v : -INFINITY;
+                    mx[h] = fmaxf(mx[h], sv[u][e]);
+                }
+            bool grow = false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 4));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 8));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 16));
+                grow |= mx[h] > m[h];
+            }
+            if (__any_sync(kFull, grow)) {  // rescale only when a row maximum grew
+                float f[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float mn = fmaxf(m[h], mx[h]);
+                    f[h] = fast_exp2(m[h] - mn);
+                    m[h] = mn;
+                    lp[h] *= f[h];
+                }
+#pragma unroll
+                for (int i = 0; i < KS; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[i][e] *= f[e & 1];
+            }
+            // P^T as operand B (k = tokens, n = row g): the accumulator layout
+            // holds (token g, rows 2 qd, 2 qd + 1) per 8x8 block; a movmatrix
+            // transpose gives (tokens 2 qd, 2 qd + 1, row g).  High part and
+            // remainder.
+            uint32_t bh[TG][2], bl[TG][2];
+#pragma unroll
+            for (int u = 0; u < TG; ++u) {
+                const float p0 = fast_exp2(sv[u][0] - m[0]);
+                const float p1 = fast_exp2(sv[u][1] - m[1]);
+                const float p2 = fast_exp2(sv[u][2] - m[0]);
+                const float p3 = fast_exp2(sv[u][3] - m[1]);
+                lp[0] += p0 + p2;
+                lp[1] += p1 + p3;
+                uint32_t h01, l01, h23, l23;
+                Pack<T>::split(p0, p1, h01, l01);
+                Pack<T>::split(p2, p3, h23, l23);
+                bh[u][0] = movm_trans(h01);
+                bh[u][1] = movm_trans(h23);
+                bl[u][0] = movm_trans(l01);
+                bl[u][1] = movm_trans(l23);
+            }
+            // ---- O^T += V^T P^T: operand A = 16 columns x 16 tokens of V
+            // (ldmatrix.trans gives (columns 0-7 | 8-15) x (tokens 0-7 | 8-15)
+            // as a0 a2 a1 a3)
+            RowAddr vr[TG];
+#pragma unroll
+            for (int u = 0; u < TG; ++u)
+                vr[u] = row_addr<D>(v_tile, v_new, zero,
+                                    tb + u * kMmaTokens + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                    n_tile, t0, it.past);
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int u = 0; u < TG; ++u) {
+                    uint32_t a[4];
+                    ldsm_x4_t(vr[u].at(2 * mt + (lane >> 4)), a[0], a[2], a[1], a[3]);
+                    mma_16816<kBf>(o[mt], a, bh[u][0], bh[u][1]);
+                    mma_16816<kBf>(o[mt], a, bl[u][0], bl[u][1]);
+                }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.empty[s]);
+        }
+        // release the query buffer once every MMA reading qb has issued
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.q_free[piece & 1]);
+
+        // ---- piece end: row sums over the lanes of a row, then the merge of
+        // the eight warps through shared memory
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            lp[h] += __shfl_xor_sync(kFull, lp[h], 4);
+            lp[h] += __shfl_xor_sync(kFull, lp[h], 8);
+            lp[h] += __shfl_xor_sync(kFull, lp[h], 16);
+        }
+        // the previous piece's readers are done with the buffers; uniform abort
+        if (consumer_bar_or(*sm.abort_flag != 0))
+            break;
+        if (g == 0) {
+            ml_buf[warp * 16 + 2 * qd] = make_float2(m[0], lp[0]);
+            ml_buf[warp * 16 + 2 * qd + 1] = make_float2(m[1], lp[1]);
+        }
+        const int RU = R_cta;
+        const int lg = obuf_lg(D, RU);
+        const int DRr = 1 << lg, rounds = D >> lg;
+        for (int r = 0; r < rounds; ++r) {
+            if (r > 0)
+                consumer_bar_sync();  // readers of the previous round are done
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int d = 16 * mt + g + 8 * hh;
+                    if ((d >> lg) != r)
+                        continue;
+                    const int dd = d & (DRr - 1);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int row = 2 * qd + e;
+                        if (row < RU)
+                            obuf[((warp * RU + row) << lg) + ((dd ^ obuf_swz(row)) & (DRr - 1))] =
+                                o[mt][2 * hh + e];
+                    }
+                }
+            consumer_bar_sync();
+            sum_warps<D, 1, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf);
+        }
+        // automatic schedule: the CTA's first and last pieces at most
+        if (!it.whole && p.counters && nsplit < kSplitList) {
+            if (threadIdx.x == 0)
                 sm.split_list[nsplit] = make_int4(it.b, it.rsg, it.kh, 0);
             ++nsplit;
         }
@@ -1816,12 +2146,17 @@ SplitFn pick_split_simt(int D, int RG)
     return RG == 4 ? pa_split_kernel<T, 128, 4, TO> : pa_split_kernel<T, 128, 8, TO>;
 }
 
+// MT = 0: the transposed kernel (at most 8 rows per pass); 1 or 2: 16 * MT rows
 template <typename T, typename TO>
 SplitFn pick_split_mma(int D, int MT)
 {
     if (D == 64)
-        return MT == 1 ? pa_mma_kernel<T, 64, 1, TO> : pa_mma_kernel<T, 64, 2, TO>;
-    return MT == 1 ? pa_mma_kernel<T, 128, 1, TO> : pa_mma_kernel<T, 128, 2, TO>;
+        return MT == 0   ? pa_mmat_kernel<T, 64, TO>
+               : MT == 1 ? pa_mma_kernel<T, 64, 1, TO>
+                         : pa_mma_kernel<T, 64, 2, TO>;
+    return MT == 0   ? pa_mmat_kernel<T, 128, TO>
+           : MT == 1 ? pa_mma_kernel<T, 128, 1, TO>
+                     : pa_mma_kernel<T, 128, 2, TO>;
 }
 
 template <typename TO>

@@ -191,6 +191,15 @@ __device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held in the ldmatrix / MMA
+// fragment layout (lane l: row l / 4, columns 2 (l % 4), 2 (l % 4) + 1).
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // D = A (16x16, row) * B (16x8, col) + D, float32 accumulators.
 template <bool kBf16>
 __device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1)
