@@ -906,9 +906,12 @@ __device__ __forceinline__ int count_piece(int* counter)
 
 // Merges every partial record of segment (it.b, it.rsg, it.kh) into the
 // output: M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
-// out = L == 0 ? O : O / L.  All consumer threads; `tot` holds rows_per_cta
-// (M, L) pairs and `fac` fac_cap floats of shared scratch.  Records written by
-// other CTAs are read through L2 (ld.global.cg).
+// out = L == 0 ? O : O / L.  Threads t0 .. t0 + kT - 1 of the consumer warps.
+// Segments of at most 128 items (4 columns of one row) are merged in one pass
+// by one thread per item; larger ones in two (the (max, sum) pairs first, into
+// `tot` (rows_per_cta pairs) and `fac` (fac_cap floats) of shared scratch,
+// then the accumulators).  Records written by other CTAs are read through L2
+// (ld.global.cg).
 template <int D, typename TO>
 __device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 seg, float2* tot,
                               float* fac, int fac_cap, int t0, int kT, int bar_id)
@@ -929,6 +932,61 @@ __device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 
     constexpr int D4 = D / 4;
     constexpr int LG4 = D4 == 16 ? 4 : 5;
     const int NI = R_cta * D4;
+    const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta;
+    if (NI <= kConsumerWarps * 16) {
+        // At most one item per thread of a half CTA: each thread merges every
+        // record of its item online, eight records' (max, sum) and accumulator
+        // loads in flight together -- one L2 round trip for up to eight
+        // records, no shared memory and no barrier.  The order of the sums
+        // depends on the record count only.
+        if (tid < NI) {
+            const int rl = tid >> LG4, d4 = tid & (D4 - 1);
+            float M = -FLT_MAX, L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < n; c0 += 8) {
+                float2 ml[8];
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (c0 + u < n) {
+                        const size_t wrow = seg_record(p, sp, c0 + u, it.rsg, it.kh) * p.row_stride + rl;
+                        ml[u] = __ldcg(&p.ws_ml[wrow]);
+                        v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + wrow * D) + d4);
+                    } else {
+                        ml[u] = make_float2(-FLT_MAX, 0.f);
+                        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float Mb = M;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    Mb = fmaxf(Mb, ml[u].x);
+                const float fs = fast_exp2(M - Mb);  // rescale of the records before this batch
+                L *= fs;
+                O.x *= fs;
+                O.y *= fs;
+                O.z *= fs;
+                O.w *= fs;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float f = fast_exp2(ml[u].x - Mb);
+                    L = fmaf(ml[u].y, f, L);
+                    O.x = fmaf(f, v[u].x, O.x);
+                    O.y = fmaf(f, v[u].y, O.y);
+                    O.z = fmaf(f, v[u].z, O.z);
+                    O.w = fmaf(f, v[u].w, O.w);
+                }
+                M = Mb;
+            }
+            const float inv = L == 0.f ? 1.f : 1.f / L;
+            TO* dst = static_cast<TO*>(p.out) + (out_row0 + rl) * D + 4 * d4;
+            dst[0] = from_float<TO>(O.x * inv);
+            dst[1] = from_float<TO>(O.y * inv);
+            dst[2] = from_float<TO>(O.z * inv);
+            dst[3] = from_float<TO>(O.w * inv);
+        }
+        return;
+    }
     int TPI = (kConsumerWarps * 32) / NI;
     TPI = TPI >= 8 ? 8 : TPI >= 4 ? 4 : TPI >= 2 ? 2 : 1;
     const int per_pass = kT / TPI;
@@ -1063,7 +1121,6 @@ __device__ void merge_segment(const SplitParams& p, const Sched& sc, const int4 
                     fma4(O[j], fa[j], va[j]);
         }
     }
-    const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         for (int o = 1; o < TPI; o <<= 1) {
@@ -1401,7 +1458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int KS = D / 16;  // k-steps of Q K^T
     constexpr int NT = D / 8;   // 8-column tiles of O
     constexpr int ROWS = 16 * MT;
-    constexpr int TS = kConsumerWarps / MT;  // warps per row group
     constexpr int TG = mma_token_groups(D, MT);  // 16-token groups per warp and stage
     constexpr int TPW = kMmaTokens * TG;     // tokens per warp and stage
 
