@@ -386,7 +386,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.spec.dtype,
         "data": "synthetic (seeded N(0,1), random block permutation)",
         "config": {"workload": w.spec.name, "B": w.spec.B, "H": w.spec.H, "KV": w.spec.KV,
                    "D": w.spec.D, "BLOCK": w.spec.BLOCK, "NQ": w.spec.NQ,

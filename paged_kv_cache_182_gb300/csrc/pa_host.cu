@@ -147,6 +147,12 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
     // float32 (CUDA-core path): 3-D {D, KV, rows}, box {D, 1, box_rows}, no swizzle.
     // 16-bit (tensor-core path): 4-D {64, D/64, KV, rows}, box {64, D/64, 1,
     // box_rows} -- one box brings both 64-column halves of box_rows token rows.
+    // L2 fills no wider than one token row of one KV head: with 128-byte rows
+    // (D = 64, 16-bit) a 256-byte promotion would also fetch the neighbouring
+    // head's row, which another CTA reads at another time
+    const CUtensorMapL2promotion promo = static_cast<size_t>(D) * es >= 256
+                                             ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                             : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     CUtensorMap map;
     CUresult rc;
     if (swz) {
@@ -159,7 +165,7 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
         cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
         rc = enc(&map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                 promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(KV),
                               static_cast<cuuint64_t>(key.rows)};
@@ -169,7 +175,7 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
         cuuint32_t estr[3] = {1u, 1u, 1u};
         rc = enc(&map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                 promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (rc != CUDA_SUCCESS)
         return PA_ERR_CUDA;
