@@ -12,11 +12,6 @@ namespace pa {
 constexpr int kConsumerWarps = 8;                     // compute warps per CTA
 constexpr int kProducerWarps = 2;                     // TMA issue: K (+ query, new rows), V
 constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
-// The transposed tensor-core kernel adds two warps that sum the consumer
-// warps' piece-end states of every piece but a CTA's last, so that the
-// consumers go on to the next piece without waiting for one another.
-constexpr int kMergeWarps = 2;
-constexpr int kThreadsT = kThreads + kMergeWarps * 32;
 constexpr int kMaxStages = 32;                        // shared-memory ring depth limit
 constexpr int kMinRing = 3;                           // stages kept before widening scratch
 constexpr int kSubBatch = 4;        // token steps per online-softmax update

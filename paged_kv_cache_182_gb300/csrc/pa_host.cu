@@ -477,8 +477,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     const SplitFn split =
         pick_split(dtype, out_dtype == PA_F32 && dtype != PA_F32, D, mma ? MT : RG);
     int occ = 1, sms = 1;
-    const int threads = mma && MT == 0 ? kThreadsT : kThreads;  // transposed kernel: merge warps
-    rc = prepare_func(reinterpret_cast<const void*>(split), threads, smem, &occ, &sms);
+    rc = prepare_func(reinterpret_cast<const void*>(split), kThreads, smem, &occ, &sms);
     if (rc != PA_OK)
         return rc;
 
@@ -547,7 +546,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(threads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;

@@ -413,12 +413,6 @@ __device__ __forceinline__ void warm_param(const Tp& x)
     }
 }
 
-// Consumer and merge warps of the transposed kernel (named barrier 4).
-__device__ __forceinline__ void merge_group_sync()
-{
-    asm volatile("bar.sync 4, %0;" ::"n"((kConsumerWarps + kMergeWarps) * 32) : "memory");
-}
-
 __device__ __forceinline__ void consumer_bar_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -625,8 +619,6 @@ struct Smem {
     uint64_t* empty;
     uint64_t* q_full;  // [2]
     uint64_t* q_free;  // [2]
-    uint64_t* stash_full;  // transposed kernel: consumer warps' piece-end states written
-    uint64_t* stash_free;  // transposed kernel: the merge warps have summed them
     int* info;
     volatile int* abort_flag;
     const void* zero16;
@@ -648,9 +640,7 @@ __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
     sm.abort_flag = sm.info + 15;
     sm.q_full = reinterpret_cast<uint64_t*>(base + 576);
     sm.q_free = sm.q_full + 2;
-    sm.zero16 = base + 640;  // 256 bytes
-    sm.stash_full = reinterpret_cast<uint64_t*>(base + 896);
-    sm.stash_free = sm.stash_full + 1;
+    sm.zero16 = base + 640;
     sm.entries = reinterpret_cast<int*>(base + 1024);
     sm.split_list = reinterpret_cast<int4*>(base + 3072);
     sm.lens = reinterpret_cast<int*>(base + p.lens_off);
@@ -673,15 +663,13 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
             mbar_init(&sm.q_full[i], 1);
             mbar_init(&sm.q_free[i], kConsumerWarps);
         }
-        mbar_init(sm.stash_full, kConsumerWarps);
-        mbar_init(sm.stash_free, kMergeWarps);
         sm.info[15] = 0;
         for (int i = 0; i < 16; ++i)
             reinterpret_cast<uint4*>(const_cast<void*>(sm.zero16))[i] = make_uint4(0, 0, 0, 0);
         fence_mbar_init();
     }
     const int cap = p.maxb * p.BLOCK;
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    for (int b = threadIdx.x; b < p.B; b += kThreads) {
         int s = p.seq_lens[b];
         if (s < 0 || s > cap) {
             if (blockIdx.x == 0 && p.status)
@@ -1409,17 +1397,16 @@ __device__ __forceinline__ int obuf_lg(int D, int RU)
 // Sums round r of the stashed states of the TS = kConsumerWarps / MT warps of
 // every row: M = max m_t, L = sum l_t 2^(m_t - M), acc = sum o_t 2^(m_t - M);
 // writes out = acc / L for a whole segment, else the partial record
-// (acc, (M, L)).  Warp w holds rows of row group w % MT.  Threads t0 ..
-// t0 + nt - 1 of the CTA.
+// (acc, (M, L)).  Warp w holds rows of row group w % MT.  All consumer threads.
 template <int D, int MT, typename TO>
 __device__ __forceinline__ void sum_warps(const SplitParams& p, const Item& it, int R_cta, int RU, int lg,
-                                          int r, const float2* ml_buf, const float* obuf, int t0, int nt)
+                                          int r, const float2* ml_buf, const float* obuf)
 {
     constexpr int TS = kConsumerWarps / MT;
     const int DRr = 1 << lg;
     const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R +
                             static_cast<size_t>(it.rsg) * p.rows_per_cta;
-    for (int idx = static_cast<int>(threadIdx.x) - t0; idx < (R_cta << lg); idx += nt) {
+    for (int idx = threadIdx.x; idx < (R_cta << lg); idx += kConsumerWarps * 32) {
         const int rl = idx >> lg, dd = idx & (DRr - 1);
         const int grp = rl >> 4, rr = rl & 15;
         float M = -FLT_MAX;
@@ -1747,7 +1734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_float2(o[i][2], o[i][3]);
             }
             consumer_bar_sync();
-            sum_warps<D, MT, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf, 0, kConsumerWarps * 32);
+            sum_warps<D, MT, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf);
         }
         // automatic schedule: the CTA's first and last pieces at most
         if (!it.whole && p.counters && nsplit < kSplitList) {
@@ -1769,13 +1756,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and sums (reduced over the lanes of a row), and O^T += V^T P^T (D x 8 rows),
 // the P fragments moved from the accumulator layout into the operand layout by
 // movmatrix transposes.  Half the MMAs and half the accumulator registers of
-// the 16-row kernel.  Pipeline, schedule and split merges are the same; the
-// piece ends differ: each consumer warp leaves its (max, sum, O) state in
-// shared memory and goes on to the next piece, and two merge warps sum the
-// eight states (stash_full / stash_free barriers).  Only the CTA's last piece
-// is merged by the consumer warps themselves, all 256 threads at once.
+// the 16-row kernel; pipeline, schedule, piece-end and split merges are the
+// same.
 template <typename T, int D, typename TO>
-__global__ void __launch_bounds__(kThreadsT, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     pa_mmat_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap)
 {
@@ -1802,38 +1786,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     grid_dependents_launch();
     const Sched sc = setup_cta(p, sm);
 
-    constexpr int kMergeT0 = (kConsumerWarps + kProducerWarps) * 32;  // first merge-warp thread
-    if (warp >= kConsumerWarps + kProducerWarps) {
-        // Merge warps: piece by piece (as the consumers walk them), sum each
-        // stash of the consumer warps' states and release it.
-        uint32_t sidx = 0;
-        bool ok = true;
-        PieceIter pm;
-        pm.first(p, sc);
-        while (pm.ok && ok) {
-            const Item it = pm.it;
-            pm.next(p, sc);
-            if (!pm.ok)
-                break;  // the CTA's last piece: merged by the consumer warps
-            const int R_cta = min(ROWS, p.R - it.rsg * ROWS);
-            const int lg = obuf_lg(D, R_cta), rounds = D >> lg;
-            for (int r = 0; r < rounds; ++r, ++sidx) {
-                ok = mbar_wait_or_abort(sm.stash_full, sidx & 1, sm.abort_flag, kWaitLimitNs);
-                ok = __all_sync(kFull, ok);
-                if (!ok) {
-                    if (lane == 0)
-                        flag_timeout(p, sm.abort_flag);
-                    break;
-                }
-                sum_warps<D, 1, TO>(p, it, R_cta, R_cta, lg, r, ml_buf, obuf, kMergeT0, kMergeWarps * 32);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(sm.stash_free);
-            }
-        }
-        merge_group_sync();  // every record and output of the non-final pieces is written
-        return;
-    }
     if (warp >= kConsumerWarps) {
         produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
@@ -1852,8 +1804,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t qbuf = smem_u32(sm.scratch + p.qbuf_off);
     uint32_t gt = 0;
     int piece = 0;
-    int nsplit = 0;      // split pieces listed since the last flush (uniform)
-    uint32_t sidx = 0;   // stashes handed to the merge warps
+    int nsplit = 0;  // split pieces listed since the last flush (uniform)
     bool alive = true;
 
     PieceIter pi;
@@ -2051,41 +2002,27 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (lane == 0)
             mbar_arrive(&sm.q_free[piece & 1]);
 
-        // ---- piece end: row sums over the lanes of a row, then this warp's
-        // state goes to shared memory ("stash", one per round of DRr columns)
+        // ---- piece end: row sums over the lanes of a row, then the merge of
+        // the eight warps through shared memory
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             lp[h] += __shfl_xor_sync(kFull, lp[h], 4);
             lp[h] += __shfl_xor_sync(kFull, lp[h], 8);
             lp[h] += __shfl_xor_sync(kFull, lp[h], 16);
         }
-        PieceIter nx = pi;
-        nx.next(p, sc);
-        const bool last = !nx.ok;  // the merge warps take every piece but the last
+        // the previous piece's readers are done with the buffers; uniform abort
+        if (consumer_bar_or(*sm.abort_flag != 0))
+            break;
+        if (g == 0) {
+            ml_buf[warp * 16 + 2 * qd] = make_float2(m[0], lp[0]);
+            ml_buf[warp * 16 + 2 * qd + 1] = make_float2(m[1], lp[1]);
+        }
         const int RU = R_cta;
         const int lg = obuf_lg(D, RU);
         const int DRr = 1 << lg, rounds = D >> lg;
-        bool stop = false;
         for (int r = 0; r < rounds; ++r) {
-            // the merge warps have summed the previous stash
-            if (sidx > 0 && alive) {
-                alive = mbar_wait_or_abort(sm.stash_free, (sidx - 1) & 1, sm.abort_flag, kWaitLimitNs);
-                alive = __all_sync(kFull, alive);
-                if (!alive && lane == 0)
-                    flag_timeout(p, sm.abort_flag);
-            }
-            if (last) {
-                // the previous round's readers are done; uniform abort
-                stop = consumer_bar_or(!alive || *sm.abort_flag != 0);
-                if (stop)
-                    break;
-            } else if (!alive) {
-                continue;
-            }
-            if (r == 0 && g == 0) {
-                ml_buf[warp * 16 + 2 * qd] = make_float2(m[0], lp[0]);
-                ml_buf[warp * 16 + 2 * qd + 1] = make_float2(m[1], lp[1]);
-            }
+            if (r > 0)
+                consumer_bar_sync();  // readers of the previous round are done
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
@@ -2102,18 +2039,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                                 o[mt][2 * hh + e];
                     }
                 }
-            if (last) {
-                consumer_bar_sync();
-                sum_warps<D, 1, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf, 0, kConsumerWarps * 32);
-            } else {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(sm.stash_full);
-                ++sidx;
-            }
+            consumer_bar_sync();
+            sum_warps<D, 1, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf);
         }
-        if (stop)
-            break;
         // automatic schedule: the CTA's first and last pieces at most
         if (!it.whole && p.counters && nsplit < kSplitList) {
             if (threadIdx.x == 0)
@@ -2121,7 +2049,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             ++nsplit;
         }
     }
-    merge_group_sync();  // the merge warps have written their pieces' records
     // uniform over the consumer warps (a late abort flag must not split them)
     if (nsplit > 0 && !consumer_bar_or(*sm.abort_flag != 0))
         flush_split_pieces<D, TO>(p, sc, sm.split_list, nsplit, tot, 2 * ROWS, obuf, kObufFloats);

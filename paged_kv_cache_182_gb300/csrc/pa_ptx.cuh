@@ -87,21 +87,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
-// Like mbar_wait_bounded, but also gives up as soon as *abort_flag is set.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   const volatile int* abort_flag, uint64_t limit_ns)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t start = global_timer_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (*abort_flag || global_timer_ns() - start > limit_ns)
-            return false;
-    }
-}
-
 // Like mbar_wait_bounded, but polls with the non-suspending test (no wake-up
 // latency after the phase completes); bounded by `limit_ns` as well.
 __device__ __forceinline__ bool mbar_spin_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
