@@ -70,6 +70,9 @@ struct CombineParams {
     int stream;  // automatic (balanced) schedule: records are per partition-kernel CTA
     int grid;    // partition-kernel CTAs (automatic schedule)
     int vunits;  // automatic schedule: virtual units charged per segment
+    // fixed partitions: the partition count of a segment follows from its length
+    const int32_t* seq_lens;
+    int partitions, NQ, BLOCK, cap;  // cap = max_blocks * BLOCK (length clamp)
 };
 
 using SplitFn = void (*)(SplitParams, CUtensorMap, CUtensorMap);

@@ -575,6 +575,11 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         cp.stream = partitions == 0 ? 1 : 0;
         cp.grid = static_cast<int>(grid);
         cp.vunits = vunits;
+        cp.seq_lens = seq_lens;
+        cp.partitions = partitions;
+        cp.NQ = NQ;
+        cp.BLOCK = BLOCK;
+        cp.cap = opts->max_blocks * BLOCK;
         const CombineFn comb = pick_combine(out_dtype, D);
         cudaLaunchConfig_t cc{};
         cc.gridDim = dim3(static_cast<unsigned>(B) * KV * NRS, static_cast<unsigned>(row_stride));

@@ -120,7 +120,8 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x)
 // 2k+1: the CTA's first and last piece).
 // Fixed partitions (P >= 1): each segment is split into P ranges of whole
 // blocks (P == 1: no split); the ranges are items dealt to CTAs round-robin;
-// record = item index.
+// range c of segment (b, rsg, kh) writes record ((b P + c) NRS + rsg) KV + kh,
+// so the merge kernel finds a segment's records without the schedule.
 struct Item {
     int b, rsg, kh, past, start, end;
     int whole;  // the piece is its whole segment
@@ -354,7 +355,7 @@ struct PieceIter {
         it.start = c * chunk;
         it.end = min(it.start + chunk, total);
         it.whole = sc.prefix[b + 1] - sc.prefix[b] == 1;
-        it.rec = item;
+        it.rec = ((b * p.partitions + c) * p.NRS + it.rsg) * p.KV + it.kh;
         it.units = 0;
     }
 };
@@ -2057,12 +2058,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -------------------------------------------------------------- merge kernel
 // One CTA of 128 threads per (segment = sequence, row group, KV head; row).
 // It finds the partial records of the segment (automatic mode: the CTAs whose
-// unit ranges overlap the segment; fixed partitions: the segment's items) and
-// merges them: M = max m, L = sum l 2^(m - M), O = sum o 2^(m - M),
-// out = L == 0 ? O : O / L.  The accumulator loads of up to eight records per
-// thread are issued before the (max, sum) loads, so a merge of up to 32
-// (D = 128) or 64 (D = 64) records costs about one L2 round trip.  Whole
-// segments were finished by the partition kernel and are skipped.
+// unit ranges overlap the segment, from the schedule the partition kernel
+// left; fixed partitions: records (b P + c) for its ranges c, the range count
+// following from the sequence length) and merges them: M = max m,
+// L = sum l 2^(m - M), O = sum o 2^(m - M), out = L == 0 ? O : O / L.  The
+// accumulator loads of up to eight records per thread are issued with the
+// (max, sum) loads (with fixed partitions, also with the length load, for all
+// P records), so a merge of up to 32 (D = 128) or 64 (D = 64) records costs
+// about one L2 round trip.  Whole segments were finished by the partition
+// kernel and are skipped.
 constexpr int kCombineFac = 1024;  // records whose factors are kept in shared memory
 
 template <int D, typename TO>
@@ -2078,9 +2082,11 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
     const int R_cta = min(p.rows_per_cta, p.R - rsg * p.rows_per_cta);
     if (rl >= R_cta)
         return;
-    const int2 sc = p.sched[b];
     int n, k0 = 0, rec_first = 0;
+    int2 sc = make_int2(0, 0);
+    int len = 0;
     if (p.stream) {
+        sc = p.sched[b];
         const int2 last = p.sched[p.B - 1];
         const long long W = static_cast<long long>(last.x) + static_cast<long long>(last.y) * U;
         const int C = static_cast<int>(W + static_cast<long long>(p.vunits) * p.B * U);
@@ -2091,14 +2097,17 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
         n = ss.n;
         rec_first = ss.rec_first;
     } else {
-        n = sc.y;
+        // fixed partitions: the count follows from the length, which is
+        // loaded together with the records (all P are loaded; those past the
+        // count are never used)
+        len = p.seq_lens[b];
+        n = p.partitions;
     }
-    if (n <= 1)
-        return;
     auto row_of = [&](int c) -> size_t {  // workspace row of record c
         const size_t rec = p.stream ? (c == 0 ? static_cast<size_t>(rec_first)
                                               : static_cast<size_t>(2 * (k0 + c)))
-                                    : (static_cast<size_t>(sc.x + c) * p.NRS + rsg) * p.KV + kh;
+                                    : (static_cast<size_t>(b) * p.partitions + c) * U +
+                                          static_cast<size_t>(rsg) * p.KV + kh;
         return rec * p.row_stride + rl;
     };
     __shared__ float fac[kCombineFac];
@@ -2114,13 +2123,23 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
         if (c < n)
             v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + row_of(c) * D) + d4);
     }
+    // this thread's first (max, sum) pair, loaded with the accumulators
+    float2 first = tid < n ? __ldcg(&p.ws_ml[row_of(tid)]) : make_float2(-FLT_MAX, 0.f);
+    if (!p.stream) {
+        const int s = len < 0 ? 0 : len > p.cap ? p.cap : len;  // the partition kernel's clamp
+        const int total = s + p.NQ;
+        const int per = (total + p.partitions - 1) / p.partitions;
+        const int chunk = ((per + p.BLOCK - 1) / p.BLOCK) * p.BLOCK;
+        n = (total + chunk - 1) / chunk;
+        if (tid >= n)
+            first = make_float2(-FLT_MAX, 0.f);
+    }
+    if (n <= 1)
+        return;  // a whole segment: written by the partition kernel
     // M and L over the records (threads split them; block reductions)
-    float2 first = make_float2(-FLT_MAX, 0.f);
     float M = -FLT_MAX;
     for (int c = tid; c < n; c += 128) {
-        const float2 ml = __ldcg(&p.ws_ml[row_of(c)]);
-        if (c == tid)
-            first = ml;
+        const float2 ml = c == tid ? first : __ldcg(&p.ws_ml[row_of(c)]);
         M = fmaxf(M, ml.x);
     }
 #pragma unroll
