@@ -1386,11 +1386,11 @@ __device__ __forceinline__ RowAddr row_addr(uint32_t tile, uint32_t fresh, uint3
 __device__ __forceinline__ int obuf_swz(int row) { return ((row >> 1) & 3) << 3; }
 
 // log2 of the round width: the widest power of two <= D whose round of RU
-// rows from every consumer warp fits kObufFloats.
-__device__ __forceinline__ int obuf_lg(int D, int RU)
+// rows from every consumer warp fits `cap` floats.
+__device__ __forceinline__ int obuf_lg(int D, int RU, int cap = kObufFloats)
 {
     int lg = 31 - __clz(D);
-    while (lg > 3 && kConsumerWarps * RU * (1 << lg) > kObufFloats)
+    while (lg > 3 && kConsumerWarps * RU * (1 << lg) > cap)
         --lg;
     return lg;
 }
@@ -1554,6 +1554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e)
                 o[i][e] = 0.f;
 
+        // The warps of the piece's last stage keep its slot until the piece-end
+        // merge is done: its 64 KB serve as the merge buffer (one round).
+        int s_hold = -1;
         for (int j = 0; j < ntiles; ++j, ++gt) {
             if (static_cast<int>(gt % nsets) != my_set)
                 continue;  // another warp set's stage
@@ -1574,8 +1577,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_tile = min(TT, it.end - t0);
             if (tb >= n_tile) {  // the stage ends before this warp's tokens
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.empty[s]);
+                if (j + 1 < ntiles) {
+                    if (lane == 0)
+                        mbar_arrive(&sm.empty[s]);
+                } else {
+                    s_hold = s;
+                }
                 continue;
             }
             // a group whose every token is visible to every row of the warp
@@ -1683,8 +1690,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_16816<kBf>(o[2 * pp + 1], alo[u], v10, v11);
                 }
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&sm.empty[s]);
+            if (j + 1 < ntiles) {
+                if (lane == 0)
+                    mbar_arrive(&sm.empty[s]);
+            } else {
+                s_hold = s;
+            }
         }
         // Release the query buffer only now.  ldmatrix completes asynchronously
         // and the fragments are first consumed by the MMAs of the tile loop: a
@@ -1712,10 +1723,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int rows_used = min(16, max(0, R_cta - row0));
         // Rounds of DRr columns: each warp writes its rows (at most RU) of the
-        // round's columns to obuf, then all threads sum the TS warps of each
-        // row.  With few rows per segment one round covers all D columns.
+        // round's columns to the merge buffer, then all threads sum the TS
+        // warps of each row.  The buffer is the piece's last stage (every warp
+        // is past its tile loop here, and the stage's slot is not yet
+        // released), so one round covers all D columns.
+        float* mbuf = reinterpret_cast<float*>(sm.ring + static_cast<size_t>((gt - 1) % S) * p.stage_bytes);
+        const int mcap = p.stage_bytes / 4;
         const int RU = min(16, R_cta);
-        const int lg = obuf_lg(D, RU);
+        const int lg = obuf_lg(D, RU, mcap);
         const int DRr = 1 << lg, TPR = DRr / 8, rounds = D >> lg;
         for (int r = 0; r < rounds; ++r) {
             if (r > 0)
@@ -1727,16 +1742,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int dd = (i - r * TPR) * 8 + 2 * qd;
                 if (g < rows_used)
                     *reinterpret_cast<float2*>(
-                        &obuf[((warp * RU + g) << lg) + ((dd ^ obuf_swz(g)) & (DRr - 1))]) =
+                        &mbuf[((warp * RU + g) << lg) + ((dd ^ obuf_swz(g)) & (DRr - 1))]) =
                         make_float2(o[i][0], o[i][1]);
                 if (g + 8 < rows_used)
                     *reinterpret_cast<float2*>(
-                        &obuf[((warp * RU + g + 8) << lg) + ((dd ^ obuf_swz(g + 8)) & (DRr - 1))]) =
+                        &mbuf[((warp * RU + g + 8) << lg) + ((dd ^ obuf_swz(g + 8)) & (DRr - 1))]) =
                         make_float2(o[i][2], o[i][3]);
             }
             consumer_bar_sync();
-            sum_warps<D, MT, TO>(p, it, R_cta, RU, lg, r, ml_buf, obuf);
+            sum_warps<D, MT, TO>(p, it, R_cta, RU, lg, r, ml_buf, mbuf);
         }
+        // the stage goes back to the producer (its TMA writes follow these
+        // generic-proxy accesses)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && s_hold >= 0)
+            mbar_arrive(&sm.empty[s_hold]);
         // automatic schedule: the CTA's first and last pieces at most
         if (!it.whole && p.counters && nsplit < kSplitList) {
             if (threadIdx.x == 0)
