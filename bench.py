@@ -286,28 +286,29 @@ def e2e_steps(w, device, steps, warmup):
     (binding.HostPlan -> pa_decode_host): per step the step's inputs (q, table,
     lengths, new rows) go host->device from pinned memory, the kernels run, the
     output comes back to pinned host memory and the host waits for it; the KV
-    cache stays resident in HBM."""
+    cache stays resident in HBM, rotated over copies larger than L2 in all."""
     from paged_kv_cache_182_gb300 import binding
 
-    kc, vc = w.k_cache.to(device), w.v_cache.to(device)
+    kc, vc, _ = rotation_copies(w, device)  # more than 3x L2, as for the device-timed value
     host = [t.pin_memory() for t in (w.q, w.block_table, w.seq_lens, w.k_new, w.v_new)]
     out = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = out.numel() * out.element_size()
     s = w.spec
-    plan = binding.HostPlan(kc, vc, B=s.B, H=s.H, NQ=s.NQ, max_blocks=int(w.block_table.shape[1]),
-                            scale=s.scale, causal=s.causal, partitions=s.partitions)
+    plans = [binding.HostPlan(k, v, B=s.B, H=s.H, NQ=s.NQ, max_blocks=int(w.block_table.shape[1]),
+                              scale=s.scale, causal=s.causal, partitions=s.partitions)
+             for k, v in zip(kc, vc)]
     stream = torch.cuda.current_stream(device)
 
-    def step():
-        plan.run(*host, out, stream)
+    def step(i):
+        plans[i % len(plans)].run(*host, out, stream)
         stream.synchronize()
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    for i in range(steps):
+        step(i)
     return (time.perf_counter() - t0) / steps * 1e3, h2d, d2h
 
 
