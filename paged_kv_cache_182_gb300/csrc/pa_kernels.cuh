@@ -651,10 +651,11 @@ __device__ __forceinline__ Smem carve(const SplitParams& p, unsigned char* raw)
     return sm;
 }
 
-// All threads: barriers, clamped lengths, the schedule.
-__device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
+// Thread 0: the ring and query-buffer barriers, the abort flag and the zero
+// row.  Touches no global memory, so it runs before the grid-dependency wait
+// (made visible to the other threads by setup_cta's first CTA barrier).
+__device__ __forceinline__ void init_cta(const SplitParams& p, const Smem& sm)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.full[s], kProducerWarps);
@@ -669,6 +670,13 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
             reinterpret_cast<uint4*>(const_cast<void*>(sm.zero16))[i] = make_uint4(0, 0, 0, 0);
         fence_mbar_init();
     }
+}
+
+// All threads, after init_cta and the grid-dependency wait: clamped lengths,
+// the schedule.
+__device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cap = p.maxb * p.BLOCK;
     for (int b = threadIdx.x; b < p.B; b += kThreads) {
         int s = p.seq_lens[b];
@@ -1219,6 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     warm_param(kmap);
     warm_param(vmap);
     // Inputs may be produced by the previous kernel on the stream.
+    init_cta(p, sm);
     grid_dependency_wait();
     grid_dependents_launch();
     const Sched sc = setup_cta(p, sm);
@@ -1475,6 +1484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     warm_param(p);
     warm_param(kmap);
     warm_param(vmap);
+    init_cta(p, sm);
     grid_dependency_wait();
     grid_dependents_launch();
     const Sched sc = setup_cta(p, sm);
@@ -1804,6 +1814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     warm_param(p);
     warm_param(kmap);
     warm_param(vmap);
+    init_cta(p, sm);
     grid_dependency_wait();
     grid_dependents_launch();
     const Sched sc = setup_cta(p, sm);
