@@ -86,6 +86,10 @@ constexpr int kMmaTokens = 16;  // tokens of one MMA group of the tensor-core ke
 // 16-row groups per pass: 64 KB stages and two independent MMA chains per warp)
 __host__ __device__ constexpr int mma_token_groups(int D, int MT) { return D == 64 || MT == 2 ? 2 : 1; }
 constexpr int kObufFloats = 4096;  // tensor-core kernel: floats of the piece-end merge buffer
+// Bytes per query row in the tensor-core kernels' query buffers: the row plus
+// 16 bytes, so that the 8 rows an ldmatrix reads at once fall in 8 different
+// bank groups (a 128- or 256-byte stride puts them all in one).
+__host__ __device__ constexpr int q_row_bytes(int D) { return D * 2 + 16; }
 SplitFn pick_split_f32(int D, int RG);
 SplitFn pick_split_f16(bool f32_out, int D, int MT);
 SplitFn pick_split_bf16(bool f32_out, int D, int MT);

@@ -456,7 +456,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     // kObufFloats floats of merge rounds and two query-row buffers; CUDA-core
     // path, per-warp states
     const int qbuf_off = 2048 + kObufFloats * 4;
-    const int merge_bytes = mma ? qbuf_off + 2 * ROWS * D * es
+    const int merge_bytes = mma ? qbuf_off + 2 * ROWS * q_row_bytes(D)
                                 : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4 +
                                       kConsumerWarps * RG * 8;
     const int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));

@@ -833,14 +833,22 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
                     break;
                 }
             }
-            if (role == 0 && lane == 0) {
+            if (role == 0) {
+                // one bulk copy per row (lane r: row r) into rows padded to
+                // q_row_bytes(D); the expected bytes are set first
                 const int rows = min(p.rows_per_cta, p.R - it.rsg * p.rows_per_cta);
-                const uint32_t qb = static_cast<uint32_t>(rows * D * sizeof(T));
-                const size_t off =
-                    ((static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta) * D;
-                unsigned char* dst = sm.scratch + p.qbuf_off + par * p.rows_per_cta * D * sizeof(T);
-                mbar_arrive_expect_tx(&sm.q_full[par], qb);
-                bulk_load(dst, static_cast<const T*>(p.q) + off, qb, &sm.q_full[par]);
+                const uint32_t rb = static_cast<uint32_t>(D * sizeof(T));
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&sm.q_full[par], rows * rb);
+                __syncwarp();
+                if (lane < rows) {
+                    const size_t off =
+                        ((static_cast<size_t>(it.b) * p.KV + it.kh) * p.R + it.rsg * p.rows_per_cta + lane) *
+                        D;
+                    unsigned char* dst =
+                        sm.scratch + p.qbuf_off + (par * p.rows_per_cta + lane) * q_row_bytes(D);
+                    bulk_load(dst, static_cast<const T*>(p.q) + off, rb, &sm.q_full[par]);
+                }
             }
         }
         const int t0 = it.start + (cur.j << p.lg_tt);
@@ -1540,7 +1548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     flag_timeout(p, sm.abort_flag);
             }
             const int qrow = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const uint32_t qaddr = qbuf + (par * ROWS + qrow) * (D * 2) + ((lane >> 4) << 4);
+            const uint32_t qaddr = qbuf + (par * ROWS + qrow) * q_row_bytes(D) + ((lane >> 4) << 4);
             const bool r0ok = row0 + g < R_cta, r1ok = row0 + g + 8 < R_cta;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -1869,7 +1877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!alive && lane == 0)
                     flag_timeout(p, sm.abort_flag);
             }
-            const uint32_t qaddr = qbuf + (par * ROWS + (lane & 7)) * (D * 2) + ((lane >> 3) << 4);
+            const uint32_t qaddr = qbuf + (par * ROWS + (lane & 7)) * q_row_bytes(D) + ((lane >> 3) << 4);
             const bool rok = g < R_cta;  // rows past the pass hold stale shared memory
 #pragma unroll
             for (int kk = 0; kk < KS / 2; ++kk) {
