@@ -678,38 +678,46 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cap = p.maxb * p.BLOCK;
-    for (int b = threadIdx.x; b < p.B; b += kThreads) {
-        int s = p.seq_lens[b];
-        if (s < 0 || s > cap) {
-            if (blockIdx.x == 0 && p.status)
-                atomicOr(p.status, PA_STATUS_BAD_LENGTH);
-            s = s < 0 ? 0 : cap;
-        }
-        sm.lens[b] = s;
-    }
-    __syncthreads();
-    if (warp == 0)
-        build_schedule(p, sm.lens, sm.prefix, sm.info, lane);
-    __syncthreads();
     Sched sc;
     sc.lens = sm.lens;
     sc.prefix = sm.prefix;
+    // Warp 0 alone: lengths, schedule and (automatic mode) this CTA's range,
+    // with warp barriers in between and one CTA barrier at the end.
+    if (warp == 0) {
+#pragma unroll 4
+        for (int b = lane; b < p.B; b += 32) {
+            int s = p.seq_lens[b];
+            if (s < 0 || s > cap) {
+                if (blockIdx.x == 0 && p.status)
+                    atomicOr(p.status, PA_STATUS_BAD_LENGTH);
+                s = s < 0 ? 0 : cap;
+            }
+            sm.lens[b] = s;
+        }
+        __syncwarp();
+        build_schedule(p, sm.lens, sm.prefix, sm.info, lane);
+        __syncwarp();
+        sc.total = sm.info[1];
+        sc.cost = sc.total + static_cast<long long>(p.vunits) * p.B * p.NRS * p.KV;
+        if (p.partitions == 0) {
+            // G = min(CTAs, C): every CTA inside a segment then holds a unit.
+            // Lanes 0 and 1 locate the starts of this CTA's range and the next's.
+            const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), sc.cost));
+            if (lane < 2) {
+                const CostPos c = static_cast<int>(blockIdx.x) < G
+                                      ? cost_start(p, sc, blockIdx.x + lane, G)
+                                      : CostPos{0, 0, 0, 0};
+                sm.info[2 + 4 * lane] = c.x;
+                sm.info[3 + 4 * lane] = c.b;
+                sm.info[4 + 4 * lane] = c.seg;
+                sm.info[5 + 4 * lane] = c.uu;
+            }
+        }
+    }
+    __syncthreads();
     sc.total = sm.info[1];
     sc.cost = sc.total + static_cast<long long>(p.vunits) * p.B * p.NRS * p.KV;
     if (p.partitions == 0) {
-        // G = min(CTAs, C): every CTA inside a segment then holds a unit.
-        // Lanes 0 and 1 locate the starts of this CTA's range and the next's.
-        const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), sc.cost));
-        if (warp == 0 && lane < 2) {
-            const CostPos c = static_cast<int>(blockIdx.x) < G
-                                  ? cost_start(p, sc, blockIdx.x + lane, G)
-                                  : CostPos{0, 0, 0, 0};
-            sm.info[2 + 4 * lane] = c.x;
-            sm.info[3 + 4 * lane] = c.b;
-            sm.info[4 + 4 * lane] = c.seg;
-            sm.info[5 + 4 * lane] = c.uu;
-        }
-        __syncthreads();
         sc.pos0 = sm.info[2];
         sc.b0 = sm.info[3];
         sc.seg0 = sm.info[4];
