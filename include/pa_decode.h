@@ -168,10 +168,13 @@ int pa_decode_static_workspace(const void *q, const void *k_cache, const void *v
  * follow the same zero rule), then the device copies of the inputs and of the
  * output.
  *
- * Enqueues on `stream`: one host-to-device copy per input, the decode, and the
- * device-to-host copy of the output.  Returns without waiting: `out` holds the
- * result once the stream has passed that copy (synchronise the stream before
- * reading it, and do not modify the inputs before then).  Errors as pa_decode;
+ * Enqueues on `stream`: the inputs' move to the device, the decode, and the
+ * device-to-host copy of the output.  When every input lies in page-locked
+ * memory (cudaHostAlloc / cudaHostRegister, 4-byte aligned), one gather kernel
+ * reads them through their device addresses; otherwise each input gets its
+ * own host-to-device copy.  Returns without waiting: `out` holds the result
+ * once the stream has passed that copy (synchronise the stream before reading
+ * it, and do not modify the inputs before then).  Errors as pa_decode;
  * PA_ERR_WORKSPACE when the workspace is too small.
  */
 int pa_decode_host(const void *q, const void *k_cache, const void *v_cache,

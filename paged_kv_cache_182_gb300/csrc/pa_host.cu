@@ -597,6 +597,50 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
 }
 
 // ------------------------------------------------------- host-buffer entry
+// Inputs in page-locked host memory are readable by the device (unified
+// addressing): one gather kernel then moves all of them into the staging area,
+// in place of one copy per input.  Segment k of blockIdx.y: 16-byte words when
+// both ends are 16-byte aligned, else 4-byte words.
+struct GatherParams {
+    const void* src[5];
+    void* dst[5];
+    int bytes[5];
+};
+
+__global__ void __launch_bounds__(256) pa_gather_kernel(const __grid_constant__ GatherParams g)
+{
+    const int k = blockIdx.y;
+    const int n = g.bytes[k];
+    const int t = blockIdx.x * blockDim.x + threadIdx.x, nt = gridDim.x * blockDim.x;
+    if (((reinterpret_cast<uintptr_t>(g.src[k]) | reinterpret_cast<uintptr_t>(g.dst[k])) & 15) == 0) {
+        const uint4* s = static_cast<const uint4*>(g.src[k]);
+        uint4* d = static_cast<uint4*>(g.dst[k]);
+        for (int i = t; i < n / 16; i += nt)
+            d[i] = s[i];
+        const int* s4 = static_cast<const int*>(g.src[k]);
+        int* d4 = static_cast<int*>(g.dst[k]);
+        for (int i = (n / 16) * 4 + t; i < n / 4; i += nt)
+            d4[i] = s4[i];
+    } else {
+        const int* s4 = static_cast<const int*>(g.src[k]);
+        int* d4 = static_cast<int*>(g.dst[k]);
+        for (int i = t; i < n / 4; i += nt)
+            d4[i] = s4[i];
+    }
+}
+
+// Device address of a host pointer when it lies in page-locked (registered or
+// cudaHostAlloc) memory, else nullptr.  Looked up on every call: a cached
+// answer could outlive the buffer it was taken for.
+const void* device_view(const void* host)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, host) == cudaSuccess && a.type == cudaMemoryTypeHost)
+        return a.devicePointer;
+    cudaGetLastError();  // a pageable pointer is not an error for the caller
+    return nullptr;
+}
+
 // Device workspace of pa_decode_host: the split workspace first (so that its
 // leading zero bytes stay at offset 0), then 256-aligned staging for q, the
 // table, the lengths, k_new, v_new and the output.
@@ -678,9 +722,31 @@ int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
                {ws + l.lens, seq_lens, static_cast<size_t>(B) * 4},
                {ws + l.knew, k_new, nb},
                {ws + l.vnew, v_new, nb}};
-    for (const auto& c : in)
-        if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    // page-locked inputs (4-byte aligned): one gather kernel; else one copy each
+    GatherParams g{};
+    bool mapped = true;
+    for (int i = 0; i < 5 && mapped; ++i) {
+        const void* dv = device_view(in[i].src);
+        mapped = dv && (reinterpret_cast<uintptr_t>(dv) & 3) == 0 && in[i].bytes < (1u << 30);
+        g.src[i] = dv;
+        g.dst[i] = in[i].dst;
+        g.bytes[i] = static_cast<int>(in[i].bytes);
+    }
+    if (mapped) {
+        size_t big = 0;
+        for (const auto& c : in)
+            big = c.bytes > big ? c.bytes : big;
+        unsigned gx = static_cast<unsigned>((big / 16 + 255) / 256);
+        gx = gx < 1 ? 1 : gx > 64 ? 64 : gx;
+        pa_gather_kernel<<<dim3(gx, 5), 256, 0, st>>>(g);
+        if (cudaGetLastError() != cudaSuccess)
             return PA_ERR_CUDA;
+        g_launches.fetch_add(1);
+    } else {
+        for (const auto& c : in)
+            if (cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+                return PA_ERR_CUDA;
+    }
     pa_opts dev = *opts;
     dev.workspace = split ? ws : nullptr;
     dev.workspace_bytes = split;

@@ -264,3 +264,27 @@ def test_host_entry_point_matches_device_call(name, P):
         want_dev = pu.run_gpu(w, partitions=P, out_dtype=torch.float32).cpu()
         assert torch.equal(out, want_dev), f"{name} P={P} step {rep}"
         pu.check(out, pu.run_oracle(w), s.dtype, "f32", f"{name} P={P} host step {rep}")
+
+
+def test_host_entry_point_pageable_buffers():
+    """Inputs and output in pageable host memory take the one-copy-per-input
+    path (no device view of them); the result equals that of pinned buffers,
+    which the device reads with one gather kernel."""
+    from paged_kv_cache_182_gb300 import binding
+
+    w = W.make(small("gqa_fp16"), seed=22)
+    s = w.spec
+    plan = binding.HostPlan(w.k_cache.cuda(), w.v_cache.cuda(), B=s.B, H=s.H, NQ=s.NQ,
+                            max_blocks=int(w.block_table.shape[1]), scale=s.scale,
+                            causal=s.causal, partitions=0, out_dtype=torch.float32)
+    outs = []
+    for pinned in (False, True):
+        host = [t.clone().pin_memory() if pinned else t.clone()
+                for t in (w.q, w.block_table, w.seq_lens, w.k_new, w.v_new)]
+        out = torch.full(w.q.shape, float("nan"), dtype=torch.float32)
+        out = out.pin_memory() if pinned else out
+        plan.run(*host, out)
+        torch.cuda.synchronize()
+        outs.append(out.clone())
+    assert torch.equal(outs[0], outs[1])
+    pu.check(outs[0], pu.run_oracle(w), s.dtype, "f32", "pageable host buffers")
