@@ -248,6 +248,7 @@ class HostPlan:
                            status=None, trace_begin=None, trace_split=None, merge_kernel=0)
         self._fixed = (ctypes.c_float(scale), H, KV, D, BLOCK, NQ, int(bool(causal)),
                        ctypes.byref(self.opts))
+        self._kc, self._vc = _ptr(k_cache), _ptr(v_cache)
 
     def run(self, q, block_table, seq_lens, k_new, v_new, out, stream=None):
         """Enqueue one step on ``stream`` (default: torch's current stream).  All
@@ -270,10 +271,13 @@ class HostPlan:
         if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
             raise TypeError("block_table and seq_lens must be int32")
         k_cache, v_cache = self.caches
-        with torch.cuda.device(self.device):
-            rc = LIB.pa_decode_host(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                                    _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(out),
-                                    *self._fixed, _stream_handle(stream))
+        args = (_ptr(q), self._kc, self._vc, _ptr(block_table), _ptr(seq_lens), _ptr(k_new),
+                _ptr(v_new), _ptr(out), *self._fixed)
+        if torch.cuda.current_device() == self.device.index:
+            rc = LIB.pa_decode_host(*args, _stream_handle(stream))
+        else:
+            with torch.cuda.device(self.device):
+                rc = LIB.pa_decode_host(*args, _stream_handle(stream))
         if rc != 0:
             raise PagedAttentionError(rc)
         return out
