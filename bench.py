@@ -109,14 +109,19 @@ def aggregate(rank_bytes: int, rank_ms: float, world: int):
 
 
 def kernel_sources_sha256() -> str:
+    """Hash of the CUDA sources and the C header with comments and whitespace
+    removed, so that a comment edit does not retire a capture of the same code."""
     import hashlib
+    import re
 
+    token = re.compile(r'("(?:\\.|[^"\\\n])*")|(//[^\n]*)|(/\*.*?\*/)', re.S)
     files = sorted((ROOT / "paged_kv_cache_182_gb300" / "csrc").glob("*.cu*"))
     files.append(ROOT / "include" / "pa_decode.h")
     h = hashlib.sha256()
     for f in files:
+        code = token.sub(lambda m: m.group(1) or " ", f.read_text())
         h.update(f.name.encode())
-        h.update(f.read_bytes())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()
 
 

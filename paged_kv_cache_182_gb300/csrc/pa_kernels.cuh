@@ -1,5 +1,5 @@
 // pa_kernels.cuh -- the sm_103a kernels of decode attention over a paged KV
-// cache: the persistent partition kernel and the log-sum-exp merge kernel.
+// cache: the persistent partition kernels and the log-sum-exp merge kernel.
 //
 // What is computed follows onnxruntime-ep-mlx 0.31.1,
 // src/ops/paged_attention.rs:
@@ -11,24 +11,30 @@
 //   PARTIALS_REDUCE  max over partitions, rescaled sums, out = sum == 0 ? o : o / sum.
 //
 // How it is computed here (GB300 design, not the page's Metal layout):
-//   * work item = (sequence, contiguous key range of whole blocks, row group,
-//     KV head); the item's CTA serves every query row of its KV head, so each
-//     K/V row is read from HBM once (the page runs one threadgroup per query
-//     head and re-reads K/V H/KV times);
-//   * the kernel is persistent: one CTA per SM walks items blockIdx.x,
-//     blockIdx.x + gridDim.x, ...; key ranges are sized on the device from the
-//     lengths so that the item count is a few times the CTA count (or P ranges
-//     per sequence when the caller fixes the partition count);
-//   * a producer warp streams cache blocks into a shared-memory ring with TMA
-//     tensor copies (one box = one block of one KV head) and the new rows with
-//     bulk copies, completing on mbarriers; it runs ahead across item
-//     boundaries, so HBM keeps streaming while the consumers merge an item;
-//   * eight consumer warps compute in float32: 16-byte shared-memory vector
-//     reads, packed f32x2 FMAs, warp-shuffle dot reductions and an online
-//     base-2 softmax updated once per four token steps;
-//   * an item that covers a whole sequence writes the normalised output;
-//     otherwise its partial state goes to the workspace and the merge kernel,
-//     launched with programmatic dependent launch, combines the partials.
+//   * a segment is (sequence, row group, KV head) over its keys; its CTA serves
+//     every query row of the KV head, so each K/V row is read from HBM once
+//     (the page runs one threadgroup per query head and re-reads K/V H/KV
+//     times);
+//   * the kernels are persistent, one CTA per SM.  Automatic split: the
+//     segments, cut into stage-sized units, are laid end to end and each CTA
+//     takes a cost-balanced contiguous range, computed on the device from the
+//     lengths (schedule section below); fixed partitions: P ranges of whole
+//     blocks per segment dealt round-robin;
+//   * two producer warps stream cache blocks into a shared-memory ring with
+//     TMA tensor copies (one box = one block of one KV head; K by one warp, V
+//     by the other) and the query and new rows with bulk copies, completing on
+//     mbarriers; they run ahead across piece boundaries;
+//   * eight consumer warps: 16-bit caches on tensor cores (mma.sync
+//     m16n8k16, float32 accumulators) -- pa_mmat_kernel with the tokens on the
+//     MMA's 16-row side for at most 8 query rows per KV head, pa_mma_kernel
+//     with the query rows there otherwise; float32 caches on CUDA cores
+//     (pa_split_kernel: 16-byte shared-memory reads, FMAs, warp-shuffle dot
+//     reductions); an online base-2 softmax throughout;
+//   * a piece that covers a whole segment writes the normalised output;
+//     otherwise its partial state goes to the workspace, and the last CTA to
+//     finish a split segment merges it in the kernel (automatic split) or the
+//     merge kernel, launched with programmatic dependent launch, combines the
+//     partials (fixed partitions).
 //
 // Every wait is bounded (PA_STATUS_TIMEOUT); no kernel traps.
 #pragma once
