@@ -1435,26 +1435,11 @@ __device__ __forceinline__ void sum_warps(const SplitParams& p, const Item& it, 
                                           int r, const float2* ml_buf, const float* obuf)
 {
     constexpr int TS = kConsumerWarps / MT;
+    constexpr int NT = kConsumerWarps * 32;
     const int DRr = 1 << lg;
     const size_t out_row0 = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.R +
                             static_cast<size_t>(it.rsg) * p.rows_per_cta;
-    for (int idx = threadIdx.x; idx < (R_cta << lg); idx += kConsumerWarps * 32) {
-        const int rl = idx >> lg, dd = idx & (DRr - 1);
-        const int grp = rl >> 4, rr = rl & 15;
-        float M = -FLT_MAX;
-#pragma unroll
-        for (int t = 0; t < TS; ++t)
-            M = fmaxf(M, ml_buf[(t * MT + grp) * 16 + rr].x);
-        float L = 0.f, acc = 0.f;
-        const int col = (dd ^ obuf_swz(rr)) & (DRr - 1);
-#pragma unroll
-        for (int t = 0; t < TS; ++t) {
-            const float2 ml = ml_buf[(t * MT + grp) * 16 + rr];
-            const float f = fast_exp2(ml.x - M);
-            L = fmaf(ml.y, f, L);
-            acc = fmaf(f, obuf[(((t * MT + grp) * RU + rr) << lg) + col], acc);
-        }
-        const int d = (r << lg) + dd;
+    auto put = [&](int rl, int d, float M, float L, float acc) {
         if (it.whole) {
             const float val = L == 0.f ? acc : acc / L;
             static_cast<TO*>(p.out)[(out_row0 + rl) * D + d] = from_float<TO>(val);
@@ -1463,6 +1448,57 @@ __device__ __forceinline__ void sum_warps(const SplitParams& p, const Item& it, 
             p.ws_o[wrow * D + d] = acc;
             if (d == 0)
                 p.ws_ml[wrow] = make_float2(M, L);
+        }
+    };
+    if constexpr (MT >= 2) {
+        // 32 rows: tpr threads per row (a power of two), each computes the
+        // row's factors 2^(m_t - M) once and sums its columns of the round
+        // with them (measured faster on 32 rows, slower on 4)
+        int tpr = 1;
+        while (tpr * 2 * R_cta <= NT && tpr * 2 <= DRr)
+            tpr *= 2;
+        for (int rl = static_cast<int>(threadIdx.x) / tpr; rl < R_cta; rl += NT / tpr) {
+            const int grp = rl >> 4, rr = rl & 15;
+            float M = -FLT_MAX;
+#pragma unroll
+            for (int t = 0; t < TS; ++t)
+                M = fmaxf(M, ml_buf[(t * MT + grp) * 16 + rr].x);
+            float f[TS];
+            float L = 0.f;
+#pragma unroll
+            for (int t = 0; t < TS; ++t) {
+                const float2 ml = ml_buf[(t * MT + grp) * 16 + rr];
+                f[t] = fast_exp2(ml.x - M);
+                L = fmaf(ml.y, f[t], L);
+            }
+            for (int dd = static_cast<int>(threadIdx.x) & (tpr - 1); dd < DRr; dd += tpr) {
+                const int col = (dd ^ obuf_swz(rr)) & (DRr - 1);
+                float acc = 0.f;
+#pragma unroll
+                for (int t = 0; t < TS; ++t)
+                    acc = fmaf(f[t], obuf[(((t * MT + grp) * RU + rr) << lg) + col], acc);
+                put(rl, (r << lg) + dd, M, L, acc);
+            }
+        }
+    } else {
+        // few rows: one output per thread and pass, factors per output
+        for (int idx = threadIdx.x; idx < (R_cta << lg); idx += NT) {
+            const int rl = idx >> lg, dd = idx & (DRr - 1);
+            const int grp = rl >> 4, rr = rl & 15;
+            float M = -FLT_MAX;
+#pragma unroll
+            for (int t = 0; t < TS; ++t)
+                M = fmaxf(M, ml_buf[(t * MT + grp) * 16 + rr].x);
+            float L = 0.f, acc = 0.f;
+            const int col = (dd ^ obuf_swz(rr)) & (DRr - 1);
+#pragma unroll
+            for (int t = 0; t < TS; ++t) {
+                const float2 ml = ml_buf[(t * MT + grp) * 16 + rr];
+                const float f = fast_exp2(ml.x - M);
+                L = fmaf(ml.y, f, L);
+                acc = fmaf(f, obuf[(((t * MT + grp) * RU + rr) << lg) + col], acc);
+            }
+            put(rl, (r << lg) + dd, M, L, acc);
         }
     }
 }
