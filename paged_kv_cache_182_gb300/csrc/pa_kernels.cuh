@@ -1514,9 +1514,9 @@ __device__ __forceinline__ void sum_warps(const SplitParams& p, const Item& it, 
 // O += P V with P kept in registers as a 16-bit high part plus a 16-bit
 // remainder (P V keeps about 22 bits of P).  Warps never wait for one another
 // inside a piece; at the end of a piece their (max, sum, O) states are merged
-// through shared memory in column rounds (one when the rows are few).  The
-// query rows of each piece arrive in one of two shared buffers filled by the
-// producer.
+// through shared memory, in the piece's last stage, whose slot the warps keep
+// until the merge is done.  The query rows of each piece arrive in one of two
+// shared buffers filled by the producer.
 template <typename T, int D, int MT, typename TO>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_mma_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap kmap,
@@ -1533,7 +1533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Smem sm = carve(p, smem_raw);
     float2* ml_buf = reinterpret_cast<float2*>(sm.scratch);         // [warps][16] (max, sum)
     float2* tot = reinterpret_cast<float2*>(sm.scratch + 1024);     // [ROWS] merged (max, sum)
-    float* obuf = reinterpret_cast<float*>(sm.scratch + 2048);      // kObufFloats merge rounds
+    float* obuf = reinterpret_cast<float*>(sm.scratch + 2048);      // kObufFloats: split-merge factors
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
