@@ -25,6 +25,7 @@ bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -365,6 +366,49 @@ def per_workload_table(device, steps, warmup, peak):
     return rows
 
 
+def append_timing(device, steps=200, warmup=10):
+    """pa_cache_append on the causal-append workload: the step's new rows
+    written over the slots of each sequence's last NQ cached tokens, back to
+    back on rotated copies of the pools; bytes = new rows read + cache rows
+    written, K and V."""
+    from paged_kv_cache_182_gb300 import binding
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    w = W.make("causal_append_fp16", seed=0, poison=False)
+    s = w.spec
+    slots = torch.full((s.B, s.NQ), -1, dtype=torch.int32)
+    for b in range(s.B):
+        past = int(w.seq_lens[b])
+        for j in range(s.NQ):
+            t = past - s.NQ + j
+            if t >= 0:
+                slots[b, j] = int(w.block_table[b, t // s.BLOCK]) * s.BLOCK + t % s.BLOCK
+    kc, vc, _ = rotation_copies(w, device)
+    kn, vn, sl = w.k_new.to(device), w.v_new.to(device), slots.to(device)
+    stream = torch.cuda.current_stream(device)
+    binding.cache_append(kc[0], vc[0], kn, vn, sl, stream=stream)  # argument checks once
+    # then the C entry point with prepared arguments, as a bound decode plan does
+    args = [[ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+             ctypes.c_void_p(kn.data_ptr()), ctypes.c_void_p(vn.data_ptr()),
+             ctypes.c_void_p(sl.data_ptr()), s.B, s.KV, s.D, s.NQ, s.BLOCK,
+             int(w.k_cache.shape[0]), binding.PA_F16, None, ctypes.c_void_p(stream.cuda_stream)]
+            for k, v in zip(kc, vc)]
+    for i in range(warmup):
+        binding.LIB.pa_cache_append(*args[i % len(args)])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        binding.LIB.pa_cache_append(*args[i % len(args)])
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / steps * 1e3
+    moved = 2 * 2 * int((slots >= 0).sum()) * s.KV * s.D * w.k_new.element_size()
+    return {"kernel": "pa_append_kernel", "workload": "causal_append_fp16 new rows",
+            "us_per_call": round(us, 2), "bytes_per_call": moved,
+            "GB_per_s": round(moved / (us * 1e-6) / 1e9, 1)}
+
+
 def run_ours(args, rank, world, local):
     from paged_kv_cache_182_gb300 import binding  # noqa: F401  (fails loudly if not built)
     from paged_kv_cache_182_gb300 import workloads as W
@@ -414,6 +458,7 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and not args.no_extras:
         line["per_workload"] = per_workload_table(device, 50, 5, peak)
+        line["cache_append"] = append_timing(device)
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -66,6 +66,7 @@ extern "C" {
 #define PA_STATUS_BAD_BLOCK 1  /* checked mode: a table entry outside [0, num_blocks) */
 #define PA_STATUS_BAD_LENGTH 2 /* seq_lens[b] < 0 or > max_blocks * BLOCK (clamped) */
 #define PA_STATUS_TIMEOUT 4    /* an internal wait gave up (the output is undefined) */
+#define PA_STATUS_BAD_SLOT 8   /* pa_cache_append: a slot < -1 or >= num_blocks * BLOCK (skipped) */
 
 /* supported sizes */
 #define PA_MAX_NQ 16
@@ -205,6 +206,33 @@ size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partition
  * 0 unless partitions == 0.  Returns 0 for invalid arguments.
  */
 size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions);
+
+/*
+ * Writes the step's new rows into the paged cache: for every sequence b, new
+ * row j and KV head kh with s = slot_mapping[b * NQ + j] >= 0,
+ *     k_cache[s / BLOCK][s % BLOCK][kh][:] = k_new[b][kh][j][:]
+ *     v_cache[s / BLOCK][s % BLOCK][kh][:] = v_new[b][kh][j][:]
+ * (a slot is physical_block * BLOCK + offset, the cache position that the
+ * block table gives a logical token: table[b][t / BLOCK] * BLOCK + t % BLOCK).
+ * This is the cache update that follows a decode step on the paged-attention
+ * page, where the host framework writes the rows back after evaluation; here
+ * it is one kernel.  Rows are copied as stored (no conversion).
+ *
+ * k_cache, v_cache: device, [num_blocks][BLOCK][KV][D], written.  k_new,
+ * v_new: device, [B][KV][NQ][D], read.  slot_mapping: device int32 [B][NQ];
+ * -1 skips a row; a slot < -1 or >= num_blocks * BLOCK skips it and ORs
+ * PA_STATUS_BAD_SLOT into *status (device int32, may be NULL).  Slots of one
+ * call should be distinct: when two rows name one slot, one of them lands,
+ * unspecified which.  dtype: PA_F32, PA_F16 or PA_BF16 (D * element bytes a
+ * multiple of 16).  Pointers of the caches and new rows 16-byte aligned,
+ * slot_mapping 4-byte aligned.
+ *
+ * Enqueues one kernel on `stream` (B == 0: nothing) and returns PA_OK, or a
+ * PA_ERR_* code before any launch (NULL pointer, sizes, alignment, dtype).
+ */
+int pa_cache_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                    const int32_t *slot_mapping, int B, int KV, int D, int NQ, int BLOCK,
+                    int num_blocks, int dtype, int *status, void *stream);
 
 /* A sentence naming what to verify for a PA_ERR_* code (static storage). */
 const char *pa_strerror(int code);

@@ -123,3 +123,37 @@ def default() -> Oracle:
 def decode(*args, **kwargs) -> np.ndarray:
     """Module-level shortcut on the default (unmutated) oracle."""
     return default().decode(*args, **kwargs)
+
+
+def cache_append(k_cache, v_cache, k_new, v_new, slot_mapping):
+    """The cache update of a decode step, written out: copies of the caches in
+    which, for every sequence b, new row j and KV head kh whose slot
+    s = slot_mapping[b, j] lies in [0, num_blocks * BLOCK),
+        cache[s // BLOCK, s % BLOCK, kh, :] = new[b, kh, j, :].
+    A slot is a cache row index, physical block * BLOCK + offset, as the
+    decode kernel of the paged-attention page names the slot of new row j
+    (onnxruntime-ep-mlx 0.31.1, src/ops/paged_attention.rs, VECTOR_BODY,
+    position[j + 1]); on that page the host writes these rows back into the
+    cache after evaluation (src/engine.rs, write_back_input_rows).  Slot -1
+    skips a row; any other slot outside the cache skips it and is reported.
+    Works on the stored values (any dtype; bfloat16 as its 16-bit pattern):
+    returns (k_cache', v_cache', bad_slot)."""
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    kn, vn = np.asarray(k_new), np.asarray(v_new)
+    slots = np.asarray(slot_mapping)
+    NB, BLOCK, KV, _ = kc.shape
+    B, _, NQ, _ = kn.shape
+    bad = False
+    for b in range(B):
+        for j in range(NQ):
+            s = int(slots[b, j])
+            if s == -1:
+                continue
+            if s < -1 or s >= NB * BLOCK:
+                bad = True
+                continue
+            for kh in range(KV):
+                kc[s // BLOCK, s % BLOCK, kh, :] = kn[b, kh, j, :]
+                vc[s // BLOCK, s % BLOCK, kh, :] = vn[b, kh, j, :]
+    return kc, vc, bad

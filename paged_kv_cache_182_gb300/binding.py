@@ -21,7 +21,7 @@ import torch
 from . import _build
 
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
-PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LENGTH, PA_STATUS_TIMEOUT = 1, 2, 4
+PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LENGTH, PA_STATUS_TIMEOUT, PA_STATUS_BAD_SLOT = 1, 2, 4, 8
 PA_MAX_NQ = 16
 _DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
@@ -71,6 +71,8 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_strerror.argtypes = [I]
     lib.pa_version.restype = I
     lib.pa_kernel_launches.restype = ctypes.c_uint64
+    lib.pa_cache_append.restype = I
+    lib.pa_cache_append.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P]
     return lib
 
 
@@ -313,3 +315,35 @@ def decode_host(q, block_table, seq_lens, k_new, v_new, *, k_cache, v_cache, sca
     plan.run(q, block_table, seq_lens, k_new, v_new, out, stream)
     stream.synchronize()
     return out
+
+
+def cache_append(k_cache, v_cache, k_new, v_new, slot_mapping, *, status=None, stream=None):
+    """Writes the new rows into the paged cache (pa_cache_append): for every
+    sequence b, new row j and KV head kh with s = slot_mapping[b, j] >= 0,
+    k_cache[s // BLOCK, s % BLOCK, kh] = k_new[b, kh, j] (and the same for V).
+    All tensors on one CUDA device: caches [num_blocks, BLOCK, KV, D], new rows
+    [B, KV, NQ, D] of the caches' dtype, slot_mapping int32 [B, NQ], status an
+    optional int32 device scalar for PA_STATUS_BAD_SLOT.  Enqueued on ``stream``
+    (default: torch's current stream)."""
+    NB, BLOCK, KV, D = k_cache.shape
+    B, kv2, NQ, d2 = k_new.shape
+    dt = k_cache.dtype
+    if dt not in _DT or v_cache.dtype != dt or k_new.dtype != dt or v_new.dtype != dt:
+        raise TypeError("caches and new rows must share one supported dtype")
+    if (tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(v_new.shape) != tuple(k_new.shape)
+            or kv2 != KV or d2 != D or tuple(slot_mapping.shape) != (B, NQ)):
+        raise ValueError("shapes: caches [NB, BLOCK, KV, D], new rows [B, KV, NQ, D], slots [B, NQ]")
+    if slot_mapping.dtype != torch.int32:
+        raise TypeError("slot_mapping must be int32")
+    for x in (k_cache, v_cache, k_new, v_new, slot_mapping):
+        if not (x.is_cuda and x.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    args = (_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), B, KV, D,
+            NQ, BLOCK, NB, _DT[dt], _ptr(status))
+    if torch.cuda.current_device() == k_cache.device.index:
+        rc = LIB.pa_cache_append(*args, _stream_handle(stream))
+    else:
+        with torch.cuda.device(k_cache.device):
+            rc = LIB.pa_cache_append(*args, _stream_handle(stream))
+    if rc != 0:
+        raise PagedAttentionError(rc)

@@ -596,6 +596,49 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     return PA_OK;
 }
 
+// ------------------------------------------------------------ cache append
+// One thread per 16 bytes of one new row of K or V (rows in k_new order
+// [B][KV][NQ]): the slot of the row's (sequence, new row) names the cache row.
+struct AppendParams {
+    uint4* k_cache;
+    uint4* v_cache;
+    const uint4* k_new;
+    const uint4* v_new;
+    const int32_t* slots;  // [B][NQ]
+    int* status;
+    long long rows;        // B * KV * NQ
+    int vpr;               // 16-byte vectors per row (D * element bytes / 16)
+    int KV, NQ;
+    long long num_slots;   // num_blocks * BLOCK
+};
+
+__global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ AppendParams a)
+{
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long per = a.rows * a.vpr;  // vectors of K (or V)
+    if (i >= 2 * per)
+        return;
+    const bool is_v = i >= per;
+    const long long k = is_v ? i - per : i;
+    const long long row = k / a.vpr;
+    const int v = static_cast<int>(k - row * a.vpr);
+    const int j = static_cast<int>(row % a.NQ);
+    const long long bk = row / a.NQ;  // b * KV + kh
+    const int kh = static_cast<int>(bk % a.KV);
+    const long long b = bk / a.KV;
+    const int s = a.slots[b * a.NQ + j];
+    if (s == -1)
+        return;
+    if (s < -1 || s >= a.num_slots) {
+        if (a.status && !is_v && v == 0 && kh == 0)
+            atomicOr(a.status, PA_STATUS_BAD_SLOT);
+        return;
+    }
+    const uint4* src = (is_v ? a.v_new : a.k_new) + row * a.vpr + v;
+    uint4* dst = (is_v ? a.v_cache : a.k_cache) + (static_cast<long long>(s) * a.KV + kh) * a.vpr + v;
+    *dst = *src;
+}
+
 // ------------------------------------------------------- host-buffer entry
 // Inputs in page-locked host memory are readable by the device (unified
 // addressing): one gather kernel then moves all of them into the staging area,
@@ -629,10 +672,53 @@ __global__ void __launch_bounds__(256) pa_gather_kernel(const __grid_constant__ 
     }
 }
 
+int pa_cache_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                    const int32_t* slot_mapping, int B, int KV, int D, int NQ, int BLOCK,
+                    int num_blocks, int dtype, int* status, void* stream)
+{
+    if (B < 0 || KV < 1 || D < 1 || NQ < 1 || BLOCK < 1 || num_blocks < 1)
+        return PA_ERR_BAD_DIMS;
+    if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+        return PA_ERR_UNSUPPORTED;
+    const long long row_bytes = static_cast<long long>(D) * elem_size(dtype);
+    if (row_bytes % 16 != 0)
+        return PA_ERR_UNSUPPORTED;
+    const long long num_slots = static_cast<long long>(num_blocks) * BLOCK;
+    const long long rows = static_cast<long long>(B) * KV * NQ;
+    if (num_slots >= (1ll << 31) || rows * (row_bytes / 16) * 2 >= (1ll << 38))
+        return PA_ERR_BAD_DIMS;
+    if (B == 0)
+        return PA_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping)
+        return PA_ERR_NULL_POINTER;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(slot_mapping, 4))
+        return PA_ERR_ALIGNMENT;
+    AppendParams a{};
+    a.k_cache = static_cast<uint4*>(k_cache);
+    a.v_cache = static_cast<uint4*>(v_cache);
+    a.k_new = static_cast<const uint4*>(k_new);
+    a.v_new = static_cast<const uint4*>(v_new);
+    a.slots = slot_mapping;
+    a.status = status;
+    a.rows = rows;
+    a.vpr = static_cast<int>(row_bytes / 16);
+    a.KV = KV;
+    a.NQ = NQ;
+    a.num_slots = num_slots;
+    const long long threads = 2 * rows * a.vpr;
+    pa_append_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0,
+                       static_cast<cudaStream_t>(stream)>>>(a);
+    if (cudaGetLastError() != cudaSuccess)
+        return PA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return PA_OK;
+}
+
 // Device address of a host pointer when it lies in page-locked (registered or
 // cudaHostAlloc) memory, else nullptr.  Looked up on every call: a cached
 // answer could outlive the buffer it was taken for.
-const void* device_view(const void* host)
+static const void* device_view(const void* host)
 {
     cudaPointerAttributes a{};
     if (cudaPointerGetAttributes(&a, host) == cudaSuccess && a.type == cudaMemoryTypeHost)

@@ -153,3 +153,24 @@ def test_host_entry_point_rejects_before_copying(lib):
     assert go(opts(workspace=0x100000, workspace_bytes=need - 1)) == -5
     assert go(opts(workspace=0x100010, workspace_bytes=need)) == -4
     assert go(opts(workspace=0x100000, workspace_bytes=need, dtype=9)) == -3
+
+
+def test_cache_append_rejects_before_launching(lib):
+    """pa_cache_append's argument checks (these calls run without a GPU)."""
+    f = lib.LIB.pa_cache_append
+    a = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(5)]
+
+    def go(*ptrs, B=2, KV=2, D=64, NQ=1, BLOCK=16, NB=4, dt=lib.PA_F16):
+        p = list(ptrs) if ptrs else a
+        return f(*p, B, KV, D, NQ, BLOCK, NB, dt, None, None)
+
+    launches = lib.kernel_launches()
+    assert go(B=0) == 0  # nothing to do
+    assert go(B=-1) == -2
+    assert go(NQ=0) == -2
+    assert go(dt=7) == -3
+    assert go(D=4) == -3  # D * 2 bytes is not a multiple of 16
+    assert go(None, *a[1:]) == -1
+    assert go(a[0], ctypes.c_void_p(0x20008), *a[2:]) == -4
+    assert go(*a[:4], ctypes.c_void_p(0x50002)) == -4  # slot_mapping 4-byte aligned
+    assert lib.kernel_launches() == launches

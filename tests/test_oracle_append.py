@@ -1,0 +1,73 @@
+"""The oracle's cache append (the cache update of a decode step) against a
+hand-worked example, its skip rules, and the decode it feeds (CPU only)."""
+import numpy as np
+
+import oracle
+import oracle_pins
+
+
+def test_hand_worked_example():
+    # 3 blocks of 2 slots, 1 KV head, D = 2; two sequences, two new rows each
+    kc = np.zeros((3, 2, 1, 2))
+    vc = np.zeros((3, 2, 1, 2))
+    kn = np.array([[[[1.0, 2.0], [3.0, 4.0]]], [[[5.0, 6.0], [7.0, 8.0]]]])  # [B=2][KV=1][NQ=2][D=2]
+    vn = -kn
+    slots = np.array([[3, -1], [0, 5]], dtype=np.int32)  # slot 3 = block 1, offset 1; 5 = block 2, offset 1
+    k2, v2, bad = oracle.cache_append(kc, vc, kn, vn, slots)
+    want_k = np.zeros((3, 2, 1, 2))
+    want_k[1, 1, 0] = [1.0, 2.0]  # sequence 0, new row 0 -> slot 3
+    want_k[0, 0, 0] = [5.0, 6.0]  # sequence 1, new row 0 -> slot 0
+    want_k[2, 1, 0] = [7.0, 8.0]  # sequence 1, new row 1 -> slot 5
+    assert np.array_equal(k2, want_k)
+    assert np.array_equal(v2, -want_k)
+    assert not bad
+    assert not kc.any()  # the inputs are not modified
+
+
+def test_skips_and_reports_bad_slots():
+    rng = np.random.default_rng(1)
+    kc = rng.standard_normal((4, 4, 2, 8))
+    vc = rng.standard_normal((4, 4, 2, 8))
+    kn = rng.standard_normal((3, 2, 2, 8))
+    vn = rng.standard_normal((3, 2, 2, 8))
+    slots = np.array([[-1, 16], [-5, 2], [15, -1]], dtype=np.int32)  # 16 slots in all
+    k2, v2, bad = oracle.cache_append(kc, vc, kn, vn, slots)
+    assert bad
+    touched = {2: (1, 1), 15: (2, 0)}  # slot -> (sequence, new row)
+    for s in range(16):
+        if s in touched:
+            b, j = touched[s]
+            assert np.array_equal(k2[s // 4, s % 4], kn[b, :, j])
+            assert np.array_equal(v2[s // 4, s % 4], vn[b, :, j])
+        else:
+            assert np.array_equal(k2[s // 4, s % 4], kc[s // 4, s % 4])
+            assert np.array_equal(v2[s // 4, s % 4], vc[s // 4, s % 4])
+
+
+def test_append_then_decode_equals_decode_with_new_rows():
+    """Appending new row 0 at the slot of logical token past (table[b][past //
+    BLOCK] * BLOCK + past % BLOCK) and decoding rows 1.. with past + 1 gives
+    bitwise the rows 1.. of decoding all new rows as new rows: the append puts
+    a row exactly where the decode's block-table gather reads token past."""
+    orc = oracle.default()
+    for causal in (False, True):
+        B, H, KV, D, BLOCK, NQ = 3, 4, 2, 8, 4, 3
+        lens = [7, 8, 0]  # 8 and 0 end on a block boundary: the next token needs a new block
+        c = oracle_pins.dense_case(B, H, KV, D, BLOCK, NQ, lens, seed=11, spare_blocks=6)
+        table = c["block_table"].copy()
+        used = set(table[table >= 0].tolist())
+        spare = [p for p in range(c["k_cache"].shape[0]) if p not in used]
+        slots = np.zeros((B, 1), dtype=np.int32)
+        for b, n in enumerate(lens):
+            if table[b, n // BLOCK] < 0:
+                table[b, n // BLOCK] = spare.pop()
+            slots[b, 0] = table[b, n // BLOCK] * BLOCK + n % BLOCK
+        full = orc.decode(c["q"], c["k_cache"], c["v_cache"], table, c["seq_lens"], c["k_new"],
+                          c["v_new"], scale=0.3, causal=causal)
+        kc2, vc2, bad = oracle.cache_append(c["k_cache"], c["v_cache"], c["k_new"][:, :, :1],
+                                            c["v_new"][:, :, :1], slots)
+        assert not bad
+        part = orc.decode(np.ascontiguousarray(c["q"][:, :, 1:]), kc2, vc2, table,
+                          c["seq_lens"] + 1, np.ascontiguousarray(c["k_new"][:, :, 1:]),
+                          np.ascontiguousarray(c["v_new"][:, :, 1:]), scale=0.3, causal=causal)
+        assert np.array_equal(full[:, :, 1:], part), f"causal={causal}"
