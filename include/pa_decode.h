@@ -221,8 +221,9 @@ size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int part
  * k_cache, v_cache: device, [num_blocks][BLOCK][KV][D], written.  k_new,
  * v_new: device, [B][KV][NQ][D], read.  slot_mapping: device int32 [B][NQ];
  * -1 skips a row; a slot < -1 or >= num_blocks * BLOCK skips it and ORs
- * PA_STATUS_BAD_SLOT into *status (device int32, may be NULL).  Slots of one
- * call should be distinct: when two rows name one slot, one of them lands,
+ * PA_STATUS_BAD_SLOT into *status (device int32, may be NULL).  When several
+ * new rows of one sequence name one slot, the last of them (largest j) is
+ * stored; when rows of different sequences name one slot, one of them lands,
  * unspecified which.  dtype: PA_F32, PA_F16 or PA_BF16 (D * element bytes a
  * multiple of 16).  Pointers of the caches and new rows 16-byte aligned,
  * slot_mapping 4-byte aligned.
@@ -233,6 +234,33 @@ size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int part
 int pa_cache_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                     const int32_t *slot_mapping, int B, int KV, int D, int NQ, int BLOCK,
                     int num_blocks, int dtype, int *status, void *stream);
+
+/*
+ * A decode step with slot patching (onnxruntime-ep-mlx 0.31.1,
+ * src/ops/paged_attention.rs, VECTOR_BODY: entry 1 + j of the position
+ * vector).  positions[b * NQ + j] is the cache slot (physical_block * BLOCK +
+ * offset) that new row j of sequence b is bound for, or -1.  On that page the
+ * kernel reads a cached key i < past whose slot a new row of its sequence is
+ * bound for from that new row instead (the last such row wins), and the host
+ * writes the new rows into the cache after the step.  Here the write comes
+ * first: this call enqueues pa_cache_append(k_cache, v_cache, k_new, v_new,
+ * positions, ...) and then pa_decode over the updated cache, so once the
+ * stream has run, the caches hold the new rows and `out` is the page's
+ * read-time substitution, provided no sequence's past covers a slot that a
+ * new row of another sequence is bound for and no two sequences name one
+ * slot (both hold when every sequence owns the blocks it writes).
+ *
+ * Arguments as pa_decode, except: k_cache and v_cache are written (the rows
+ * named by positions); positions is device int32 [batch][NQ], 4-byte aligned,
+ * NULL for a plain pa_decode.  Slots < -1 or >= num_blocks * BLOCK are skipped
+ * and OR PA_STATUS_BAD_SLOT into *opts->status.  Every argument is checked
+ * before the first launch; returns PA_OK or a PA_ERR_* code.
+ */
+int pa_decode_positions(const void *q, void *k_cache, void *v_cache,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        const void *k_new, const void *v_new, const int32_t *positions,
+                        void *out, float scale, int H, int KV, int D, int BLOCK, int NQ,
+                        int causal, const pa_opts *opts, void *stream);
 
 /* A sentence naming what to verify for a PA_ERR_* code (static storage). */
 const char *pa_strerror(int code);

@@ -62,17 +62,24 @@ class Oracle:
         I = ctypes.c_int
         f.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_double, I, I, I, I, I, I, I, I,
                       ctypes.c_int64, P, I]
+        g = self.lib.pa_oracle_decode_positions
+        g.restype = ctypes.c_int
+        g.argtypes = f.argtypes[:7] + [P] + f.argtypes[7:]
         self.lib.pa_oracle_max_threads.restype = ctypes.c_int
 
     def max_threads(self) -> int:
         return int(self.lib.pa_oracle_max_threads())
 
     def decode(self, q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *,
-               scale: float, causal: bool, row_mask=None, threads: int = 0) -> np.ndarray:
+               scale: float, causal: bool, row_mask=None, threads: int = 0,
+               positions=None) -> np.ndarray:
         """Attention output [B, H, NQ, D] in float64.
 
         Array shapes: q [B,H,NQ,D]; k_cache/v_cache [NB,BLOCK,KV,D];
-        block_table [B,MAXB] int32; seq_lens [B] int32; k_new/v_new [B,KV,NQ,D].
+        block_table [B,MAXB] int32; seq_lens [B] int32; k_new/v_new [B,KV,NQ,D];
+        positions (optional) [B,NQ] int32, the cache slot each new row is bound
+        for or -1: a cached key of sequence b whose slot is positions[b, j]
+        reads new row j instead (the last such j).
         Any float dtype is accepted and converted exactly to float64.
         """
         q = _f64(q)
@@ -93,10 +100,17 @@ class Oracle:
             if row_mask.size != B * H * NQ:
                 raise ValueError("oracle: row_mask must have B*H*NQ entries")
             mask_ptr = row_mask.ctypes.data
-        rc = self.lib.pa_oracle_decode(
-            q.ctypes.data, kc.ctypes.data, vc.ctypes.data, table.ctypes.data, lens.ctypes.data,
-            kn.ctypes.data, vn.ctypes.data, out.ctypes.data, float(scale), B, H, KV, D, BLOCK,
-            NQ, int(bool(causal)), table.shape[1], NB, mask_ptr, int(threads))
+        tail = (out.ctypes.data, float(scale), B, H, KV, D, BLOCK, NQ, int(bool(causal)),
+                table.shape[1], NB, mask_ptr, int(threads))
+        head = (q.ctypes.data, kc.ctypes.data, vc.ctypes.data, table.ctypes.data,
+                lens.ctypes.data, kn.ctypes.data, vn.ctypes.data)
+        if positions is None:
+            rc = self.lib.pa_oracle_decode(*head, *tail)
+        else:
+            pos = np.ascontiguousarray(positions, dtype=np.int32)
+            if pos.shape != (B, NQ):
+                raise ValueError("oracle: positions must be [B, NQ]")
+            rc = self.lib.pa_oracle_decode_positions(*head, pos.ctypes.data, *tail)
         if rc != 0:
             raise ValueError(f"oracle: pa_oracle_decode returned {rc}")
         return out

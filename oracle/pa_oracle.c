@@ -16,6 +16,8 @@
  *     kh     = h / (H / KV)                      (grouped-query map)
  *     total  = past + (causal ? r + 1 : NQ)       (keys visible to row r)
  *     key i  = cache row table[i / BLOCK] * BLOCK + i % BLOCK   if i <  past
+ *              (new row j instead when that cache row is the slot
+ *              positions[j] names, for the last such j)
  *            = new row i - past                                  if i >= past
  *     s_i    = sum_d (scale * q[h][r][d]) * k_i[d]
  *     out    = sum_i softmax(s)_i * v_i ,   out = 0 when no key is visible.
@@ -31,7 +33,12 @@
  *     cached length; here seq_lens[b] is the cached length of sequence b and
  *     each sequence has its own row of the block table.
  *   - The NQ new rows always come from k_new / v_new (the page's i >= past
- *     branch); the page's slot-patching by position[1 + j] is not modelled.
+ *     branch).  Slot patching (the page's position[1 + j]: new row j is
+ *     bound for cache slot position[1 + j], and a cached key i < past whose
+ *     slot offset / (KV * D) equals it reads new row j instead; the last
+ *     such j wins) is modelled by pa_oracle_decode_positions, with
+ *     positions[b][j] for sequence b; pa_oracle_decode is the same with no
+ *     positions.
  *   - The empty-row convention (sum == 0 -> output the zero accumulator)
  *     follows the `sum == 0` guards of VECTOR_REDUCE and PARTIALS_REDUCE.
  *
@@ -70,17 +77,28 @@ int pa_oracle_max_threads(void)
 }
 
 /* Returns a pointer to the D values of key (or value) i of sequence b and KV
- * head kh, or NULL when the block table points outside the pool. */
+ * head kh, or NULL when the block table points outside the pool.  With
+ * `positions` (NULL: none), a cached key whose slot a new row is bound for
+ * reads that new row. */
 static const double *key_row(const double *cache, const double *fresh,
-                             const int32_t *block_table, int b, int kh, int i,
-                             int past, int KV, int D, int BLOCK, int NQ,
-                             int max_blocks, int64_t num_blocks)
+                             const int32_t *block_table, const int32_t *positions,
+                             int b, int kh, int i, int past, int KV, int D,
+                             int BLOCK, int NQ, int max_blocks, int64_t num_blocks)
 {
     if (i < past) {
         int32_t physical = block_table[(int64_t)b * max_blocks + i / BLOCK];
         if (physical < 0 || (int64_t)physical >= num_blocks)
             return NULL;
         int64_t slot = (int64_t)physical * BLOCK + i % BLOCK;
+        int bound = -1; /* the last new row bound for this slot */
+        if (positions)
+            for (int p = 0; p < NQ; ++p) {
+                int32_t target = positions[(int64_t)b * NQ + p];
+                if (target >= 0 && (int64_t)target == slot)
+                    bound = p;
+            }
+        if (bound >= 0)
+            return fresh + (((int64_t)b * KV + kh) * NQ + bound) * D;
         return cache + (slot * KV + kh) * D;
     }
     int j = i - past; /* new row j of this step */
@@ -88,17 +106,20 @@ static const double *key_row(const double *cache, const double *fresh,
 }
 
 /*
- * Full decode step.  `row_mask`, when not NULL, has B*H*NQ bytes; rows whose
- * byte is 0 are skipped and left untouched in `out` (used to sample rows of
- * very large cases).  `threads` <= 0 means the OpenMP default.
+ * Full decode step.  `positions`, when not NULL, is int32 [B][NQ]: the cache
+ * slot new row j of sequence b is bound for, or a negative value for none.
+ * `row_mask`, when not NULL, has B*H*NQ bytes; rows whose byte is 0 are
+ * skipped and left untouched in `out` (used to sample rows of very large
+ * cases).  `threads` <= 0 means the OpenMP default.
  */
-int pa_oracle_decode(const double *q, const double *k_cache,
-                     const double *v_cache, const int32_t *block_table,
-                     const int32_t *seq_lens, const double *k_new,
-                     const double *v_new, double *out, double scale, int B,
-                     int H, int KV, int D, int BLOCK, int NQ, int causal,
-                     int max_blocks, int64_t num_blocks,
-                     const uint8_t *row_mask, int threads)
+int pa_oracle_decode_positions(const double *q, const double *k_cache,
+                               const double *v_cache, const int32_t *block_table,
+                               const int32_t *seq_lens, const double *k_new,
+                               const double *v_new, const int32_t *positions,
+                               double *out, double scale, int B, int H, int KV,
+                               int D, int BLOCK, int NQ, int causal,
+                               int max_blocks, int64_t num_blocks,
+                               const uint8_t *row_mask, int threads)
 {
     if (B < 0 || H < 1 || KV < 1 || H % KV != 0 || D < 1 || BLOCK < 1 ||
         NQ < 1 || max_blocks < 0 || num_blocks < 0)
@@ -140,8 +161,8 @@ int pa_oracle_decode(const double *q, const double *k_cache,
         /* scores s_i = sum_d (scale * q_d) * k_i[d] */
         int bad = 0;
         for (int i = 0; i < total && !bad; ++i) {
-            const double *k = key_row(k_cache, k_new, block_table, b, kh, i,
-                                      past, KV, D, BLOCK, NQ, max_blocks,
+            const double *k = key_row(k_cache, k_new, block_table, positions, b,
+                                      kh, i, past, KV, D, BLOCK, NQ, max_blocks,
                                       num_blocks);
             if (!k) {
                 bad = 1;
@@ -174,8 +195,8 @@ int pa_oracle_decode(const double *q, const double *k_cache,
         for (int d = 0; d < D; ++d)
             orow[d] = 0.0;
         for (int i = 0; i < total; ++i) {
-            const double *v = key_row(v_cache, v_new, block_table, b, kh, i,
-                                      past, KV, D, BLOCK, NQ, max_blocks,
+            const double *v = key_row(v_cache, v_new, block_table, positions, b,
+                                      kh, i, past, KV, D, BLOCK, NQ, max_blocks,
                                       num_blocks);
             for (int d = 0; d < D; ++d)
                 orow[d] += s[i] * v[d];
@@ -186,4 +207,18 @@ int pa_oracle_decode(const double *q, const double *k_cache,
         free(s);
     }
     return status;
+}
+
+int pa_oracle_decode(const double *q, const double *k_cache,
+                     const double *v_cache, const int32_t *block_table,
+                     const int32_t *seq_lens, const double *k_new,
+                     const double *v_new, double *out, double scale, int B,
+                     int H, int KV, int D, int BLOCK, int NQ, int causal,
+                     int max_blocks, int64_t num_blocks,
+                     const uint8_t *row_mask, int threads)
+{
+    return pa_oracle_decode_positions(q, k_cache, v_cache, block_table, seq_lens,
+                                      k_new, v_new, NULL, out, scale, B, H, KV,
+                                      D, BLOCK, NQ, causal, max_blocks,
+                                      num_blocks, row_mask, threads);
 }

@@ -57,6 +57,9 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_decode.restype = I
     lib.pa_decode.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I, I, I,
                               ctypes.POINTER(PaOpts), P]
+    lib.pa_decode_positions.restype = I
+    lib.pa_decode_positions.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I,
+                                        I, I, ctypes.POINTER(PaOpts), P]
     lib.pa_decode_static_workspace.restype = I
     lib.pa_decode_static_workspace.argtypes = lib.pa_decode.argtypes
     lib.pa_workspace_bytes.restype = ctypes.c_size_t
@@ -215,6 +218,33 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *, scale: f
                 causal=causal, partitions=partitions, out=out, out_dtype=out_dtype,
                 workspace=workspace, status=status, checked=checked, merge_kernel=merge_kernel)
     return plan.run(stream)
+
+
+def decode_positions(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, positions, *,
+                     scale: float, causal: bool = False, partitions: int = 0, out=None,
+                     out_dtype=None, workspace=None, status=None, checked: bool = False,
+                     stream=None, merge_kernel: bool = False):
+    """A decode step with slot patching (pa_decode_positions): new row j of
+    sequence b is bound for cache slot positions[b, j] (physical block * BLOCK
+    + offset, or -1).  Stores the new rows at their slots in ``k_cache`` /
+    ``v_cache`` and attends over the updated cache, so that a cached key whose
+    slot a new row of its sequence is bound for reads that row (the last such
+    row wins).  ``positions``: int32 [B, NQ] on the device.  Other arguments
+    as ``decode``; returns ``out``."""
+    plan = Plan(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, scale=scale,
+                causal=causal, partitions=partitions, out=out, out_dtype=out_dtype,
+                workspace=workspace, status=status, checked=checked, merge_kernel=merge_kernel)
+    B, _, NQ, _ = q.shape
+    if positions.dtype != torch.int32 or tuple(positions.shape) != (B, NQ):
+        raise ValueError("positions must be an int32 [B, NQ] tensor")
+    if not (positions.is_cuda and positions.is_contiguous()):
+        raise ValueError("positions must be a contiguous CUDA tensor")
+    args = plan._args[:7] + [_ptr(positions)] + plan._args[7:]
+    with torch.cuda.device(plan.device):
+        rc = LIB.pa_decode_positions(*args, _stream_handle(stream))
+    if rc != 0:
+        raise PagedAttentionError(rc)
+    return plan.out
 
 
 class HostPlan:

@@ -347,10 +347,18 @@ size_t pa_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int part
     return ws_bound(batch, H, KV, D, NQ, partitions).sched;
 }
 
-int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-              const int32_t* seq_lens, const void* k_new, const void* v_new, void* out,
-              float scale, int H, int KV, int D, int BLOCK, int NQ, int causal,
-              const pa_opts* opts, void* stream)
+static int launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int32_t* slots, long long rows, int vpr, int KV, int NQ,
+                         long long num_slots, int* status, cudaStream_t stream);
+
+// pa_decode, and pa_decode_positions when `positions` is not NULL: then the
+// new rows are first stored at their slots in the (writable) caches, after
+// every argument has been checked.
+static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, const void* k_new,
+                       const void* v_new, const int32_t* positions, void* out, float scale,
+                       int H, int KV, int D, int BLOCK, int NQ, int causal, const pa_opts* opts,
+                       void* stream)
 {
     if (!opts)
         return PA_ERR_NULL_POINTER;
@@ -380,8 +388,10 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
         return PA_ERR_NULL_POINTER;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
-        !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(positions, 4))
         return PA_ERR_ALIGNMENT;
+    if (positions && static_cast<long long>(B) * KV * NQ * D * 8 >= (1ll << 38))
+        return PA_ERR_BAD_DIMS;  // threads of the append kernel
 
     const int R = (H / KV) * NQ;
     const bool mma = dtype != PA_F32;
@@ -536,6 +546,14 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     p.stage_off = stage_off;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (positions) {
+        const int es_row = D * es;
+        rc = launch_append(const_cast<void*>(k_cache), const_cast<void*>(v_cache), k_new, v_new,
+                           positions, static_cast<long long>(B) * KV * NQ, es_row / 16, KV, NQ,
+                           static_cast<long long>(opts->num_blocks) * BLOCK, opts->status, st);
+        if (rc != PA_OK)
+            return rc;
+    }
     if (opts->trace_begin &&
         cudaEventRecord(static_cast<cudaEvent_t>(opts->trace_begin), st) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -596,9 +614,29 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     return PA_OK;
 }
 
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+              const int32_t* seq_lens, const void* k_new, const void* v_new, void* out,
+              float scale, int H, int KV, int D, int BLOCK, int NQ, int causal,
+              const pa_opts* opts, void* stream)
+{
+    return decode_impl(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, nullptr, out,
+                       scale, H, KV, D, BLOCK, NQ, causal, opts, stream);
+}
+
+int pa_decode_positions(const void* q, void* k_cache, void* v_cache, const int32_t* block_table,
+                        const int32_t* seq_lens, const void* k_new, const void* v_new,
+                        const int32_t* positions, void* out, float scale, int H, int KV, int D,
+                        int BLOCK, int NQ, int causal, const pa_opts* opts, void* stream)
+{
+    return decode_impl(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, positions, out,
+                       scale, H, KV, D, BLOCK, NQ, causal, opts, stream);
+}
+
 // ------------------------------------------------------------ cache append
 // One thread per 16 bytes of one new row of K or V (rows in k_new order
 // [B][KV][NQ]): the slot of the row's (sequence, new row) names the cache row.
+// When several new rows of one sequence name one slot, only the last of them
+// (largest j) is stored, so the result does not depend on thread order.
 struct AppendParams {
     uint4* k_cache;
     uint4* v_cache;
@@ -634,6 +672,9 @@ __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ 
             atomicOr(a.status, PA_STATUS_BAD_SLOT);
         return;
     }
+    for (int jj = j + 1; jj < a.NQ; ++jj)
+        if (a.slots[b * a.NQ + jj] == s)
+            return;  // a later new row of this sequence lands here
     const uint4* src = (is_v ? a.v_new : a.k_new) + row * a.vpr + v;
     uint4* dst = (is_v ? a.v_cache : a.k_cache) + (static_cast<long long>(s) * a.KV + kh) * a.vpr + v;
     *dst = *src;
@@ -694,21 +735,29 @@ int pa_cache_append(void* k_cache, void* v_cache, const void* k_new, const void*
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) ||
         !aligned(v_new, 16) || !aligned(slot_mapping, 4))
         return PA_ERR_ALIGNMENT;
+    return launch_append(k_cache, v_cache, k_new, v_new, slot_mapping, rows,
+                         static_cast<int>(row_bytes / 16), KV, NQ, num_slots, status,
+                         static_cast<cudaStream_t>(stream));
+}
+
+static int launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int32_t* slots, long long rows, int vpr, int KV, int NQ,
+                         long long num_slots, int* status, cudaStream_t stream)
+{
     AppendParams a{};
     a.k_cache = static_cast<uint4*>(k_cache);
     a.v_cache = static_cast<uint4*>(v_cache);
     a.k_new = static_cast<const uint4*>(k_new);
     a.v_new = static_cast<const uint4*>(v_new);
-    a.slots = slot_mapping;
+    a.slots = slots;
     a.status = status;
     a.rows = rows;
-    a.vpr = static_cast<int>(row_bytes / 16);
+    a.vpr = vpr;
     a.KV = KV;
     a.NQ = NQ;
     a.num_slots = num_slots;
     const long long threads = 2 * rows * a.vpr;
-    pa_append_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0,
-                       static_cast<cudaStream_t>(stream)>>>(a);
+    pa_append_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess)
         return PA_ERR_CUDA;
     g_launches.fetch_add(1);

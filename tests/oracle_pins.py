@@ -15,7 +15,12 @@ oracle disagrees with:
   * the grouped-query map (query head h reads KV head h // (H / KV)) with
     constant value rows;
   * causal truncation: causal row r equals row r of a non-causal call that
-    sees only new rows 0..r.
+    sees only new rows 0..r;
+  * slot patching (the position vector's entries 1 + j on the same page,
+    VECTOR_BODY): torch SDPA on dense keys/values in which every cached token
+    whose slot a new row of its own sequence is bound for holds that row (the
+    last such row), and bitwise equality with a plain call when no position
+    names a cached slot of its sequence.
 
 The semantics pinned are those of onnxruntime-ep-mlx 0.31.1,
 src/ops/paged_attention.rs (VECTOR_BODY, VECTOR_REDUCE, PARTIALS_REDUCE), with
@@ -226,6 +231,62 @@ def pin_causal_truncation(orc):
     assert np.array_equal(run(orc, one, 0.25, True), run(orc, one, 0.25, False))
 
 
+def slot_of(c, b, t):
+    """Cache slot (physical block * BLOCK + offset) of token t of sequence b."""
+    BLOCK = c["k_cache"].shape[1]
+    return int(c["block_table"][b, t // BLOCK]) * BLOCK + t % BLOCK
+
+
+def patched_dense(c, positions):
+    """Dense per-sequence keys/values with the slot patch applied token by
+    token: cached token t of sequence b takes new row j when positions[b, j]
+    is its slot, later j overriding earlier ones."""
+    dk = [x.copy() for x in c["dense_k"]]
+    dv = [x.copy() for x in c["dense_v"]]
+    for b, n in enumerate(c["seq_lens"].tolist()):
+        for t in range(n):
+            for j in range(positions.shape[1]):
+                if positions[b, j] >= 0 and positions[b, j] == slot_of(c, b, t):
+                    dk[b][:, t] = c["k_new"][b][:, j]
+                    dv[b][:, t] = c["v_new"][b][:, j]
+    out = dict(c)
+    out["dense_k"], out["dense_v"] = dk, dv
+    return out
+
+
+def positions_case():
+    c = dense_case(3, 8, 2, 16, 4, 4, [9, 14, 0], seed=23)
+    s = lambda b, t: slot_of(c, b, t)
+    positions = np.array([
+        [s(0, 3), -1, s(0, 3), s(0, 9)],          # rows 0 and 2 name one cached slot; 9 = past
+        [s(1, 0), s(0, 5), s(1, 13), 1 << 30],    # another sequence's slot; out of the pool
+        [s(0, 1), -5, -1, s(1, 2)],               # no past: nothing to patch
+    ], dtype=np.int32)
+    return c, positions
+
+
+def pin_positions_sdpa(orc):
+    c, positions = positions_case()
+    for causal in (False, True):
+        got = run(orc, c, 0.3, causal, positions=positions)
+        want = sdpa_reference(patched_dense(c, positions), 0.3, causal)
+        assert np.all(np.isfinite(got)), "non-finite oracle output with positions"
+        err = float(np.max(np.abs(got - want)))
+        assert err < 1e-12, f"slot patching (causal={causal}): max abs err {err}"
+
+
+def pin_positions_neutral(orc):
+    c, positions = positions_case()
+    base = run(orc, c, 0.3, True)
+    none = -np.ones_like(positions)
+    assert np.array_equal(run(orc, c, 0.3, True, positions=none), base)
+    # slots at or past each sequence's length, or in another sequence's blocks
+    away = np.array([[slot_of(c, 0, 9), slot_of(c, 0, 10), -1, slot_of(c, 1, 4)],
+                     [slot_of(c, 1, 14), slot_of(c, 0, 0), -1, -1],
+                     [slot_of(c, 1, 1), -1, -1, -1]], dtype=np.int32)
+    assert np.array_equal(run(orc, c, 0.3, True, positions=away), base)
+
+
 ALL_PINS = [
     pin_sdpa_dense,
     pin_permutation_bitwise,
@@ -235,6 +296,8 @@ ALL_PINS = [
     pin_hard_max,
     pin_gqa_map,
     pin_causal_truncation,
+    pin_positions_sdpa,
+    pin_positions_neutral,
 ]
 
 

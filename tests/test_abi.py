@@ -174,3 +174,32 @@ def test_cache_append_rejects_before_launching(lib):
     assert go(a[0], ctypes.c_void_p(0x20008), *a[2:]) == -4
     assert go(*a[:4], ctypes.c_void_p(0x50002)) == -4  # slot_mapping 4-byte aligned
     assert lib.kernel_launches() == launches
+
+
+def test_decode_positions_rejects_before_launching(lib):
+    """pa_decode_positions checks every argument, its own and pa_decode's,
+    before it enqueues the append (these calls run without a GPU)."""
+    f = lib.LIB.pa_decode_positions
+    ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+
+    def go(opts, **kw):
+        names = ("q", "kc", "vc", "table", "lens", "kn", "vn", "pos", "out")
+        a = dict(zip(names, ptrs))
+        a.update(kw)
+        return f(*(a[n] for n in names), ctypes.c_float(0.1), 32, 8, 128, 16, 1, 0, opts, None)
+
+    def opts(**kw):
+        o = dict(batch=8, max_blocks=257, num_blocks=2048, dtype=lib.PA_F16, out_dtype=-1,
+                 partitions=1, checked=0, workspace=None, workspace_bytes=0, status=None,
+                 trace_begin=None, trace_split=None, merge_kernel=0)
+        o.update(kw)
+        return ctypes.byref(lib.PaOpts(**o))
+
+    launches = lib.kernel_launches()
+    assert go(None) == -1
+    assert go(opts(batch=0)) == 0
+    assert go(opts(), kc=None) == -1
+    assert go(opts(), pos=ctypes.c_void_p(0x80002)) == -4  # positions 4-byte aligned
+    assert go(opts(dtype=9)) == -3
+    assert go(opts(partitions=0)) == -5  # the decode's workspace is checked first
+    assert lib.kernel_launches() == launches

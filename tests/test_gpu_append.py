@@ -95,3 +95,10 @@ def test_empty_batch_launches_nothing():
                          torch.zeros(0, 1, 1, 64, dtype=torch.float16, device="cuda"),
                          torch.zeros(0, 1, dtype=torch.int32, device="cuda"))
     assert binding.kernel_launches() == before
+
+
+def test_rows_of_one_sequence_naming_one_slot():
+    """Two new rows of one sequence bound for one slot: the later row lands."""
+    B, NQ, BLOCK, NB = 3, 4, 16, 4
+    slots = [7, 20, 7, 7,  33, -1, 33, 2,  50, 51, 52, 50]
+    run_case("bf16", B, 2, 128, NQ, BLOCK, NB, slots, seed=4)

@@ -71,3 +71,32 @@ def test_append_then_decode_equals_decode_with_new_rows():
                           c["seq_lens"] + 1, np.ascontiguousarray(c["k_new"][:, :, 1:]),
                           np.ascontiguousarray(c["v_new"][:, :, 1:]), scale=0.3, causal=causal)
         assert np.array_equal(full[:, :, 1:], part), f"causal={causal}"
+
+
+def test_later_row_of_a_sequence_wins():
+    kc = np.zeros((2, 2, 1, 2))
+    vc = np.zeros((2, 2, 1, 2))
+    kn = np.array([[[[1.0, 1.0], [2.0, 2.0], [3.0, 3.0]]]])  # [B=1][KV=1][NQ=3][D=2]
+    k2, _, _ = oracle.cache_append(kc, vc, kn, -kn, np.array([[1, 2, 1]], dtype=np.int32))
+    assert np.array_equal(k2[0, 1, 0], [3.0, 3.0])  # rows 0 and 2 name slot 1: row 2 lands
+    assert np.array_equal(k2[1, 0, 0], [2.0, 2.0])
+
+
+def test_slot_patch_equals_decode_after_append():
+    """Decode with the slot patch over the old cache equals a plain decode over
+    the cache with the new rows stored at their slots, when every sequence
+    names only slots of its own blocks: the page's read-time substitution and
+    its write-back describe one step."""
+    c, _ = oracle_pins.positions_case()
+    s = lambda b, t: oracle_pins.slot_of(c, b, t)
+    positions = np.array([[s(0, 3), -1, s(0, 3), s(0, 9)],
+                          [s(1, 0), s(1, 7), s(1, 13), s(1, 14)],
+                          [-1, -1, -1, -1]], dtype=np.int32)
+    for causal in (False, True):
+        got = oracle_pins.run(oracle.default(), c, 0.3, causal, positions=positions)
+        kc, vc, bad = oracle.cache_append(c["k_cache"], c["v_cache"], c["k_new"], c["v_new"],
+                                          positions)
+        assert not bad
+        after = dict(c, k_cache=kc, v_cache=vc)
+        want = oracle_pins.run(oracle.default(), after, 0.3, causal)
+        assert np.array_equal(got, want)

@@ -32,6 +32,12 @@ MUTANTS = {
     "no_normalisation": ("if (denom != 0.0)", "if (0)"),
     "values_from_keys": ("const double *v = key_row(v_cache, v_new,", "const double *v = key_row(k_cache, k_new,"),
     "new_rows_from_head_zero": ("fresh + (((int64_t)b * KV + kh) * NQ + j) * D", "fresh + (((int64_t)b * KV) * NQ + j) * D"),
+    "positions_first_wins": ("bound = p;", "if (bound < 0) bound = p;"),
+    "positions_sequence_ignored": ("positions[(int64_t)b * NQ + p]", "positions[p]"),
+    "positions_ignored": ("if (bound >= 0)", "if (0)"),
+    "patched_row_zero": ("NQ + bound) * D", "NQ + 0) * D"),
+    "patched_from_head_zero": ("fresh + (((int64_t)b * KV + kh) * NQ + bound) * D",
+                               "fresh + (((int64_t)b * KV) * NQ + bound) * D"),
     "head_row_swapped": ("const int r = (int)(flat % NQ);\n        const int h = (int)((flat / NQ) % H);",
                          "const int h = (int)(flat % H);\n        const int r = (int)((flat / H) % NQ);"),
 }
