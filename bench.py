@@ -409,6 +409,54 @@ def append_timing(device, steps=200, warmup=10):
             "GB_per_s": round(moved / (us * 1e-6) / 1e9, 1)}
 
 
+def prefill_flops(w):
+    """Algorithmic flops of a causal prefill: row r of sequence b attends to
+    past + r + 1 keys, 2 flops per multiply-add in q.k and in p.v."""
+    s = w.spec
+    keys = sum(s.NQ * past + s.NQ * (s.NQ + 1) // 2 for past in w.seq_lens.tolist())
+    return 4 * s.H * s.D * keys
+
+
+def prefill_timing(device, steps=20, warmup=3):
+    """pa_prefill on the prefill workload (NQ = 512 new rows after 1024 cached
+    tokens), back to back on rotated copies of the pools; the stores of the
+    new rows rewrite the same values each call."""
+    from paged_kv_cache_182_gb300 import binding
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    w = W.make_prefill("prefill_fp16", seed=0)
+    s = w.spec
+    kc, vc, pool_bytes = rotation_copies(w, device)
+    q, table, lens, kn, vn = (t.to(device) for t in (w.q, w.block_table, w.seq_lens,
+                                                      w.k_new, w.v_new))
+    out = torch.empty(q.shape, dtype=q.dtype, device=device)
+    plans = [binding.PrefillPlan(q, k, v, table, lens, kn, vn, scale=s.scale, out=out)
+             for k, v in zip(kc, vc)]
+    stream = torch.cuda.current_stream(device)
+    for i in range(warmup):
+        plans[i % len(plans)].run(stream)
+    torch.cuda.synchronize()
+    launches = binding.kernel_launches()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        plans[i % len(plans)].run(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / steps * 1e3
+    flops = prefill_flops(w)
+    peak = float(json.loads((ROOT / "MEASURED_PEAKS.json").read_text())["bf16_tflops"]) \
+        if (ROOT / "MEASURED_PEAKS.json").exists() else 1900.0
+    tflops = flops / (us * 1e-6) / 1e12
+    return {"workload": f"prefill_fp16 (B={s.B}, H={s.H}, KV={s.KV}, D={s.D}, BLOCK={s.BLOCK}, "
+                        f"past={int(w.seq_lens[0])}, NQ={s.NQ}, causal)",
+            "us_per_call": round(us, 1), "new_tokens_per_s": round(s.B * s.NQ / (us * 1e-6), 1),
+            "flops_per_call": flops, "TFLOP_per_s": round(tflops, 2),
+            "frac_of_measured_tensor_peak": round(tflops / peak, 4),
+            "launches_per_call": (binding.kernel_launches() - launches) // steps,
+            "l2": f"{len(plans)} copies of the KV pools ({pool_bytes // 2**20} MiB) rotated"}
+
+
 def run_ours(args, rank, world, local):
     from paged_kv_cache_182_gb300 import binding  # noqa: F401  (fails loudly if not built)
     from paged_kv_cache_182_gb300 import workloads as W
@@ -459,6 +507,7 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_extras:
         line["per_workload"] = per_workload_table(device, 50, 5, peak)
         line["cache_append"] = append_timing(device)
+        line["prefill"] = prefill_timing(device)
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -69,7 +69,8 @@ extern "C" {
 #define PA_STATUS_BAD_SLOT 8   /* pa_cache_append: a slot < -1 or >= num_blocks * BLOCK (skipped) */
 
 /* supported sizes */
-#define PA_MAX_NQ 16
+#define PA_MAX_NQ 16           /* new rows per sequence of one decode call */
+#define PA_MAX_PREFILL 65536   /* new rows per sequence of one pa_prefill call */
 
 /* scratch built into the library for pa_decode_static_workspace (16 MiB) */
 #define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
@@ -261,6 +262,45 @@ int pa_decode_positions(const void *q, void *k_cache, void *v_cache,
                         const void *k_new, const void *v_new, const int32_t *positions,
                         void *out, float scale, int H, int KV, int D, int BLOCK, int NQ,
                         int causal, const pa_opts *opts, void *stream);
+
+/*
+ * Causal prefill of NQ new tokens per sequence over the paged cache (the
+ * chunked form of the decode step: onnxruntime-ep-mlx 0.31.1,
+ * src/ops/paged_attention.rs, VECTOR_BODY with its causal bound, for any
+ * number of new rows).  New row j of sequence b is token past + j, past =
+ * seq_lens[b]; its output row r attends to keys 0 .. past + r: the cached
+ * keys through the block table and new rows 0 .. r.  The call also stores the
+ * new rows in the cache at the slots the block table gives those tokens,
+ * table[b][t / BLOCK] * BLOCK + t % BLOCK for t = past + j, so the table must
+ * hold blocks for past + NQ tokens (a token beyond it, or an entry outside
+ * [0, num_blocks), skips that row's store and ORs PA_STATUS_BAD_SLOT into
+ * *opts->status; the decode then reports PA_STATUS_BAD_LENGTH).
+ *
+ * It enqueues the store of all new rows, then causal decodes of chunks of at
+ * most PA_MAX_NQ rows: chunk [r0, r0 + n) attends to past + r0 cached tokens
+ * (the earlier rows are in the cache by then) and its n rows as new rows.
+ * With NQ > PA_MAX_NQ the chunk's q, k_new, v_new and output pass through
+ * staging in the workspace.
+ *
+ * Arguments as pa_decode with causal = 1, except: NQ is 1 .. PA_MAX_PREFILL;
+ * k_cache and v_cache are written; opts->workspace holds at least
+ * pa_prefill_workspace_bytes() bytes (256-aligned; its first
+ * pa_prefill_workspace_zero_bytes() bytes zero before the first use, and left
+ * zero by every call that completes), or, for NQ <= PA_MAX_NQ, what pa_decode
+ * needs; opts->trace_begin / trace_split are ignored.  Every argument of every
+ * chunk is checked before the first launch; returns PA_OK or a PA_ERR_* code.
+ */
+int pa_prefill(const void *q, void *k_cache, void *v_cache, const int32_t *block_table,
+               const int32_t *seq_lens, const void *k_new, const void *v_new, void *out,
+               float scale, int H, int KV, int D, int BLOCK, int NQ, const pa_opts *opts,
+               void *stream);
+
+/* Workspace of pa_prefill and its leading bytes that must be zero (0 for
+ * invalid arguments or batch == 0).  out_dtype as in pa_opts (-1 = dtype). */
+size_t pa_prefill_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions,
+                                  int dtype, int out_dtype);
+size_t pa_prefill_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions,
+                                       int dtype, int out_dtype);
 
 /* A sentence naming what to verify for a PA_ERR_* code (static storage). */
 const char *pa_strerror(int code);

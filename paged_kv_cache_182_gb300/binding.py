@@ -60,6 +60,13 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_decode_positions.restype = I
     lib.pa_decode_positions.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I,
                                         I, I, ctypes.POINTER(PaOpts), P]
+    lib.pa_prefill.restype = I
+    lib.pa_prefill.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I, I,
+                               ctypes.POINTER(PaOpts), P]
+    lib.pa_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.pa_prefill_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
+    lib.pa_prefill_workspace_zero_bytes.restype = ctypes.c_size_t
+    lib.pa_prefill_workspace_zero_bytes.argtypes = [I, I, I, I, I, I, I, I]
     lib.pa_decode_static_workspace.restype = I
     lib.pa_decode_static_workspace.argtypes = lib.pa_decode.argtypes
     lib.pa_workspace_bytes.restype = ctypes.c_size_t
@@ -245,6 +252,73 @@ def decode_positions(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, p
     if rc != 0:
         raise PagedAttentionError(rc)
     return plan.out
+
+
+class PrefillPlan:
+    """One prepared prefill call (pa_prefill) on fixed device tensors: NQ new
+    rows per sequence after ``seq_lens`` cached tokens, causal, any NQ up to
+    PA_MAX_PREFILL.  ``run`` stores the new rows in the caches at the slots
+    the block table gives tokens seq_lens[b] + j and writes the attention
+    output into ``out``; the workspace is allocated (zeroed) here."""
+
+    def __init__(self, q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *,
+                 scale: float, partitions: int = 0, out=None, out_dtype=None, status=None,
+                 checked: bool = False):
+        B, H, NQ, D = q.shape
+        NB, BLOCK, KV, D2 = k_cache.shape
+        if (D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape)
+                or tuple(k_new.shape) != (B, KV, NQ, D) or tuple(v_new.shape) != (B, KV, NQ, D)):
+            raise ValueError("inconsistent q / cache / new-row shapes")
+        if block_table.ndim != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+            raise ValueError("block_table must be [B, max_blocks] and seq_lens [B]")
+        if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+            raise TypeError("block_table and seq_lens must be int32")
+        dt = q.dtype
+        if dt not in _DT or any(t.dtype != dt for t in (k_cache, v_cache, k_new, v_new)):
+            raise TypeError("q, caches and new rows must share one supported dtype")
+        tensors = (q, k_cache, v_cache, block_table, seq_lens, k_new, v_new)
+        for t in tensors:
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError("all tensors must be contiguous CUDA tensors")
+        odt = dt if out_dtype is None else out_dtype
+        if out is None:
+            out = torch.empty((B, H, NQ, D), dtype=odt, device=q.device)
+        elif tuple(out.shape) != (B, H, NQ, D) or not out.is_contiguous() or out.dtype != odt:
+            raise ValueError("out must be a contiguous [B, H, NQ, D] tensor of the output dtype")
+        need = int(LIB.pa_prefill_workspace_bytes(B, H, KV, D, NQ, int(partitions), _DT[dt],
+                                                  _DT[odt]))
+        if need == 0 and B > 0:
+            raise ValueError("unsupported sizes")
+        self.workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=q.device)
+        self.tensors, self.out, self.status, self.device = tensors, out, status, q.device
+        self.opts = PaOpts(
+            batch=B, max_blocks=int(block_table.shape[1]), num_blocks=NB, dtype=_DT[dt],
+            out_dtype=_DT[odt], partitions=int(partitions), checked=int(bool(checked)),
+            workspace=self.workspace.data_ptr(), workspace_bytes=need,
+            status=None if status is None else status.data_ptr(), trace_begin=None,
+            trace_split=None, merge_kernel=0)
+        self._args = [_ptr(t) for t in tensors] + [_ptr(out), ctypes.c_float(scale), H, KV, D,
+                                                   BLOCK, NQ, ctypes.byref(self.opts)]
+
+    def run(self, stream=None):
+        with torch.cuda.device(self.device):
+            rc = LIB.pa_prefill(*self._args, _stream_handle(stream))
+        if rc != 0:
+            raise PagedAttentionError(rc)
+        return self.out
+
+
+def prefill(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *, scale: float,
+            partitions: int = 0, out=None, out_dtype=None, status=None, checked: bool = False,
+            stream=None):
+    """Causal prefill (pa_prefill): new row j of sequence b is token
+    seq_lens[b] + j; output row r attends to keys 0 .. seq_lens[b] + r.  The
+    new rows are stored in ``k_cache`` / ``v_cache`` at the slots the block
+    table gives their tokens (the table must hold blocks for them).  q
+    [B, H, NQ, D], new rows [B, KV, NQ, D]; returns ``out``."""
+    return PrefillPlan(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, scale=scale,
+                       partitions=partitions, out=out, out_dtype=out_dtype, status=status,
+                       checked=checked).run(stream)
 
 
 class HostPlan:

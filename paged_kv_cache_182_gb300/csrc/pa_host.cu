@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -353,12 +354,12 @@ static int launch_append(void* k_cache, void* v_cache, const void* k_new, const 
 
 // pa_decode, and pa_decode_positions when `positions` is not NULL: then the
 // new rows are first stored at their slots in the (writable) caches, after
-// every argument has been checked.
+// every argument has been checked.  With launch == false: the checks alone.
 static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_table, const int32_t* seq_lens, const void* k_new,
                        const void* v_new, const int32_t* positions, void* out, float scale,
                        int H, int KV, int D, int BLOCK, int NQ, int causal, const pa_opts* opts,
-                       void* stream)
+                       void* stream, bool launch = true)
 {
     if (!opts)
         return PA_ERR_NULL_POINTER;
@@ -545,6 +546,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     p.merge_off = merge_off;
     p.stage_off = stage_off;
 
+    if (!launch)
+        return PA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (positions) {
         const int es_row = D * es;
@@ -893,6 +896,296 @@ int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
     if (cudaMemcpyAsync(out, ws + l.out, static_cast<size_t>(B) * H * NQ * D * eo,
                         cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+// ------------------------------------------------------------------ prefill
+// A prefill of NQ new tokens per sequence runs as the cache append of all new
+// rows (slots from the block table) followed by causal decodes of chunks of at
+// most PA_MAX_NQ rows: chunk [r0, r0 + n) sees seq_lens[b] + r0 cached tokens
+// (the earlier chunks' rows are in the cache by then) and its own rows as new
+// rows, so row r attends to keys 0 .. seq_lens[b] + r.
+
+// New row j of sequence b is token seq_lens[b] + j: its slot comes from the
+// block table.  One thread per 16 bytes of one new row of K or V.
+struct PrefillAppendParams {
+    uint4* k_cache;
+    uint4* v_cache;
+    const uint4* k_new;
+    const uint4* v_new;
+    const int32_t* table;     // [B][maxb]
+    const int32_t* seq_lens;  // [B]
+    int* status;
+    long long rows;           // B * KV * NQ
+    int vpr, KV, NQ, BLOCK, maxb, num_blocks;
+};
+
+__global__ void __launch_bounds__(256)
+    pa_prefill_append_kernel(const __grid_constant__ PrefillAppendParams a)
+{
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long per = a.rows * a.vpr;
+    if (i >= 2 * per)
+        return;
+    const bool is_v = i >= per;
+    const long long k = is_v ? i - per : i;
+    const long long row = k / a.vpr;
+    const int v = static_cast<int>(k - row * a.vpr);
+    const int j = static_cast<int>(row % a.NQ);
+    const long long bk = row / a.NQ;  // b * KV + kh
+    const int kh = static_cast<int>(bk % a.KV);
+    const long long b = bk / a.KV;
+    const bool reporter = a.status && !is_v && v == 0 && kh == 0;
+    const int past = a.seq_lens[b];
+    if (past < 0) {
+        if (reporter)
+            atomicOr(a.status, PA_STATUS_BAD_LENGTH);
+        return;
+    }
+    const long long t = static_cast<long long>(past) + j;
+    const long long blk = t / a.BLOCK;
+    const int phys = blk < a.maxb ? a.table[b * a.maxb + blk] : -1;
+    if (phys < 0 || phys >= a.num_blocks) {
+        if (reporter)
+            atomicOr(a.status, PA_STATUS_BAD_SLOT);
+        return;
+    }
+    const long long slot = static_cast<long long>(phys) * a.BLOCK + (t - blk * a.BLOCK);
+    const uint4* src = (is_v ? a.v_new : a.k_new) + row * a.vpr + v;
+    uint4* dst = (is_v ? a.v_cache : a.k_cache) + (slot * a.KV + kh) * a.vpr + v;
+    *dst = *src;
+}
+
+// Rows [src_r0, src_r0 + n) of each of `outer` groups of src_rows rows to rows
+// [dst_r0, dst_r0 + n) of groups of dst_rows rows (vpr 16-byte vectors a row):
+// a chunk's q, k_new, v_new into staging, or its output back.
+struct RowCopy {
+    const uint4* src;
+    uint4* dst;
+    long long outer;
+    int src_rows, src_r0, dst_rows, dst_r0, n, vpr;
+};
+
+struct ChunkCopyParams {
+    RowCopy seg[3];           // blockIdx.y selects one
+    const int32_t* lens_in;   // with lens_out: lens_out[b] = lens_in[b] + add
+    int32_t* lens_out;        // (a negative length is kept, for the decode to report)
+    int B, add;
+};
+
+__global__ void __launch_bounds__(256) pa_chunk_copy_kernel(const __grid_constant__ ChunkCopyParams c)
+{
+    const RowCopy s = c.seg[blockIdx.y];
+    const long long total = s.outer * s.n * s.vpr;
+    const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += step) {
+        const long long rest = i / s.vpr;
+        const int v = static_cast<int>(i - rest * s.vpr);
+        const long long o = rest / s.n;
+        const int r = static_cast<int>(rest - o * s.n);
+        s.dst[(o * s.dst_rows + s.dst_r0 + r) * s.vpr + v] =
+            s.src[(o * s.src_rows + s.src_r0 + r) * s.vpr + v];
+    }
+    if (c.lens_out && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int b = threadIdx.x; b < c.B; b += blockDim.x) {
+            const long long len = c.lens_in[b];
+            const long long moved = len < 0 ? len : len + c.add;
+            c.lens_out[b] = static_cast<int32_t>(moved > INT32_MAX ? INT32_MAX : moved);
+        }
+}
+
+static int launch_chunk_copy(const ChunkCopyParams& c, int nseg, cudaStream_t st)
+{
+    long long most = 0;
+    for (int k = 0; k < nseg; ++k) {
+        const long long t = c.seg[k].outer * c.seg[k].n * c.seg[k].vpr;
+        most = t > most ? t : most;
+    }
+    long long gx = (most + 255) / 256;
+    gx = gx < 1 ? 1 : gx > 1216 ? 1216 : gx;  // grid-stride beyond 8 CTAs per SM
+    pa_chunk_copy_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(nseg)), 256, 0,
+                           st>>>(c);
+    if (cudaGetLastError() != cudaSuccess)
+        return PA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return PA_OK;
+}
+
+// Workspace of pa_prefill: the decode workspace of the largest chunk layout
+// first (its leading zero bytes at offset 0), then 256-aligned staging for a
+// chunk's q, k_new, v_new, output and lengths.
+struct PrefillLayout {
+    size_t split, zero, q, knew, vnew, out, lens, total;
+};
+
+static bool prefill_dtypes_ok(int dtype, int out_dtype)
+{
+    const bool in = dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16;
+    return in && (out_dtype < 0 || out_dtype == dtype || out_dtype == PA_F32);
+}
+
+static PrefillLayout prefill_layout(int B, int H, int KV, int D, int NQ, int partitions, int dtype,
+                                    int out_dtype)
+{
+    PrefillLayout l{};
+    const int C = NQ < PA_MAX_NQ ? NQ : PA_MAX_NQ;
+    for (int n = 1; n <= C; ++n) {
+        const size_t w = pa_workspace_bytes(B, H, KV, D, n, partitions);
+        const size_t z = pa_workspace_zero_bytes(B, H, KV, D, n, partitions);
+        l.split = w > l.split ? w : l.split;
+        l.zero = z > l.zero ? z : l.zero;
+    }
+    const size_t es = elem_size(dtype), eo = elem_size(out_dtype < 0 ? dtype : out_dtype);
+    size_t off = align_up(l.split, 256);
+    l.q = off;
+    off = align_up(off + static_cast<size_t>(B) * H * C * D * es, 256);
+    l.knew = off;
+    off = align_up(off + static_cast<size_t>(B) * KV * C * D * es, 256);
+    l.vnew = off;
+    off = align_up(off + static_cast<size_t>(B) * KV * C * D * es, 256);
+    l.out = off;
+    off = align_up(off + static_cast<size_t>(B) * H * C * D * eo, 256);
+    l.lens = off;
+    off = align_up(off + static_cast<size_t>(B) * 4, 256);
+    l.total = off;
+    return l;
+}
+
+static bool prefill_args_ok(int batch, int H, int KV, int D, int NQ, int partitions, int dtype,
+                            int out_dtype)
+{
+    return ws_args_ok(batch, H, KV, D, 1, partitions) && NQ >= 1 && NQ <= PA_MAX_PREFILL &&
+           batch <= kMaxBatch && prefill_dtypes_ok(dtype, out_dtype);
+}
+
+size_t pa_prefill_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions,
+                                  int dtype, int out_dtype)
+{
+    if (!prefill_args_ok(batch, H, KV, D, NQ, partitions, dtype, out_dtype) || batch == 0)
+        return 0;
+    return prefill_layout(batch, H, KV, D, NQ, partitions, dtype, out_dtype).total;
+}
+
+size_t pa_prefill_workspace_zero_bytes(int batch, int H, int KV, int D, int NQ, int partitions,
+                                       int dtype, int out_dtype)
+{
+    if (!prefill_args_ok(batch, H, KV, D, NQ, partitions, dtype, out_dtype) || batch == 0)
+        return 0;
+    return prefill_layout(batch, H, KV, D, NQ, partitions, dtype, out_dtype).zero;
+}
+
+int pa_prefill(const void* q, void* k_cache, void* v_cache, const int32_t* block_table,
+               const int32_t* seq_lens, const void* k_new, const void* v_new, void* out,
+               float scale, int H, int KV, int D, int BLOCK, int NQ, const pa_opts* opts,
+               void* stream)
+{
+    if (!opts)
+        return PA_ERR_NULL_POINTER;
+    const int B = opts->batch;
+    if (B < 0 || H < 1 || KV < 1 || H % KV != 0 || NQ < 1 || opts->partitions < 0 ||
+        opts->max_blocks < 1 || opts->num_blocks < 1)
+        return PA_ERR_BAD_DIMS;
+    if (NQ > PA_MAX_PREFILL || (D != 64 && D != 128) || !prefill_dtypes_ok(opts->dtype, opts->out_dtype))
+        return PA_ERR_UNSUPPORTED;
+    if (B == 0)
+        return PA_OK;
+    if (B > kMaxBatch)
+        return PA_ERR_UNSUPPORTED;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !k_new || !v_new || !out)
+        return PA_ERR_NULL_POINTER;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_ALIGNMENT;
+    const int dtype = opts->dtype;
+    const int out_dtype = opts->out_dtype < 0 ? dtype : opts->out_dtype;
+    const int vpr = D * static_cast<int>(elem_size(dtype)) / 16;
+    const int vpr_o = D * static_cast<int>(elem_size(out_dtype)) / 16;
+    const long long rows = static_cast<long long>(B) * KV * NQ;
+    if (rows * vpr * 2 >= (1ll << 38))
+        return PA_ERR_BAD_DIMS;
+    const int C = NQ < PA_MAX_NQ ? NQ : PA_MAX_NQ;
+    const int last = NQ - (NQ - 1) / C * C;  // rows of the last chunk, 1 .. C
+    pa_opts dopts = *opts;
+    dopts.trace_begin = nullptr;
+    dopts.trace_split = nullptr;
+    unsigned char* ws = static_cast<unsigned char*>(opts->workspace);
+    const bool direct = NQ <= PA_MAX_NQ;  // one chunk: the caller's buffers serve the decode
+    PrefillLayout l{};
+    if (!direct) {
+        l = prefill_layout(B, H, KV, D, NQ, opts->partitions, dtype, opts->out_dtype);
+        if (!ws || opts->workspace_bytes < l.total)
+            return PA_ERR_WORKSPACE;
+        if (!aligned(ws, 256))
+            return PA_ERR_ALIGNMENT;
+        dopts.workspace = l.split ? ws : nullptr;
+        dopts.workspace_bytes = l.split;
+    }
+    const void* cq = direct ? q : ws + l.q;
+    const void* ckn = direct ? k_new : ws + l.knew;
+    const void* cvn = direct ? v_new : ws + l.vnew;
+    void* cout = direct ? out : ws + l.out;
+    const int32_t* clens = direct ? seq_lens : reinterpret_cast<const int32_t*>(ws + l.lens);
+    // every decode of the call is checked before the first launch
+    for (int n : {C, last}) {
+        const int rc = decode_impl(cq, k_cache, v_cache, block_table, clens, ckn, cvn, nullptr,
+                                   cout, scale, H, KV, D, BLOCK, n, 1, &dopts, stream, false);
+        if (rc != PA_OK)
+            return rc;
+    }
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    PrefillAppendParams a{};
+    a.k_cache = static_cast<uint4*>(k_cache);
+    a.v_cache = static_cast<uint4*>(v_cache);
+    a.k_new = static_cast<const uint4*>(k_new);
+    a.v_new = static_cast<const uint4*>(v_new);
+    a.table = block_table;
+    a.seq_lens = seq_lens;
+    a.status = opts->status;
+    a.rows = rows;
+    a.vpr = vpr;
+    a.KV = KV;
+    a.NQ = NQ;
+    a.BLOCK = BLOCK;
+    a.maxb = opts->max_blocks;
+    a.num_blocks = opts->num_blocks;
+    const long long threads = 2 * rows * vpr;
+    pa_prefill_append_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess)
+        return PA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    if (direct)
+        return decode_impl(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, nullptr, out,
+                           scale, H, KV, D, BLOCK, NQ, 1, &dopts, stream);
+
+    for (int r0 = 0; r0 < NQ; r0 += C) {
+        const int n = NQ - r0 < C ? NQ - r0 : C;
+        ChunkCopyParams in{};
+        in.seg[0] = {static_cast<const uint4*>(q), reinterpret_cast<uint4*>(ws + l.q),
+                     static_cast<long long>(B) * H, NQ, r0, n, 0, n, vpr};
+        in.seg[1] = {static_cast<const uint4*>(k_new), reinterpret_cast<uint4*>(ws + l.knew),
+                     static_cast<long long>(B) * KV, NQ, r0, n, 0, n, vpr};
+        in.seg[2] = {static_cast<const uint4*>(v_new), reinterpret_cast<uint4*>(ws + l.vnew),
+                     static_cast<long long>(B) * KV, NQ, r0, n, 0, n, vpr};
+        in.lens_in = seq_lens;
+        in.lens_out = reinterpret_cast<int32_t*>(ws + l.lens);
+        in.B = B;
+        in.add = r0;
+        int rc = launch_chunk_copy(in, 3, st);
+        if (rc == PA_OK)
+            rc = decode_impl(cq, k_cache, v_cache, block_table, clens, ckn, cvn, nullptr, cout,
+                             scale, H, KV, D, BLOCK, n, 1, &dopts, stream);
+        if (rc != PA_OK)
+            return rc;
+        ChunkCopyParams back{};
+        back.seg[0] = {reinterpret_cast<const uint4*>(ws + l.out), static_cast<uint4*>(out),
+                       static_cast<long long>(B) * H, n, 0, NQ, r0, n, vpr_o};
+        rc = launch_chunk_copy(back, 1, st);
+        if (rc != PA_OK)
+            return rc;
+    }
     return PA_OK;
 }
 

@@ -25,6 +25,13 @@ permutation of the pool, so logically adjacent blocks are scattered.  With
 ``poison=True`` every pool block no table references and every cache slot past
 a sequence's length is set to NaN, so a stray read of either shows up as NaN
 in the output.  Table entries past a sequence's last block are -1.
+
+Prefill workloads (``PREFILL_SPECS``, ``make_prefill``) draw the same way with
+the table covering past + NQ tokens per sequence: the blocks of the NQ new
+tokens are allocated and their slots poisoned (NaN) until the prefill stores
+the new rows there.
+
+  prefill_fp16       B=4  H=32 KV=8 D=128 BLOCK=16 past=1024, NQ=512 causal       fp16
 """
 from __future__ import annotations
 
@@ -86,6 +93,11 @@ SPECS = {
 }
 
 ORDER = ["tiny_fp32", "gqa_fp16", "long_bf16", "causal_append_fp16", "ragged_fp16"]
+
+PREFILL_SPECS = {
+    "prefill_fp16": Spec("prefill_fp16", "f16", B=4, H=32, KV=8, D=128, BLOCK=16, past=1024,
+                         NQ=512, causal=True),
+}
 
 
 @dataclass
@@ -217,3 +229,24 @@ def algorithmic_bytes(w: Workload, out_elem_bytes: int | None = None) -> int:
     qo = s.B * s.H * s.NQ * s.D * (e + oe)
     table = 4 * int(((lens + s.BLOCK - 1) // s.BLOCK).sum())
     return kv + qo + table + 4 * s.B
+
+
+def make_prefill(spec: Spec | str, seed: int = 0, lens=None) -> Workload:
+    """A prefill workload: ``seq_lens`` are the cached tokens, and the block
+    table also holds the blocks of the NQ new tokens of every sequence, whose
+    cache slots are NaN (the prefill writes them)."""
+    if isinstance(spec, str):
+        spec = PREFILL_SPECS[spec]
+    past = _draw_lens(spec, torch.Generator().manual_seed(int(seed)))
+    if lens is not None:
+        past = torch.as_tensor(lens, dtype=torch.int32).reshape(spec.B)
+    w = make(spec, seed, poison=True, lens=(past + spec.NQ).tolist())
+    nan = float("nan")
+    for b, n in enumerate(past.tolist()):
+        for t in range(n, n + spec.NQ):
+            phys = int(w.block_table[b, t // spec.BLOCK])
+            w.k_cache[phys, t % spec.BLOCK] = nan
+            w.v_cache[phys, t % spec.BLOCK] = nan
+    w.seq_lens = past.clone()
+    w.meta["prefill"] = True
+    return w

@@ -105,6 +105,7 @@ SDPA_CASES = [
     (3, 6, 3, 32, 16, 2, False, [17, 1, 32]),
     (1, 2, 1, 64, 16, 4, True, [100]),
     (2, 8, 1, 8, 2, 2, True, [7, 3]),
+    (2, 4, 2, 16, 8, 40, True, [0, 21]),  # a prefill-sized chunk of new rows
 ]
 
 

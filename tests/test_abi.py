@@ -203,3 +203,56 @@ def test_decode_positions_rejects_before_launching(lib):
     assert go(opts(dtype=9)) == -3
     assert go(opts(partitions=0)) == -5  # the decode's workspace is checked first
     assert lib.kernel_launches() == launches
+
+
+def test_prefill_rejects_before_launching(lib):
+    """pa_prefill's own checks and those of its chunk decodes come before any
+    launch (these calls run without a GPU)."""
+    f = lib.LIB.pa_prefill
+    ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+
+    def go(opts, NQ=100, D=128, **kw):
+        names = ("q", "kc", "vc", "table", "lens", "kn", "vn", "out")
+        a = dict(zip(names, ptrs))
+        a.update(kw)
+        return f(*(a[n] for n in names), ctypes.c_float(0.1), 32, 8, D, 16, NQ, opts, None)
+
+    def opts(**kw):
+        o = dict(batch=4, max_blocks=96, num_blocks=384, dtype=lib.PA_F16, out_dtype=-1,
+                 partitions=0, checked=0, workspace=None, workspace_bytes=0, status=None,
+                 trace_begin=None, trace_split=None, merge_kernel=0)
+        o.update(kw)
+        return ctypes.byref(lib.PaOpts(**o))
+
+    need = lib.LIB.pa_prefill_workspace_bytes(4, 32, 8, 128, 100, 0, lib.PA_F16, -1)
+    launches = lib.kernel_launches()
+    assert go(None) == -1
+    assert go(opts(), NQ=0) == -2
+    assert go(opts(), NQ=65537) == -3
+    assert go(opts(), D=96) == -3
+    assert go(opts(batch=0)) == 0
+    assert go(opts(), q=None) == -1
+    assert go(opts()) == -5  # no workspace
+    assert go(opts(workspace=0x100000, workspace_bytes=need - 1)) == -5
+    assert go(opts(workspace=0x100010, workspace_bytes=need)) == -4
+    assert go(opts(workspace=0x100000, workspace_bytes=need), kn=ctypes.c_void_p(0x70008)) == -4
+    assert go(opts(workspace=0x100000, workspace_bytes=need, out_dtype=lib.PA_BF16)) == -3
+    assert lib.kernel_launches() == launches
+
+
+def test_prefill_workspace_sizes(lib):
+    pb = lib.LIB.pa_prefill_workspace_bytes
+    pz = lib.LIB.pa_prefill_workspace_zero_bytes
+    B, H, KV, D = 4, 32, 8, 128
+    staging = B * H * 16 * D * 2 * 2 + 2 * B * KV * 16 * D * 2 + B * 4  # q, out, k/v new, lens
+    split = max(lib.LIB.pa_workspace_bytes(B, H, KV, D, n, 0) for n in range(1, 17))
+    assert pb(B, H, KV, D, 512, 0, lib.PA_F16, -1) >= split + staging
+    assert pb(B, H, KV, D, 512, 0, lib.PA_F16, -1) < split + staging + 6 * 256
+    assert pz(B, H, KV, D, 512, 0, lib.PA_F16, -1) == max(
+        lib.LIB.pa_workspace_zero_bytes(B, H, KV, D, n, 0) for n in range(1, 17))
+    assert pb(B, H, KV, D, 8, 0, lib.PA_F16, -1) >= lib.LIB.pa_workspace_bytes(B, H, KV, D, 8, 0)
+    assert pz(B, H, KV, D, 512, 1, lib.PA_F16, -1) == 0
+    assert pb(B, H, KV, D, 0, 0, lib.PA_F16, -1) == 0
+    assert pb(B, H, KV, D, 65537, 0, lib.PA_F16, -1) == 0
+    assert pb(B, H, KV, 96, 512, 0, lib.PA_F16, -1) == 0
+    assert pb(B, H, KV, D, 512, 0, 7, -1) == 0
