@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table and the CPU baseline")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time only the causal prefill of the prefill workload (one JSON "
+                         "line, --steps timed calls after --warmup)")
     return ap.parse_args()
 
 
@@ -575,7 +578,12 @@ def main():
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py --impl ours needs a CUDA device")
-        run_ours(args, rank, world, local)
+        if args.prefill:
+            if rank == 0:
+                line = prefill_timing(torch.device("cuda", local), args.steps, args.warmup)
+                print(json.dumps({"mode": "prefill", **line}), flush=True)
+        else:
+            run_ours(args, rank, world, local)
     if world > 1:
         import torch.distributed as dist
 
