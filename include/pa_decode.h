@@ -28,6 +28,12 @@
  * Table entries are read only for blocks that hold visible keys; entries past
  * a sequence's last block and cache slots past its length are never read.
  *
+ * Entry points: pa_decode, pa_decode_static_workspace and pa_decode_host
+ * read the caches; pa_cache_append (the step's new rows into their slots),
+ * pa_decode_positions (a decode step with slot patching) and pa_prefill (a
+ * causal prefill of up to PA_MAX_PREFILL new rows, in chunks) also write the
+ * new rows into them.
+ *
  * Errors: functions return PA_OK (0) or a negative PA_ERR_* code before
  * anything is launched; pa_strerror() names what to verify.  Conditions that
  * only the device can see (a table entry outside the pool in checked mode, a
@@ -66,7 +72,8 @@ extern "C" {
 #define PA_STATUS_BAD_BLOCK 1  /* checked mode: a table entry outside [0, num_blocks) */
 #define PA_STATUS_BAD_LENGTH 2 /* seq_lens[b] < 0 or > max_blocks * BLOCK (clamped) */
 #define PA_STATUS_TIMEOUT 4    /* an internal wait gave up (the output is undefined) */
-#define PA_STATUS_BAD_SLOT 8   /* pa_cache_append: a slot < -1 or >= num_blocks * BLOCK (skipped) */
+#define PA_STATUS_BAD_SLOT 8   /* a new row's slot < -1 or >= num_blocks * BLOCK, or (pa_prefill)
+                                  its token beyond the table: the row is not stored */
 
 /* supported sizes */
 #define PA_MAX_NQ 16           /* new rows per sequence of one decode call */

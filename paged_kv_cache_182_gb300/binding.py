@@ -10,6 +10,12 @@ Tensor layouts (row-major, contiguous):
   block_table      [B, max_blocks]          int32
   seq_lens         [B]                      int32 (cached tokens per sequence)
   k_new, v_new     [B, KV, NQ, D]
+
+Entry points: ``decode`` / ``Plan`` (device tensors), ``decode_host`` /
+``HostPlan`` (host tensors, device-resident caches), ``cache_append`` (new
+rows into their cache slots), ``decode_positions`` (a decode step with slot
+patching) and ``prefill`` / ``PrefillPlan`` (causal prefill of any number of
+new rows up to PA_MAX_PREFILL).
 """
 from __future__ import annotations
 
@@ -23,6 +29,7 @@ from . import _build
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LENGTH, PA_STATUS_TIMEOUT, PA_STATUS_BAD_SLOT = 1, 2, 4, 8
 PA_MAX_NQ = 16
+PA_MAX_PREFILL = 65536
 _DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 LIBRARY = _build.LIBRARY

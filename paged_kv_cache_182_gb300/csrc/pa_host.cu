@@ -7,6 +7,11 @@
 // batch, queries, causal, scale, and a partition count); the batch, the
 // table stride and the pool size cross the boundary as values instead of
 // template constants, and the workspace is caller-owned.
+//
+// Also here: the cache append kernel, the slot-patched decode (append, then
+// decode), the host-buffer entry (gather kernel or copies, decode, copy back)
+// and the chunked prefill (store of the new rows, then 16-row chunk decodes
+// through staging).
 
 #include <cuda.h>
 #include <cudaTypedefs.h>

@@ -256,3 +256,17 @@ def test_prefill_workspace_sizes(lib):
     assert pb(B, H, KV, D, 65537, 0, lib.PA_F16, -1) == 0
     assert pb(B, H, KV, 96, 512, 0, lib.PA_F16, -1) == 0
     assert pb(B, H, KV, D, 512, 0, 7, -1) == 0
+
+
+def test_binding_constants_match_the_header(lib):
+    """Every #define of include/pa_decode.h that the binding mirrors has the
+    header's value."""
+    text = (ROOT / "include" / "pa_decode.h").read_text()
+    defines = {}
+    for name, value in re.findall(r"#define\s+(PA_[A-Z0-9_]+)\s+\(?(-?\d+)\)?", text):
+        defines[name] = int(value)
+    mirrored = [n for n in defines if hasattr(lib, n)]
+    assert {"PA_F32", "PA_F16", "PA_BF16", "PA_MAX_NQ", "PA_MAX_PREFILL",
+            "PA_STATUS_BAD_SLOT"} <= set(mirrored)
+    for name in mirrored:
+        assert getattr(lib, name) == defines[name], name
