@@ -102,3 +102,10 @@ def test_rows_of_one_sequence_naming_one_slot():
     B, NQ, BLOCK, NB = 3, 4, 16, 4
     slots = [7, 20, 7, 7,  33, -1, 33, 2,  50, 51, 52, 50]
     run_case("bf16", B, 2, 128, NQ, BLOCK, NB, slots, seed=4)
+
+
+def test_golden_writeback_rows():
+    """The engine page's printed write-back example (cache [3][4][2][8] of
+    2-byte elements, rows 9, 2, 1, 2 at axis 1) as a slot mapping; the oracle
+    side is pinned to the printed byte ranges by the CPU tests."""
+    run_case("f16", 1, 2, 8, 4, 4, 3, [9, 2, 1, 2], seed=5)

@@ -1,5 +1,7 @@
 """The oracle's cache append (the cache update of a decode step) against a
 hand-worked example, its skip rules, and the decode it feeds (CPU only)."""
+from pathlib import Path
+
 import numpy as np
 
 import oracle
@@ -100,3 +102,54 @@ def test_slot_patch_equals_decode_after_append():
         after = dict(c, k_cache=kc, v_cache=vc)
         want = oracle_pins.run(oracle.default(), after, 0.3, causal)
         assert np.array_equal(got, want)
+
+
+GOLDEN = Path(__file__).resolve().parent / "golden" / "writeback_ranges.txt"
+
+
+def golden_writebacks():
+    cases = []
+    for line in GOLDEN.read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        shape, itemsize, axis, rows, ranges = (f.strip() for f in line.split("|"))
+        cases.append(dict(
+            shape=[int(x) for x in shape.split(",")], itemsize=int(itemsize), axis=int(axis),
+            rows=[] if rows == "-" else [int(x) for x in rows.split(",")],
+            ranges=None if ranges == "error" else
+            [] if ranges == "-" else [tuple(int(y) for y in r.split("-")) for r in ranges.split(",")]))
+    return cases
+
+
+def as_cache_shape(shape, axis):
+    """A paged cache [num_blocks][BLOCK][KV][D] whose rows at its axis 1 (the
+    slots, physical block * BLOCK + offset) are the page's rows at `axis`: a
+    rank-4 shape cut at axis 1 is one as it stands."""
+    if len(shape) == 4 and axis == 1:
+        return tuple(shape)
+    lead = int(np.prod(shape[:axis + 1]))
+    block = shape[axis] if axis >= 1 else 1
+    return (lead // block, block, 1, int(np.prod(shape[axis + 1:])))
+
+
+def test_writeback_ranges_golden():
+    """The cache rows the append writes for a slot mapping are exactly the
+    byte ranges the engine page prints for its write-back of those rows."""
+    dt = {2: np.float16, 4: np.float32}
+    cases = golden_writebacks()
+    assert len(cases) == 4
+    for c in cases:
+        shape = as_cache_shape(c["shape"], c["axis"])
+        kc = np.zeros(shape, dtype=dt[c["itemsize"]])
+        n = max(len(c["rows"]), 1)
+        kn = np.zeros((1, shape[2], n, shape[3]), dtype=kc.dtype)
+        kn.view(np.uint8)[...] = 0x5A  # every byte of a new row nonzero
+        slots = np.array([c["rows"] or [-1]], dtype=np.int32)
+        k2, _, bad = oracle.cache_append(kc, kc.copy(), kn, kn, slots)
+        written = np.flatnonzero(k2.view(np.uint8).reshape(-1))
+        if c["ranges"] is None:
+            assert bad and written.size == 0
+            continue
+        want = np.concatenate([np.arange(a, b) for a, b in c["ranges"]] or [np.zeros(0, int)])
+        assert not bad
+        assert np.array_equal(written, want), (c, written)
