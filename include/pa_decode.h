@@ -147,8 +147,9 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
  *     returns PA_ERR_STATIC_LIMIT and launches nothing (use fewer partitions,
  *     partitions == 1, or pa_decode with your own workspace).
  *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture
- *     starts.
+ *     that device current, and so does the first call after the device's
+ *     context was reset or replaced (the address is cached per context); make
+ *     those calls before any stream capture starts.
  *   - All calls on a device share the array, which keeps whatever the last
  *     call left in it.  Nothing in it has to start at zero (this entry point
  *     always merges split sequences with the separate merge kernel, and each
@@ -204,7 +205,8 @@ size_t pa_host_workspace_bytes(int batch, int max_blocks, int H, int KV, int D, 
  * Depends only on the arguments, not on the device or the lengths: it holds
  * a per-sequence schedule and one float32 partial state (max, sum, D
  * accumulators) per query row for every key range the split can produce.
- * Returns 0 for invalid arguments.
+ * Returns 0 for arguments pa_decode rejects (including batch > 4096, which
+ * pa_decode reports as PA_ERR_UNSUPPORTED).
  */
 size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions);
 

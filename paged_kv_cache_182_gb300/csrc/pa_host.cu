@@ -333,10 +333,12 @@ static WsLayout ws_bound(int batch, int H, int KV, int D, int NQ, int partitions
     return best;
 }
 
+// Sizes pa_decode accepts (batch up to kMaxBatch: the partition kernels keep
+// the schedule in shared memory); the size queries return 0 for the rest.
 static bool ws_args_ok(int batch, int H, int KV, int D, int NQ, int partitions)
 {
-    return batch >= 0 && H >= 1 && KV >= 1 && H % KV == 0 && (D == 64 || D == 128) && NQ >= 1 &&
-           NQ <= PA_MAX_NQ && partitions >= 0;
+    return batch >= 0 && batch <= kMaxBatch && H >= 1 && KV >= 1 && H % KV == 0 &&
+           (D == 64 || D == 128) && NQ >= 1 && NQ <= PA_MAX_NQ && partitions >= 0;
 }
 
 size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions)

@@ -107,6 +107,46 @@ def test_rejects_invalid_arguments(lib):
     assert call(lib, partitions=0, workspace=0x100010, workspace_bytes=1 << 30) == -4
 
 
+def test_batch_limit_is_unsupported_not_a_workspace_limit(lib):
+    """Above 4096 sequences the size queries return 0 (as for every argument
+    pa_decode rejects), so the static-scratch entry reports the batch limit
+    (PA_ERR_UNSUPPORTED), not PA_ERR_STATIC_LIMIT: fewer partitions cannot fix
+    such a call."""
+    assert lib.workspace_bytes(4096, 32, 8, 128, 1, 0) > 0
+    assert lib.workspace_bytes(4097, 32, 8, 128, 1, 0) == 0
+    assert lib.workspace_bytes(4097, 32, 8, 128, 1, 32) == 0
+    assert lib.workspace_zero_bytes(4097, 32, 8, 128, 1, 0) == 0
+    assert call(lib, batch=4097, partitions=0) == -3
+    o = lib.PaOpts(batch=4097, max_blocks=4, num_blocks=8, dtype=lib.PA_F16, out_dtype=-1,
+                   partitions=32, checked=0, workspace=None, workspace_bytes=0, status=None,
+                   trace_begin=None, trace_split=None)
+    before = lib.kernel_launches()
+    rc = lib.LIB.pa_decode_static_workspace(Fake.q, Fake.kc, Fake.vc, Fake.table, Fake.lens,
+                                            Fake.kn, Fake.vn, Fake.out, ctypes.c_float(0.1), 32,
+                                            8, 128, 16, 1, 0, ctypes.byref(o), None)
+    assert rc == -3
+    assert lib.kernel_launches() == before
+
+
+def test_static_entry_without_a_device_fails_cleanly(lib):
+    """The static-scratch entry looks its array up under the current CUDA
+    context; with no device at all that lookup fails with PA_ERR_CUDA instead
+    of handing a kernel a host-side stand-in address."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a CUDA device")
+    o = lib.PaOpts(batch=2, max_blocks=4, num_blocks=8, dtype=lib.PA_F16, out_dtype=-1,
+                   partitions=0, checked=0, workspace=None, workspace_bytes=0, status=None,
+                   trace_begin=None, trace_split=None)
+    before = lib.kernel_launches()
+    rc = lib.LIB.pa_decode_static_workspace(Fake.q, Fake.kc, Fake.vc, Fake.table, Fake.lens,
+                                            Fake.kn, Fake.vn, Fake.out, ctypes.c_float(0.1), 8,
+                                            2, 64, 16, 1, 0, ctypes.byref(o), None)
+    assert rc == -6
+    assert lib.kernel_launches() == before
+
+
 def test_empty_batch_is_a_no_op(lib):
     before = lib.kernel_launches()
     assert call(lib, batch=0) == 0
