@@ -138,7 +138,7 @@ struct Item {
 __device__ __forceinline__ int chunk_of(const SplitParams& p, int total)
 {
     const int per = p.partitions == 1 ? total : (total + p.partitions - 1) / p.partitions;
-    return ((per + p.BLOCK - 1) / p.BLOCK) * p.BLOCK;
+    return ((per + p.BLOCK - 1) >> p.lg_block) << p.lg_block;
 }
 
 // Shared-memory schedule built once per CTA.
@@ -192,41 +192,66 @@ __device__ __forceinline__ SegSpan seg_span(int x0, int nu, int g, int V, int C,
     return r;
 }
 
-// Executed by one full warp after `lens` is in shared memory.  CTA 0 also
-// records every sequence's (prefix, count) for the merge kernel.
-__device__ __forceinline__ void build_schedule(const SplitParams& p, const int* lens, int* prefix,
-                                               int* info, int lane)
+// Warp 0 alone: loads and clamps the lengths into `lens` (a length beyond the
+// table sets PA_STATUS_BAD_LENGTH) and writes the exclusive prefix of the
+// per-sequence counts into `prefix` (automatic mode: the units of all NRS * KV
+// segments of a sequence; fixed partitions: its key ranges), up to four
+// 32-sequence chunks of loads in flight at once.  CTA 0 also records every
+// sequence's (prefix, count) for the merge kernel.  Returns the prefix total.
+__device__ __forceinline__ int scan_lengths(const SplitParams& p, int* lens, int* prefix, int lane)
 {
     const int U = p.NRS * p.KV;
     const bool stream = p.partitions == 0;
+    const int cap = p.maxb << p.lg_block;
     int run = 0;
-    for (int base = 0; base < p.B; base += 32) {
-        const int b = base + lane;
-        int n = 0;
-        if (b < p.B) {
-            const int total = lens[b] + p.NQ;
-            const int chunk = stream ? p.TT : chunk_of(p, total);
-            n = (total + chunk - 1) / chunk;
-        }
-        const int w = stream ? n * U : n;
-        int incl = w;
+    for (int base = 0; base < p.B; base += 128) {
+        int sv[4];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o)
-                incl += y;
+        for (int i = 0; i < 4; ++i) {
+            const int b = base + 32 * i + lane;
+            sv[i] = b < p.B ? __ldg(p.seq_lens + b) : 0;
         }
-        if (b < p.B) {
-            prefix[b] = run + incl - w;
-            if (blockIdx.x == 0 && p.sched)
-                p.sched[b] = make_int2(run + incl - w, n);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (base + 32 * i >= p.B)
+                break;  // warp-uniform
+            const int b = base + 32 * i + lane;
+            int n = 0;
+            if (b < p.B) {
+                int v = sv[i];
+                if (v < 0 || v > cap) {
+                    if (blockIdx.x == 0 && p.status)
+                        atomicOr(p.status, PA_STATUS_BAD_LENGTH);
+                    v = v < 0 ? 0 : cap;
+                }
+                lens[b] = v;
+                const int total = v + p.NQ;
+                if (stream) {
+                    n = (total + p.TT - 1) >> p.lg_tt;
+                } else {
+                    const int chunk = chunk_of(p, total);
+                    n = (total + chunk - 1) / chunk;
+                }
+            }
+            const int w = stream ? n * U : n;
+            int incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            if (b < p.B) {
+                prefix[b] = run + incl - w;
+                if (blockIdx.x == 0 && p.sched)
+                    p.sched[b] = make_int2(run + incl - w, n);
+            }
+            run += __shfl_sync(kFull, incl, 31);
         }
-        run += __shfl_sync(kFull, incl, 31);
     }
-    if (lane == 0) {
+    if (lane == 0)
         prefix[p.B] = run;
-        info[1] = stream ? run : run * U;
-    }
+    return run;
 }
 
 __device__ __forceinline__ int last_le(const int* prefix, int B, long long x)
@@ -242,13 +267,34 @@ __device__ __forceinline__ int last_le(const int* prefix, int B, long long x)
     return lo;
 }
 
+// Last b in [0, B) whose cost prefix prefix[b] + VU * b is <= T (warp-
+// collective; the cost prefix is non-decreasing and 0 at b = 0): a ballot over
+// every 32nd sequence, then one within the chunk found.
+__device__ __forceinline__ int last_cost_le(const int* prefix, int B, int VU, int T, int lane)
+{
+    int lo = 0;
+    for (int base = 0; base < B; base += 32 * 32) {
+        const int b = base + 32 * lane;
+        const unsigned m = __ballot_sync(kFull, b < B && prefix[b] + VU * b <= T);
+        if (m == 0)
+            break;
+        lo = base + 32 * (31 - __clz(m));
+        if (m != kFull)
+            break;
+    }
+    const int b = lo + lane;
+    const unsigned m = __ballot_sync(kFull, b < B && prefix[b] + VU * b <= T);
+    return lo + 31 - __clz(m);
+}
+
 // First real unit of CTA k of G (automatic mode): the smallest x with
 // c(x) >= ceil(k C / G), or W when there is none, with its sequence, segment
-// and unit within the segment.  C < 2^31 and G <= kMaxGrid keep it in int32.
+// and unit within the segment (warp-collective, the same in every lane).
+// C < 2^31 and G <= kMaxGrid keep it in int32.
 struct CostPos {
     int x, b, seg, uu;
 };
-__device__ __forceinline__ CostPos cost_start(const SplitParams& p, const Sched& sc, int k, int G)
+__device__ __forceinline__ CostPos cost_start(const SplitParams& p, const Sched& sc, int k, int G, int lane)
 {
     const int C = static_cast<int>(sc.cost);
     const int q = C / G, r = C - q * G;
@@ -256,14 +302,7 @@ __device__ __forceinline__ CostPos cost_start(const SplitParams& p, const Sched&
     if (T >= C)
         return CostPos{sc.total, p.B, 0, 0};
     const int VU = p.vunits * p.NRS * p.KV;  // cost of one sequence's virtual units
-    int lo = 0, hi = p.B - 1;  // last b whose cost prefix is <= T
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sc.prefix[mid] + VU * mid <= T)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
+    const int lo = last_cost_le(sc.prefix, p.B, VU, T, lane);
     const int nb = (sc.lens[lo] + p.NQ + p.TT - 1) >> p.lg_tt;
     const int local = T - (sc.prefix[lo] + VU * lo);
     const int per = nb + p.vunits;
@@ -406,19 +445,18 @@ __device__ __forceinline__ size_t seg_record(const SplitParams& p, const SegPiec
     return (static_cast<size_t>(sp.item0 + c) * p.NRS + rsg) * p.KV + kh;
 }
 
-// Reads one word of every 32 bytes of a kernel parameter, so that its
-// constant-cache lines are fetched together at entry instead of one by one at
+// One word of every 32 bytes of a kernel parameter (0 past its end): the
+// loads of all three parameters are issued together at entry, so that their
+// constant-cache lines arrive in one round trip instead of one by one at
 // their first use on the issue path.
 template <typename Tp>
-__device__ __forceinline__ void warm_param(const Tp& x)
+__device__ __forceinline__ int param_word(const Tp& x)
 {
     constexpr int kWords = static_cast<int>(sizeof(Tp) / 4);
     const int i = static_cast<int>(threadIdx.x) * 8;
-    if (i < kWords) {
-        const int v = reinterpret_cast<const int*>(&x)[i];
-        asm volatile("" ::"r"(v));
-    }
+    return i < kWords ? reinterpret_cast<const int*>(&x)[i] : 0;
 }
+
 
 __device__ __forceinline__ void consumer_bar_sync()
 {
@@ -678,45 +716,69 @@ __device__ __forceinline__ void init_cta(const SplitParams& p, const Smem& sm)
     }
 }
 
-// All threads, after init_cta and the grid-dependency wait: clamped lengths,
-// the schedule.
+// Block-table bytes prefetched into L2 at entry, at most: a table this small
+// is fetched whole (all CTAs together, one 128-byte line per thread), so that
+// the producers' first table reads, which wait on the schedule, hit in L2.
+constexpr long long kTablePrefetchBytes = 512 * 1024;
+
+// Entry of the partition kernels, before anything that reads inputs the
+// previous kernel on the stream may still write: the tensor maps are fetched
+// (producer warps), the block table is prefetched into L2 (coherent: a later
+// write by the previous kernel still wins), the parameters are warmed, the
+// barriers initialised; then the grid-dependency wait.
+__device__ __forceinline__ void kernel_entry(const SplitParams& p, const CUtensorMap& kmap,
+                                             const CUtensorMap& vmap, const Smem& sm)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= kConsumerWarps && lane == 0)
+        tma_prefetch_desc(warp == kConsumerWarps ? &kmap : &vmap);
+    const long long tbytes = static_cast<long long>(p.B) * p.maxb * 4;
+    if (tbytes <= kTablePrefetchBytes) {
+        const long long line = static_cast<long long>(threadIdx.x) * gridDim.x + blockIdx.x;
+        if (line * 128 < tbytes)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.table) + line * 128));
+    }
+    const int w0 = param_word(p), w1 = param_word(kmap), w2 = param_word(vmap);
+    asm volatile("" ::"r"(w0), "r"(w1), "r"(w2));
+    init_cta(p, sm);
+    grid_dependency_wait();
+    grid_dependents_launch();
+}
+
+// All threads, after kernel_entry: clamped lengths, the schedule.
 __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cap = p.maxb * p.BLOCK;
     Sched sc;
     sc.lens = sm.lens;
     sc.prefix = sm.prefix;
     // Warp 0 alone: lengths, schedule and (automatic mode) this CTA's range,
     // with warp barriers in between and one CTA barrier at the end.
     if (warp == 0) {
-#pragma unroll 4
-        for (int b = lane; b < p.B; b += 32) {
-            int s = p.seq_lens[b];
-            if (s < 0 || s > cap) {
-                if (blockIdx.x == 0 && p.status)
-                    atomicOr(p.status, PA_STATUS_BAD_LENGTH);
-                s = s < 0 ? 0 : cap;
-            }
-            sm.lens[b] = s;
-        }
+        const int run = scan_lengths(p, sm.lens, sm.prefix, lane);
         __syncwarp();
-        build_schedule(p, sm.lens, sm.prefix, sm.info, lane);
-        __syncwarp();
-        sc.total = sm.info[1];
+        sc.total = p.partitions == 0 ? run : run * p.NRS * p.KV;
         sc.cost = sc.total + static_cast<long long>(p.vunits) * p.B * p.NRS * p.KV;
+        if (lane == 0)
+            sm.info[1] = sc.total;
         if (p.partitions == 0) {
             // G = min(CTAs, C): every CTA inside a segment then holds a unit.
-            // Lanes 0 and 1 locate the starts of this CTA's range and the next's.
+            // The starts of this CTA's range and of the next CTA's.
             const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), sc.cost));
-            if (lane < 2) {
-                const CostPos c = static_cast<int>(blockIdx.x) < G
-                                      ? cost_start(p, sc, blockIdx.x + lane, G)
-                                      : CostPos{0, 0, 0, 0};
-                sm.info[2 + 4 * lane] = c.x;
-                sm.info[3 + 4 * lane] = c.b;
-                sm.info[4 + 4 * lane] = c.seg;
-                sm.info[5 + 4 * lane] = c.uu;
+            CostPos c0{0, 0, 0, 0}, c1{0, 0, 0, 0};
+            if (static_cast<int>(blockIdx.x) < G) {
+                c0 = cost_start(p, sc, blockIdx.x, G, lane);
+                c1 = cost_start(p, sc, blockIdx.x + 1, G, lane);
+            }
+            if (lane == 0) {
+                sm.info[2] = c0.x;
+                sm.info[3] = c0.b;
+                sm.info[4] = c0.seg;
+                sm.info[5] = c0.uu;
+                sm.info[6] = c1.x;
+                sm.info[7] = c1.b;
+                sm.info[8] = c1.seg;
+                sm.info[9] = c1.uu;
             }
         }
     }
@@ -791,9 +853,7 @@ template <typename T, int D, bool kSwizzled>
 __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, const CUtensorMap* kmap,
                         const CUtensorMap* vmap, int role, int lane)
 {
-    const CUtensorMap* map = role == 0 ? kmap : vmap;
-    if (lane == 0)
-        tma_prefetch_desc(map);
+    const CUtensorMap* map = role == 0 ? kmap : vmap;  // fetched at kernel entry
     const int S = p.stages;
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows * D * sizeof(T));
     const uint32_t new_bytes = static_cast<uint32_t>(p.NQ * D * sizeof(T));
@@ -1245,13 +1305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = p.stages;
     const int TT = p.TT;
 
-    warm_param(p);
-    warm_param(kmap);
-    warm_param(vmap);
-    // Inputs may be produced by the previous kernel on the stream.
-    init_cta(p, sm);
-    grid_dependency_wait();
-    grid_dependents_launch();
+    // inputs may be produced by the previous kernel on the stream
+    kernel_entry(p, kmap, vmap, sm);
     const Sched sc = setup_cta(p, sm);
 
     if (warp >= kConsumerWarps) {
@@ -1539,12 +1594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
 
-    warm_param(p);
-    warm_param(kmap);
-    warm_param(vmap);
-    init_cta(p, sm);
-    grid_dependency_wait();
-    grid_dependents_launch();
+    // inputs may be produced by the previous kernel on the stream
+    kernel_entry(p, kmap, vmap, sm);
     const Sched sc = setup_cta(p, sm);
 
     if (warp >= kConsumerWarps) {
@@ -1869,12 +1920,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
 
-    warm_param(p);
-    warm_param(kmap);
-    warm_param(vmap);
-    init_cta(p, sm);
-    grid_dependency_wait();
-    grid_dependents_launch();
+    // inputs may be produced by the previous kernel on the stream
+    kernel_entry(p, kmap, vmap, sm);
     const Sched sc = setup_cta(p, sm);
 
     if (warp >= kConsumerWarps) {
