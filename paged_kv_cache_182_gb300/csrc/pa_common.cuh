@@ -20,7 +20,7 @@ constexpr int kMmaStageBytes = 65536;  // tensor-core path: K + V tile bytes per
 constexpr int kHeaderBytes = 3584;  // barriers, scalars, zero row, table entries, split list
 constexpr int kMaxBatch = 4096;     // sequences per call (the schedule lives in smem)
 constexpr int kMaxGrid = 1024;      // partition-kernel CTAs at most (sizes the workspace)
-constexpr int kPieceStages = 2;   // automatic schedule: stages charged per segment
+constexpr int kPieceStages = 1;   // automatic schedule: stages charged per segment
 constexpr int kPieceStages2 = 6;  // the same with two 16-row groups per CTA pass
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
