@@ -93,6 +93,13 @@ __host__ __device__ constexpr int q_row_bytes(int D) { return D * 2 + 16; }
 SplitFn pick_split_f32(int D, int RG);
 SplitFn pick_split_f16(bool f32_out, int D, int MT);
 SplitFn pick_split_bf16(bool f32_out, int D, int MT);
+// Tensor-core prefill (pa_prefill_tc.cu): whether a prefill of these sizes
+// takes it, and its launch (the new rows already stored in the cache).
+bool prefill_tc_supported(int dtype, int D, int H, int KV, int NQ);
+int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, const int32_t* table,
+                      const int32_t* seq_lens, void* out, float scale, int B, int H, int KV, int BLOCK,
+                      int NQ, int maxb, int num_blocks, int dtype, int out_dtype, int* status,
+                      cudaStream_t st, uint64_t* launches);
 CombineFn pick_combine_f32(int D);
 CombineFn pick_combine_f16(int D);
 CombineFn pick_combine_bf16(int D);

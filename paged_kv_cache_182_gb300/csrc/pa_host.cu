@@ -908,10 +908,13 @@ int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
 
 // ------------------------------------------------------------------ prefill
 // A prefill of NQ new tokens per sequence runs as the cache append of all new
-// rows (slots from the block table) followed by causal decodes of chunks of at
-// most PA_MAX_NQ rows: chunk [r0, r0 + n) sees seq_lens[b] + r0 cached tokens
-// (the earlier chunks' rows are in the cache by then) and its own rows as new
-// rows, so row r attends to keys 0 .. seq_lens[b] + r.
+// rows (slots from the block table), then
+//   - for 16-bit caches with D = 128 and more than PA_MAX_NQ new rows, one
+//     tensor-core launch (pa_prefill_tc.cu) over 128-row query tiles;
+//   - otherwise causal decodes of chunks of at most PA_MAX_NQ rows: chunk
+//     [r0, r0 + n) sees seq_lens[b] + r0 cached tokens (the earlier chunks'
+//     rows are in the cache by then) and its own rows as new rows.
+// Either way row r attends to keys 0 .. seq_lens[b] + r.
 
 // New row j of sequence b is token seq_lens[b] + j: its slot comes from the
 // block table.  One thread per 16 bytes of one new row of K or V.
@@ -1166,6 +1169,15 @@ int pa_prefill(const void* q, void* k_cache, void* v_cache, const int32_t* block
     if (direct)
         return decode_impl(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, nullptr, out,
                            scale, H, KV, D, BLOCK, NQ, 1, &dopts, stream);
+    if (prefill_tc_supported(dtype, D, H, KV, NQ)) {
+        // 16-bit caches, D = 128: one tensor-core launch over all rows
+        uint64_t n = 0;
+        const int rc = launch_prefill_tc(q, k_cache, v_cache, block_table, seq_lens, out, scale, B, H,
+                                         KV, BLOCK, NQ, opts->max_blocks, opts->num_blocks, dtype,
+                                         out_dtype, opts->status, st, &n);
+        g_launches.fetch_add(n);
+        return rc;
+    }
 
     for (int r0 = 0; r0 < NQ; r0 += C) {
         const int n = NQ - r0 < C ? NQ - r0 : C;

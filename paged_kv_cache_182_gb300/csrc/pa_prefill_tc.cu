@@ -1,0 +1,622 @@
+// pa_prefill_tc.cu -- causal prefill on the sm_103a fifth-generation tensor
+// cores (tcgen05: MMAs from shared-memory descriptors, accumulators in tensor
+// memory), the path pa_prefill takes for 16-bit caches with D = 128.
+//
+// What is computed is the decode definition of onnxruntime-ep-mlx 0.31.1,
+// src/ops/paged_attention.rs (VECTOR_BODY) with many new rows: new row r of
+// sequence b (token past + r, past = seq_lens[b]) attends to keys
+// 0 .. past + r, the cached ones through the block table and the new ones,
+// which pa_prefill stores into the cache first; the engine page
+// (src/engine.rs) keeps a prefill configuration next to the decode one.
+//
+// How: one CTA per (sequence, KV head, tile of 128 query rows); a tile's rows
+// are the g = H / KV query heads of the KV head times T = 128 / g consecutive
+// new rows (head-major), so that one K/V tile serves all of them.  Per key
+// tile of 128 tokens, fetched by TMA one cache block at a time through the
+// block table:
+//   S  = Q K^T            M 128 (rows), N 128 (keys), K = D; A and B K-major
+//   softmax               one thread per row reads its S row from tensor memory,
+//                         masks keys past its causal bound, keeps the running
+//                         maximum and sum, rescales its O row in tensor memory
+//                         when the maximum grew, and writes P as a 16-bit high
+//                         part plus a 16-bit remainder (about 22 bits of P) to
+//                         shared memory;
+//   O += P_hi V + P_lo V  M 128, N = D, K 128 (keys); V as an MN-major operand.
+// Warps 0-3: softmax and epilogue (thread i = row i = tensor-memory lane i);
+// warp 4: TMA producer (two stages of K and V); warp 5: MMA issuer (one
+// thread).  The handshakes are mbarriers; every wait is bounded, and a wait
+// that gives up reports PA_STATUS_TIMEOUT.  Tensor memory (256 columns: S and
+// O) is allocated by warp 0 and freed on every path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_decode.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kTcD = 128;           // head size of this path
+constexpr int kTcTile = 128;        // query rows of a CTA tile, keys of a key tile
+constexpr int kTcHalf = 16384;      // one 64-column half of a 128-row tile, bytes
+constexpr int kTcThreads = 192;     // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr uint32_t kTcCols = 256;   // tensor-memory columns: S | O
+constexpr int kTcSmem = 14 * kTcHalf + 1024 + 256;  // Q 2, K 4, V 4, P 4 halves; align; barriers
+
+struct PrefillTcParams {
+    const int32_t* table;     // [B][maxb]
+    const int32_t* seq_lens;  // [B] cached tokens before the new rows
+    void* out;                // [B][H][NQ][D]
+    int* status;
+    float qscale;             // scale * log2(e)
+    int B, H, KV, NQ, BLOCK, maxb, num_blocks, g, T, tiles;  // tiles: row tiles per (b, kh)
+};
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand (tcgen05
+// format: start address, leading and stride byte offsets in 16-byte units,
+// descriptor version 1, swizzle mode 2 = 128 bytes).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFF) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile of
+// 128-byte rows (eight-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128(int r, int c)
+{
+    return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// Instruction descriptor of kind::f16 with float32 accumulation, M = 128:
+// A and B both bf16 (or both f16), A K-major, B K-major or MN-major.
+template <bool kBf>
+__device__ __forceinline__ uint32_t idesc(int n, bool b_mn_major)
+{
+    const uint32_t t = kBf ? 1u : 0u;
+    return (1u << 4) | (t << 7) | (t << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kTcTile >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 columns of this warp's 32 tensor-memory lanes; the wait takes the
+// registers as operands, so that no use of them is scheduled before it.
+struct Cols32 {
+    uint32_t r[32];
+};
+__device__ __forceinline__ void tmem_ld32(Cols32& c, uint32_t taddr)
+{
+    uint32_t* r = c.r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+__device__ __forceinline__ void tmem_st32(const Cols32& c, uint32_t taddr)
+{
+    const uint32_t* r = c.r;
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, int c4, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Two floats as a 16-bit pair rounded to nearest (high part) and the pair of
+// what remains (x - high), also rounded: together about 22 bits of x.
+template <typename T>
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo)
+{
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        const float2 hf = __half22float2(h);
+        const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+    }
+}
+
+template <typename TO>
+__device__ __forceinline__ void store_row(TO* dst, const float* v);  // 32 values
+template <>
+__device__ __forceinline__ void store_row<float>(float* dst, const float* v)
+{
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+template <>
+__device__ __forceinline__ void store_row<__half>(__half* dst, const float* v)
+{
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __half2 h = __floats2half2_rn(v[j + 2 * k], v[j + 2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(dst + j) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+template <>
+__device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, const float* v)
+{
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[j + 2 * k], v[j + 2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(dst + j) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+struct TcBars {
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_done;
+    uint32_t tmem;
+    int abort;
+};
+
+template <typename T, typename TO>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    pa_prefill_tc_kernel(const __grid_constant__ PrefillTcParams p, const __grid_constant__ CUtensorMap qmap,
+                         const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap)
+{
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* sQ = base;                  // 2 halves
+    unsigned char* sK = base + 2 * kTcHalf;    // 2 stages x 2 halves
+    unsigned char* sV = base + 6 * kTcHalf;    // 2 stages x 2 halves
+    unsigned char* sP = base + 10 * kTcHalf;   // P_hi (2 token halves), P_lo (2 token halves)
+    TcBars& bars = *reinterpret_cast<TcBars*>(base + 14 * kTcHalf);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rt = blockIdx.x % p.tiles;
+    const int kh = (blockIdx.x / p.tiles) % p.KV;
+    const int b = blockIdx.x / (p.tiles * p.KV);
+    const int r_base = rt * p.T;
+    const int r_last = min(r_base + p.T, p.NQ) - 1;  // last new row of the tile
+    const int cap = p.maxb * p.BLOCK - p.NQ;         // largest past the table can hold
+    int past = p.seq_lens[b];
+    if (past < 0 || past > cap) {
+        if (tid == 0 && rt == 0 && kh == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_BAD_LENGTH);
+        past = past < 0 ? 0 : (cap < 0 ? 0 : cap);
+    }
+    const int end = past + p.NQ;                                 // keys of the sequence
+    const int ntiles = (past + r_last + 1 + kTcTile - 1) / kTcTile;  // keys 0 .. past + r_last
+
+    if (tid == 0) {
+        mbar_init(&bars.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.kv_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.s_free, 128);
+        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.o_done, 1);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars.tmem)),
+                     "r"(kTcCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = bars.tmem, tO = bars.tmem + kTcTile;
+    volatile int* abort_flag = &bars.abort;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.status)
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+    };
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        // Lane k issues the K and V boxes (both 64-column halves) of cache block
+        // k of each key tile; the table entries of the next tile are loaded
+        // while the current one is in flight.
+        const int boxes = kTcTile / p.BLOCK;
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            mbar_arrive_expect_tx(&bars.q_full, 2 * kTcHalf);
+            for (int h = 0; h < 2; ++h)
+                tma_load_5d(sQ + h * kTcHalf, &qmap, 0, h, r_base, kh * p.g, b, &bars.q_full);
+        }
+        auto entry = [&](int t) {  // cache row of this lane's block in tile t, or out of range
+            const int tok = t * kTcTile + lane * p.BLOCK;
+            const int blk = tok / p.BLOCK;
+            int row0 = p.num_blocks * p.BLOCK;  // past the pool: the box reads zeros
+            if (lane < boxes && t < ntiles && tok < end && blk < p.maxb) {
+                const int phys = p.table[static_cast<size_t>(b) * p.maxb + blk];
+                if (phys >= 0 && phys < p.num_blocks)
+                    row0 = phys * p.BLOCK;
+            }
+            return row0;
+        };
+        int row_next = entry(0);
+        int issued = 0;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t & 1;
+            const int row0 = row_next;
+            if (t >= 2) {
+                bool ok = !*abort_flag && mbar_wait_bounded(&bars.kv_empty[s], ((t >> 1) - 1) & 1, kWaitLimitNs);
+                ok = __all_sync(kFull, ok);
+                if (!ok) {
+                    if (lane == 0)
+                        fail();
+                    break;
+                }
+            }
+            if (lane == 0)
+                mbar_arrive_expect_tx(&bars.kv_full[s], 4 * kTcHalf);
+            __syncwarp();
+            if (lane < boxes)
+                for (int h = 0; h < 2; ++h) {
+                    const int off = s * 2 * kTcHalf + h * kTcHalf + lane * p.BLOCK * 128;
+                    tma_load_4d(sK + off, &kmap, 0, h, kh, row0, &bars.kv_full[s]);
+                    tma_load_4d(sV + off, &vmap, 0, h, kh, row0, &bars.kv_full[s]);
+                }
+            issued = t + 1;
+            row_next = entry(t + 1);
+        }
+        // no copy may land after the CTA's memory is released: wait (bounded)
+        // for the last tile issued on each stage and for q
+        if (lane == 0) {
+            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
+                mbar_wait_bounded(&bars.kv_full[t & 1], (t >> 1) & 1, kWaitLimitNs);
+            mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // -------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
+            const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+            const uint32_t phi = smem_u32(sP), plo = smem_u32(sP + 2 * kTcHalf);
+            const uint32_t id_s = idesc<kBf>(kTcTile, false), id_o = idesc<kBf>(kTcD, true);
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t & 1;
+                ok = !*abort_flag && mbar_wait_bounded(&bars.kv_full[s], (t >> 1) & 1, kWaitLimitNs);
+                if (ok && t > 0)
+                    ok = mbar_wait_bounded(&bars.s_free, (t - 1) & 1, kWaitLimitNs);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                // S = Q K^T over the head dimension: K-steps of 16 columns, four
+                // per 64-column half
+                for (int ks = 0; ks < kTcD / 16; ++ks) {
+                    const uint32_t o = (ks >> 2) * kTcHalf + (ks & 3) * 32;
+                    umma(tS, smem_desc(qa + o, 16, 1024), smem_desc(ka + s * 2 * kTcHalf + o, 16, 1024),
+                         id_s, ks > 0);
+                }
+                umma_commit(&bars.s_full);
+                ok = mbar_wait_bounded(&bars.p_full, t & 1, kWaitLimitNs);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                // O += P_hi V + P_lo V over the tile's keys: V is MN-major (its
+                // rows are keys, 64 columns of D per half, the halves 16 KB apart)
+                for (int part = 0; part < 2; ++part)
+                    for (int ks = 0; ks < kTcTile / 16; ++ks) {
+                        const uint32_t pa = (part ? plo : phi) + (ks >> 2) * kTcHalf + (ks & 3) * 32;
+                        umma(tO, smem_desc(pa, 16, 1024), smem_desc(va + s * 2 * kTcHalf + ks * 2048, kTcHalf, 1024),
+                             id_o, t > 0 || part > 0 || ks > 0);
+                    }
+                umma_commit(&bars.o_done);
+                umma_commit(&bars.kv_empty[s]);
+            }
+            if (!ok)
+                fail();
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------- softmax and epilogue (rows)
+        const int i = tid;  // tile row = tensor-memory lane
+        const int hg = i / p.T, tt = i - hg * p.T;
+        const int r = r_base + tt;
+        const bool real = r < p.NQ;
+        const int limit = past + r;  // last visible key
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int s = t & 1;
+            ok = __all_sync(kFull, !*abort_flag && mbar_wait_bounded(&bars.s_full, t & 1, kWaitLimitNs));
+            if (!ok)
+                break;
+            tc_fence_after();
+            float sc[kTcTile];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                Cols32 x;
+                tmem_ld32(x, tS + lane_off + c * 32);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int key = t * kTcTile + c * 32 + j;
+                    sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.s_free);
+            float mt = m;
+#pragma unroll
+            for (int j = 0; j < kTcTile; ++j)
+                mt = fmaxf(mt, sc[j]);
+            const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf)
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kTcTile; ++j) {
+                sc[j] = fast_exp2(sc[j] - mt);
+                sum += sc[j];
+            }
+            l = l * alpha + sum;
+            m = mt;
+            // keys past the sequence end inside its last cache block hold other
+            // data (not finite for certain): their V rows are zeroed, since
+            // P = 0 does not cancel a non-finite value in the MMA
+            const int tok = t * kTcTile + i;
+            if (t * kTcTile + kTcTile > end) {  // uniform over the CTA
+                // the stage has landed (s_full came after it); the wait orders
+                // these stores after the copy's writes
+                ok = __all_sync(kFull, mbar_wait_bounded(&bars.kv_full[s], (t >> 1) & 1, kWaitLimitNs));
+                if (ok && tok >= end)
+                    for (int h = 0; h < 2; ++h) {
+                        uint4* row = reinterpret_cast<uint4*>(sV + s * 2 * kTcHalf + h * kTcHalf + i * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            row[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+            }
+            if (t > 0) {
+                // the previous tile's P.V is complete: P may be overwritten and
+                // O rescaled (warp-uniform: tcgen05.ld/st are warp-wide)
+                ok = __all_sync(kFull, ok && mbar_wait_bounded(&bars.o_done, (t - 1) & 1, kWaitLimitNs));
+                if (!ok)
+                    break;
+                tc_fence_after();
+                if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        Cols32 x;
+                        tmem_ld32(x, tO + lane_off + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
+                        tmem_st32(x, tO + lane_off + c * 32);
+                    }
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            // P as high part + remainder, K-major A operand (128-byte swizzle):
+            // row i, keys 8c .. 8c + 7 in chunk c & 7 of token half c >> 3
+#pragma unroll
+            for (int c = 0; c < kTcTile / 8; ++c) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    split_pair<T>(sc[c * 8 + 2 * k], sc[c * 8 + 2 * k + 1], hi[k], lo[k]);
+                const uint32_t off = (c >> 3) * kTcHalf + sw128(i, c & 7);
+                *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(sP + 2 * kTcHalf + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars.p_full);
+        }
+        if (ok)
+            ok = __all_sync(kFull, mbar_wait_bounded(&bars.o_done, (ntiles - 1) & 1, kWaitLimitNs));
+        if (!ok) {
+            if (lane == 0)
+                fail();
+        } else {
+            tc_fence_after();
+            const int h = kh * p.g + hg;
+            TO* o = static_cast<TO*>(p.out) + ((static_cast<size_t>(b) * p.H + h) * p.NQ + r) * kTcD;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                Cols32 x;
+                tmem_ld32(x, tO + lane_off + c * 32);
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __uint_as_float(x.r[j]) * inv;
+                if (real)
+                    store_row<TO>(o + c * 32, v);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(bars.tmem), "r"(kTcCols)
+                     : "memory");
+}
+
+using PrefillTcFn = void (*)(PrefillTcParams, CUtensorMap, CUtensorMap, CUtensorMap);
+
+PrefillTcFn pick_prefill_tc(int dtype, bool f32_out)
+{
+    if (dtype == PA_BF16)
+        return f32_out ? pa_prefill_tc_kernel<__nv_bfloat16, float>
+                       : pa_prefill_tc_kernel<__nv_bfloat16, __nv_bfloat16>;
+    return f32_out ? pa_prefill_tc_kernel<__half, float> : pa_prefill_tc_kernel<__half, __half>;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int dtype, int D, int H, int KV, int NQ)
+{
+    const int g = H / KV;
+    return (dtype == PA_F16 || dtype == PA_BF16) && D == kTcD && g >= 1 && g <= kTcTile &&
+           kTcTile % g == 0 && NQ > PA_MAX_NQ;
+}
+
+// Enqueues the tensor-core prefill on `st` (the new rows must already be in
+// the cache).  Returns PA_OK or a PA_ERR_* code before any launch.
+int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, const int32_t* table,
+                      const int32_t* seq_lens, void* out, float scale, int B, int H, int KV, int BLOCK,
+                      int NQ, int maxb, int num_blocks, int dtype, int out_dtype, int* status,
+                      cudaStream_t st, uint64_t* launches)
+{
+    auto enc = tc_encoder();
+    if (!enc)
+        return PA_ERR_DRIVER;
+    const int g = H / KV, T = kTcTile / g;
+    const CUtensorMapDataType dt =
+        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap qmap, kmap, vmap;
+    {
+        // q [B][H][NQ][D] as {64, 2, NQ, H, B}; box {64, 1, T, g, 1}: one
+        // 64-column half of the tile's 128 rows (g heads x T new rows)
+        cuuint64_t dims[5] = {64u, 2u, static_cast<cuuint64_t>(NQ), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+        cuuint64_t str[4] = {128u, kTcD * 2u, static_cast<cuuint64_t>(NQ) * kTcD * 2,
+                             static_cast<cuuint64_t>(H) * NQ * kTcD * 2};
+        cuuint32_t box[5] = {64u, 1u, static_cast<cuuint32_t>(T), static_cast<cuuint32_t>(g), 1u};
+        cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
+        if (enc(&qmap, dt, 5, const_cast<void*>(q), dims, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PA_ERR_CUDA;
+    }
+    for (int w = 0; w < 2; ++w) {
+        // caches [rows][KV][D] as {64, 2, KV, rows}; box {64, 1, 1, BLOCK}: one
+        // half of one cache block of one KV head
+        cuuint64_t dims[4] = {64u, 2u, static_cast<cuuint64_t>(KV),
+                              static_cast<cuuint64_t>(num_blocks) * BLOCK};
+        cuuint64_t str[3] = {128u, kTcD * 2u, static_cast<cuuint64_t>(KV) * kTcD * 2};
+        cuuint32_t box[4] = {64u, 1u, 1u, static_cast<cuuint32_t>(BLOCK)};
+        cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+        if (enc(w ? &vmap : &kmap, dt, 4, const_cast<void*>(w ? v_cache : k_cache), dims, str, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PA_ERR_CUDA;
+    }
+    PrefillTcParams prm{};
+    prm.table = table;
+    prm.seq_lens = seq_lens;
+    prm.out = out;
+    prm.status = status;
+    prm.qscale = scale * kLog2e;
+    prm.B = B;
+    prm.H = H;
+    prm.KV = KV;
+    prm.NQ = NQ;
+    prm.BLOCK = BLOCK;
+    prm.maxb = maxb;
+    prm.num_blocks = num_blocks;
+    prm.g = g;
+    prm.T = T;
+    prm.tiles = (NQ + T - 1) / T;
+    const PrefillTcFn fn = pick_prefill_tc(dtype, out_dtype == PA_F32);
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcSmem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const long long grid = static_cast<long long>(B) * KV * prm.tiles;
+    if (grid >= (1ll << 31))
+        return PA_ERR_BAD_DIMS;
+    fn<<<static_cast<unsigned>(grid), kTcThreads, kTcSmem, st>>>(prm, qmap, kmap, vmap);
+    if (cudaGetLastError() != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (launches)
+        ++*launches;
+    return PA_OK;
+}
+
+}  // namespace pa

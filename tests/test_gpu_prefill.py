@@ -60,6 +60,10 @@ CASES = [
     ("f32", 4, 2, 64, 16, 33, [1, 70]),
     ("f16", 16, 8, 128, 8, 16, [20, 0, 64]),     # one chunk: no staging
     ("f16", 8, 2, 64, 16, 1, [300]),             # one new row
+    # the tensor-core path (16-bit, D = 128, more than 16 new rows)
+    ("bf16", 16, 16, 128, 32, 45, [0, 130]),     # one head per tile: 128 rows, partial
+    ("bf16", 64, 4, 128, 64, 70, [9, 1000]),     # 16 heads x 8 rows a tile, BLOCK 64
+    ("f16", 16, 2, 128, 8, 130, [250, 3]),       # 8 heads x 16 rows, 16 blocks a key tile
 ]
 
 
@@ -69,6 +73,11 @@ def test_prefill_small(case, P):
     dt, H, KV, D, BLOCK, NQ, lens = case
     spec = W.Spec("prefill", dt, B=len(lens), H=H, KV=KV, D=D, BLOCK=BLOCK, NQ=NQ, causal=True)
     run_case(W.make_prefill(spec, seed=21, lens=lens), P)
+
+
+def test_prefill_tensor_core_native_output():
+    spec = W.Spec("prefill", "bf16", B=2, H=32, KV=8, D=128, BLOCK=16, NQ=77, causal=True)
+    run_case(W.make_prefill(spec, seed=24, lens=[513, 64]), 0, out_dtype=None)
 
 
 def test_prefill_full_workload():
