@@ -22,11 +22,15 @@
 //                         part plus a 16-bit remainder (about 22 bits of P) to
 //                         shared memory;
 //   O += P_hi V + P_lo V  M 128, N = D, K 128 (keys); V as an MN-major operand.
-// Warps 0-3: softmax and epilogue (thread i = row i = tensor-memory lane i);
-// warp 4: TMA producer (two stages of K and V); warp 5: MMA issuer (one
-// thread).  The handshakes are mbarriers; every wait is bounded, and a wait
-// that gives up reports PA_STATUS_TIMEOUT.  Tensor memory (256 columns: S and
-// O) is allocated by warp 0 and freed on every path.
+// Warps 0-7: softmax and epilogue, two threads a row (warps w and w + 4 take
+// the low and the high 64 columns of tensor-memory lanes 32 (w % 4) ..; they
+// exchange the row maximum of each key tile through shared memory); warp 8:
+// TMA producer (two stages of K and V); warp 9: MMA issuer (one thread).  S
+// is double-buffered in tensor memory, so that the MMA of key tile t + 1 runs
+// while the softmax works on tile t.  The handshakes are mbarriers; every
+// wait is bounded, and a wait that gives up reports PA_STATUS_TIMEOUT.  Tensor
+// memory (512 columns: S twice, O) is allocated by warp 0 and freed on every
+// path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -47,9 +51,12 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kTcD = 128;           // head size of this path
 constexpr int kTcTile = 128;        // query rows of a CTA tile, keys of a key tile
 constexpr int kTcHalf = 16384;      // one 64-column half of a 128-row tile, bytes
-constexpr int kTcThreads = 192;     // warps 0-3 softmax, 4 TMA, 5 MMA
-constexpr uint32_t kTcCols = 256;   // tensor-memory columns: S | O
-constexpr int kTcSmem = 14 * kTcHalf + 1024 + 256;  // Q 2, K 4, V 4, P 4 halves; align; barriers
+constexpr int kTcSoftmax = 256;     // softmax threads (warps 0-7)
+constexpr int kTcThreads = 320;     // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr uint32_t kTcCols = 512;   // tensor-memory columns: S0 | S1 | O | (unused)
+// Q 2, K 4, V 4, P 4 halves, then the barriers and the row-maximum exchange;
+// the dynamic shared-memory base must be 1024-aligned (checked at entry)
+constexpr int kTcSmem = 14 * kTcHalf + 3072;
 
 struct PrefillTcParams {
     const int32_t* table;     // [B][maxb]
@@ -164,6 +171,22 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Barrier of the 64 threads of two warps (named barrier `id`) that also returns
+// the OR of `v` over them, so that both warps take the same decision after it.
+__device__ __forceinline__ bool pair_bar_or(int id, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, 64, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
 // Two floats as a 16-bit pair rounded to nearest (high part) and the pair of
 // what remains (x - high), also rounded: together about 22 bits of x.
 template <typename T>
@@ -223,10 +246,12 @@ __device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, con
 }
 
 struct TcBars {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_done;
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done;
     uint32_t tmem;
     int abort;
+    float xchg[2][2][kTcTile];  // [tile parity][column half][row]: partial row maxima, then sums
 };
+static_assert(sizeof(TcBars) <= 3072, "barrier area");
 
 template <typename T, typename TO>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -235,7 +260,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 {
     constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    if ((smem_u32(smem_raw) & 1023u) != 0) {  // the layout leaves no room to realign
+        if (threadIdx.x == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+        return;
+    }
+    unsigned char* base = smem_raw;
     unsigned char* sQ = base;                  // 2 halves
     unsigned char* sK = base + 2 * kTcHalf;    // 2 stages x 2 halves
     unsigned char* sV = base + 6 * kTcHalf;    // 2 stages x 2 halves
@@ -263,10 +293,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.kv_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
+            mbar_init(&bars.s_full[s], 1);
+            mbar_init(&bars.s_free[s], kTcSoftmax);
         }
-        mbar_init(&bars.s_full, 1);
-        mbar_init(&bars.s_free, 128);
-        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.p_full, kTcSoftmax);
         mbar_init(&bars.o_done, 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -281,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = bars.tmem, tO = bars.tmem + kTcTile;
+    const uint32_t tS0 = bars.tmem, tO = bars.tmem + 2 * kTcTile;  // S(t) at tS0 + 128 (t & 1)
     volatile int* abort_flag = &bars.abort;
     auto fail = [&]() {
         *abort_flag = 1;
@@ -289,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             atomicOr(p.status, PA_STATUS_TIMEOUT);
     };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
         // Lane k issues the K and V boxes (both 64-column halves) of cache block
         // k of each key tile; the table entries of the next tile are loaded
@@ -348,29 +378,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // -------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
             const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
             const uint32_t phi = smem_u32(sP), plo = smem_u32(sP + 2 * kTcHalf);
             const uint32_t id_s = idesc<kBf>(kTcTile, false), id_o = idesc<kBf>(kTcD, true);
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int s = t & 1;
-                ok = !*abort_flag && mbar_wait_bounded(&bars.kv_full[s], (t >> 1) & 1, kWaitLimitNs);
-                if (ok && t > 0)
-                    ok = mbar_wait_bounded(&bars.s_free, (t - 1) & 1, kWaitLimitNs);
-                if (!ok)
-                    break;
+            // S(u) = Q K(u)^T over the head dimension (K-steps of 16 columns, four
+            // per 64-column half) into S buffer u & 1, once tile u has landed and
+            // the softmax has read S(u - 2) from that buffer
+            auto issue_s = [&](int u) {
+                const int su = u & 1;
+                bool good = !*abort_flag && mbar_wait_bounded(&bars.kv_full[su], (u >> 1) & 1, kWaitLimitNs);
+                if (good && u >= 2)
+                    good = mbar_wait_bounded(&bars.s_free[su], ((u >> 1) - 1) & 1, kWaitLimitNs);
+                if (!good)
+                    return false;
                 tc_fence_after();
-                // S = Q K^T over the head dimension: K-steps of 16 columns, four
-                // per 64-column half
                 for (int ks = 0; ks < kTcD / 16; ++ks) {
                     const uint32_t o = (ks >> 2) * kTcHalf + (ks & 3) * 32;
-                    umma(tS, smem_desc(qa + o, 16, 1024), smem_desc(ka + s * 2 * kTcHalf + o, 16, 1024),
-                         id_s, ks > 0);
+                    umma(tS0 + su * kTcTile, smem_desc(qa + o, 16, 1024),
+                         smem_desc(ka + su * 2 * kTcHalf + o, 16, 1024), id_s, ks > 0);
                 }
-                umma_commit(&bars.s_full);
+                umma_commit(&bars.s_full[su]);
+                return true;
+            };
+            if (ok && ntiles > 0)
+                ok = issue_s(0);
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t & 1;
+                if (t + 1 < ntiles && !issue_s(t + 1)) {
+                    ok = false;
+                    break;
+                }
                 ok = mbar_wait_bounded(&bars.p_full, t & 1, kWaitLimitNs);
                 if (!ok)
                     break;
@@ -392,41 +433,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------- softmax and epilogue (rows)
-        const int i = tid;  // tile row = tensor-memory lane
-        const int hg = i / p.T, tt = i - hg * p.T;
+        const int row = (warp & 3) * 32 + lane;  // tile row = tensor-memory lane
+        const int part = warp >> 2;              // columns [64 part, 64 part + 64)
+        const int hg = row / p.T, tt = row - hg * p.T;
         const int r = r_base + tt;
         const bool real = r < p.NQ;
         const int limit = past + r;  // last visible key
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        float m = -INFINITY, l = 0.f;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t col0 = part * 64;
+        const int pair_bar = 1 + (warp & 3);  // named barrier of warps w, w + 4
+        float m = -INFINITY, l = 0.f;  // running maximum; this thread's share of the sum
+        // The two warps of a row meet at one barrier per tile (the maximum
+        // exchange), and leave the loop only there, together: a wait that gave
+        // up (`fault`, warp-uniform) is OR-ed into that barrier.
         bool ok = true;
-        for (int t = 0; t < ntiles && ok; ++t) {
+        bool fault = false;
+        for (int t = 0; t < ntiles; ++t) {
             const int s = t & 1;
-            ok = __all_sync(kFull, !*abort_flag && mbar_wait_bounded(&bars.s_full, t & 1, kWaitLimitNs));
-            if (!ok)
-                break;
-            tc_fence_after();
-            float sc[kTcTile];
+            const bool got = __all_sync(
+                kFull, !fault && !*abort_flag && mbar_wait_bounded(&bars.s_full[s], (t >> 1) & 1, kWaitLimitNs));
+            float sc[64];
+            float pm = -INFINITY;
+            if (got) {
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                Cols32 x;
-                tmem_ld32(x, tS + lane_off + c * 32);
+                for (int c = 0; c < 2; ++c) {
+                    Cols32 x;
+                    tmem_ld32(x, tS0 + s * kTcTile + lane_off + col0 + c * 32);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int key = t * kTcTile + c * 32 + j;
-                    sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
+                    for (int j = 0; j < 32; ++j) {
+                        const int key = t * kTcTile + col0 + c * 32 + j;
+                        sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
+                        pm = fmaxf(pm, sc[c * 32 + j]);
+                    }
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.s_free);
-            float mt = m;
-#pragma unroll
-            for (int j = 0; j < kTcTile; ++j)
-                mt = fmaxf(mt, sc[j]);
+            mbar_arrive(&bars.s_free[s]);
+            // the other half of the row's maximum
+            bars.xchg[s][part][row] = pm;
+            if (pair_bar_or(pair_bar, !got)) {
+                ok = false;
+                break;
+            }
+            const float mt = fmaxf(m, fmaxf(pm, bars.xchg[s][part ^ 1][row]));
             const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf)
             float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < kTcTile; ++j) {
+            for (int j = 0; j < 64; ++j) {
                 sc[j] = fast_exp2(sc[j] - mt);
                 sum += sc[j];
             }
@@ -435,48 +489,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // keys past the sequence end inside its last cache block hold other
             // data (not finite for certain): their V rows are zeroed, since
             // P = 0 does not cancel a non-finite value in the MMA
-            const int tok = t * kTcTile + i;
+            const int tok = t * kTcTile + row;
             if (t * kTcTile + kTcTile > end) {  // uniform over the CTA
                 // the stage has landed (s_full came after it); the wait orders
                 // these stores after the copy's writes
-                ok = __all_sync(kFull, mbar_wait_bounded(&bars.kv_full[s], (t >> 1) & 1, kWaitLimitNs));
-                if (ok && tok >= end)
-                    for (int h = 0; h < 2; ++h) {
-                        uint4* row = reinterpret_cast<uint4*>(sV + s * 2 * kTcHalf + h * kTcHalf + i * 128);
+                const bool landed =
+                    __all_sync(kFull, mbar_wait_bounded(&bars.kv_full[s], (t >> 1) & 1, kWaitLimitNs));
+                fault |= !landed;
+                if (landed && tok >= end) {
+                    uint4* vrow = reinterpret_cast<uint4*>(sV + s * 2 * kTcHalf + part * kTcHalf + row * 128);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            row[c] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    for (int c = 0; c < 8; ++c)
+                        vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             if (t > 0) {
                 // the previous tile's P.V is complete: P may be overwritten and
                 // O rescaled (warp-uniform: tcgen05.ld/st are warp-wide)
-                ok = __all_sync(kFull, ok && mbar_wait_bounded(&bars.o_done, (t - 1) & 1, kWaitLimitNs));
-                if (!ok)
-                    break;
-                tc_fence_after();
-                if (__any_sync(kFull, alpha != 1.f)) {
+                const bool done = __all_sync(
+                    kFull, !fault && mbar_wait_bounded(&bars.o_done, (t - 1) & 1, kWaitLimitNs));
+                fault |= !done;
+                if (done) {
+                    tc_fence_after();
+                    if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        Cols32 x;
-                        tmem_ld32(x, tO + lane_off + c * 32);
+                        for (int c = 0; c < 2; ++c) {
+                            Cols32 x;
+                            tmem_ld32(x, tO + lane_off + col0 + c * 32);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
-                        tmem_st32(x, tO + lane_off + c * 32);
+                            for (int j = 0; j < 32; ++j)
+                                x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
+                            tmem_st32(x, tO + lane_off + col0 + c * 32);
+                        }
                     }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
             // P as high part + remainder, K-major A operand (128-byte swizzle):
-            // row i, keys 8c .. 8c + 7 in chunk c & 7 of token half c >> 3
+            // row `row`, keys 64 part + 8c .. + 7 in chunk c of token half `part`
 #pragma unroll
-            for (int c = 0; c < kTcTile / 8; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     split_pair<T>(sc[c * 8 + 2 * k], sc[c * 8 + 2 * k + 1], hi[k], lo[k]);
-                const uint32_t off = (c >> 3) * kTcHalf + sw128(i, c & 7);
+                const uint32_t off = part * kTcHalf + sw128(row, c);
                 *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4*>(sP + 2 * kTcHalf + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
@@ -485,19 +542,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(&bars.p_full);
         }
         if (ok)
-            ok = __all_sync(kFull, mbar_wait_bounded(&bars.o_done, (ntiles - 1) & 1, kWaitLimitNs));
+            ok = __all_sync(kFull, !fault && mbar_wait_bounded(&bars.o_done, (ntiles - 1) & 1, kWaitLimitNs));
+        // the row sum over both halves, through the exchange slots of tile
+        // parity ntiles & 1: the partner's last read of them came before the
+        // last tile's barrier
+        const int sl = ntiles & 1;
+        if (ok)
+            bars.xchg[sl][part][row] = l;
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
         if (!ok) {
             if (lane == 0)
                 fail();
         } else {
             tc_fence_after();
+            const float L = l + bars.xchg[sl][part ^ 1][row];
             const int h = kh * p.g + hg;
-            TO* o = static_cast<TO*>(p.out) + ((static_cast<size_t>(b) * p.H + h) * p.NQ + r) * kTcD;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            TO* o = static_cast<TO*>(p.out) + ((static_cast<size_t>(b) * p.H + h) * p.NQ + r) * kTcD + col0;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 Cols32 x;
-                tmem_ld32(x, tO + lane_off + c * 32);
+                tmem_ld32(x, tO + lane_off + col0 + c * 32);
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
