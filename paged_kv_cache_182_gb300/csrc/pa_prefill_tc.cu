@@ -24,8 +24,10 @@
 //   O += P_hi V + P_lo V  M 128, N = D, K 128 (keys); V as an MN-major operand.
 // Warps 0-7: softmax and epilogue, two threads a row (warps w and w + 4 take
 // the low and the high 64 columns of tensor-memory lanes 32 (w % 4) ..; they
-// exchange the row maximum of each key tile through shared memory); warp 8:
-// TMA producer (two stages of K and V); warp 9: MMA issuer (one thread).  S
+// exchange the row maximum of each key tile through shared memory); warps 8
+// and 9: TMA producers of K and of V (two stages each; a K stage is free again
+// once its S is computed, a V stage once its P.V is); warp 10: MMA issuer (one
+// thread).  S
 // is double-buffered in tensor memory, so that the MMA of key tile t + 1 runs
 // while the softmax works on tile t.  The handshakes are mbarriers; every
 // wait is bounded, and a wait that gives up reports PA_STATUS_TIMEOUT.  Tensor
@@ -52,7 +54,7 @@ constexpr int kTcD = 128;           // head size of this path
 constexpr int kTcTile = 128;        // query rows of a CTA tile, keys of a key tile
 constexpr int kTcHalf = 16384;      // one 64-column half of a 128-row tile, bytes
 constexpr int kTcSoftmax = 256;     // softmax threads (warps 0-7)
-constexpr int kTcThreads = 320;     // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kTcThreads = 352;     // warps 0-7 softmax, 8-9 TMA (K, V), 10 MMA
 constexpr uint32_t kTcCols = 512;   // tensor-memory columns: S0 | S1 | O | (unused)
 // Q 2, K 4, V 4, P 4 halves, then the barriers and the row-maximum exchange;
 // the dynamic shared-memory base must be 1024-aligned (checked at entry)
@@ -246,7 +248,7 @@ __device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, con
 }
 
 struct TcBars {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done;
+    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, o_done;
     uint32_t tmem;
     int abort;
     float xchg[2][2][kTcTile];  // [tile parity][column half][row]: partial row maxima, then sums
@@ -291,8 +293,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         mbar_init(&bars.q_full, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars.kv_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
             mbar_init(&bars.s_full[s], 1);
             mbar_init(&bars.s_free[s], kTcSoftmax);
         }
@@ -319,19 +323,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             atomicOr(p.status, PA_STATUS_TIMEOUT);
     };
 
-    if (warp == 8) {
-        // ------------------------------------------------------------ TMA producer
-        // Lane k issues the K and V boxes (both 64-column halves) of cache block
-        // k of each key tile; the table entries of the next tile are loaded
-        // while the current one is in flight.
+    if (warp == 8 || warp == 9) {
+        // ----------------------------------------------------------- TMA producers
+        // Warp 8 issues the K boxes (and q), warp 9 the V boxes: lane k the
+        // boxes (both 64-column halves) of cache block k of each key tile; the
+        // table entries of the next tile are loaded while the current one is in
+        // flight.
+        const bool is_v = warp == 9;
+        const CUtensorMap* map = is_v ? &vmap : &kmap;
+        unsigned char* ring = is_v ? sV : sK;
+        uint64_t* full = is_v ? bars.v_full : bars.k_full;
+        uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
         const int boxes = kTcTile / p.BLOCK;
         if (lane == 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            mbar_arrive_expect_tx(&bars.q_full, 2 * kTcHalf);
-            for (int h = 0; h < 2; ++h)
-                tma_load_5d(sQ + h * kTcHalf, &qmap, 0, h, r_base, kh * p.g, b, &bars.q_full);
+            tma_prefetch_desc(map);
+            if (!is_v) {
+                tma_prefetch_desc(&qmap);
+                mbar_arrive_expect_tx(&bars.q_full, 2 * kTcHalf);
+                for (int h = 0; h < 2; ++h)
+                    tma_load_5d(sQ + h * kTcHalf, &qmap, 0, h, r_base, kh * p.g, b, &bars.q_full);
+            }
         }
         auto entry = [&](int t) {  // cache row of this lane's block in tile t, or out of range
             const int tok = t * kTcTile + lane * p.BLOCK;
@@ -350,7 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int s = t & 1;
             const int row0 = row_next;
             if (t >= 2) {
-                bool ok = !*abort_flag && mbar_wait_bounded(&bars.kv_empty[s], ((t >> 1) - 1) & 1, kWaitLimitNs);
+                bool ok = !*abort_flag && mbar_wait_bounded(&empty[s], ((t >> 1) - 1) & 1, kWaitLimitNs);
                 ok = __all_sync(kFull, ok);
                 if (!ok) {
                     if (lane == 0)
@@ -359,26 +370,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (lane == 0)
-                mbar_arrive_expect_tx(&bars.kv_full[s], 4 * kTcHalf);
+                mbar_arrive_expect_tx(&full[s], 2 * kTcHalf);
             __syncwarp();
             if (lane < boxes)
-                for (int h = 0; h < 2; ++h) {
-                    const int off = s * 2 * kTcHalf + h * kTcHalf + lane * p.BLOCK * 128;
-                    tma_load_4d(sK + off, &kmap, 0, h, kh, row0, &bars.kv_full[s]);
-                    tma_load_4d(sV + off, &vmap, 0, h, kh, row0, &bars.kv_full[s]);
-                }
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(ring + s * 2 * kTcHalf + h * kTcHalf + lane * p.BLOCK * 128, map, 0, h, kh, row0,
+                                &full[s]);
             issued = t + 1;
             row_next = entry(t + 1);
         }
         // no copy may land after the CTA's memory is released: wait (bounded)
-        // for the last tile issued on each stage and for q
+        // for the last tile issued on each stage (and for q)
         if (lane == 0) {
             for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-                mbar_wait_bounded(&bars.kv_full[t & 1], (t >> 1) & 1, kWaitLimitNs);
-            mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
+                mbar_wait_bounded(&full[t & 1], (t >> 1) & 1, kWaitLimitNs);
+            if (!is_v)
+                mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 10) {
         // -------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
@@ -386,11 +396,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t phi = smem_u32(sP), plo = smem_u32(sP + 2 * kTcHalf);
             const uint32_t id_s = idesc<kBf>(kTcTile, false), id_o = idesc<kBf>(kTcD, true);
             // S(u) = Q K(u)^T over the head dimension (K-steps of 16 columns, four
-            // per 64-column half) into S buffer u & 1, once tile u has landed and
-            // the softmax has read S(u - 2) from that buffer
+            // per 64-column half) into S buffer u & 1, once K(u) has landed and
+            // the softmax has read S(u - 2) from that buffer; K's stage is
+            // released when these MMAs complete
             auto issue_s = [&](int u) {
                 const int su = u & 1;
-                bool good = !*abort_flag && mbar_wait_bounded(&bars.kv_full[su], (u >> 1) & 1, kWaitLimitNs);
+                bool good = !*abort_flag && mbar_wait_bounded(&bars.k_full[su], (u >> 1) & 1, kWaitLimitNs);
                 if (good && u >= 2)
                     good = mbar_wait_bounded(&bars.s_free[su], ((u >> 1) - 1) & 1, kWaitLimitNs);
                 if (!good)
@@ -402,6 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          smem_desc(ka + su * 2 * kTcHalf + o, 16, 1024), id_s, ks > 0);
                 }
                 umma_commit(&bars.s_full[su]);
+                umma_commit(&bars.k_empty[su]);
                 return true;
             };
             if (ok && ntiles > 0)
@@ -413,6 +425,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 ok = mbar_wait_bounded(&bars.p_full, t & 1, kWaitLimitNs);
+                if (ok)
+                    ok = mbar_wait_bounded(&bars.v_full[s], (t >> 1) & 1, kWaitLimitNs);
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -425,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              id_o, t > 0 || part > 0 || ks > 0);
                     }
                 umma_commit(&bars.o_done);
-                umma_commit(&bars.kv_empty[s]);
+                umma_commit(&bars.v_empty[s]);
             }
             if (!ok)
                 fail();
@@ -491,10 +505,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // P = 0 does not cancel a non-finite value in the MMA
             const int tok = t * kTcTile + row;
             if (t * kTcTile + kTcTile > end) {  // uniform over the CTA
-                // the stage has landed (s_full came after it); the wait orders
-                // these stores after the copy's writes
+                // the V stage has landed; the wait orders these stores after the
+                // copy's writes (and they come before p_full, which P.V waits for)
                 const bool landed =
-                    __all_sync(kFull, mbar_wait_bounded(&bars.kv_full[s], (t >> 1) & 1, kWaitLimitNs));
+                    __all_sync(kFull, mbar_wait_bounded(&bars.v_full[s], (t >> 1) & 1, kWaitLimitNs));
                 fault |= !landed;
                 if (landed && tok >= end) {
                     uint4* vrow = reinterpret_cast<uint4*>(sV + s * 2 * kTcHalf + part * kTcHalf + row * 128);
