@@ -456,7 +456,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t col0 = part * 64;
         const int pair_bar = 1 + (warp & 3);  // named barrier of warps w, w + 4
-        float m = -INFINITY, l = 0.f;  // running maximum; this thread's share of the sum
+        // m: the maximum the exponentials are taken against (the running
+        // maximum, moved only when the maximum grows by more than 2^8: P stays
+        // at most 256, and O / l is the same for any reference); l: this
+        // thread's share of the sum
+        float m = -INFINITY, l = 0.f;
+        const int vis = past + r_base;  // every row of the tile sees keys 0 .. vis
         // The two warps of a row meet at one barrier per tile (the maximum
         // exchange), and leave the loop only there, together: a wait that gave
         // up (`fault`, warp-uniform) is OR-ed into that barrier.
@@ -470,15 +475,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float pm = -INFINITY;
             if (got) {
                 tc_fence_after();
+                const bool masked = t * kTcTile + kTcTile - 1 > vis;  // uniform over the CTA
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     Cols32 x;
                     tmem_ld32(x, tS0 + s * kTcTile + lane_off + col0 + c * 32);
+                    if (masked) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int key = t * kTcTile + col0 + c * 32 + j;
-                        sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
-                        pm = fmaxf(pm, sc[c * 32 + j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int key = t * kTcTile + col0 + c * 32 + j;
+                            sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
+                            pm = fmaxf(pm, sc[c * 32 + j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            sc[c * 32 + j] = __uint_as_float(x.r[j]) * p.qscale;
+                            pm = fmaxf(pm, sc[c * 32 + j]);
+                        }
                     }
                 }
             }
@@ -490,8 +504,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = false;
                 break;
             }
-            const float mt = fmaxf(m, fmaxf(pm, bars.xchg[s][part ^ 1][row]));
-            const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf)
+            const float tile_max = fmaxf(pm, bars.xchg[s][part ^ 1][row]);
+            // both threads of the row take the same decision from the same values
+            const float mt = tile_max > m + 8.f ? tile_max : m;
+            const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf), else 1 or tiny
             float sum = 0.f;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
