@@ -275,7 +275,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcBars& bars = *reinterpret_cast<TcBars*>(base + 14 * kTcHalf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rt = blockIdx.x % p.tiles;
+    // the last row tiles see the most keys: they are launched first, so that
+    // the short ones fill the last wave
+    const int rt = p.tiles - 1 - static_cast<int>(blockIdx.x % p.tiles);
     const int kh = (blockIdx.x / p.tiles) % p.KV;
     const int b = blockIdx.x / (p.tiles * p.KV);
     const int r_base = rt * p.T;
