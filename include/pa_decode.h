@@ -107,6 +107,17 @@ typedef struct pa_opts {
                            merges its partial states; 1, a separate log-sum-exp
                            merge kernel does (no counters needed).  Fixed
                            partitions (P >= 2) always use the merge kernel */
+    /* Failure testing (0 = off, the default of a zero-filled pa_opts):
+     * wait_limit_ns        limit of every wait inside the partition kernel
+     *                      (0: 2 seconds); a wait that runs out sets
+     *                      PA_STATUS_TIMEOUT, every warp of the CTA leaves, and
+     *                      no copy is left in flight when it exits
+     * debug_withhold_stage k > 0: the V-issuing warp of each partition-kernel
+     *                      CTA leaves its k-th pipeline stage out, so that the
+     *                      waits for that stage run out (the output is then
+     *                      undefined; zero the split counters again after it) */
+    unsigned long long wait_limit_ns;
+    int debug_withhold_stage;
 } pa_opts;
 
 /*
@@ -199,6 +210,40 @@ int pa_decode_host(const void *q, const void *k_cache, const void *v_cache,
  */
 size_t pa_host_workspace_bytes(int batch, int max_blocks, int H, int KV, int D, int NQ,
                                int partitions, int dtype, int out_dtype);
+
+/*
+ * How the automatic split (partitions == 0) of pa_decode divides a batch: the
+ * counterpart of the paged attention page's partition chooser
+ * (onnxruntime-ep-mlx 0.31.1, src/ops/paged_attention.rs: fn partitions, and
+ * fn vector, which launches one threadgroup per partition).  Where the page
+ * picks one partition count from a table of Apple GPU sizes, the partition
+ * kernel here lays every (sequence, row group, KV head) segment end to end,
+ * cut into stage-sized units, and gives each of its persistent CTAs an equal
+ * share of the cost (units plus a fixed charge per segment); a segment is
+ * split where a CTA's share ends inside it.  This call repeats that
+ * arithmetic on the host for given lengths.
+ *   host_seq_lens  HOST int32 [batch] cached tokens per sequence, or NULL: all
+ *                  sequences hold max_len tokens
+ *   max_len        the table's capacity in tokens (max_blocks * BLOCK): lengths
+ *                  are clamped to [0, max_len] as the kernel does
+ *   sms            CTAs of the partition kernel (one per SM), or 0: the SM count
+ *                  of the current device
+ * Fills *plan and returns plan->max_pieces (>= 1: the effective partition
+ * count, the most pieces one segment is split into), or a PA_ERR_* code
+ * (PA_ERR_CUDA when sms == 0 and no device answers).
+ */
+typedef struct pa_split_plan {
+    int grid;            /* partition-kernel CTAs launched */
+    int active;          /* CTAs that receive units (min(grid, total cost)) */
+    int segments;        /* (sequence, row group, KV head) segments */
+    int pieces;          /* pieces over all segments (a segment's piece per CTA) */
+    int split_segments;  /* segments cut between two or more CTAs */
+    int records;         /* partial records those pieces write (merged after) */
+    int max_pieces;      /* the most pieces of one segment */
+} pa_split_plan;
+
+int pa_choose_partitions(const int32_t *host_seq_lens, int max_len, int batch, int H, int KV, int D,
+                         int BLOCK, int NQ, int dtype, int sms, pa_split_plan *plan);
 
 /*
  * Bytes of workspace pa_decode needs for these sizes (0 when partitions == 1).

@@ -50,7 +50,14 @@ class PaOpts(ctypes.Structure):
         ("trace_begin", ctypes.c_void_p),
         ("trace_split", ctypes.c_void_p),
         ("merge_kernel", ctypes.c_int),
+        ("wait_limit_ns", ctypes.c_ulonglong),
+        ("debug_withhold_stage", ctypes.c_int),
     ]
+
+
+class SplitPlan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "grid", "active", "segments", "pieces", "split_segments", "records", "max_pieces")]
 
 
 def load(path: Path = LIBRARY) -> ctypes.CDLL:
@@ -88,6 +95,8 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_strerror.argtypes = [I]
     lib.pa_version.restype = I
     lib.pa_kernel_launches.restype = ctypes.c_uint64
+    lib.pa_choose_partitions.restype = I
+    lib.pa_choose_partitions.argtypes = [P, I, I, I, I, I, I, I, I, I, ctypes.POINTER(SplitPlan)]
     lib.pa_cache_append.restype = I
     lib.pa_cache_append.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P]
     return lib
@@ -108,6 +117,24 @@ def strerror(code: int) -> str:
 
 def kernel_launches() -> int:
     return int(LIB.pa_kernel_launches())
+
+
+def choose_partitions(seq_lens, max_len: int, H: int, KV: int, D: int, BLOCK: int, NQ: int,
+                      dtype=torch.float16, sms: int = 0, batch: int | None = None) -> SplitPlan:
+    """The automatic split pa_decode makes of a batch with these host lengths
+    (pa_choose_partitions); ``seq_lens=None`` means every sequence holds
+    ``max_len`` tokens (then ``batch`` gives their number)."""
+    if seq_lens is None:
+        arr, B = None, int(batch)
+    else:
+        lens = torch.as_tensor(seq_lens, dtype=torch.int32).contiguous().cpu()
+        arr, B = ctypes.c_void_p(lens.data_ptr()), int(lens.numel())
+    plan = SplitPlan()
+    rc = LIB.pa_choose_partitions(arr, int(max_len), B, H, KV, D, BLOCK, NQ, _DT[dtype], int(sms),
+                                  ctypes.byref(plan))
+    if rc < 0:
+        raise PagedAttentionError(rc)
+    return plan
 
 
 def workspace_bytes(B: int, H: int, KV: int, D: int, NQ: int, partitions: int = 0) -> int:

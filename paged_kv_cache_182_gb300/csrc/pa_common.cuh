@@ -59,6 +59,8 @@ struct SplitParams {
     int prefix_off;
     int merge_off;
     int stage_off;
+    unsigned long long wait_ns;  // limit of every mbarrier wait
+    int withhold;      // test switch: each CTA's V producer leaves its stage withhold - 1 out (0: off)
 };
 
 struct CombineParams {

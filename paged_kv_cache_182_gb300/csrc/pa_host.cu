@@ -62,6 +62,24 @@ int tokens_per_stage(int D, int es, int BLOCK)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Tokens per pipeline stage (the automatic schedule's unit).  Tensor-core
+// path: up to 64 KB stages, at most 8 warps (TPW tokens x row groups) per
+// stage: 128 tokens at D = 128, 256 at D = 64 (128 with 32 rows per pass); at
+// most 16 cache blocks per stage.
+int stage_tokens(int dtype, int D, int BLOCK, int MT)
+{
+    const int es = static_cast<int>(elem_size(dtype));
+    if (dtype == PA_F32)
+        return tokens_per_stage(D, es, BLOCK);
+    int TT = kMmaStageBytes / (2 * D * es);
+    const int TPW = kMmaTokens * mma_token_groups(D, MT);  // tokens per consumer warp and stage
+    if ((TT / TPW) * row_groups(MT) > kConsumerWarps)
+        TT = kConsumerWarps / row_groups(MT) * TPW;
+    if (TT > 16 * BLOCK)  // at most 16 boxes (one per block) per stage and role
+        TT = 16 * BLOCK;
+    return TT;
+}
+
 int ilog2(int x)  // x is a power of two
 {
     int l = 0;
@@ -341,6 +359,71 @@ static bool ws_args_ok(int batch, int H, int KV, int D, int NQ, int partitions)
            (D == 64 || D == 128) && NQ >= 1 && NQ <= PA_MAX_NQ && partitions >= 0;
 }
 
+int pa_choose_partitions(const int32_t* host_seq_lens, int max_len, int batch, int H, int KV, int D,
+                         int BLOCK, int NQ, int dtype, int sms, pa_split_plan* plan)
+{
+    if (!plan)
+        return PA_ERR_NULL_POINTER;
+    *plan = pa_split_plan{};
+    if (batch < 0 || H < 1 || KV < 1 || H % KV != 0 || max_len < 0 || sms < 0)
+        return PA_ERR_BAD_DIMS;
+    if ((D != 64 && D != 128) || (BLOCK != 8 && BLOCK != 16 && BLOCK != 32 && BLOCK != 64) || NQ < 1 ||
+        NQ > PA_MAX_NQ || (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16) || batch > kMaxBatch)
+        return PA_ERR_UNSUPPORTED;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    // the partition kernel's choices (decode_impl): rows per pass, stage size,
+    // charge per segment, one persistent CTA per SM
+    const int R = (H / KV) * NQ;
+    const int MT = mma_tiles(R);
+    const int rows_per_cta = rows_per_pass(dtype, R);
+    const int NRS = (R + rows_per_cta - 1) / rows_per_cta;
+    const int U = NRS * KV;
+    const int TT = stage_tokens(dtype, D, BLOCK, MT);
+    const long long V = dtype != PA_F32 && MT > 1 ? kPieceStages2 : kPieceStages;
+    const int grid = sms < kMaxGrid ? sms : kMaxGrid;
+    plan->grid = grid;
+    plan->segments = batch * U;
+    if (batch == 0)
+        return 1;
+    auto length = [&](int b) {
+        const long long s = host_seq_lens ? host_seq_lens[b] : max_len;
+        return s < 0 ? 0 : s > max_len ? max_len : s;  // the kernel's clamp
+    };
+    // cost: real unit x of segment g sits at x + V (g + 1); CTA k of G owns the
+    // cost positions [ceil(k C / G), ceil((k + 1) C / G))
+    long long W = 0;
+    for (int b = 0; b < batch; ++b)
+        W += (length(b) + NQ + TT - 1) / TT * U;
+    const long long C = W + V * batch * U;
+    if (C >= (1ll << 31))
+        return PA_ERR_BAD_DIMS;
+    const long long G = grid < C ? grid : C;
+    plan->active = static_cast<int>(G);
+    auto owner = [&](long long c) { return c * G / C < G - 1 ? c * G / C : G - 1; };
+    long long x0 = 0, g = 0;
+    int most = 1;
+    for (int b = 0; b < batch; ++b) {
+        const long long nu = (length(b) + NQ + TT - 1) / TT;
+        for (int s = 0; s < U; ++s, ++g, x0 += nu) {
+            const long long c0 = x0 + V * (g + 1);
+            const int n = static_cast<int>(owner(c0 + nu - 1) - owner(c0) + 1);
+            plan->pieces += n;
+            if (n > 1) {
+                ++plan->split_segments;
+                plan->records += n;
+            }
+            most = n > most ? n : most;
+        }
+    }
+    plan->max_pieces = most;
+    return most;
+}
+
 size_t pa_workspace_bytes(int batch, int H, int KV, int D, int NQ, int partitions)
 {
     if (!ws_args_ok(batch, H, KV, D, NQ, partitions) || partitions == 1 || batch == 0)
@@ -413,18 +496,11 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     if (records >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
     const int es = static_cast<int>(elem_size(dtype));
-    // tensor-core path: up to 64 KB stages, at most 8 warps (TPW tokens x row
-    // groups) per stage: 128 tokens at D = 128, 256 at D = 64 (128 with 32 rows
-    // per pass); at most 16 cache blocks per stage
-    int TT = mma ? kMmaStageBytes / (2 * D * es) : tokens_per_stage(D, es, BLOCK);
+    const int TT = stage_tokens(dtype, D, BLOCK, MT);
     const int TPW = kMmaTokens * mma_token_groups(D, MT);  // tokens per consumer warp and stage
-    if (mma && (TT / TPW) * row_groups(MT) > kConsumerWarps)
-        TT = kConsumerWarps / row_groups(MT) * TPW;
-    if (mma && TT > 16 * BLOCK)  // at most 16 boxes (one per block) per stage and role
-        TT = 16 * BLOCK;
     // automatic schedule: units of one stage.  Each segment is charged the
     // measured cost of a piece in stages (the consumer warps' merge and the
-    // start of the next piece): about two, six with two row groups per pass
+    // start of the next piece): about one, six with two row groups per pass
     // (four merge rounds)
     const int vunits = MT > 1 ? kPieceStages2 : kPieceStages;
     // (the units of all segments are counted in int32)
@@ -552,6 +628,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     p.prefix_off = prefix_off;
     p.merge_off = merge_off;
     p.stage_off = stage_off;
+    p.wait_ns = opts->wait_limit_ns ? opts->wait_limit_ns : kWaitLimitNs;
+    p.withhold = opts->debug_withhold_stage > 0 ? opts->debug_withhold_stage : 0;
 
     if (!launch)
         return PA_OK;

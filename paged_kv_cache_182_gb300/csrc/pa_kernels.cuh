@@ -883,7 +883,7 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
             asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
         }
         if (ph > 0) {
-            bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.empty[s], (ph - 1) & 1, kWaitLimitNs);
+            bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.empty[s], (ph - 1) & 1, p.wait_ns);
             ok = __all_sync(kFull, ok);
             if (!ok) {
                 if (lane == 0)
@@ -899,7 +899,7 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
             const int par = piece & 1;
             if (role == 0 && piece >= 2) {
                 bool ok = !*sm.abort_flag &&
-                          mbar_wait_bounded(&sm.q_free[par], ((piece >> 1) - 1) & 1, kWaitLimitNs);
+                          mbar_wait_bounded(&sm.q_free[par], ((piece >> 1) - 1) & 1, p.wait_ns);
                 ok = __all_sync(kFull, ok);
                 if (!ok) {
                     if (lane == 0)
@@ -937,11 +937,14 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
                 atomicOr(p.status, PA_STATUS_BAD_BLOCK);
         }
         unsigned char* st = sm.ring + static_cast<size_t>(s) * p.stage_bytes;
-        if (lane == 0)
+        // test switch (pa_opts.debug_withhold_stage): every CTA's V producer
+        // leaves one stage out, so that the consumers' wait for it runs out
+        const bool withheld = p.withhold > 0 && role == 1 && gt + 1 == static_cast<uint32_t>(p.withhold);
+        if (lane == 0 && !withheld)
             mbar_arrive_expect_tx(&sm.full[s], nb * box_bytes + (has_new ? 2u * new_bytes : 0u));
         __syncwarp();  // entries written by other lanes' cp.async are visible
         // One warp instruction issues every box of the stage (lane i: box i).
-        if (lane < nb) {
+        if (lane < nb && !withheld) {
             const int phys = ent[lane];
             // Out-of-pool coordinates read as zeros: the copy never faults.
             const int z = (phys << p.lg_block) + ((t0 + (lane << p.lg_box)) & (p.BLOCK - 1));
@@ -976,10 +979,10 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
     if (*sm.abort_flag && lane == 0) {
         const uint32_t first = gt > static_cast<uint32_t>(S) ? gt - S : 0u;
         for (uint32_t g = first; g < gt; ++g)
-            mbar_wait_bounded(&sm.full[g % S], (g / S) & 1, kWaitLimitNs);
+            mbar_wait_bounded(&sm.full[g % S], (g / S) & 1, p.wait_ns);
         if (role == 0)
             for (int pc = max(0, piece - 1); pc <= piece; ++pc)
-                mbar_wait_bounded(&sm.q_full[pc & 1], (pc >> 1) & 1, kWaitLimitNs);
+                mbar_wait_bounded(&sm.q_full[pc & 1], (pc >> 1) & 1, p.wait_ns);
     }
 }
 
@@ -1336,7 +1339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = gt % S;
             if (alive) {
                 alive = !*sm.abort_flag &&
-                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, kWaitLimitNs);
+                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, p.wait_ns);
                 alive = __all_sync(kFull, alive);
                 if (!alive && lane == 0)
                     flag_timeout(p, sm.abort_flag);
@@ -1643,7 +1646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int par = piece & 1;
             if (alive) {
                 alive = !*sm.abort_flag &&
-                        mbar_wait_bounded(&sm.q_full[par], (piece >> 1) & 1, kWaitLimitNs);
+                        mbar_wait_bounded(&sm.q_full[par], (piece >> 1) & 1, p.wait_ns);
                 alive = __all_sync(kFull, alive);
                 if (!alive && lane == 0)
                     flag_timeout(p, sm.abort_flag);
@@ -1682,7 +1685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = gt % S;
             if (alive) {
                 alive = !*sm.abort_flag &&
-                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, kWaitLimitNs);
+                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, p.wait_ns);
                 alive = __all_sync(kFull, alive);
                 if (!alive && lane == 0)
                     flag_timeout(p, sm.abort_flag);
@@ -1969,7 +1972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int par = piece & 1;
             if (alive) {
                 alive = !*sm.abort_flag &&
-                        mbar_wait_bounded(&sm.q_full[par], (piece >> 1) & 1, kWaitLimitNs);
+                        mbar_wait_bounded(&sm.q_full[par], (piece >> 1) & 1, p.wait_ns);
                 alive = __all_sync(kFull, alive);
                 if (!alive && lane == 0)
                     flag_timeout(p, sm.abort_flag);
@@ -2003,7 +2006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = gt % S;
             if (alive) {
                 alive = !*sm.abort_flag &&
-                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, kWaitLimitNs);
+                        mbar_wait_bounded(&sm.full[s], (gt / S) & 1, p.wait_ns);
                 alive = __all_sync(kFull, alive);
                 if (!alive && lane == 0)
                     flag_timeout(p, sm.abort_flag);

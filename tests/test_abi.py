@@ -310,3 +310,76 @@ def test_binding_constants_match_the_header(lib):
             "PA_STATUS_BAD_SLOT"} <= set(mirrored)
     for name in mirrored:
         assert getattr(lib, name) == defines[name], name
+
+
+def _brute_force_split(lens, max_len, U, TT, V, grid):
+    """The automatic split by its definition: segments of ceil((len + NQ) / TT)
+    units each, laid end to end with V virtual units charged before each
+    segment; CTA k of G owns the cost positions [ceil(k C / G),
+    ceil((k + 1) C / G)); a segment's pieces are the CTAs its real units fall
+    in (NQ = 1 here)."""
+    units = [(min(max(n, 0), max_len) + 1 + TT - 1) // TT for n in lens]
+    C = sum(u * U for u in units) + V * len(lens) * U
+    G = min(grid, C)
+    starts = [-(-k * C // G) for k in range(G + 1)]  # ceil(k C / G)
+
+    def owner(c):
+        k = 0
+        while starts[k + 1] <= c:
+            k += 1
+        return k
+
+    counts = []
+    x0 = g = 0
+    for u in units:
+        for _ in range(U):
+            c0 = x0 + V * (g + 1)
+            counts.append(len({owner(c) for c in range(c0, c0 + u)}))
+            x0 += u
+            g += 1
+    return counts, G
+
+
+def test_choose_partitions_matches_its_definition(lib):
+    """pa_choose_partitions against a brute-force walk of the cost positions
+    (16-bit caches, D = 128, 4 query rows per KV head: 128-token stages, one
+    charged unit per segment), on random length mixes and SM counts."""
+    import random
+
+    import torch
+
+    rng = random.Random(5)
+    for trial in range(40):
+        B = rng.randint(1, 40)
+        KV = rng.choice([1, 2, 8])
+        lens = [rng.choice([0, 1, rng.randint(0, 300), rng.randint(0, 20000)]) for _ in range(B)]
+        max_len = rng.choice([4096, 16384, 32768])
+        sms = rng.choice([1, 7, 148, 152, 300])
+        plan = lib.choose_partitions(lens, max_len, 4 * KV, KV, 128, 16, 1, torch.float16, sms=sms)
+        counts, G = _brute_force_split(lens, max_len, KV, 128, 1, min(sms, 1024))
+        assert plan.active == G and plan.grid == min(sms, 1024)
+        assert plan.segments == len(counts)
+        assert plan.pieces == sum(counts)
+        assert plan.split_segments == sum(1 for n in counts if n > 1)
+        assert plan.records == sum(n for n in counts if n > 1)
+        assert plan.max_pieces == max(counts)
+    # no lengths: every sequence holds max_len tokens
+    a = lib.choose_partitions(None, 32768, 32, 8, 128, 16, 1, torch.bfloat16, sms=152, batch=1)
+    b = lib.choose_partitions([32768], 32768, 32, 8, 128, 16, 1, torch.bfloat16, sms=152)
+    assert (a.pieces, a.max_pieces) == (b.pieces, b.max_pieces) == (152, 19)
+    short = lib.choose_partitions([10] * 1000, 4096, 32, 8, 128, 16, 1, torch.float16, sms=152)
+    assert short.max_pieces == 1 and short.records == 0
+    with pytest.raises(lib.PagedAttentionError):
+        lib.choose_partitions([5], 100, 32, 7, 128, 16, 1, torch.float16, sms=152)
+
+
+def test_failure_test_switches_are_off_by_default(lib):
+    """A zero-filled pa_opts (what the binding builds) leaves the wait limit at
+    its default and withholds no stage."""
+    o = lib.PaOpts()
+    assert o.wait_limit_ns == 0 and o.debug_withhold_stage == 0
+    header = (ROOT / "include" / "pa_decode.h").read_text()
+    assert "unsigned long long wait_limit_ns;" in header
+    assert "int debug_withhold_stage;" in header
+    names = [f[0] for f in lib.PaOpts._fields_]
+    assert names[-2:] == ["wait_limit_ns", "debug_withhold_stage"]
