@@ -67,6 +67,8 @@ extern "C" {
 #define PA_ERR_DRIVER (-7)       /* the tensor-map encoder of the driver is unavailable */
 #define PA_ERR_STATIC_LIMIT (-8) /* pa_decode_static_workspace: the call needs more
                                     scratch than PA_STATIC_WORKSPACE_BYTES */
+#define PA_ERR_NOT_PINNED (-9)   /* pa_host_register: the range is not page-locked host
+                                    memory mapped for the device */
 
 /* device status bits, OR-ed into *opts->status when it is not NULL */
 #define PA_STATUS_BAD_BLOCK 1  /* checked mode: a table entry outside [0, num_blocks) */
@@ -204,6 +206,22 @@ int pa_decode_host(const void *q, const void *k_cache, const void *v_cache,
                    int NQ, int causal, const pa_opts *opts, void *stream);
 
 /*
+ * Declares the page-locked host memory [ptr, ptr + bytes) (cudaHostAlloc,
+ * cudaHostRegister, a pinned framework tensor) to pa_decode_host, which then
+ * takes its device address from this record instead of asking the runtime on
+ * every call, and writes an `out` that lies in such a region directly from
+ * the kernels (no separate copy back).  The whole range must be page-locked
+ * and mapped for the device (else PA_ERR_NOT_PINNED); registering the same
+ * ptr again replaces its extent; at most 64 regions (else PA_ERR_BAD_DIMS).
+ * Call pa_host_unregister(ptr) before the memory is freed or unpinned: a
+ * record that outlives its buffer makes the kernels read or write memory that
+ * no longer belongs to it.  Host-side bookkeeping only (thread-safe); nothing
+ * is enqueued.
+ */
+int pa_host_register(const void *ptr, size_t bytes);
+int pa_host_unregister(const void *ptr);  /* PA_OK, or PA_ERR_NULL_POINTER if unknown */
+
+/*
  * Device workspace bytes of pa_decode_host for these sizes (opts->max_blocks,
  * opts->dtype and opts->out_dtype as in the call; -1 = same as dtype).
  * Returns 0 for invalid arguments.
@@ -234,7 +252,8 @@ size_t pa_host_workspace_bytes(int batch, int max_blocks, int H, int KV, int D, 
  */
 typedef struct pa_split_plan {
     int grid;            /* partition-kernel CTAs launched */
-    int active;          /* CTAs that receive units (min(grid, total cost)) */
+    int active;          /* CTAs that receive units: each at least 4 stages of cost,
+                            unless the segments are more; at most grid and the cost */
     int segments;        /* (sequence, row group, KV head) segments */
     int pieces;          /* pieces over all segments (a segment's piece per CTA) */
     int split_segments;  /* segments cut between two or more CTAs */

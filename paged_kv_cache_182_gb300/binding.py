@@ -95,6 +95,10 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_strerror.argtypes = [I]
     lib.pa_version.restype = I
     lib.pa_kernel_launches.restype = ctypes.c_uint64
+    lib.pa_host_register.restype = I
+    lib.pa_host_register.argtypes = [P, ctypes.c_size_t]
+    lib.pa_host_unregister.restype = I
+    lib.pa_host_unregister.argtypes = [P]
     lib.pa_choose_partitions.restype = I
     lib.pa_choose_partitions.argtypes = [P, I, I, I, I, I, I, I, I, I, ctypes.POINTER(SplitPlan)]
     lib.pa_cache_append.restype = I
@@ -390,10 +394,49 @@ class HostPlan:
                        ctypes.byref(self.opts))
         self._kc, self._vc = _ptr(k_cache), _ptr(v_cache)
 
-    def run(self, q, block_table, seq_lens, k_new, v_new, out, stream=None):
-        """Enqueue one step on ``stream`` (default: torch's current stream).  All
-        six tensors are host tensors; ``out`` holds the result once the stream
-        has been synchronised."""
+    def register(self, *tensors):
+        """Declare pinned host tensors to the library (pa_host_register): their
+        device addresses are then not looked up on every step, and an ``out``
+        among them is written by the kernels in place.  The plan keeps them
+        alive and releases the records in ``close``."""
+        if not hasattr(self, "_registered"):
+            self._registered = []
+        for x in tensors:
+            if x.is_cuda or not x.is_contiguous():
+                raise ValueError("only contiguous host tensors can be registered")
+            rc = LIB.pa_host_register(ctypes.c_void_p(x.data_ptr()), x.numel() * x.element_size())
+            if rc != 0:
+                raise PagedAttentionError(rc)
+            self._registered.append(x)
+
+    def close(self):
+        """Release the records of the registered tensors (before freeing them)."""
+        for x in getattr(self, "_registered", []):
+            LIB.pa_host_unregister(ctypes.c_void_p(x.data_ptr()))
+        self._registered = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may be gone
+            pass
+
+    def bind(self, q, block_table, seq_lens, k_new, v_new, out, stream=None):
+        """Check the step's host tensors once and fix them and the stream for
+        ``run_bound`` (a loop that refills the same pinned buffers each step)."""
+        self._check(q, block_table, seq_lens, k_new, v_new, out)
+        self._bound = (_ptr(q), self._kc, self._vc, _ptr(block_table), _ptr(seq_lens), _ptr(k_new),
+                       _ptr(v_new), _ptr(out), *self._fixed, _stream_handle(stream))
+        self._bound_out = out
+
+    def run_bound(self):
+        """One step on the tensors fixed by ``bind``: one foreign call."""
+        rc = LIB.pa_decode_host(*self._bound)
+        if rc != 0:
+            raise PagedAttentionError(rc)
+        return self._bound_out
+
+    def _check(self, q, block_table, seq_lens, k_new, v_new, out):
         s = self.shape
         if (tuple(q.shape) != (s["B"], s["H"], s["NQ"], s["D"]) or
                 tuple(block_table.shape) != (s["B"], s["max_blocks"]) or
@@ -410,7 +453,12 @@ class HostPlan:
             raise TypeError("out must have the plan's output dtype")
         if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
             raise TypeError("block_table and seq_lens must be int32")
-        k_cache, v_cache = self.caches
+
+    def run(self, q, block_table, seq_lens, k_new, v_new, out, stream=None):
+        """Enqueue one step on ``stream`` (default: torch's current stream).  All
+        six tensors are host tensors; ``out`` holds the result once the stream
+        has been synchronised."""
+        self._check(q, block_table, seq_lens, k_new, v_new, out)
         args = (_ptr(q), self._kc, self._vc, _ptr(block_table), _ptr(seq_lens), _ptr(k_new),
                 _ptr(v_new), _ptr(out), *self._fixed)
         if torch.cuda.current_device() == self.device.index:

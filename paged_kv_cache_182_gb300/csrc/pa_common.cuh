@@ -22,6 +22,22 @@ constexpr int kMaxBatch = 4096;     // sequences per call (the schedule lives in
 constexpr int kMaxGrid = 1024;      // partition-kernel CTAs at most (sizes the workspace)
 constexpr int kPieceStages = 1;   // automatic schedule: stages charged per segment
 constexpr int kPieceStages2 = 6;  // the same with two 16-row groups per CTA pass
+constexpr long long kMinCtaCost = 4;  // automatic schedule: stages of cost a CTA takes at least
+
+// CTAs of `grid` that the automatic schedule gives units to, for total cost C
+// over `segments` segments: every CTA at least kMinCtaCost stages of cost (a
+// short batch is not cut into pieces whose merges cost more than their work),
+// unless there are more segments than that, and never more than C (so that
+// every CTA inside a segment holds a unit of it).
+__host__ __device__ inline int active_ctas(long long grid, long long C, long long segments)
+{
+    long long want = (C + kMinCtaCost - 1) / kMinCtaCost;
+    if (want < segments)
+        want = segments;
+    if (want > C)
+        want = C;
+    return static_cast<int>(grid < want ? grid : want);
+}
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 

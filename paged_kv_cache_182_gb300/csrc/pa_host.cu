@@ -322,6 +322,9 @@ const char* pa_strerror(int code)
     case PA_ERR_DRIVER:
         return "PagedAttention: cannot reach the driver's tensor-map encoder; verify the CUDA "
                "driver version";
+    case PA_ERR_NOT_PINNED:
+        return "PagedAttention: the host range is not page-locked memory mapped for the device; "
+               "verify cudaHostAlloc / cudaHostRegister (or a pinned tensor) covers all of it";
     case PA_ERR_STATIC_LIMIT:
         return "PagedAttention: the call needs more scratch than the library's built-in "
                "PA_STATIC_WORKSPACE_BYTES; verify pa_workspace_bytes(), use fewer partitions, "
@@ -385,8 +388,11 @@ int pa_choose_partitions(const int32_t* host_seq_lens, int max_len, int batch, i
     const int U = NRS * KV;
     const int TT = stage_tokens(dtype, D, BLOCK, MT);
     const long long V = dtype != PA_F32 && MT > 1 ? kPieceStages2 : kPieceStages;
-    const int grid = sms < kMaxGrid ? sms : kMaxGrid;
-    plan->grid = grid;
+    long long grid = sms < kMaxGrid ? sms : kMaxGrid;
+    const long long cost_bound = static_cast<long long>(batch) * U * ((static_cast<long long>(max_len) + NQ + TT - 1) / TT + V);
+    if (grid > cost_bound && batch > 0)
+        grid = cost_bound;  // as pa_decode launches it (with max_len = max_blocks * BLOCK)
+    plan->grid = static_cast<int>(grid);
     plan->segments = batch * U;
     if (batch == 0)
         return 1;
@@ -402,7 +408,7 @@ int pa_choose_partitions(const int32_t* host_seq_lens, int max_len, int batch, i
     const long long C = W + V * batch * U;
     if (C >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
-    const long long G = grid < C ? grid : C;
+    const long long G = active_ctas(grid, C, static_cast<long long>(batch) * U);
     plan->active = static_cast<int>(G);
     auto owner = [&](long long c) { return c * G / C < G - 1 ? c * G / C : G - 1; };
     long long x0 = 0, g = 0;
@@ -604,6 +610,15 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     long long grid = static_cast<long long>(sms) * occ;  // persistent CTAs
     if (grid > kMaxGrid)
         grid = kMaxGrid;
+    if (partitions == 0) {
+        // no more CTAs than the schedule's cost (at most this, as every length
+        // is clamped to the table): the device uses min(CTAs, cost) of them, so
+        // a small batch no longer starts a CTA on every SM for nothing
+        const long long seg_units = (static_cast<long long>(opts->max_blocks) * BLOCK + NQ + TT - 1) / TT;
+        const long long cost_bound = static_cast<long long>(B) * NRS * KV * (seg_units + vunits);
+        if (grid > cost_bound)
+            grid = cost_bound;
+    }
     if (partitions != 0 && grid > records)  // fixed partitions: no more CTAs than items
         grid = records;
     p.qbuf_off = qbuf_off;
@@ -852,16 +867,85 @@ static int launch_append(void* k_cache, void* v_cache, const void* k_new, const 
     return PA_OK;
 }
 
-// Device address of a host pointer when it lies in page-locked (registered or
-// cudaHostAlloc) memory, else nullptr.  Looked up on every call: a cached
-// answer could outlive the buffer it was taken for.
-static const void* device_view(const void* host)
+// Page-locked host regions declared by pa_host_register: their device
+// addresses are taken from here, without a runtime query per call.
+namespace {
+struct HostRegion {
+    const char* lo;
+    size_t bytes;
+    const char* dev;
+};
+std::mutex g_host_mutex;
+constexpr int kHostRegions = 64;
+HostRegion g_host[kHostRegions];
+int g_host_count = 0;
+
+// Device address of [host, host + bytes) when it lies inside one registered
+// region, else nullptr.
+const void* registered_view(const void* host, size_t bytes)
+{
+    const char* p = static_cast<const char*>(host);
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    for (int i = 0; i < g_host_count; ++i) {
+        const HostRegion& r = g_host[i];
+        if (p >= r.lo && bytes <= r.bytes && static_cast<size_t>(p - r.lo) <= r.bytes - bytes)
+            return r.dev + (p - r.lo);
+    }
+    return nullptr;
+}
+
+// The runtime's device address of a host pointer in page-locked memory, else
+// nullptr (a pageable pointer is not an error for the caller).
+const void* query_view(const void* host)
 {
     cudaPointerAttributes a{};
     if (cudaPointerGetAttributes(&a, host) == cudaSuccess && a.type == cudaMemoryTypeHost)
         return a.devicePointer;
-    cudaGetLastError();  // a pageable pointer is not an error for the caller
+    cudaGetLastError();
     return nullptr;
+}
+}  // namespace
+
+// Device address of [host, host + bytes) when it lies in page-locked memory:
+// from a registered region, else asked of the runtime (on every call: an
+// answer cached without registration could outlive the buffer it was taken for).
+static const void* device_view(const void* host, size_t bytes)
+{
+    const void* r = registered_view(host, bytes);
+    return r ? r : query_view(host);
+}
+
+int pa_host_register(const void* ptr, size_t bytes)
+{
+    if (!ptr || bytes == 0)
+        return PA_ERR_NULL_POINTER;
+    const char* lo = static_cast<const char*>(ptr);
+    const char* d0 = static_cast<const char*>(query_view(lo));
+    const char* d1 = static_cast<const char*>(query_view(lo + bytes - 1));
+    if (!d0 || d1 != d0 + (bytes - 1))  // the whole range page-locked, mapped contiguously
+        return PA_ERR_NOT_PINNED;
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    for (int i = 0; i < g_host_count; ++i)
+        if (g_host[i].lo == lo) {  // registered again: the new extent replaces the old
+            g_host[i].bytes = bytes;
+            g_host[i].dev = d0;
+            return PA_OK;
+        }
+    if (g_host_count == kHostRegions)
+        return PA_ERR_BAD_DIMS;
+    g_host[g_host_count++] = HostRegion{lo, bytes, d0};
+    return PA_OK;
+}
+
+int pa_host_unregister(const void* ptr)
+{
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    for (int i = 0; i < g_host_count; ++i)
+        if (g_host[i].lo == ptr) {
+            g_host[i] = g_host[--g_host_count];
+            return PA_OK;
+        }
+    return PA_ERR_NULL_POINTER;
 }
 
 // Device workspace of pa_decode_host: the split workspace first (so that its
@@ -949,7 +1033,7 @@ int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
     GatherParams g{};
     bool mapped = true;
     for (int i = 0; i < 5 && mapped; ++i) {
-        const void* dv = device_view(in[i].src);
+        const void* dv = device_view(in[i].src, in[i].bytes);
         mapped = dv && (reinterpret_cast<uintptr_t>(dv) & 3) == 0 && in[i].bytes < (1u << 30);
         g.src[i] = dv;
         g.dst[i] = in[i].dst;
@@ -973,13 +1057,15 @@ int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
     pa_opts dev = *opts;
     dev.workspace = split ? ws : nullptr;
     dev.workspace_bytes = split;
+    // a registered output is written by the kernels in place (no copy back)
+    const size_t out_bytes = static_cast<size_t>(B) * H * NQ * D * eo;
+    void* out_dev = const_cast<void*>(registered_view(out, out_bytes));
     const int rc = pa_decode(ws + l.q, k_cache, v_cache, reinterpret_cast<const int32_t*>(ws + l.table),
                              reinterpret_cast<const int32_t*>(ws + l.lens), ws + l.knew, ws + l.vnew,
-                             ws + l.out, scale, H, KV, D, BLOCK, NQ, causal, &dev, stream);
-    if (rc != PA_OK)
+                             out_dev ? out_dev : ws + l.out, scale, H, KV, D, BLOCK, NQ, causal, &dev, stream);
+    if (rc != PA_OK || out_dev)
         return rc;
-    if (cudaMemcpyAsync(out, ws + l.out, static_cast<size_t>(B) * H * NQ * D * eo,
-                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (cudaMemcpyAsync(out, ws + l.out, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;
 }

@@ -420,7 +420,7 @@ __device__ __forceinline__ SegPieces seg_pieces(const SplitParams& p, const Sche
     SegPieces sp;
     if (p.partitions == 0) {
         const int C = static_cast<int>(sc.cost);
-        const int G = min(static_cast<int>(gridDim.x), C);
+        const int G = active_ctas(gridDim.x, C, static_cast<long long>(p.B) * p.NRS * p.KV);
         const int units = (sc.lens[b] + p.NQ + p.TT - 1) >> p.lg_tt;
         const int gl = rsg * p.KV + kh;
         const SegSpan ss = seg_span(sc.prefix[b] + gl * units, units, b * p.NRS * p.KV + gl, p.vunits, C, G);
@@ -762,9 +762,9 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
         if (lane == 0)
             sm.info[1] = sc.total;
         if (p.partitions == 0) {
-            // G = min(CTAs, C): every CTA inside a segment then holds a unit.
-            // The starts of this CTA's range and of the next CTA's.
-            const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), sc.cost));
+            // G <= C: every CTA inside a segment then holds a unit.  The starts
+            // of this CTA's range and of the next CTA's.
+            const int G = active_ctas(gridDim.x, sc.cost, static_cast<long long>(p.B) * p.NRS * p.KV);
             CostPos c0{0, 0, 0, 0}, c1{0, 0, 0, 0};
             if (static_cast<int>(blockIdx.x) < G) {
                 c0 = cost_start(p, sc, blockIdx.x, G, lane);
@@ -2230,7 +2230,7 @@ __global__ void __launch_bounds__(128) pa_combine_kernel(const __grid_constant__
         const int2 last = p.sched[p.B - 1];
         const long long W = static_cast<long long>(last.x) + static_cast<long long>(last.y) * U;
         const int C = static_cast<int>(W + static_cast<long long>(p.vunits) * p.B * U);
-        const int G = min(p.grid, C);
+        const int G = active_ctas(p.grid, C, static_cast<long long>(p.B) * U);
         const int gl = rsg * p.KV + kh;
         const SegSpan ss = seg_span(sc.x + gl * sc.y, sc.y, b * U + gl, p.vunits, C, G);
         k0 = ss.k0;

@@ -315,12 +315,14 @@ def test_binding_constants_match_the_header(lib):
 def _brute_force_split(lens, max_len, U, TT, V, grid):
     """The automatic split by its definition: segments of ceil((len + NQ) / TT)
     units each, laid end to end with V virtual units charged before each
-    segment; CTA k of G owns the cost positions [ceil(k C / G),
-    ceil((k + 1) C / G)); a segment's pieces are the CTAs its real units fall
-    in (NQ = 1 here)."""
+    segment; G CTAs take part (each at least 4 stages of cost unless there are
+    more segments than that, at most C); CTA k of G owns the cost positions
+    [ceil(k C / G), ceil((k + 1) C / G)); a segment's pieces are the CTAs its
+    real units fall in (NQ = 1 here)."""
     units = [(min(max(n, 0), max_len) + 1 + TT - 1) // TT for n in lens]
     C = sum(u * U for u in units) + V * len(lens) * U
-    G = min(grid, C)
+    # every CTA at least 4 stages of cost, unless the segments are more; never more than C
+    G = min(grid, min(C, max(len(units) * U, -(-C // 4))))
     starts = [-(-k * C // G) for k in range(G + 1)]  # ceil(k C / G)
 
     def owner(c):
@@ -356,8 +358,9 @@ def test_choose_partitions_matches_its_definition(lib):
         max_len = rng.choice([4096, 16384, 32768])
         sms = rng.choice([1, 7, 148, 152, 300])
         plan = lib.choose_partitions(lens, max_len, 4 * KV, KV, 128, 16, 1, torch.float16, sms=sms)
-        counts, G = _brute_force_split(lens, max_len, KV, 128, 1, min(sms, 1024))
-        assert plan.active == G and plan.grid == min(sms, 1024)
+        bound = B * KV * ((max_len + 1 + 127) // 128 + 1)  # pa_decode's launch: no idle CTAs
+        counts, G = _brute_force_split(lens, max_len, KV, 128, 1, min(sms, 1024, bound))
+        assert plan.active == G and plan.grid == min(sms, 1024, bound)
         assert plan.segments == len(counts)
         assert plan.pieces == sum(counts)
         assert plan.split_segments == sum(1 for n in counts if n > 1)
@@ -383,3 +386,16 @@ def test_failure_test_switches_are_off_by_default(lib):
     assert "int debug_withhold_stage;" in header
     names = [f[0] for f in lib.PaOpts._fields_]
     assert names[-2:] == ["wait_limit_ns", "debug_withhold_stage"]
+
+
+def test_host_register_rejects_memory_that_is_not_page_locked(lib):
+    """pa_host_register accepts only page-locked host memory (here: a plain
+    Python buffer, which is not), and unregistering an unknown pointer is an
+    error; nothing is enqueued either way."""
+    buf = ctypes.create_string_buffer(4096)
+    before = lib.kernel_launches()
+    assert lib.LIB.pa_host_register(ctypes.addressof(buf), 4096) == -9
+    assert lib.LIB.pa_host_register(None, 4096) == -1
+    assert lib.LIB.pa_host_unregister(ctypes.addressof(buf)) == -1
+    assert "page-locked" in lib.strerror(-9)
+    assert lib.kernel_launches() == before

@@ -288,3 +288,35 @@ def test_host_entry_point_pageable_buffers():
         outs.append(out.clone())
     assert torch.equal(outs[0], outs[1])
     pu.check(outs[0], pu.run_oracle(w), s.dtype, "f32", "pageable host buffers")
+
+
+@pytest.mark.parametrize("name", ["gqa_fp16", "ragged_fp16", "tiny_fp32"])
+def test_host_entry_point_registered_buffers(name):
+    """Registered pinned buffers (pa_host_register): the step's inputs are read
+    through their recorded device addresses and the output is written by the
+    kernels in place (no copy back); over two steps on one bound plan the
+    result equals pa_decode's bit for bit.  After unregistering, the same
+    buffers take the per-call path and give the same result."""
+    from paged_kv_cache_182_gb300 import binding
+
+    w = W.make(small(name), seed=25)
+    s = w.spec
+    plan = binding.HostPlan(w.k_cache.cuda(), w.v_cache.cuda(), B=s.B, H=s.H, NQ=s.NQ,
+                            max_blocks=int(w.block_table.shape[1]), scale=s.scale,
+                            causal=s.causal, partitions=0, out_dtype=torch.float32)
+    host = [t.clone().pin_memory() for t in (w.q, w.block_table, w.seq_lens, w.k_new, w.v_new)]
+    out = torch.full(w.q.shape, float("nan"), dtype=torch.float32).pin_memory()
+    plan.register(*host, out)
+    plan.bind(*host, out)
+    want = pu.run_gpu(w, partitions=0, out_dtype=torch.float32).cpu()
+    for step in range(2):
+        out.fill_(float("nan"))
+        plan.run_bound()
+        torch.cuda.synchronize()
+        assert torch.equal(out, want), f"{name} registered step {step}"
+    plan.close()
+    out.fill_(float("nan"))
+    plan.run(*host, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
+    pu.check(out, pu.run_oracle(w), s.dtype, "f32", f"{name} registered host buffers")
