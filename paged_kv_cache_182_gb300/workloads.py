@@ -250,3 +250,100 @@ def make_prefill(spec: Spec | str, seed: int = 0, lens=None) -> Workload:
     w.seq_lens = past.clone()
     w.meta["prefill"] = True
     return w
+
+
+# ---------------------------------------------------------------------------
+# Dense attention backward (VJP) inputs.
+#
+# Shapes follow onnxruntime-ep-mlx 0.31.1, src/ops/attention_vjp/dense.rs,
+# fn execute: q, y, g [B, HQ, SQ, D]; k, v [B, HK, SK, D]; an optional mask
+# of dims [MB, MH, MQ, W] that broadcasts against the scores [B, HQ, SQ, SK]
+# (MB in {1, B}, MH in {1, HQ}, MQ in {1, SQ}, W in {1..SK}).
+#
+# Recipe: a CPU torch.Generator seeded with ``seed`` draws q, k, v, y, g as
+# N(0,1) float32 (y scaled by 1/4, the size of a softmax average of unit
+# values), cast to the dtype; then the mask: boolean = Bernoulli(keep) as
+# uint8, additive = N(0,1) float32 with -inf where a Bernoulli(1 - keep) hits.
+# Tests that want y to be the true forward output compute it themselves.
+# ---------------------------------------------------------------------------
+
+
+@dataclass(frozen=True)
+class VjpSpec:
+    name: str
+    dtype: str  # "f32" | "f16" | "bf16"
+    B: int
+    HQ: int
+    HK: int
+    SQ: int
+    SK: int
+    D: int
+    causal: bool = False
+    mask_kind: int = 0  # 0 none, 1 boolean (uint8), 2 additive (float32)
+    mask_dims: tuple = (1, 1, 1, 1)
+    keep: float = 0.9
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+
+VJP_SPECS = {
+    # Llama-style grouped-query training shape: 4 sequences of 2048 tokens,
+    # 32 query heads on 8 key/value heads, causal.
+    "vjp_bf16": VjpSpec("vjp_bf16", "bf16", B=4, HQ=32, HK=8, SQ=2048, SK=2048, D=128,
+                        causal=True),
+}
+
+
+@dataclass
+class VjpInputs:
+    spec: VjpSpec
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    y: torch.Tensor
+    g: torch.Tensor
+    mask: torch.Tensor | None
+    seed: int = 0
+
+    def tensors(self):
+        return (self.q, self.k, self.v, self.y, self.g, self.mask)
+
+    def to(self, device) -> "VjpInputs":
+        moved = [None if t is None else t.to(device) for t in self.tensors()]
+        return VjpInputs(self.spec, *moved, seed=self.seed)
+
+
+def make_vjp(spec: VjpSpec | str, seed: int = 0) -> VjpInputs:
+    if isinstance(spec, str):
+        spec = VJP_SPECS[spec]
+    if spec.HQ % spec.HK != 0:
+        raise ValueError("HQ must be a multiple of HK")
+    g = torch.Generator().manual_seed(int(seed))
+    dt = DTYPES[spec.dtype]
+    q = _randn((spec.B, spec.HQ, spec.SQ, spec.D), g, 1.0, dt)
+    k = _randn((spec.B, spec.HK, spec.SK, spec.D), g, 1.0, dt)
+    v = _randn((spec.B, spec.HK, spec.SK, spec.D), g, 1.0, dt)
+    y = _randn((spec.B, spec.HQ, spec.SQ, spec.D), g, 0.25, dt)
+    grad = _randn((spec.B, spec.HQ, spec.SQ, spec.D), g, 1.0, dt)
+    mask = None
+    if spec.mask_kind == 1:
+        mask = (torch.rand(spec.mask_dims, generator=g) < spec.keep).to(torch.uint8)
+    elif spec.mask_kind == 2:
+        mask = torch.randn(spec.mask_dims, generator=g, dtype=torch.float32)
+        hit = torch.rand(spec.mask_dims, generator=g) >= spec.keep
+        mask = torch.where(hit, torch.full_like(mask, float("-inf")), mask)
+    return VjpInputs(spec, q, k, v, y, grad, mask, seed)
+
+
+def vjp_flops(spec: VjpSpec) -> int:
+    """Flops of the five products of the backward (scores, dv, dp, dq, dk),
+    2 * D each per visible (query row, key) pair: with the causal mask only
+    pairs ki <= qi count.  Other masks are not subtracted."""
+    if spec.causal:
+        n = min(spec.SQ, spec.SK)
+        pairs = n * (n + 1) // 2 + max(0, spec.SQ - spec.SK) * spec.SK
+    else:
+        pairs = spec.SQ * spec.SK
+    return 10 * spec.B * spec.HQ * spec.D * pairs
