@@ -35,6 +35,7 @@ Readings of points the page leaves open:
     as given (float).  A mask whose width exceeds sk is an error here (the
     page's addition would fail to broadcast).
   - scale must be positive: the page takes its square root.
+  - The maximum over no keys (sk = 0) is -inf, so such rows are empty.
 
 Pins (tests/test_oracle_vjp.py): torch float64 autograd of
 scaled_dot_product_attention, central finite differences of a loop-written
@@ -86,10 +87,10 @@ def probabilities(q, k, scale: float, causal: bool = False, mask=None, mask_kind
         qi = np.arange(sq).reshape(sq, 1)
         ki = np.arange(sk)
         scores = np.where(ki <= qi, scores, -np.inf)
-    maximum = np.max(scores, axis=-1, keepdims=True)
+    maximum = np.max(scores, axis=-1, keepdims=True, initial=-np.inf)
     empty = maximum == -np.inf
     safe = np.where(empty, 0.0, scores)
-    shifted = np.exp(safe - np.max(safe, axis=-1, keepdims=True))
+    shifted = np.exp(safe - np.max(safe, axis=-1, keepdims=True, initial=-np.inf))
     probability = shifted / np.sum(shifted, axis=-1, keepdims=True)
     return np.where(empty, 0.0, probability)
 
