@@ -14,8 +14,10 @@ Tensor layouts (row-major, contiguous):
 Entry points: ``decode`` / ``Plan`` (device tensors), ``decode_host`` /
 ``HostPlan`` (host tensors, device-resident caches), ``cache_append`` (new
 rows into their cache slots), ``decode_positions`` (a decode step with slot
-patching) and ``prefill`` / ``PrefillPlan`` (causal prefill of any number of
-new rows up to PA_MAX_PREFILL).
+patching), ``prefill`` / ``PrefillPlan`` (causal prefill of any number of
+new rows up to PA_MAX_PREFILL) and ``attention_vjp`` / ``VjpPlan`` (dense
+attention backward, ``include/pa_attention_vjp.h``: q, y, g [B, HQ, SQ, D],
+k, v [B, HK, SK, D]).
 """
 from __future__ import annotations
 
@@ -52,6 +54,21 @@ class PaOpts(ctypes.Structure):
         ("merge_kernel", ctypes.c_int),
         ("wait_limit_ns", ctypes.c_ulonglong),
         ("debug_withhold_stage", ctypes.c_int),
+    ]
+
+
+class VjpOpts(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("out_dtype", ctypes.c_int),
+        ("causal", ctypes.c_int),
+        ("mask_kind", ctypes.c_int),
+        ("mask_dims", ctypes.c_int * 4),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("status", ctypes.c_void_p),
+        ("kernel", ctypes.c_int),
+        ("wait_limit_ns", ctypes.c_ulonglong),
     ]
 
 
@@ -101,6 +118,11 @@ def load(path: Path = LIBRARY) -> ctypes.CDLL:
     lib.pa_host_unregister.argtypes = [P]
     lib.pa_choose_partitions.restype = I
     lib.pa_choose_partitions.argtypes = [P, I, I, I, I, I, I, I, I, I, ctypes.POINTER(SplitPlan)]
+    lib.pa_attention_vjp.restype = I
+    lib.pa_attention_vjp.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, I, I, I, I, I, I,
+                                     ctypes.POINTER(VjpOpts), P]
+    lib.pa_attention_vjp_workspace_bytes.restype = ctypes.c_size_t
+    lib.pa_attention_vjp_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.pa_cache_append.restype = I
     lib.pa_cache_append.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P]
     return lib
@@ -157,7 +179,7 @@ def new_workspace(B, H, KV, D, NQ, partitions=0, device="cuda"):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None or t.data_ptr() == 0 else ctypes.c_void_p(t.data_ptr())
 
 
 def _stream_handle(stream):
@@ -533,3 +555,91 @@ def cache_append(k_cache, v_cache, k_new, v_new, slot_mapping, *, status=None, s
             rc = LIB.pa_cache_append(*args, _stream_handle(stream))
     if rc != 0:
         raise PagedAttentionError(rc)
+
+
+PA_VJP_MASK_NONE, PA_VJP_MASK_BOOL, PA_VJP_MASK_ADD = 0, 1, 2
+
+
+def vjp_workspace_bytes(B: int, HQ: int, SQ: int, D: int, dtype=torch.bfloat16,
+                        out_dtype=None) -> int:
+    odt = -1 if out_dtype is None else _DT[out_dtype]
+    return int(LIB.pa_attention_vjp_workspace_bytes(B, HQ, SQ, D, _DT[dtype], odt))
+
+
+class VjpPlan:
+    """One prepared attention backward (pa_attention_vjp) on fixed device
+    tensors: q, y, g [B, HQ, SQ, D] and k, v [B, HK, SK, D] of one dtype, an
+    optional mask (uint8 = boolean, float32 = additive) of dims [MB, MH, MQ, W]
+    broadcasting against the scores [B, HQ, SQ, SK].  ``run()`` enqueues the
+    kernels and returns (dq, dk, dv); the outputs and the workspace are
+    allocated once, here (or given as ``out``)."""
+
+    def __init__(self, q, k, v, y, g, mask=None, *, scale: float, causal: bool = False,
+                 out_dtype=None, kernel: int = 0, status=None, wait_limit_ns: int = 0, out=None):
+        B, HQ, SQ, D = q.shape
+        b2, HK, SK, d2 = k.shape
+        dt = q.dtype
+        if dt not in _DT or any(t.dtype != dt for t in (k, v, y, g)):
+            raise TypeError("q, k, v, y, g must share one supported dtype")
+        if (b2 != B or d2 != D or tuple(v.shape) != tuple(k.shape) or tuple(y.shape) != tuple(q.shape)
+                or tuple(g.shape) != tuple(q.shape)):
+            raise ValueError("shapes: q, y, g [B, HQ, SQ, D]; k, v [B, HK, SK, D]")
+        for x in (q, k, v, y, g) + (() if mask is None else (mask,)):
+            if not (x.is_cuda and x.is_contiguous()):
+                raise ValueError("all tensors must be contiguous CUDA tensors")
+        o = VjpOpts()
+        o.dtype = _DT[dt]
+        odt = dt if out_dtype is None else out_dtype
+        o.out_dtype = -1 if out_dtype is None else _DT[out_dtype]
+        o.causal = int(bool(causal))
+        if mask is None:
+            o.mask_kind = PA_VJP_MASK_NONE
+        else:
+            if mask.dim() != 4:
+                raise ValueError("mask must have 4 dims [MB, MH, MQ, W]")
+            if mask.dtype == torch.uint8 or mask.dtype == torch.bool:
+                mask = mask.to(torch.uint8)
+                o.mask_kind = PA_VJP_MASK_BOOL
+            elif mask.dtype == torch.float32:
+                o.mask_kind = PA_VJP_MASK_ADD
+            else:
+                raise TypeError("mask must be uint8/bool (boolean) or float32 (additive)")
+            for e in range(4):
+                o.mask_dims[e] = int(mask.shape[e])
+        dev = q.device
+        if out is None:
+            out = tuple(torch.empty(t.shape, dtype=odt, device=dev) for t in (q, k, k))
+        self.dq, self.dk, self.dv = out
+        for t, ref in zip(out, (q, k, k)):
+            if t.dtype != odt or tuple(t.shape) != tuple(ref.shape) or not t.is_contiguous():
+                raise ValueError("out: dq like q, dk and dv like k, of the output dtype")
+        need = int(LIB.pa_attention_vjp_workspace_bytes(B, HQ, SQ, D, o.dtype, o.out_dtype))
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        o.workspace = _ptr(self.workspace)
+        o.workspace_bytes = int(self.workspace.numel())
+        o.status = _ptr(status)
+        o.kernel = int(kernel)
+        o.wait_limit_ns = int(wait_limit_ns)
+        self.opts = o
+        self._keep = (q, k, v, y, g, mask, status)
+        self.device = dev
+        self._args = (_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(g), _ptr(mask), _ptr(self.dq),
+                      _ptr(self.dk), _ptr(self.dv), ctypes.c_float(scale), B, HQ, HK, SQ, SK, D,
+                      ctypes.byref(self.opts))
+
+    def run(self, stream=None):
+        if torch.cuda.current_device() == self.device.index:
+            rc = LIB.pa_attention_vjp(*self._args, _stream_handle(stream))
+        else:
+            with torch.cuda.device(self.device):
+                rc = LIB.pa_attention_vjp(*self._args, _stream_handle(stream))
+        if rc != 0:
+            raise PagedAttentionError(rc)
+        return self.dq, self.dk, self.dv
+
+
+def attention_vjp(q, k, v, y, g, mask=None, *, scale: float, causal: bool = False,
+                  out_dtype=None, kernel: int = 0, status=None, stream=None, out=None):
+    """dq, dk, dv of attention (pa_attention_vjp): see ``VjpPlan``."""
+    return VjpPlan(q, k, v, y, g, mask, scale=scale, causal=causal, out_dtype=out_dtype,
+                   kernel=kernel, status=status, out=out).run(stream)

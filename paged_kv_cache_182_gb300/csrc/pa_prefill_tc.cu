@@ -45,9 +45,12 @@
 #include "pa_common.cuh"
 #include "pa_decode.h"
 #include "pa_ptx.cuh"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace {
+
+using namespace tc;
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kTcD = 128;           // head size of this path
@@ -68,184 +71,6 @@ struct PrefillTcParams {
     float qscale;             // scale * log2(e)
     int B, H, KV, NQ, BLOCK, maxb, num_blocks, g, T, tiles;  // tiles: row tiles per (b, kh)
 };
-
-// Shared-memory matrix descriptor of a 128-byte-swizzled operand (tcgen05
-// format: start address, leading and stride byte offsets in 16-byte units,
-// descriptor version 1, swizzle mode 2 = 128 bytes).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((addr & 0x3FFFF) >> 4);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile of
-// 128-byte rows (eight-row atoms of 1024 bytes).
-__device__ __forceinline__ uint32_t sw128(int r, int c)
-{
-    return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-}
-
-// Instruction descriptor of kind::f16 with float32 accumulation, M = 128:
-// A and B both bf16 (or both f16), A K-major, B K-major or MN-major.
-template <bool kBf>
-__device__ __forceinline__ uint32_t idesc(int n, bool b_mn_major)
-{
-    const uint32_t t = kBf ? 1u : 0u;
-    return (1u << 4) | (t << 7) | (t << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
-           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kTcTile >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 columns of this warp's 32 tensor-memory lanes; the wait takes the
-// registers as operands, so that no use of them is scheduled before it.
-struct Cols32 {
-    uint32_t r[32];
-};
-__device__ __forceinline__ void tmem_ld32(Cols32& c, uint32_t taddr)
-{
-    uint32_t* r = c.r;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                   "+r"(r[30]), "+r"(r[31])::"memory");
-}
-
-__device__ __forceinline__ void tmem_st32(const Cols32& c, uint32_t taddr)
-{
-    const uint32_t* r = c.r;
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            int c3, int c4, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Barrier of the 64 threads of two warps (named barrier `id`) that also returns
-// the OR of `v` over them, so that both warps take the same decision after it.
-__device__ __forceinline__ bool pair_bar_or(int id, bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, 64, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(id)
-        : "memory");
-    return r != 0;
-}
-
-// Two floats as a 16-bit pair rounded to nearest (high part) and the pair of
-// what remains (x - high), also rounded: together about 22 bits of x.
-template <typename T>
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo)
-{
-    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        const float2 hf = __bfloat1622float2(h);
-        const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-        hi = *reinterpret_cast<const uint32_t*>(&h);
-        lo = *reinterpret_cast<const uint32_t*>(&l);
-    } else {
-        const __half2 h = __floats2half2_rn(a, b);
-        const float2 hf = __half22float2(h);
-        const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-        hi = *reinterpret_cast<const uint32_t*>(&h);
-        lo = *reinterpret_cast<const uint32_t*>(&l);
-    }
-}
-
-template <typename TO>
-__device__ __forceinline__ void store_row(TO* dst, const float* v);  // 32 values
-template <>
-__device__ __forceinline__ void store_row<float>(float* dst, const float* v)
-{
-#pragma unroll
-    for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-}
-template <>
-__device__ __forceinline__ void store_row<__half>(__half* dst, const float* v)
-{
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const __half2 h = __floats2half2_rn(v[j + 2 * k], v[j + 2 * k + 1]);
-            w[k] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(dst + j) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-template <>
-__device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, const float* v)
-{
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(v[j + 2 * k], v[j + 2 * k + 1]);
-            w[k] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(dst + j) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
 
 struct TcBars {
     uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, o_done;
@@ -619,20 +444,6 @@ PrefillTcFn pick_prefill_tc(int dtype, bool f32_out)
         return f32_out ? pa_prefill_tc_kernel<__nv_bfloat16, float>
                        : pa_prefill_tc_kernel<__nv_bfloat16, __nv_bfloat16>;
     return f32_out ? pa_prefill_tc_kernel<__half, float> : pa_prefill_tc_kernel<__half, __half>;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tc_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            ptr = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }();
-    return fn;
 }
 
 }  // namespace

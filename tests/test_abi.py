@@ -399,3 +399,69 @@ def test_host_register_rejects_memory_that_is_not_page_locked(lib):
     assert lib.LIB.pa_host_unregister(ctypes.addressof(buf)) == -1
     assert "page-locked" in lib.strerror(-9)
     assert lib.kernel_launches() == before
+
+
+def test_vjp_rejects_before_launching(lib):
+    """pa_attention_vjp checks every argument before its first launch (these
+    calls run without a GPU)."""
+    f = lib.LIB.pa_attention_vjp
+    ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+    names = ("q", "k", "v", "y", "g", "mask", "dq", "dk", "dv")
+
+    def go(opts, B=2, HQ=8, HK=2, SQ=64, SK=80, D=128, scale=0.1, **kw):
+        a = dict(zip(names, ptrs))
+        a.update(kw)
+        return f(*(a[n] for n in names), ctypes.c_float(scale), B, HQ, HK, SQ, SK, D, opts, None)
+
+    def opts(**kw):
+        o = dict(dtype=lib.PA_BF16, out_dtype=-1, causal=0, mask_kind=0, workspace=None,
+                 workspace_bytes=0, status=None, kernel=0, wait_limit_ns=0)
+        dims = kw.pop("mask_dims", (1, 1, 1, 1))
+        o.update(kw)
+        s = lib.VjpOpts(**o)
+        for e in range(4):
+            s.mask_dims[e] = dims[e]
+        return ctypes.byref(s)
+
+    need = lib.LIB.pa_attention_vjp_workspace_bytes(2, 8, 64, 128, lib.PA_BF16, -1)
+    ok = dict(workspace=0x100000, workspace_bytes=need)
+    launches = lib.kernel_launches()
+    assert go(None) == -1
+    assert go(opts(**ok), q=None) == -1
+    assert go(opts(**ok), dv=None) == -1
+    assert go(opts(**ok, mask_kind=1, mask_dims=(1, 1, 1, 80)), mask=None) == -1
+    assert go(opts(**ok), HQ=6, HK=4) == -2
+    assert go(opts(**ok), HK=0) == -2
+    assert go(opts(**ok), SQ=-1) == -2
+    assert go(opts(**ok), scale=0.0) == -2
+    assert go(opts(**ok), scale=-0.5) == -2
+    assert go(opts(**ok), scale=math.inf) == -2
+    assert go(opts(**ok, mask_kind=3)) == -2
+    assert go(opts(**ok, mask_kind=1, mask_dims=(3, 1, 1, 80))) == -2   # MB not 1 or B
+    assert go(opts(**ok, mask_kind=1, mask_dims=(1, 4, 1, 80))) == -2   # MH not 1 or HQ
+    assert go(opts(**ok, mask_kind=1, mask_dims=(1, 1, 63, 80))) == -2  # MQ not 1 or SQ
+    assert go(opts(**ok, mask_kind=2, mask_dims=(2, 8, 64, 81))) == -2  # wider than SK
+    assert go(opts(**ok, mask_kind=2, mask_dims=(2, 8, 64, 0))) == -2
+    assert go(opts(**ok), D=257) == -3
+    assert go(opts(**ok, dtype=7)) == -3
+    assert go(opts(**ok, out_dtype=lib.PA_F16)) == -3  # bf16 inputs, f16 outputs
+    assert go(opts(**ok), B=70000, SQ=1, SK=1, D=8, HQ=2, HK=1) == -3
+    assert go(opts(**ok), k=ctypes.c_void_p(0x20008)) == -4
+    assert go(opts(workspace=0x100010, workspace_bytes=need)) == -4
+    assert go(opts()) == -1  # no workspace
+    assert go(opts(workspace=0x100000, workspace_bytes=need - 1)) == -5
+    assert go(opts(**ok), B=0) == 0
+    assert go(opts(**ok), SQ=0, SK=0) == 0
+    assert lib.kernel_launches() == launches
+
+
+def test_vjp_workspace_bytes(lib):
+    wb = lib.LIB.pa_attention_vjp_workspace_bytes
+    rows = 2 * 8 * 128  # B * HQ * SQ rounded up to 128 rows
+    assert wb(2, 8, 100, 64, lib.PA_F32, -1) == 2 * rows * 4  # lse2 and delta only
+    assert wb(2, 8, 100, 64, lib.PA_BF16, lib.PA_F32) == 2 * rows * 4
+    acc = -(-2 * 8 * 100 * 64 * 4 // 256) * 256
+    assert wb(2, 8, 100, 64, lib.PA_BF16, -1) == 2 * rows * 4 + acc  # + float32 dq accumulator
+    assert wb(2, 8, 100, 64, 9, -1) == 0
+    assert wb(2, 8, 100, 64, lib.PA_BF16, lib.PA_F16) == 0
+    assert wb(-1, 8, 100, 64, lib.PA_BF16, -1) == 0
