@@ -443,7 +443,7 @@ extern "C" int pa_attention_vjp(const void* q, const void* k, const void* v, con
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint64_t launches = 0;
     int rc;
-    if (o.kernel != 1 && vjp_tc_supported(o.dtype, D, HQ / HK))
+    if (o.kernel != 1 && vjp_tc_supported(o.dtype, D, HQ / HK, o.mask_kind))
         rc = launch_vjp_tc(p, o.dtype, odt == PA_F32, st, &launches);
     else
         rc = pick_simt(o.dtype, odt == PA_F32)(p, st, &launches);

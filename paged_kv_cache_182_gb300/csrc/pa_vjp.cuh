@@ -61,7 +61,7 @@ __device__ __forceinline__ float vjp_bias(const VjpParams& p, int b, int h, int 
 // Tensor-core path (pa_vjp_tc.cu): whether these sizes take it, and its
 // launches (row statistics and the backward; dq rounding is left to the
 // caller).  Returns PA_OK or a PA_ERR_* code.
-bool vjp_tc_supported(int dtype, int D, int groups);
+bool vjp_tc_supported(int dtype, int D, int groups, int mask_kind);
 int launch_vjp_tc(const VjpParams& p, int dtype, bool f32_out, cudaStream_t st, uint64_t* launches);
 
 // Adds to the library's count of kernel launches (pa_kernel_launches).

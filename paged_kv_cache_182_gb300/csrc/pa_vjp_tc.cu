@@ -1,12 +1,708 @@
-// pa_vjp_tc.cu -- tcgen05 kernels of the attention backward (placeholder
-// until they land: every size takes the CUDA-core kernels).
+// pa_vjp_tc.cu -- the attention backward on the sm_103a tensor cores
+// (tcgen05 MMAs from shared-memory descriptors, accumulators in tensor
+// memory, operands staged by TMA), for 16-bit inputs with D = 128 and no
+// mask beyond the causal rule.
+//
+// Operation: onnxruntime-ep-mlx 0.31.1, src/ops/attention_vjp/dense.rs,
+// fn execute (p, dv = p^T g, dp = g v^T, delta = rowsum(y g),
+// ds = p (dp - delta), dq = scale ds k, dk = scale ds^T q, the group sums of
+// dk and dv, causal ki <= qi, p = 0 on rows with no visible key).
+//
+// Two kernels:
+//
+// vjp_stats_tc -- one CTA per (batch, query head, 128 query rows):
+//   S = Q K^T per 128-key tile (M 128 rows, N 128 keys, K = D; both operands
+//   K-major), double-buffered in tensor memory; two threads a row (64 key
+//   columns each) keep a running maximum and sum in base 2 over all tiles
+//   and merge them at the end: lse2 = max + log2(sum), +inf for a row that
+//   sees no key.  The same threads compute delta = rowsum(y g) and zero the
+//   float32 dq accumulator rows.  Warp 8 loads Q once and K tiles into a
+//   two-stage ring; warp 9 issues the MMAs.
+//
+// vjp_main_tc -- one CTA per (batch, key/value head, 128 keys): K and V of
+//   the tile stay in shared memory; dK and dV accumulate in tensor memory
+//   over every 64-row tile of every query head of the group.  Per row tile:
+//     S^T  = K Q^T          M 128 keys, N 64 rows, K = D      (both K-major)
+//     dP^T = V dO^T         same shapes
+//     softmax threads: P^T = exp2(s2 - lse2), dS^T = P^T (dP^T - delta) scale,
+//                      both written as 16-bit K-major operands
+//     dV  += P^T dO         M 128 keys, N = D, K 64 rows      (dO MN-major)
+//     dK  += dS^T Q         same, Q MN-major
+//     dQ^T = K^T dS^T       M = D, N 64 rows, K 128 keys      (both MN-major)
+//   and the softmax threads add dQ^T into the float32 accumulator (one
+//   reduction per element, coalesced over D).  Warp 8 loads K, V once and
+//   Q, dO, lse2, delta per row tile into a two-stage ring; warp 9 issues the
+//   MMAs (one thread).  Tensor memory (512 columns): dK | dV | S^T | dP^T |
+//   dQ^T.
+//
+// Every wait is bounded (p.wait_ns); a wait that gives up ORs
+// PA_STATUS_TIMEOUT into p.status, and every path frees the tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
 #include "pa_decode.h"
+#include "pa_ptx.cuh"
+#include "pa_tc.cuh"
 #include "pa_vjp.cuh"
 
 namespace pa {
+namespace {
 
-bool vjp_tc_supported(int, int, int) { return false; }
+using namespace tc;
 
-int launch_vjp_tc(const VjpParams&, int, bool, cudaStream_t, uint64_t*) { return PA_ERR_UNSUPPORTED; }
+constexpr unsigned kAll = 0xffffffffu;
+constexpr int kD = 128;         // head size of this path
+constexpr int kKeys = 128;      // keys per tile (both kernels)
+constexpr int kSRows = 128;     // query rows per CTA of the statistics kernel
+constexpr int kRows = 64;       // query rows per step of the backward kernel
+constexpr int kThreads = 320;   // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kSoftmax = 256;
+constexpr int kHalf128 = 16384;  // one 64-column half of a 128-row tile, bytes
+constexpr int kHalf64 = 8192;    // one 64-column half of a 64-row tile, bytes
+
+struct StatsBars {
+    uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_free[2];
+    uint32_t tmem;
+    int abort;
+    float xm[kSRows], xl[kSRows], xd[kSRows];  // the high-half thread's max, sum, delta part
+};
+// Q (2 halves), K ring (2 stages x 2 halves), then the barriers
+constexpr int kStatsSmem = 6 * kHalf128 + 2048;
+static_assert(sizeof(StatsBars) <= 2048, "statistics barrier area");
+
+struct MainBars {
+    uint64_t kv_full, qd_full[2], qd_empty[2], sd_full, ds_ready, dq_full, dq_free;
+    uint32_t tmem;
+    int abort;
+};
+// K, V (2 halves each), Q and dO rings (2 stages x 2 halves of 64 rows), P^T,
+// dS^T (one 16 KB block each), row statistics (2 stages x 512 bytes), barriers
+constexpr int kMainSmem = 4 * kHalf128 + 8 * kHalf64 + 2 * kHalf128 + 1024 + 1024;
+
+__device__ __forceinline__ void red_add(float* addr, float v)
+{
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w)
+{
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+    else
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// ---------------------------------------------------------------------------
+// Row statistics.  grid = B * HQ * ceil(SQ / 128), the row tiles that see the
+// most keys (causal) first.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    vjp_stats_tc(const __grid_constant__ VjpParams p, const __grid_constant__ CUtensorMap qmap,
+                 const __grid_constant__ CUtensorMap kmap)
+{
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+        if (threadIdx.x == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+        return;
+    }
+    unsigned char* sQ = smem_raw;
+    unsigned char* sK = smem_raw + 2 * kHalf128;
+    StatsBars& bars = *reinterpret_cast<StatsBars*>(smem_raw + 6 * kHalf128);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles = (p.SQ + kSRows - 1) / kSRows;
+    const int rt = tiles - 1 - static_cast<int>(blockIdx.x % tiles);
+    const int h = (blockIdx.x / tiles) % p.HQ;
+    const int b = blockIdx.x / (tiles * p.HQ);
+    const int kh = h / p.groups;
+    const int i0 = rt * kSRows;
+    const int nk = p.causal ? min(p.SK, i0 + kSRows) : p.SK;
+    const int ntiles = (nk + kKeys - 1) / kKeys;
+    const uint64_t wait_ns = p.wait_ns;
+
+    if (tid == 0) {
+        mbar_init(&bars.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.s_full[s], 1);
+            mbar_init(&bars.s_free[s], kSoftmax);
+        }
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars.tmem)),
+                     "r"(256)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = bars.tmem;  // S(t) at tS + 128 (t & 1)
+    volatile int* abort_flag = &bars.abort;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.status)
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+    };
+
+    if (warp == 8) {
+        // --------------------------------------------------------------- TMA
+        if (lane == 0 && ntiles > 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf128);
+            for (int hh = 0; hh < 2; ++hh)
+                tma_load_4d(sQ + hh * kHalf128, &qmap, 0, hh, i0, b * p.HQ + h, &bars.q_full);
+            int issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t & 1;
+                if (t >= 2 && (*abort_flag || !mbar_wait_bounded(&bars.k_empty[s], ((t >> 1) - 1) & 1, wait_ns))) {
+                    fail();
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars.k_full[s], 2 * kHalf128);
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load_4d(sK + s * 2 * kHalf128 + hh * kHalf128, &kmap, 0, hh, t * kKeys, b * p.HK + kh,
+                                &bars.k_full[s]);
+                issued = t + 1;
+            }
+            // no copy may land after the CTA's memory is released
+            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
+                mbar_wait_bounded(&bars.k_full[t & 1], (t >> 1) & 1, wait_ns);
+            mbar_wait_bounded(&bars.q_full, 0, wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // --------------------------------------------------------------- MMA
+        if (lane == 0 && ntiles > 0) {
+            bool ok = mbar_wait_bounded(&bars.q_full, 0, wait_ns);
+            const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK);
+            const uint32_t id = idesc<kBf>(kKeys, false);
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t & 1;
+                ok = !*abort_flag && mbar_wait_bounded(&bars.k_full[s], (t >> 1) & 1, wait_ns);
+                if (ok && t >= 2)
+                    ok = mbar_wait_bounded(&bars.s_free[s], ((t >> 1) - 1) & 1, wait_ns);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t o = (ks >> 2) * kHalf128 + (ks & 3) * 32;
+                    umma(tS + s * kKeys, smem_desc(qa + o, 16, 1024),
+                         smem_desc(ka + s * 2 * kHalf128 + o, 16, 1024), id, ks > 0);
+                }
+                umma_commit(&bars.s_full[s]);
+                umma_commit(&bars.k_empty[s]);
+            }
+            if (!ok)
+                fail();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------ statistics (two threads a row)
+        const int row = (warp & 3) * 32 + lane;
+        const int part = warp >> 2;  // key columns [64 part, 64 part + 64), d columns likewise
+        const int i = i0 + row;
+        const bool real = i < p.SQ;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        // delta share and the accumulator rows (while the first tiles load)
+        float dpart = 0.f;
+        if (real) {
+            const int64_t r = (static_cast<int64_t>(b) * p.HQ + h) * p.SQ + i;
+            const uint4* y = reinterpret_cast<const uint4*>(static_cast<const T*>(p.y) + r * kD + part * 64);
+            const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.g) + r * kD + part * 64);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 yv = y[c], gv = g[c];
+                const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 a = unpack2<T>(ya[e]), bb = unpack2<T>(ga[e]);
+                    dpart = fmaf(a.x, bb.x, dpart);
+                    dpart = fmaf(a.y, bb.y, dpart);
+                }
+            }
+            float4* acc = reinterpret_cast<float4*>(p.dq_sum + r * kD + part * 64);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float m = -INFINITY, l = 0.f;
+        bool fault = false;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t & 1;
+            const bool got =
+                __all_sync(kAll, !fault && !*abort_flag && mbar_wait_bounded(&bars.s_full[s], (t >> 1) & 1, wait_ns));
+            if (!got) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+            float sc[64];
+            float pm = -INFINITY;
+            const int kbase = t * kKeys + part * 64;
+            const bool edge = kbase + 63 >= nk || (p.causal && kbase + 63 > i0);  // warp-uniform
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                Cols32 x;
+                tmem_ld32(x, tS + s * kKeys + lane_off + part * 64 + c * 32);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float v = __uint_as_float(x.r[j]) * p.scale_log2;
+                    if (edge) {
+                        const int key = kbase + c * 32 + j;
+                        if (key >= p.SK || (p.causal && key > i))
+                            v = -INFINITY;
+                    }
+                    sc[c * 32 + j] = v;
+                    pm = fmaxf(pm, v);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.s_free[s]);
+            const float mt = fmaxf(m, pm);
+            if (mt != -INFINITY) {
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    sum += fast_exp2(sc[j] - mt);
+                l = l * fast_exp2(m - mt) + sum;
+                m = mt;
+            }
+        }
+        // merge the two halves of every row
+        if (part == 1) {
+            bars.xm[row] = m;
+            bars.xl[row] = l;
+            bars.xd[row] = dpart;
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+        if (fault) {
+            if (lane == 0)
+                fail();
+        } else if (part == 0) {
+            const float m1 = bars.xm[row], l1 = bars.xl[row];
+            const float mt = fmaxf(m, m1);
+            const int64_t srow = (static_cast<int64_t>(b) * p.HQ + h) * p.sqp + i;
+            if (!real) {  // padding rows up to sqp: no key, no gradient
+                p.lse[srow] = INFINITY;
+                p.delta[srow] = 0.f;
+            } else if (mt == -INFINITY) {
+                p.lse[srow] = INFINITY;
+            } else {
+                const float lt = l * exp2f(m - mt) + l1 * exp2f(m1 - mt);
+                p.lse[srow] = mt + log2f(lt);
+            }
+            if (real)
+                p.delta[srow] = dpart + bars.xd[row];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(bars.tmem), "r"(256) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Backward.  grid = ceil(SK / 128) * B * HK, key tile fastest-varying last:
+// the key tiles that the most (causal) rows see are launched first.
+template <typename T, typename TO>
+__global__ void __launch_bounds__(kThreads, 1)
+    vjp_main_tc(const __grid_constant__ VjpParams p, const __grid_constant__ CUtensorMap qmap,
+                const __grid_constant__ CUtensorMap gmap, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap)
+{
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+        if (threadIdx.x == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+        return;
+    }
+    unsigned char* sK = smem_raw;                         // 2 halves of 16 KB
+    unsigned char* sV = sK + 2 * kHalf128;                // 2 halves
+    unsigned char* sQ = sV + 2 * kHalf128;                // 2 stages x 2 halves of 8 KB
+    unsigned char* sG = sQ + 4 * kHalf64;                 // 2 stages x 2 halves
+    unsigned char* sP = sG + 4 * kHalf64;                 // P^T: 128 keys x 64 rows
+    unsigned char* sS = sP + kHalf128;                    // dS^T
+    float* sStat = reinterpret_cast<float*>(sS + kHalf128);  // 2 stages x (64 lse2, 64 delta)
+    MainBars& bars = *reinterpret_cast<MainBars*>(sS + kHalf128 + 1024);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int BH = p.B * p.HK;
+    const int kt = blockIdx.x / BH;
+    const int b = (blockIdx.x % BH) / p.HK;
+    const int kh = blockIdx.x % p.HK;
+    const int k0 = kt * kKeys;
+    const int nrt = (p.SQ + kRows - 1) / kRows;
+    const int r_first = p.causal ? min(k0 / kRows, nrt) : 0;
+    const int per_head = nrt - r_first;
+    const int n = per_head * p.groups;
+    const uint64_t wait_ns = p.wait_ns;
+
+    if (tid == 0) {
+        mbar_init(&bars.kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.qd_full[s], 1);
+            mbar_init(&bars.qd_empty[s], 1);
+        }
+        mbar_init(&bars.sd_full, 1);
+        mbar_init(&bars.ds_ready, kSoftmax);
+        mbar_init(&bars.dq_full, 1);
+        mbar_init(&bars.dq_free, kSoftmax);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars.tmem)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tdK = bars.tmem, tdV = bars.tmem + 128, tS = bars.tmem + 256, tP = bars.tmem + 320,
+                   tQ = bars.tmem + 384;
+    volatile int* abort_flag = &bars.abort;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.status)
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+    };
+    auto step_head = [&](int it, int& h, int& i0) {
+        const int gi = it / per_head;
+        h = kh * p.groups + gi;
+        i0 = (r_first + it - gi * per_head) * kRows;
+    };
+
+    if (warp == 8) {
+        // --------------------------------------------------------------- TMA
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&gmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            mbar_arrive_expect_tx(&bars.kv_full, 4 * kHalf128);
+            for (int hh = 0; hh < 2; ++hh) {
+                tma_load_4d(sK + hh * kHalf128, &kmap, 0, hh, k0, b * p.HK + kh, &bars.kv_full);
+                tma_load_4d(sV + hh * kHalf128, &vmap, 0, hh, k0, b * p.HK + kh, &bars.kv_full);
+            }
+            int issued = 0;
+            for (int it = 0; it < n; ++it) {
+                const int st = it & 1;
+                if (it >= 2 &&
+                    (*abort_flag || !mbar_wait_bounded(&bars.qd_empty[st], ((it >> 1) - 1) & 1, wait_ns))) {
+                    fail();
+                    break;
+                }
+                int h, i0;
+                step_head(it, h, i0);
+                mbar_arrive_expect_tx(&bars.qd_full[st], 4 * kHalf64 + 512);
+                for (int hh = 0; hh < 2; ++hh) {
+                    tma_load_4d(sQ + st * 2 * kHalf64 + hh * kHalf64, &qmap, 0, hh, i0, b * p.HQ + h,
+                                &bars.qd_full[st]);
+                    tma_load_4d(sG + st * 2 * kHalf64 + hh * kHalf64, &gmap, 0, hh, i0, b * p.HQ + h,
+                                &bars.qd_full[st]);
+                }
+                const int64_t srow = (static_cast<int64_t>(b) * p.HQ + h) * p.sqp + i0;
+                bulk_load(sStat + st * 128, p.lse + srow, 256, &bars.qd_full[st]);
+                bulk_load(sStat + st * 128 + 64, p.delta + srow, 256, &bars.qd_full[st]);
+                issued = it + 1;
+            }
+            for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
+                mbar_wait_bounded(&bars.qd_full[it & 1], (it >> 1) & 1, wait_ns);
+            mbar_wait_bounded(&bars.kv_full, 0, wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // --------------------------------------------------------------- MMA
+        if (lane == 0 && n > 0) {
+            const uint32_t ka = smem_u32(sK), va = smem_u32(sV), qa = smem_u32(sQ), ga = smem_u32(sG);
+            const uint32_t pa = smem_u32(sP), sa = smem_u32(sS);
+            const uint32_t id_s = idesc<kBf>(kRows, false);        // N 64, both K-major
+            const uint32_t id_o = idesc<kBf>(kD, true);            // N 128, B MN-major
+            const uint32_t id_q = idesc<kBf>(kRows, true, true);   // N 64, A and B MN-major
+            bool ok = mbar_wait_bounded(&bars.kv_full, 0, wait_ns);
+            for (int it = 0; it < n && ok; ++it) {
+                const int st = it & 1;
+                ok = !*abort_flag && mbar_wait_bounded(&bars.qd_full[st], (it >> 1) & 1, wait_ns);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t q_st = qa + st * 2 * kHalf64, g_st = ga + st * 2 * kHalf64;
+                // S^T = K Q^T and dP^T = V dO^T over the head dimension
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t ok128 = (ks >> 2) * kHalf128 + (ks & 3) * 32;
+                    const uint32_t ok64 = (ks >> 2) * kHalf64 + (ks & 3) * 32;
+                    umma(tS, smem_desc(ka + ok128, 16, 1024), smem_desc(q_st + ok64, 16, 1024), id_s, ks > 0);
+                    umma(tP, smem_desc(va + ok128, 16, 1024), smem_desc(g_st + ok64, 16, 1024), id_s, ks > 0);
+                }
+                umma_commit(&bars.sd_full);
+                ok = mbar_wait_bounded(&bars.ds_ready, it & 1, wait_ns);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                // dV += P^T dO, dK += dS^T Q over the step's 64 rows (dO and Q
+                // MN-major: rows are the reduction, 64 columns of D per half)
+                for (int ks = 0; ks < kRows / 16; ++ks) {
+                    const uint32_t acc = it > 0 || ks > 0;
+                    umma(tdV, smem_desc(pa + ks * 32, 16, 1024), smem_desc(g_st + ks * 2048, kHalf64, 1024), id_o,
+                         acc);
+                    umma(tdK, smem_desc(sa + ks * 32, 16, 1024), smem_desc(q_st + ks * 2048, kHalf64, 1024), id_o,
+                         acc);
+                }
+                if (it > 0) {
+                    ok = mbar_wait_bounded(&bars.dq_free, (it - 1) & 1, wait_ns);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                }
+                // dQ^T = K^T dS^T over the tile's 128 keys (K as an MN-major A:
+                // D is its row dimension, in two 64-wide halves 16 KB apart)
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    umma(tQ, smem_desc(ka + ks * 2048, kHalf128, 1024), smem_desc(sa + ks * 2048, 1024, 1024),
+                         id_q, ks > 0);  // dS^T: N = 64 is one swizzle span, its LBO is not used
+                umma_commit(&bars.dq_full);
+                umma_commit(&bars.qd_empty[st]);
+            }
+            if (!ok)
+                fail();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- softmax and dQ reduction
+        // tensor-memory lane = key (S^T, dP^T, dK, dV) or d (dQ^T); this
+        // thread takes columns [32 part, 32 part + 32) of the 64-wide blocks
+        const int ln = (warp & 3) * 32 + lane;
+        const int part = warp >> 2;
+        const int key = k0 + ln;
+        const bool key_ok = key < p.SK;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        bool fault = false;
+        for (int it = 0; it < n; ++it) {
+            const int st = it & 1;
+            int h, i0;
+            step_head(it, h, i0);
+            bool got = !fault && !*abort_flag && mbar_wait_bounded(&bars.sd_full, it & 1, wait_ns);
+            got = got && mbar_wait_bounded(&bars.qd_full[st], (it >> 1) & 1, wait_ns);
+            if (!__all_sync(kAll, got)) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+            const float* lse = sStat + st * 128 + part * 32;
+            const float* dlt = sStat + st * 128 + 64 + part * 32;
+            const int rb = i0 + part * 32;  // first row of this thread's columns
+            float pv[32];
+            {
+                Cols32 x;
+                tmem_ld32(x, tS + lane_off + part * 32);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int row = rb + j;
+                    const bool vis = key_ok && row < p.SQ && (!p.causal || key <= row);
+                    pv[j] = vis ? fast_exp2(__uint_as_float(x.r[j]) * p.scale_log2 - lse[j]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
+                *reinterpret_cast<uint4*>(sP + sw128(ln, part * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            {
+                Cols32 x;
+                tmem_ld32(x, tP + lane_off + part * 32);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)  // (rows past SQ: p = 0 and their delta is not read)
+                    pv[j] = pv[j] != 0.f ? pv[j] * (__uint_as_float(x.r[j]) - dlt[j]) * p.scale : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
+                *reinterpret_cast<uint4*>(sS + sw128(ln, part * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars.ds_ready);
+            // dQ^T: lane = d, columns = the rows of this step
+            got = __all_sync(kAll, mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
+            if (!got) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+            {
+                Cols32 x;
+                tmem_ld32(x, tQ + lane_off + part * 32);
+                float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + rb) * kD + ln;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (rb + j < p.SQ)
+                        red_add(dst + static_cast<int64_t>(j) * kD, __uint_as_float(x.r[j]));
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.dq_free);
+        }
+        if (fault) {
+            if (lane == 0)
+                fail();
+        } else {
+            // dK and dV of this thread's key: columns [64 part, 64 part + 64)
+            // (the tensor-memory loads are warp-wide; only the stores depend on the key)
+            TO* dk = static_cast<TO*>(p.dk) + ((static_cast<int64_t>(b) * p.HK + kh) * p.SK + key) * kD + part * 64;
+            TO* dv = static_cast<TO*>(p.dv) + ((static_cast<int64_t>(b) * p.HK + kh) * p.SK + key) * kD + part * 64;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                if (n > 0) {
+                    Cols32 x;
+                    tmem_ld32(x, tdK + lane_off + part * 64 + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __uint_as_float(x.r[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = 0.f;
+                }
+                if (key_ok)
+                    store_row<TO>(dk + c * 32, v);
+                if (n > 0) {
+                    Cols32 x;
+                    tmem_ld32(x, tdV + lane_off + part * 64 + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __uint_as_float(x.r[j]);
+                }
+                if (key_ok)
+                    store_row<TO>(dv + c * 32, v);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(bars.tmem), "r"(512) : "memory");
+}
+
+using StatsFn = void (*)(VjpParams, CUtensorMap, CUtensorMap);
+using MainFn = void (*)(VjpParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap);
+
+// [B * heads][rows][128] 16-bit as {64, 2, rows, B * heads}; box {64, 1, box_rows, 1}:
+// one 64-column half of box_rows rows of one head
+int encode_rows(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int rows, int heads, int box_rows)
+{
+    auto enc = tc_encoder();
+    if (!enc)
+        return PA_ERR_DRIVER;
+    cuuint64_t dims[4] = {64u, 2u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+    cuuint64_t str[3] = {128u, kD * 2u, static_cast<cuuint64_t>(rows) * kD * 2};
+    cuuint32_t box[4] = {64u, 1u, static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+    return enc(map, dt, 4, const_cast<void*>(base), dims, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+                   CUDA_SUCCESS
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool vjp_tc_supported(int dtype, int D, int groups, int mask_kind)
+{
+    return (dtype == PA_F16 || dtype == PA_BF16) && D == kD && groups >= 1 && mask_kind == 0;
+}
+
+int launch_vjp_tc(const VjpParams& p, int dtype, bool f32_out, cudaStream_t st, uint64_t* launches)
+{
+    const CUtensorMapDataType dt =
+        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const bool bf = dtype == PA_BF16;
+    if (p.SQ > 0) {
+        CUtensorMap qmap, kmap;
+        int rc = encode_rows(&qmap, p.q, dt, p.SQ, p.B * p.HQ, kSRows);
+        if (rc == PA_OK && p.SK > 0)
+            rc = encode_rows(&kmap, p.k, dt, p.SK, p.B * p.HK, kKeys);
+        else
+            kmap = qmap;  // no key tile is ever loaded
+        if (rc != PA_OK)
+            return rc;
+        const StatsFn fn = bf ? vjp_stats_tc<__nv_bfloat16> : vjp_stats_tc<__half>;
+        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStatsSmem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        const long long grid = static_cast<long long>(p.B) * p.HQ * ((p.SQ + kSRows - 1) / kSRows);
+        if (grid >= (1ll << 31))
+            return PA_ERR_BAD_DIMS;
+        fn<<<static_cast<unsigned>(grid), kThreads, kStatsSmem, st>>>(p, qmap, kmap);
+        if (cudaGetLastError() != cudaSuccess)
+            return PA_ERR_CUDA;
+        ++*launches;
+    }
+    if (p.SK > 0) {
+        CUtensorMap qmap, gmap, kmap, vmap;
+        int rc = encode_rows(&kmap, p.k, dt, p.SK, p.B * p.HK, kKeys);
+        if (rc == PA_OK)
+            rc = encode_rows(&vmap, p.v, dt, p.SK, p.B * p.HK, kKeys);
+        if (rc == PA_OK && p.SQ > 0) {
+            rc = encode_rows(&qmap, p.q, dt, p.SQ, p.B * p.HQ, kRows);
+            if (rc == PA_OK)
+                rc = encode_rows(&gmap, p.g, dt, p.SQ, p.B * p.HQ, kRows);
+        } else {
+            qmap = gmap = kmap;  // no row tile is ever loaded
+        }
+        if (rc != PA_OK)
+            return rc;
+        MainFn fn;
+        if (bf)
+            fn = f32_out ? vjp_main_tc<__nv_bfloat16, float> : vjp_main_tc<__nv_bfloat16, __nv_bfloat16>;
+        else
+            fn = f32_out ? vjp_main_tc<__half, float> : vjp_main_tc<__half, __half>;
+        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMainSmem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        const long long grid = static_cast<long long>(p.B) * p.HK * ((p.SK + kKeys - 1) / kKeys);
+        if (grid >= (1ll << 31))
+            return PA_ERR_BAD_DIMS;
+        fn<<<static_cast<unsigned>(grid), kThreads, kMainSmem, st>>>(p, qmap, gmap, kmap, vmap);
+        if (cudaGetLastError() != cudaSuccess)
+            return PA_ERR_CUDA;
+        ++*launches;
+    }
+    return PA_OK;
+}
 
 }  // namespace pa

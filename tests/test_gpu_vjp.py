@@ -159,3 +159,99 @@ def test_repeat_calls_reuse_the_workspace():
     torch.cuda.synchronize()
     for a, b in zip(first, second):
         assert torch.equal(a, b) or torch.allclose(a.float(), b.float(), atol=0, rtol=2.0 ** -7)
+
+
+# --------------------------------------------------------------- tensor cores
+TC_TOL = {"bf16": 4 * UNIT["bf16"], "f16": 4 * UNIT["f16"]}
+
+TC_CASES = {
+    # name: (B, HQ, HK, SQ, SK, causal)
+    "one_tile": (1, 2, 1, 64, 128, False),
+    "ragged_gqa4": (2, 8, 2, 200, 300, False),
+    "ragged_gqa4_causal": (2, 8, 2, 200, 300, True),
+    "tall_causal": (1, 4, 4, 300, 130, True),
+    "wide_causal_mha": (2, 3, 3, 70, 333, True),
+    "single": (1, 2, 2, 1, 1, False),
+    "gqa8_square": (1, 16, 2, 256, 256, True),
+}
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("name", sorted(TC_CASES))
+def test_tensor_cores_match_the_oracle(name, dtype):
+    B, HQ, HK, SQ, SK, causal = TC_CASES[name]
+    s = _spec(dtype=dtype, B=B, HQ=HQ, HK=HK, SQ=SQ, SK=SK, D=128, causal=causal)
+    scale = 1.0 / np.sqrt(128)
+    x = _with_forward_y(wl.make_vjp(s, seed=11), scale)
+    st = _status()
+    got = _run(x, scale, out_dtype=torch.float32, status=st)
+    assert int(st.item()) == 0, f"status {int(st.item())}"
+    _check(got, _oracle(x, scale), TC_TOL[dtype], label=f"{name}/{dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tensor_cores_native_outputs(dtype):
+    s = _spec(dtype=dtype, B=1, HQ=8, HK=2, SQ=190, SK=170, D=128, causal=True)
+    scale = 1.0 / np.sqrt(128)
+    x = _with_forward_y(wl.make_vjp(s, seed=12), scale)
+    st = _status()
+    got = _run(x, scale, status=st)
+    assert int(st.item()) == 0
+    assert all(t.dtype == x.q.dtype for t in got)
+    _check(got, _oracle(x, scale), TC_TOL[dtype], out_fmt=dtype, label=f"native {dtype}")
+
+
+def test_tensor_cores_agree_with_cuda_cores():
+    """The two kernel families on the same inputs: within the tensor-core bound."""
+    s = _spec(dtype="bf16", B=1, HQ=4, HK=1, SQ=150, SK=260, D=128, causal=False)
+    x = _with_forward_y(wl.make_vjp(s, seed=13), 0.09)
+    a = _run(x, 0.09, out_dtype=torch.float32)
+    b = _run(x, 0.09, out_dtype=torch.float32, kernel=1)
+    _check(a, [t.double().numpy() for t in b], TC_TOL["bf16"], label="tc vs simt")
+
+
+def test_tensor_cores_empty_key_set_and_rows():
+    """SK = 0 (every row empty: dq = 0) and SQ = 0 (dk = dv = 0) on the 16-bit path."""
+    from paged_kv_cache_182_gb300 import binding
+
+    for sq, sk in ((0, 200), (130, 0)):
+        s = _spec(dtype="bf16", B=1, HQ=2, HK=1, SQ=sq, SK=sk, D=128)
+        x = wl.make_vjp(s, seed=14)
+        d = x.to("cuda")
+        out = tuple(torch.full_like(t, float("nan")) for t in (d.q, d.k, d.k))
+        binding.attention_vjp(d.q, d.k, d.v, d.y, d.g, scale=0.1, out=out)
+        torch.cuda.synchronize()
+        for t in out:
+            assert torch.all(t == 0)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_full_size_sampled(seed):
+    """The benchmarked shape (4 x 2048 tokens, 32 query heads on 8 key/value
+    heads, D 128, bf16, causal) in the launch configuration the bench times;
+    two (batch, key/value head) groups checked against the oracle, which
+    needs only that group's rows."""
+    from paged_kv_cache_182_gb300 import binding
+
+    s = wl.VJP_SPECS["vjp_bf16"]
+    x = wl.make_vjp(s, seed=seed)
+    d = x.to("cuda")
+    st = _status()
+    dq, dk, dv = binding.attention_vjp(d.q, d.k, d.v, d.y, d.g, scale=1 / np.sqrt(s.D),
+                                       causal=True, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(seed)
+    g = s.HQ // s.HK
+    for _ in range(2):
+        b, kh = int(rng.integers(s.B)), int(rng.integers(s.HK))
+        hs = slice(kh * g, kh * g + g)
+        sub = [_np(t[b:b + 1, hs]) for t in (x.q, x.y, x.g)]
+        kv = [_np(t[b:b + 1, kh:kh + 1]) for t in (x.k, x.v)]
+        want = orc.attention_vjp(sub[0], kv[0], kv[1], sub[1], sub[2], 1 / np.sqrt(s.D), True)
+        got = [dq[b:b + 1, hs].cpu(), dk[b:b + 1, kh:kh + 1].cpu(), dv[b:b + 1, kh:kh + 1].cpu()]
+        _check(got, want, TC_TOL["bf16"], out_fmt="bf16", label=f"full b={b} kh={kh}")
