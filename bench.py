@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table and the CPU baseline")
+    ap.add_argument("--vjp", action="store_true",
+                    help="time only the attention backward on its benchmarked shape (one JSON "
+                         "line, --steps timed calls after --warmup)")
     ap.add_argument("--prefill", action="store_true",
                     help="time only the causal prefill of the prefill workload (one JSON "
                          "line, --steps timed calls after --warmup)")
@@ -476,6 +479,41 @@ def prefill_timing(device, steps=20, warmup=3):
             "l2": f"{len(plans)} copies of the KV pools ({pool_bytes // 2**20} MiB) rotated"}
 
 
+def vjp_timing(device, steps=10, warmup=3):
+    """pa_attention_vjp on the benchmarked backward shape (4 sequences of 2048
+    tokens, 32 query heads on 8 key/value heads, D 128, bf16, causal), back to
+    back; q, k, v, y, g and the outputs (about 350 MB) are larger than L2."""
+    from paged_kv_cache_182_gb300 import binding
+    from paged_kv_cache_182_gb300 import workloads as W
+
+    s = W.VJP_SPECS["vjp_bf16"]
+    x = W.make_vjp(s, seed=0).to(device)
+    plan = binding.VjpPlan(x.q, x.k, x.v, x.y, x.g, scale=1.0 / math.sqrt(s.D), causal=s.causal)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        plan.run(stream)
+    torch.cuda.synchronize()
+    launches = binding.kernel_launches()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        plan.run(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / steps * 1e3
+    flops = W.vjp_flops(s)
+    peak = float(json.loads((ROOT / "MEASURED_PEAKS.json").read_text())["bf16_tflops"]) \
+        if (ROOT / "MEASURED_PEAKS.json").exists() else 1900.0
+    tflops = flops / (us * 1e-6) / 1e12
+    return {"workload": f"vjp_bf16 (B={s.B}, HQ={s.HQ}, HK={s.HK}, SQ={s.SQ}, SK={s.SK}, "
+                        f"D={s.D}, causal)",
+            "us_per_call": round(us, 1), "tokens_per_s": round(s.B * s.SQ / (us * 1e-6), 1),
+            "flops_per_call": flops, "TFLOP_per_s": round(tflops, 2),
+            "frac_of_measured_tensor_peak": round(tflops / peak, 4),
+            "launches_per_call": (binding.kernel_launches() - launches) // steps,
+            "l2": "inputs and outputs (about 350 MB) larger than L2"}
+
+
 def run_ours(args, rank, world, local):
     from paged_kv_cache_182_gb300 import binding  # noqa: F401  (fails loudly if not built)
     from paged_kv_cache_182_gb300 import workloads as W
@@ -527,6 +565,7 @@ def run_ours(args, rank, world, local):
         line["per_workload"] = per_workload_table(device, 50, 5, peak, peak_kind)
         line["cache_append"] = append_timing(device)
         line["prefill"] = prefill_timing(device)
+        line["attention_vjp"] = vjp_timing(device)
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -594,7 +633,11 @@ def main():
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py --impl ours needs a CUDA device")
-        if args.prefill:
+        if args.vjp:
+            if rank == 0:
+                line = vjp_timing(torch.device("cuda", local), args.steps, args.warmup)
+                print(json.dumps({"mode": "attention_vjp", **line}), flush=True)
+        elif args.prefill:
             if rank == 0:
                 line = prefill_timing(torch.device("cuda", local), args.steps, args.warmup)
                 print(json.dumps({"mode": "prefill", **line}), flush=True)

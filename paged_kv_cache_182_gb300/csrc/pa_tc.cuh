@@ -99,6 +99,26 @@ __device__ __forceinline__ void tmem_ld32(Cols32& c, uint32_t taddr)
                    "+r"(r[30]), "+r"(r[31])::"memory");
 }
 
+// 16 columns of this warp's 32 tensor-memory lanes (as tmem_ld32).
+struct Cols16 {
+    uint32_t r[16];
+};
+__device__ __forceinline__ void tmem_ld16(Cols16& c, uint32_t taddr)
+{
+    uint32_t* r = c.r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
+}
+
 __device__ __forceinline__ void tmem_st32(const Cols32& c, uint32_t taddr)
 {
     const uint32_t* r = c.r;

@@ -77,13 +77,23 @@ constexpr int kStatsSmem = 6 * kHalf128 + 2048;
 static_assert(sizeof(StatsBars) <= 2048, "statistics barrier area");
 
 struct MainBars {
-    uint64_t kv_full, qd_full[2], qd_empty[2], sd_full, ds_ready, dq_full, dq_free;
+    // ds_ready alternates by step parity: a softmax thread may finish step
+    // it + 1 before the others have arrived for step it
+    uint64_t kv_full, qd_full[3], qd_empty[3], p_free[2], sd_full[2], sd_free[2], ds_ready[2], dq_full, dq_free,
+        mma_done;
     uint32_t tmem;
     int abort;
 };
-// K, V (2 halves each), Q and dO rings (2 stages x 2 halves of 64 rows), P^T,
-// dS^T (one 16 KB block each), row statistics (2 stages x 512 bytes), barriers
-constexpr int kMainSmem = 4 * kHalf128 + 8 * kHalf64 + 2 * kHalf128 + 1024 + 1024;
+constexpr int kStages = 3;                             // Q / dO / row-statistics ring of the backward
+constexpr int kMSoftmax = 512;                         // warps 0-15: softmax, 16 rows a thread
+constexpr int kDqThreads = 128;                        // warps 18-21: dQ^T reduction
+constexpr int kMainThreads = kMSoftmax + 64 + kDqThreads;  // + warp 16 TMA, warp 17 MMA: 704
+// K, V (2 halves each), the Q and dO rings (3 stages x 2 halves of 64 rows),
+// P^T and dS^T (2 buffers of 16 KB each), row statistics (3 stages x 512
+// bytes), barriers
+constexpr int kMainSmem = 4 * kHalf128 + 12 * kHalf64 + 4 * kHalf128 + kStages * 512 + 512;
+static_assert(sizeof(MainBars) <= 512, "backward barrier area");
+static_assert(kMainSmem <= 232448, "backward shared memory");
 
 __device__ __forceinline__ void red_add(float* addr, float v)
 {
@@ -329,10 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Backward.  grid = ceil(SK / 128) * B * HK, key tile fastest-varying last:
+// Backward.  grid = ceil(SK / 128) * B * HK, (batch, key/value head) fastest:
 // the key tiles that the most (causal) rows see are launched first.
 template <typename T, typename TO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, 1)
     vjp_main_tc(const __grid_constant__ VjpParams p, const __grid_constant__ CUtensorMap qmap,
                 const __grid_constant__ CUtensorMap gmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap)
@@ -344,14 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(p.status, PA_STATUS_TIMEOUT);
         return;
     }
-    unsigned char* sK = smem_raw;                         // 2 halves of 16 KB
-    unsigned char* sV = sK + 2 * kHalf128;                // 2 halves
-    unsigned char* sQ = sV + 2 * kHalf128;                // 2 stages x 2 halves of 8 KB
-    unsigned char* sG = sQ + 4 * kHalf64;                 // 2 stages x 2 halves
-    unsigned char* sP = sG + 4 * kHalf64;                 // P^T: 128 keys x 64 rows
-    unsigned char* sS = sP + kHalf128;                    // dS^T
-    float* sStat = reinterpret_cast<float*>(sS + kHalf128);  // 2 stages x (64 lse2, 64 delta)
-    MainBars& bars = *reinterpret_cast<MainBars*>(sS + kHalf128 + 1024);
+    unsigned char* sK = smem_raw;                     // 2 halves of 16 KB
+    unsigned char* sV = sK + 2 * kHalf128;            // 2 halves
+    unsigned char* sQ = sV + 2 * kHalf128;            // kStages x 2 halves of 8 KB
+    unsigned char* sG = sQ + kStages * 2 * kHalf64;   // kStages x 2 halves
+    unsigned char* sP = sG + kStages * 2 * kHalf64;   // 2 buffers of P^T (128 keys x 64 rows)
+    unsigned char* sS = sP + 2 * kHalf128;            // 2 buffers of dS^T
+    float* sStat = reinterpret_cast<float*>(sS + 2 * kHalf128);  // kStages x (64 lse2, 64 delta)
+    MainBars& bars = *reinterpret_cast<MainBars*>(sS + 2 * kHalf128 + kStages * 512);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int BH = p.B * p.HK;
@@ -367,14 +377,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&bars.kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars.qd_full[s], 1);
             mbar_init(&bars.qd_empty[s], 1);
         }
-        mbar_init(&bars.sd_full, 1);
-        mbar_init(&bars.ds_ready, kSoftmax);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.p_free[s], 1);
+            mbar_init(&bars.sd_full[s], 1);
+            mbar_init(&bars.sd_free[s], kMSoftmax);
+            mbar_init(&bars.ds_ready[s], kMSoftmax);
+        }
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_free, kSoftmax);
+        mbar_init(&bars.dq_free, kDqThreads);
+        mbar_init(&bars.mma_done, 1);
         bars.abort = 0;
         fence_mbar_init();
     }
@@ -388,8 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tdK = bars.tmem, tdV = bars.tmem + 128, tS = bars.tmem + 256, tP = bars.tmem + 320,
-                   tQ = bars.tmem + 384;
+    // tensor memory: dK | dV | S^T (two buffers of 64 columns) | dP^T (two
+    // buffers); dQ^T of step it goes to S buffer it & 1 once its softmax has
+    // read S^T
+    const uint32_t tdK = bars.tmem, tdV = bars.tmem + 128, tS = bars.tmem + 256, tP = bars.tmem + 384;
     volatile int* abort_flag = &bars.abort;
     auto fail = [&]() {
         *abort_flag = 1;
@@ -401,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         h = kh * p.groups + gi;
         i0 = (r_first + it - gi * per_head) * kRows;
     };
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+    const int ln = (warp & 3) * 32 + lane;                                   // key, or d for dQ^T
 
-    if (warp == 8) {
+    if (warp == 16) {
         // --------------------------------------------------------------- TMA
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&qmap);
@@ -416,9 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int issued = 0;
             for (int it = 0; it < n; ++it) {
-                const int st = it & 1;
-                if (it >= 2 &&
-                    (*abort_flag || !mbar_wait_bounded(&bars.qd_empty[st], ((it >> 1) - 1) & 1, wait_ns))) {
+                const int st = it % kStages, round = it / kStages;
+                if (it >= kStages &&
+                    (*abort_flag || !mbar_wait_bounded(&bars.qd_empty[st], (round - 1) & 1, wait_ns))) {
                     fail();
                     break;
                 }
@@ -436,48 +455,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sStat + st * 128 + 64, p.delta + srow, 256, &bars.qd_full[st]);
                 issued = it + 1;
             }
-            for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
-                mbar_wait_bounded(&bars.qd_full[it & 1], (it >> 1) & 1, wait_ns);
+            // no copy may land after the CTA's memory is released
+            for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
+                mbar_wait_bounded(&bars.qd_full[it % kStages], (it / kStages) & 1, wait_ns);
             mbar_wait_bounded(&bars.kv_full, 0, wait_ns);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 17) {
         // --------------------------------------------------------------- MMA
+        // Around step it: S^T and dP^T of step it + 1 as soon as their stage has
+        // landed and their buffers are free; once the softmax of step it is
+        // done, dV, dK and dQ^T of step it.  The softmax of step it + 1 thus
+        // overlaps the products of step it.
         if (lane == 0 && n > 0) {
-            const uint32_t ka = smem_u32(sK), va = smem_u32(sV), qa = smem_u32(sQ), ga = smem_u32(sG);
-            const uint32_t pa = smem_u32(sP), sa = smem_u32(sS);
             const uint32_t id_s = idesc<kBf>(kRows, false);        // N 64, both K-major
             const uint32_t id_o = idesc<kBf>(kD, true);            // N 128, B MN-major
             const uint32_t id_q = idesc<kBf>(kRows, true, true);   // N 64, A and B MN-major
-            bool ok = mbar_wait_bounded(&bars.kv_full, 0, wait_ns);
-            for (int it = 0; it < n && ok; ++it) {
-                const int st = it & 1;
-                ok = !*abort_flag && mbar_wait_bounded(&bars.qd_full[st], (it >> 1) & 1, wait_ns);
-                if (!ok)
-                    break;
+            // descriptors of the operand bases; a byte offset o adds o >> 4
+            const uint64_t dK_k = smem_desc(smem_u32(sK), 16, 1024);          // K, K-major A
+            const uint64_t dK_mn = smem_desc(smem_u32(sK), kHalf128, 1024);   // K, MN-major A
+            const uint64_t dV_k = smem_desc(smem_u32(sV), 16, 1024);
+            const uint64_t dQ_k = smem_desc(smem_u32(sQ), 16, 1024);          // Q, dO: K-major B
+            const uint64_t dG_k = smem_desc(smem_u32(sG), 16, 1024);
+            const uint64_t dQ_mn = smem_desc(smem_u32(sQ), kHalf64, 1024);    // Q, dO: MN-major B
+            const uint64_t dG_mn = smem_desc(smem_u32(sG), kHalf64, 1024);
+            const uint64_t dP_k = smem_desc(smem_u32(sP), 16, 1024);          // P^T, dS^T: K-major A
+            const uint64_t dS_k = smem_desc(smem_u32(sS), 16, 1024);
+            const uint64_t dS_mn = smem_desc(smem_u32(sS), 1024, 1024);       // dS^T: MN-major B, one span
+            auto at = [](uint64_t d, uint32_t off) { return d + (off >> 4); };
+            // S^T = K Q^T and dP^T = V dO^T of step u over the head dimension,
+            // into buffers u & 1
+            auto issue_sd = [&](int u) {
+                const int b2 = u & 1, qs = u % kStages;
+                if (*abort_flag || !mbar_wait_bounded(&bars.qd_full[qs], (u / kStages) & 1, wait_ns))
+                    return false;
+                // the buffers' previous contents: S^T, dP^T of step u - 2 (read
+                // by its softmax) and dQ^T of step u - 2 (read by the dQ warps)
+                if (u >= 2 && (!mbar_wait_bounded(&bars.sd_free[b2], ((u >> 1) - 1) & 1, wait_ns) ||
+                               !mbar_wait_bounded(&bars.dq_free, (u - 2) & 1, wait_ns)))
+                    return false;
                 tc_fence_after();
-                const uint32_t q_st = qa + st * 2 * kHalf64, g_st = ga + st * 2 * kHalf64;
-                // S^T = K Q^T and dP^T = V dO^T over the head dimension
+                const uint32_t qo = qs * 2 * kHalf64;
+#pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t ok128 = (ks >> 2) * kHalf128 + (ks & 3) * 32;
-                    const uint32_t ok64 = (ks >> 2) * kHalf64 + (ks & 3) * 32;
-                    umma(tS, smem_desc(ka + ok128, 16, 1024), smem_desc(q_st + ok64, 16, 1024), id_s, ks > 0);
-                    umma(tP, smem_desc(va + ok128, 16, 1024), smem_desc(g_st + ok64, 16, 1024), id_s, ks > 0);
+                    const uint32_t o128 = (ks >> 2) * kHalf128 + (ks & 3) * 32;
+                    const uint32_t o64 = qo + (ks >> 2) * kHalf64 + (ks & 3) * 32;
+                    umma(tS + b2 * kRows, at(dK_k, o128), at(dQ_k, o64), id_s, ks > 0);
+                    umma(tP + b2 * kRows, at(dV_k, o128), at(dG_k, o64), id_s, ks > 0);
                 }
-                umma_commit(&bars.sd_full);
-                ok = mbar_wait_bounded(&bars.ds_ready, it & 1, wait_ns);
+                umma_commit(&bars.sd_full[b2]);
+                return true;
+            };
+            bool ok = mbar_wait_bounded(&bars.kv_full, 0, wait_ns) && issue_sd(0);
+            for (int it = 0; it < n && ok; ++it) {
+                const int qs = it % kStages, pbuf = it & 1;
+                if (it + 1 < n && !(ok = issue_sd(it + 1)))
+                    break;
+                ok = mbar_wait_bounded(&bars.ds_ready[pbuf], (it >> 1) & 1, wait_ns);
                 if (!ok)
                     break;
                 tc_fence_after();
+                const uint32_t qo = qs * 2 * kHalf64, po = pbuf * kHalf128;
                 // dV += P^T dO, dK += dS^T Q over the step's 64 rows (dO and Q
                 // MN-major: rows are the reduction, 64 columns of D per half)
+#pragma unroll
                 for (int ks = 0; ks < kRows / 16; ++ks) {
                     const uint32_t acc = it > 0 || ks > 0;
-                    umma(tdV, smem_desc(pa + ks * 32, 16, 1024), smem_desc(g_st + ks * 2048, kHalf64, 1024), id_o,
-                         acc);
-                    umma(tdK, smem_desc(sa + ks * 32, 16, 1024), smem_desc(q_st + ks * 2048, kHalf64, 1024), id_o,
-                         acc);
+                    umma(tdV, at(dP_k, po + ks * 32), at(dG_mn, qo + ks * 2048), id_o, acc);
+                    umma(tdK, at(dS_k, po + ks * 32), at(dQ_mn, qo + ks * 2048), id_o, acc);
                 }
+                // the dQ warps have read dQ^T of step it - 1 (so that dq_full
+                // never runs two phases ahead of them)
                 if (it > 0) {
                     ok = mbar_wait_bounded(&bars.dq_free, (it - 1) & 1, wait_ns);
                     if (!ok)
@@ -485,131 +533,180 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                 }
                 // dQ^T = K^T dS^T over the tile's 128 keys (K as an MN-major A:
-                // D is its row dimension, in two 64-wide halves 16 KB apart)
+                // D is its row dimension, in two 64-wide halves 16 KB apart;
+                // dS^T's N = 64 is one swizzle span), into S buffer it & 1
+#pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    umma(tQ, smem_desc(ka + ks * 2048, kHalf128, 1024), smem_desc(sa + ks * 2048, 1024, 1024),
-                         id_q, ks > 0);  // dS^T: N = 64 is one swizzle span, its LBO is not used
+                    umma(tS + pbuf * kRows, at(dK_mn, ks * 2048), at(dS_mn, po + ks * 2048), id_q, ks > 0);
                 umma_commit(&bars.dq_full);
-                umma_commit(&bars.qd_empty[st]);
+                umma_commit(&bars.qd_empty[qs]);
+                umma_commit(&bars.p_free[pbuf]);
             }
-            if (!ok)
+            if (ok)
+                umma_commit(&bars.mma_done);
+            else
                 fail();
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------- softmax and dQ reduction
-        // tensor-memory lane = key (S^T, dP^T, dK, dV) or d (dQ^T); this
-        // thread takes columns [32 part, 32 part + 32) of the 64-wide blocks
-        const int ln = (warp & 3) * 32 + lane;
-        const int part = warp >> 2;
-        const int key = k0 + ln;
-        const bool key_ok = key < p.SK;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    } else if (warp >= 18) {
+        // -------------------------------------------------- dQ^T reduction
+        // lane = d, the 64 columns the step's rows
         bool fault = false;
-        for (int it = 0; it < n; ++it) {
-            const int st = it & 1;
+        for (int it = 0; it < n && !fault; ++it) {
             int h, i0;
             step_head(it, h, i0);
-            bool got = !fault && !*abort_flag && mbar_wait_bounded(&bars.sd_full, it & 1, wait_ns);
-            got = got && mbar_wait_bounded(&bars.qd_full[st], (it >> 1) & 1, wait_ns);
-            if (!__all_sync(kAll, got)) {
-                fault = true;
-                break;
-            }
-            tc_fence_after();
-            const float* lse = sStat + st * 128 + part * 32;
-            const float* dlt = sStat + st * 128 + 64 + part * 32;
-            const int rb = i0 + part * 32;  // first row of this thread's columns
-            float pv[32];
-            {
-                Cols32 x;
-                tmem_ld32(x, tS + lane_off + part * 32);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int row = rb + j;
-                    const bool vis = key_ok && row < p.SQ && (!p.causal || key <= row);
-                    pv[j] = vis ? fast_exp2(__uint_as_float(x.r[j]) * p.scale_log2 - lse[j]) : 0.f;
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(sP + sw128(ln, part * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            {
-                Cols32 x;
-                tmem_ld32(x, tP + lane_off + part * 32);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)  // (rows past SQ: p = 0 and their delta is not read)
-                    pv[j] = pv[j] != 0.f ? pv[j] * (__uint_as_float(x.r[j]) - dlt[j]) * p.scale : 0.f;
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(sS + sw128(ln, part * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars.ds_ready);
-            // dQ^T: lane = d, columns = the rows of this step
-            got = __all_sync(kAll, mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
+            const bool got =
+                __all_sync(kAll, !*abort_flag && mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
             if (!got) {
                 fault = true;
                 break;
             }
             tc_fence_after();
-            {
-                Cols32 x;
-                tmem_ld32(x, tQ + lane_off + part * 32);
-                float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + rb) * kD + ln;
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (rb + j < p.SQ)
-                        red_add(dst + static_cast<int64_t>(j) * kD, __uint_as_float(x.r[j]));
-            }
+            const uint32_t tQ = tS + (it & 1) * kRows;
+            Cols32 x0, x1;
+            tmem_ld32(x0, tQ + lane_off);
+            tmem_ld32(x1, tQ + lane_off + 32);
             tc_fence_before();
             mbar_arrive(&bars.dq_free);
+            float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + i0) * kD + ln;
+            const int rows = min(kRows, p.SQ - i0);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < rows)
+                    red_add(dst + static_cast<int64_t>(j) * kD, __uint_as_float(x0.r[j]));
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (32 + j < rows)
+                    red_add(dst + static_cast<int64_t>(32 + j) * kD, __uint_as_float(x1.r[j]));
         }
+        if (fault && lane == 0)
+            fail();
+    } else {
+        // ----------------------------------------------------------- softmax
+        // tensor-memory lane = key; this thread takes rows [16 part, 16 part + 16)
+        const int part = warp >> 2;
+        const int key = k0 + ln;
+        const bool key_ok = key < p.SK;
+        const bool keys_all = k0 + kKeys <= p.SK;  // every key of the tile is real
+        bool fault = false;
+        for (int it = 0; it < n; ++it) {
+            const int pbuf = it & 1, qs = it % kStages;
+            int h, i0;
+            step_head(it, h, i0);
+            bool got = !fault && !*abort_flag && mbar_wait_bounded(&bars.sd_full[pbuf], (it >> 1) & 1, wait_ns);
+            got = got && mbar_wait_bounded(&bars.qd_full[qs], (it / kStages) & 1, wait_ns);
+            // P^T / dS^T buffer pbuf was last read by the products of step it - 2
+            if (it >= 2)
+                got = got && mbar_wait_bounded(&bars.p_free[pbuf], ((it >> 1) - 1) & 1, wait_ns);
+            if (!__all_sync(kAll, got)) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+            const int rb = i0 + part * 16;  // first row of this thread's columns
+            // no mask on this thread's block: every key real, every row real,
+            // and (causal) the last key at or before the first row (warp-uniform)
+            const bool plain = keys_all && rb + 16 <= p.SQ && (!p.causal || k0 + kKeys - 1 <= rb);
+            const float4* l4 = reinterpret_cast<const float4*>(sStat + qs * 128 + part * 16);
+            const float4* d4 = reinterpret_cast<const float4*>(sStat + qs * 128 + 64 + part * 16);
+            unsigned char* pb = sP + pbuf * kHalf128;
+            unsigned char* sb = sS + pbuf * kHalf128;
+            float pv[16];
+            {
+                Cols16 x;
+                tmem_ld16(x, tS + pbuf * kRows + lane_off + part * 16);
+                const float c = p.scale_log2;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 l = l4[q4];
+                    const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * q4 + e;
+                        pv[j] = fast_exp2(fmaf(__uint_as_float(x.r[j]), c, -lv[e]));
+                    }
+                }
+                if (!plain) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int row = rb + j;
+                        if (!(key_ok && row < p.SQ && (!p.causal || key <= row)))
+                            pv[j] = 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
+                *reinterpret_cast<uint4*>(pb + sw128(ln, part * 2 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            {
+                Cols16 x;
+                tmem_ld16(x, tP + pbuf * kRows + lane_off + part * 16);
+                tc_fence_before();
+                mbar_arrive(&bars.sd_free[pbuf]);  // S^T and dP^T of this step are read
+                const float sc = p.scale;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 d = d4[q4];
+                    const float dv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * q4 + e;
+                        const float ds = pv[j] * sc * (__uint_as_float(x.r[j]) - dv[e]);
+                        // rows past SQ: p = 0, and their delta is not defined
+                        pv[j] = plain || pv[j] != 0.f ? ds : 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
+                *reinterpret_cast<uint4*>(sb + sw128(ln, part * 2 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars.ds_ready[pbuf]);
+        }
+        if (!fault && n > 0)
+            fault = !__all_sync(kAll, !*abort_flag && mbar_wait_bounded(&bars.mma_done, 0, wait_ns));
         if (fault) {
             if (lane == 0)
                 fail();
         } else {
-            // dK and dV of this thread's key: columns [64 part, 64 part + 64)
+            // dK and dV of this thread's key: columns [32 part, 32 part + 32)
             // (the tensor-memory loads are warp-wide; only the stores depend on the key)
-            TO* dk = static_cast<TO*>(p.dk) + ((static_cast<int64_t>(b) * p.HK + kh) * p.SK + key) * kD + part * 64;
-            TO* dv = static_cast<TO*>(p.dv) + ((static_cast<int64_t>(b) * p.HK + kh) * p.SK + key) * kD + part * 64;
+            tc_fence_after();
+            const int64_t o = ((static_cast<int64_t>(b) * p.HK + kh) * p.SK + key) * kD + part * 32;
+            float v[32];
+            if (n > 0) {
+                Cols32 x;
+                tmem_ld32(x, tdK + lane_off + part * 32);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                if (n > 0) {
-                    Cols32 x;
-                    tmem_ld32(x, tdK + lane_off + part * 64 + c * 32);
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __uint_as_float(x.r[j]);
+            } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __uint_as_float(x.r[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = 0.f;
-                }
-                if (key_ok)
-                    store_row<TO>(dk + c * 32, v);
-                if (n > 0) {
-                    Cols32 x;
-                    tmem_ld32(x, tdV + lane_off + part * 64 + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __uint_as_float(x.r[j]);
-                }
-                if (key_ok)
-                    store_row<TO>(dv + c * 32, v);
+                for (int j = 0; j < 32; ++j)
+                    v[j] = 0.f;
             }
+            if (key_ok)
+                store_row<TO>(static_cast<TO*>(p.dk) + o, v);
+            if (n > 0) {
+                Cols32 x;
+                tmem_ld32(x, tdV + lane_off + part * 32);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __uint_as_float(x.r[j]);
+            }
+            if (key_ok)
+                store_row<TO>(static_cast<TO*>(p.dv) + o, v);
         }
     }
     tc_fence_before();
@@ -697,7 +794,7 @@ int launch_vjp_tc(const VjpParams& p, int dtype, bool f32_out, cudaStream_t st, 
         const long long grid = static_cast<long long>(p.B) * p.HK * ((p.SK + kKeys - 1) / kKeys);
         if (grid >= (1ll << 31))
             return PA_ERR_BAD_DIMS;
-        fn<<<static_cast<unsigned>(grid), kThreads, kMainSmem, st>>>(p, qmap, gmap, kmap, vmap);
+        fn<<<static_cast<unsigned>(grid), kMainThreads, kMainSmem, st>>>(p, qmap, gmap, kmap, vmap);
         if (cudaGetLastError() != cudaSuccess)
             return PA_ERR_CUDA;
         ++*launches;
