@@ -21,19 +21,23 @@
 //
 // vjp_main_tc -- one CTA per (batch, key/value head, 128 keys): K and V of
 //   the tile stay in shared memory; dK and dV accumulate in tensor memory
-//   over every 64-row tile of every query head of the group.  Per row tile:
-//     S^T  = K Q^T          M 128 keys, N 64 rows, K = D      (both K-major)
+//   over every 128-row step of every query head of the group.  Per step:
+//     S^T  = K Q^T          M 128 keys, N 128 rows, K = D     (both K-major)
 //     dP^T = V dO^T         same shapes
-//     softmax threads: P^T = exp2(s2 - lse2), dS^T = P^T (dP^T - delta) scale,
-//                      both written as 16-bit K-major operands
-//     dV  += P^T dO         M 128 keys, N = D, K 64 rows      (dO MN-major)
-//     dK  += dS^T Q         same, Q MN-major
-//     dQ^T = K^T dS^T       M = D, N 64 rows, K 128 keys      (both MN-major)
-//   and the softmax threads add dQ^T into the float32 accumulator (one
-//   reduction per element, coalesced over D).  Warp 8 loads K, V once and
-//   Q, dO, lse2, delta per row tile into a two-stage ring; warp 9 issues the
-//   MMAs (one thread).  Tensor memory (512 columns): dK | dV | S^T | dP^T |
-//   dQ^T.
+//     softmax threads: P = exp2(s2 - lse2), written back over S^T in tensor
+//                      memory as 16-bit pairs; dS^T = P (dP^T - delta) scale,
+//                      written to shared memory as a 16-bit operand
+//     dV  += P dO           M 128 keys, N = D, K 128 rows     (P from tensor
+//                                                              memory, dO MN-major)
+//     dK  += dS^T Q         same, dS^T K-major, Q MN-major
+//     dQ^T = K^T dS^T       M = D, N 128 rows, K 128 keys     (both MN-major),
+//                           into the dP^T columns the softmax has read
+//   and the same threads read dQ^T back and add it into the float32
+//   accumulator (one reduction per element, coalesced over D).  Every MMA
+//   has N = 128: a tcgen05 MMA of M = 128 costs at least as much as N = 64
+//   does.  Warp 16 loads K, V once and Q, dO, lse2, delta per step into a
+//   two-stage ring; warp 17 issues the MMAs (one thread).  Tensor memory
+//   (512 columns): dK | dV | S^T (then P) | dP^T (then dQ^T).
 //
 // Every wait is bounded (p.wait_ns); a wait that gives up ORs
 // PA_STATUS_TIMEOUT into p.status, and every path frees the tensor memory.
@@ -77,21 +81,17 @@ constexpr int kStatsSmem = 6 * kHalf128 + 2048;
 static_assert(sizeof(StatsBars) <= 2048, "statistics barrier area");
 
 struct MainBars {
-    // ds_ready alternates by step parity: a softmax thread may finish step
-    // it + 1 before the others have arrived for step it
-    uint64_t kv_full, qd_full[3], qd_empty[3], p_free[2], sd_full[2], sd_free[2], ds_ready[2], dq_full, dq_free,
-        mma_done;
+    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, mma_done;
     uint32_t tmem;
     int abort;
 };
-constexpr int kStages = 3;                             // Q / dO / row-statistics ring of the backward
-constexpr int kMSoftmax = 512;                         // warps 0-15: softmax, 16 rows a thread
-constexpr int kDqThreads = 128;                        // warps 18-21: dQ^T reduction
-constexpr int kMainThreads = kMSoftmax + 64 + kDqThreads;  // + warp 16 TMA, warp 17 MMA: 704
-// K, V (2 halves each), the Q and dO rings (3 stages x 2 halves of 64 rows),
-// P^T and dS^T (2 buffers of 16 KB each), row statistics (3 stages x 512
-// bytes), barriers
-constexpr int kMainSmem = 4 * kHalf128 + 12 * kHalf64 + 4 * kHalf128 + kStages * 512 + 512;
+constexpr int kBRows = 128;                            // query rows per step of the backward kernel
+constexpr int kMSoftmax = 512;                         // warps 0-15: softmax and dQ^T, 32 rows a thread
+constexpr int kMainThreads = kMSoftmax + 64;           // + warp 16 TMA, warp 17 MMA: 576
+// K, V (2 halves of 16 KB each), the Q and dO rings (2 stages x 2 halves of
+// 16 KB), dS^T (2 halves of 16 KB: rows 0-63 and 64-127), row statistics
+// (2 stages x 1 KB), barriers
+constexpr int kMainSmem = 4 * kHalf128 + 8 * kHalf128 + 2 * kHalf128 + 2 * 1024 + 512;
 static_assert(sizeof(MainBars) <= 512, "backward barrier area");
 static_assert(kMainSmem <= 232448, "backward shared memory");
 
@@ -354,14 +354,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             atomicOr(p.status, PA_STATUS_TIMEOUT);
         return;
     }
-    unsigned char* sK = smem_raw;                     // 2 halves of 16 KB
-    unsigned char* sV = sK + 2 * kHalf128;            // 2 halves
-    unsigned char* sQ = sV + 2 * kHalf128;            // kStages x 2 halves of 8 KB
-    unsigned char* sG = sQ + kStages * 2 * kHalf64;   // kStages x 2 halves
-    unsigned char* sP = sG + kStages * 2 * kHalf64;   // 2 buffers of P^T (128 keys x 64 rows)
-    unsigned char* sS = sP + 2 * kHalf128;            // 2 buffers of dS^T
-    float* sStat = reinterpret_cast<float*>(sS + 2 * kHalf128);  // kStages x (64 lse2, 64 delta)
-    MainBars& bars = *reinterpret_cast<MainBars*>(sS + 2 * kHalf128 + kStages * 512);
+    unsigned char* sK = smem_raw;                  // 2 halves of 16 KB
+    unsigned char* sV = sK + 2 * kHalf128;         // 2 halves
+    unsigned char* sQ = sV + 2 * kHalf128;         // 2 stages x 2 halves of 16 KB
+    unsigned char* sG = sQ + 4 * kHalf128;         // 2 stages x 2 halves
+    unsigned char* sS = sG + 4 * kHalf128;         // dS^T: rows 0-63 | rows 64-127
+    float* sStat = reinterpret_cast<float*>(sS + 2 * kHalf128);  // 2 stages x (128 lse2, 128 delta)
+    MainBars& bars = *reinterpret_cast<MainBars*>(sS + 2 * kHalf128 + 2048);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int BH = p.B * p.HK;
@@ -369,26 +368,24 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int b = (blockIdx.x % BH) / p.HK;
     const int kh = blockIdx.x % p.HK;
     const int k0 = kt * kKeys;
-    const int nrt = (p.SQ + kRows - 1) / kRows;
-    const int r_first = p.causal ? min(k0 / kRows, nrt) : 0;
+    const int nrt = (p.SQ + kBRows - 1) / kBRows;
+    const int r_first = p.causal ? min(k0 / kBRows, nrt) : 0;
     const int per_head = nrt - r_first;
     const int n = per_head * p.groups;
     const uint64_t wait_ns = p.wait_ns;
 
     if (tid == 0) {
         mbar_init(&bars.kv_full, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.qd_full[s], 1);
             mbar_init(&bars.qd_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars.p_free[s], 1);
-            mbar_init(&bars.sd_full[s], 1);
-            mbar_init(&bars.sd_free[s], kMSoftmax);
-            mbar_init(&bars.ds_ready[s], kMSoftmax);
-        }
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.dp_full, 1);
+        mbar_init(&bars.p_ready, kMSoftmax);
+        mbar_init(&bars.ds_ready, kMSoftmax);
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_free, kDqThreads);
+        mbar_init(&bars.dq_free, kMSoftmax);
         mbar_init(&bars.mma_done, 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -403,9 +400,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // tensor memory: dK | dV | S^T (two buffers of 64 columns) | dP^T (two
-    // buffers); dQ^T of step it goes to S buffer it & 1 once its softmax has
-    // read S^T
+    // tensor memory: dK | dV | S^T (P overwrites it, packed 16-bit) | dP^T (dQ^T
+    // overwrites it once the softmax has read dP^T)
     const uint32_t tdK = bars.tmem, tdV = bars.tmem + 128, tS = bars.tmem + 256, tP = bars.tmem + 384;
     volatile int* abort_flag = &bars.abort;
     auto fail = [&]() {
@@ -416,7 +412,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     auto step_head = [&](int it, int& h, int& i0) {
         const int gi = it / per_head;
         h = kh * p.groups + gi;
-        i0 = (r_first + it - gi * per_head) * kRows;
+        i0 = (r_first + it - gi * per_head) * kBRows;
     };
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
     const int ln = (warp & 3) * 32 + lane;                                   // key, or d for dQ^T
@@ -435,112 +431,114 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             }
             int issued = 0;
             for (int it = 0; it < n; ++it) {
-                const int st = it % kStages, round = it / kStages;
-                if (it >= kStages &&
-                    (*abort_flag || !mbar_wait_bounded(&bars.qd_empty[st], (round - 1) & 1, wait_ns))) {
+                const int st = it & 1;
+                if (it >= 2 &&
+                    (*abort_flag || !mbar_wait_bounded(&bars.qd_empty[st], ((it >> 1) - 1) & 1, wait_ns))) {
                     fail();
                     break;
                 }
                 int h, i0;
                 step_head(it, h, i0);
-                mbar_arrive_expect_tx(&bars.qd_full[st], 4 * kHalf64 + 512);
+                mbar_arrive_expect_tx(&bars.qd_full[st], 4 * kHalf128 + 1024);
                 for (int hh = 0; hh < 2; ++hh) {
-                    tma_load_4d(sQ + st * 2 * kHalf64 + hh * kHalf64, &qmap, 0, hh, i0, b * p.HQ + h,
+                    tma_load_4d(sQ + st * 2 * kHalf128 + hh * kHalf128, &qmap, 0, hh, i0, b * p.HQ + h,
                                 &bars.qd_full[st]);
-                    tma_load_4d(sG + st * 2 * kHalf64 + hh * kHalf64, &gmap, 0, hh, i0, b * p.HQ + h,
+                    tma_load_4d(sG + st * 2 * kHalf128 + hh * kHalf128, &gmap, 0, hh, i0, b * p.HQ + h,
                                 &bars.qd_full[st]);
                 }
                 const int64_t srow = (static_cast<int64_t>(b) * p.HQ + h) * p.sqp + i0;
-                bulk_load(sStat + st * 128, p.lse + srow, 256, &bars.qd_full[st]);
-                bulk_load(sStat + st * 128 + 64, p.delta + srow, 256, &bars.qd_full[st]);
+                bulk_load(sStat + st * 256, p.lse + srow, 512, &bars.qd_full[st]);
+                bulk_load(sStat + st * 256 + 128, p.delta + srow, 512, &bars.qd_full[st]);
                 issued = it + 1;
             }
             // no copy may land after the CTA's memory is released
-            for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
-                mbar_wait_bounded(&bars.qd_full[it % kStages], (it / kStages) & 1, wait_ns);
+            for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
+                mbar_wait_bounded(&bars.qd_full[it & 1], (it >> 1) & 1, wait_ns);
             mbar_wait_bounded(&bars.kv_full, 0, wait_ns);
         }
         __syncwarp();
     } else if (warp == 17) {
         // --------------------------------------------------------------- MMA
-        // Around step it: S^T and dP^T of step it + 1 as soon as their stage has
-        // landed and their buffers are free; once the softmax of step it is
-        // done, dV, dK and dQ^T of step it.  The softmax of step it + 1 thus
-        // overlaps the products of step it.
+        // Per step it: dV += P dO (P from tensor memory) once the softmax has
+        // written P; dK += dS^T Q and dQ^T = K^T dS^T once it has written dS^T;
+        // then S^T of step it + 1 (into the P columns, after dV in the pipe)
+        // and, once the dQ warps have read dQ^T, dP^T of step it + 1.
         if (lane == 0 && n > 0) {
-            const uint32_t id_s = idesc<kBf>(kRows, false);        // N 64, both K-major
-            const uint32_t id_o = idesc<kBf>(kD, true);            // N 128, B MN-major
-            const uint32_t id_q = idesc<kBf>(kRows, true, true);   // N 64, A and B MN-major
+            const uint32_t id_s = idesc<kBf>(kBRows, false);       // S^T, dP^T: N 128 rows, both K-major
+            const uint32_t id_o = idesc<kBf>(kD, true);            // dV, dK: N 128 (D), B MN-major
+            const uint32_t id_q = idesc<kBf>(kBRows, true, true);  // dQ^T: N 128 rows, A and B MN-major
             // descriptors of the operand bases; a byte offset o adds o >> 4
             const uint64_t dK_k = smem_desc(smem_u32(sK), 16, 1024);          // K, K-major A
             const uint64_t dK_mn = smem_desc(smem_u32(sK), kHalf128, 1024);   // K, MN-major A
             const uint64_t dV_k = smem_desc(smem_u32(sV), 16, 1024);
             const uint64_t dQ_k = smem_desc(smem_u32(sQ), 16, 1024);          // Q, dO: K-major B
             const uint64_t dG_k = smem_desc(smem_u32(sG), 16, 1024);
-            const uint64_t dQ_mn = smem_desc(smem_u32(sQ), kHalf64, 1024);    // Q, dO: MN-major B
-            const uint64_t dG_mn = smem_desc(smem_u32(sG), kHalf64, 1024);
-            const uint64_t dP_k = smem_desc(smem_u32(sP), 16, 1024);          // P^T, dS^T: K-major A
-            const uint64_t dS_k = smem_desc(smem_u32(sS), 16, 1024);
-            const uint64_t dS_mn = smem_desc(smem_u32(sS), 1024, 1024);       // dS^T: MN-major B, one span
+            const uint64_t dQ_mn = smem_desc(smem_u32(sQ), kHalf128, 1024);   // Q, dO: MN-major B
+            const uint64_t dG_mn = smem_desc(smem_u32(sG), kHalf128, 1024);
+            const uint64_t dS_k = smem_desc(smem_u32(sS), 16, 1024);          // dS^T: K-major A
+            const uint64_t dS_mn = smem_desc(smem_u32(sS), kHalf128, 1024);   // dS^T: MN-major B
             auto at = [](uint64_t d, uint32_t off) { return d + (off >> 4); };
-            // S^T = K Q^T and dP^T = V dO^T of step u over the head dimension,
-            // into buffers u & 1
-            auto issue_sd = [&](int u) {
-                const int b2 = u & 1, qs = u % kStages;
-                if (*abort_flag || !mbar_wait_bounded(&bars.qd_full[qs], (u / kStages) & 1, wait_ns))
-                    return false;
-                // the buffers' previous contents: S^T, dP^T of step u - 2 (read
-                // by its softmax) and dQ^T of step u - 2 (read by the dQ warps)
-                if (u >= 2 && (!mbar_wait_bounded(&bars.sd_free[b2], ((u >> 1) - 1) & 1, wait_ns) ||
-                               !mbar_wait_bounded(&bars.dq_free, (u - 2) & 1, wait_ns)))
+            // K-major k-step ks of a 128-column operand: 64-column halves 16 KB apart
+            auto kmaj = [](int ks) { return static_cast<uint32_t>((ks >> 2) * kHalf128 + (ks & 3) * 32); };
+            auto issue_s = [&](int u) {  // S^T = K Q^T of step u
+                const int su = u & 1;
+                if (*abort_flag || !mbar_wait_bounded(&bars.qd_full[su], (u >> 1) & 1, wait_ns))
                     return false;
                 tc_fence_after();
-                const uint32_t qo = qs * 2 * kHalf64;
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t o128 = (ks >> 2) * kHalf128 + (ks & 3) * 32;
-                    const uint32_t o64 = qo + (ks >> 2) * kHalf64 + (ks & 3) * 32;
-                    umma(tS + b2 * kRows, at(dK_k, o128), at(dQ_k, o64), id_s, ks > 0);
-                    umma(tP + b2 * kRows, at(dV_k, o128), at(dG_k, o64), id_s, ks > 0);
-                }
-                umma_commit(&bars.sd_full[b2]);
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    umma(tS, at(dK_k, kmaj(ks)), at(dQ_k, su * 2 * kHalf128 + kmaj(ks)), id_s, ks > 0);
+                umma_commit(&bars.s_full);
                 return true;
             };
-            bool ok = mbar_wait_bounded(&bars.kv_full, 0, wait_ns) && issue_sd(0);
+            auto issue_dp = [&](int u) {  // dP^T = V dO^T of step u (its stage has landed)
+                const int su = u & 1;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    umma(tP, at(dV_k, kmaj(ks)), at(dG_k, su * 2 * kHalf128 + kmaj(ks)), id_s, ks > 0);
+                umma_commit(&bars.dp_full);
+            };
+            bool ok = mbar_wait_bounded(&bars.kv_full, 0, wait_ns) && issue_s(0);
+            if (ok)
+                issue_dp(0);
             for (int it = 0; it < n && ok; ++it) {
-                const int qs = it % kStages, pbuf = it & 1;
-                if (it + 1 < n && !(ok = issue_sd(it + 1)))
-                    break;
-                ok = mbar_wait_bounded(&bars.ds_ready[pbuf], (it >> 1) & 1, wait_ns);
+                const int st = it & 1;
+                const uint32_t qo = st * 2 * kHalf128;
+                ok = mbar_wait_bounded(&bars.p_ready, it & 1, wait_ns);
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t qo = qs * 2 * kHalf64, po = pbuf * kHalf128;
-                // dV += P^T dO, dK += dS^T Q over the step's 64 rows (dO and Q
-                // MN-major: rows are the reduction, 64 columns of D per half)
+                // dV += P dO: P (keys x rows) from tensor memory, rows 32 k .. 32 k + 31
+                // packed in columns 32 k .. 32 k + 15 of the S^T block; dO MN-major
 #pragma unroll
-                for (int ks = 0; ks < kRows / 16; ++ks) {
-                    const uint32_t acc = it > 0 || ks > 0;
-                    umma(tdV, at(dP_k, po + ks * 32), at(dG_mn, qo + ks * 2048), id_o, acc);
-                    umma(tdK, at(dS_k, po + ks * 32), at(dQ_mn, qo + ks * 2048), id_o, acc);
-                }
-                // the dQ warps have read dQ^T of step it - 1 (so that dq_full
-                // never runs two phases ahead of them)
-                if (it > 0) {
-                    ok = mbar_wait_bounded(&bars.dq_free, (it - 1) & 1, wait_ns);
+                for (int ks = 0; ks < kBRows / 16; ++ks)
+                    umma_ts(tdV, tS + (ks >> 1) * 32 + (ks & 1) * 8, at(dG_mn, qo + ks * 2048), id_o,
+                            it > 0 || ks > 0);
+                ok = mbar_wait_bounded(&bars.ds_ready, it & 1, wait_ns);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                // dK += dS^T Q (dS^T K-major over rows, Q MN-major)
+#pragma unroll
+                for (int ks = 0; ks < kBRows / 16; ++ks)
+                    umma(tdK, at(dS_k, kmaj(ks)), at(dQ_mn, qo + ks * 2048), id_o, it > 0 || ks > 0);
+                // dQ^T = K^T dS^T over the tile's 128 keys (both MN-major: K's rows
+                // and dS^T's rows are keys) into the dP^T columns, which the
+                // softmax has read
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    umma(tP, at(dK_mn, ks * 2048), at(dS_mn, ks * 2048), id_q, ks > 0);
+                umma_commit(&bars.dq_full);
+                umma_commit(&bars.qd_empty[st]);
+                if (it + 1 < n) {
+                    if (!(ok = issue_s(it + 1)))
+                        break;
+                    ok = mbar_wait_bounded(&bars.dq_free, it & 1, wait_ns);
                     if (!ok)
                         break;
                     tc_fence_after();
+                    issue_dp(it + 1);
                 }
-                // dQ^T = K^T dS^T over the tile's 128 keys (K as an MN-major A:
-                // D is its row dimension, in two 64-wide halves 16 KB apart;
-                // dS^T's N = 64 is one swizzle span), into S buffer it & 1
-#pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks)
-                    umma(tS + pbuf * kRows, at(dK_mn, ks * 2048), at(dS_mn, po + ks * 2048), id_q, ks > 0);
-                umma_commit(&bars.dq_full);
-                umma_commit(&bars.qd_empty[qs]);
-                umma_commit(&bars.p_free[pbuf]);
             }
             if (ok)
                 umma_commit(&bars.mma_done);
@@ -548,131 +546,124 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                 fail();
         }
         __syncwarp();
-    } else if (warp >= 18) {
-        // -------------------------------------------------- dQ^T reduction
-        // lane = d, the 64 columns the step's rows
-        bool fault = false;
-        for (int it = 0; it < n && !fault; ++it) {
-            int h, i0;
-            step_head(it, h, i0);
-            const bool got =
-                __all_sync(kAll, !*abort_flag && mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
-            if (!got) {
-                fault = true;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tQ = tS + (it & 1) * kRows;
-            Cols32 x0, x1;
-            tmem_ld32(x0, tQ + lane_off);
-            tmem_ld32(x1, tQ + lane_off + 32);
-            tc_fence_before();
-            mbar_arrive(&bars.dq_free);
-            float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + i0) * kD + ln;
-            const int rows = min(kRows, p.SQ - i0);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (j < rows)
-                    red_add(dst + static_cast<int64_t>(j) * kD, __uint_as_float(x0.r[j]));
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (32 + j < rows)
-                    red_add(dst + static_cast<int64_t>(32 + j) * kD, __uint_as_float(x1.r[j]));
-        }
-        if (fault && lane == 0)
-            fail();
     } else {
-        // ----------------------------------------------------------- softmax
-        // tensor-memory lane = key; this thread takes rows [16 part, 16 part + 16)
+        // ------------------------------------------- softmax and dQ^T reduction
+        // tensor-memory lane = key (S^T, dP^T, dK, dV) or d (dQ^T); this thread
+        // takes rows [32 part, 32 part + 32)
         const int part = warp >> 2;
         const int key = k0 + ln;
         const bool key_ok = key < p.SK;
         const bool keys_all = k0 + kKeys <= p.SK;  // every key of the tile is real
         bool fault = false;
         for (int it = 0; it < n; ++it) {
-            const int pbuf = it & 1, qs = it % kStages;
+            const int st = it & 1;
             int h, i0;
             step_head(it, h, i0);
-            bool got = !fault && !*abort_flag && mbar_wait_bounded(&bars.sd_full[pbuf], (it >> 1) & 1, wait_ns);
-            got = got && mbar_wait_bounded(&bars.qd_full[qs], (it / kStages) & 1, wait_ns);
-            // P^T / dS^T buffer pbuf was last read by the products of step it - 2
-            if (it >= 2)
-                got = got && mbar_wait_bounded(&bars.p_free[pbuf], ((it >> 1) - 1) & 1, wait_ns);
+            bool got = !fault && !*abort_flag && mbar_wait_bounded(&bars.s_full, it & 1, wait_ns);
+            got = got && mbar_wait_bounded(&bars.qd_full[st], (it >> 1) & 1, wait_ns);
             if (!__all_sync(kAll, got)) {
                 fault = true;
                 break;
             }
             tc_fence_after();
-            const int rb = i0 + part * 16;  // first row of this thread's columns
+            const int rb = i0 + part * 32;  // first row of this thread's columns
             // no mask on this thread's block: every key real, every row real,
             // and (causal) the last key at or before the first row (warp-uniform)
-            const bool plain = keys_all && rb + 16 <= p.SQ && (!p.causal || k0 + kKeys - 1 <= rb);
-            const float4* l4 = reinterpret_cast<const float4*>(sStat + qs * 128 + part * 16);
-            const float4* d4 = reinterpret_cast<const float4*>(sStat + qs * 128 + 64 + part * 16);
-            unsigned char* pb = sP + pbuf * kHalf128;
-            unsigned char* sb = sS + pbuf * kHalf128;
-            float pv[16];
-            {
+            const bool plain = keys_all && rb + 32 <= p.SQ && (!p.causal || k0 + kKeys - 1 <= rb);
+            const float4* l4 = reinterpret_cast<const float4*>(sStat + st * 256 + part * 32);
+            const float4* d4 = reinterpret_cast<const float4*>(sStat + st * 256 + 128 + part * 32);
+            float pv[32];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
                 Cols16 x;
-                tmem_ld16(x, tS + pbuf * kRows + lane_off + part * 16);
+                tmem_ld16(x, tS + lane_off + part * 32 + hf * 16);
                 const float c = p.scale_log2;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 l = l4[q4];
+                    const float4 l = l4[hf * 4 + q4];
                     const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * q4 + e;
-                        pv[j] = fast_exp2(fmaf(__uint_as_float(x.r[j]), c, -lv[e]));
-                    }
-                }
-                if (!plain) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int row = rb + j;
-                        if (!(key_ok && row < p.SQ && (!p.causal || key <= row)))
-                            pv[j] = 0.f;
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        pv[hf * 16 + 4 * q4 + e] = fast_exp2(fmaf(__uint_as_float(x.r[4 * q4 + e]), c, -lv[e]));
                 }
             }
+            if (!plain) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(pb + sw128(ln, part * 2 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int j = 0; j < 32; ++j) {
+                    const int row = rb + j;
+                    if (!(key_ok && row < p.SQ && (!p.causal || key <= row)))
+                        pv[j] = 0.f;
+                }
             }
+            // P (16-bit pairs) into the first 16 of this thread's 32 S^T columns
             {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2<T>(pv[2 * e], pv[2 * e + 1]);
+                tmem_st16(w, tS + lane_off + part * 32);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.p_ready);
+            got = __all_sync(kAll, mbar_wait_bounded(&bars.dp_full, it & 1, wait_ns));
+            if (!got) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
                 Cols16 x;
-                tmem_ld16(x, tP + pbuf * kRows + lane_off + part * 16);
-                tc_fence_before();
-                mbar_arrive(&bars.sd_free[pbuf]);  // S^T and dP^T of this step are read
+                tmem_ld16(x, tP + lane_off + part * 32 + hf * 16);
                 const float sc = p.scale;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 d = d4[q4];
+                    const float4 d = d4[hf * 4 + q4];
                     const float dv[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * q4 + e;
-                        const float ds = pv[j] * sc * (__uint_as_float(x.r[j]) - dv[e]);
+                        const int j = hf * 16 + 4 * q4 + e;
+                        const float ds = pv[j] * sc * (__uint_as_float(x.r[4 * q4 + e]) - dv[e]);
                         // rows past SQ: p = 0, and their delta is not defined
                         pv[j] = plain || pv[j] != 0.f ? ds : 0.f;
                     }
                 }
             }
+            // dS^T (K-major over rows): rows 32 part .. + 31 are chunks 4 (part & 1) ..
+            // + 3 of the 128-byte row of this key in row half part >> 1
+            unsigned char* sb = sS + (part >> 1) * kHalf128;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     w[e] = pack2<T>(pv[8 * c + 2 * e], pv[8 * c + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(sb + sw128(ln, part * 2 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(sb + sw128(ln, (part & 1) * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars.ds_ready[pbuf]);
+            mbar_arrive(&bars.ds_ready);
+            // dQ^T of the step (lane = d, columns = rows): read, hand the columns
+            // back for the next dP^T, then add into the float32 accumulator
+            got = __all_sync(kAll, mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
+            if (!got) {
+                fault = true;
+                break;
+            }
+            tc_fence_after();
+            {
+                Cols32 x;
+                tmem_ld32(x, tP + lane_off + part * 32);
+                tc_fence_before();
+                mbar_arrive(&bars.dq_free);
+                float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + rb) * kD + ln;
+                const int rows = min(32, p.SQ - rb);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < rows)
+                        red_add(dst + static_cast<int64_t>(j) * kD, __uint_as_float(x.r[j]));
+            }
         }
         if (!fault && n > 0)
             fault = !__all_sync(kAll, !*abort_flag && mbar_wait_bounded(&bars.mma_done, 0, wait_ns));
@@ -775,9 +766,9 @@ int launch_vjp_tc(const VjpParams& p, int dtype, bool f32_out, cudaStream_t st, 
         if (rc == PA_OK)
             rc = encode_rows(&vmap, p.v, dt, p.SK, p.B * p.HK, kKeys);
         if (rc == PA_OK && p.SQ > 0) {
-            rc = encode_rows(&qmap, p.q, dt, p.SQ, p.B * p.HQ, kRows);
+            rc = encode_rows(&qmap, p.q, dt, p.SQ, p.B * p.HQ, kBRows);
             if (rc == PA_OK)
-                rc = encode_rows(&gmap, p.g, dt, p.SQ, p.B * p.HQ, kRows);
+                rc = encode_rows(&gmap, p.g, dt, p.SQ, p.B * p.HQ, kBRows);
         } else {
             qmap = gmap = kmap;  // no row tile is ever loaded
         }
