@@ -246,17 +246,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t r = (static_cast<int64_t>(b) * p.HQ + h) * p.SQ + i;
             const uint4* y = reinterpret_cast<const uint4*>(static_cast<const T*>(p.y) + r * kD + part * 64);
             const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.g) + r * kD + part * 64);
+            float d8[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint4 yv = y[c], gv = g[c];
                 const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+                float acc = 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 a = unpack2<T>(ya[e]), bb = unpack2<T>(ga[e]);
-                    dpart = fmaf(a.x, bb.x, dpart);
-                    dpart = fmaf(a.y, bb.y, dpart);
+                    acc = fmaf(a.x, bb.x, acc);
+                    acc = fmaf(a.y, bb.y, acc);
                 }
+                d8[c] = acc;
             }
+            dpart = ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
             float4* acc = reinterpret_cast<float4*>(p.dq_sum + r * kD + part * 64);
 #pragma unroll
             for (int c = 0; c < 16; ++c)
@@ -273,8 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            // raw scores (scale > 0 commutes with the maximum); eight
+            // independent partial maxima and sums keep the dependency chains short
             float sc[64];
-            float pm = -INFINITY;
+            float pm8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                pm8[e] = -INFINITY;
             const int kbase = t * kKeys + part * 64;
             const bool edge = kbase + 63 >= nk || (p.causal && kbase + 63 > i0);  // warp-uniform
 #pragma unroll
@@ -283,24 +292,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(x, tS + s * kKeys + lane_off + part * 64 + c * 32);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    float v = __uint_as_float(x.r[j]) * p.scale_log2;
+                    float v = __uint_as_float(x.r[j]);
                     if (edge) {
                         const int key = kbase + c * 32 + j;
                         if (key >= p.SK || (p.causal && key > i))
                             v = -INFINITY;
                     }
                     sc[c * 32 + j] = v;
-                    pm = fmaxf(pm, v);
+                    pm8[j & 7] = fmaxf(pm8[j & 7], v);
                 }
             }
             tc_fence_before();
             mbar_arrive(&bars.s_free[s]);
-            const float mt = fmaxf(m, pm);
+            const float pm = fmaxf(fmaxf(fmaxf(pm8[0], pm8[1]), fmaxf(pm8[2], pm8[3])),
+                                   fmaxf(fmaxf(pm8[4], pm8[5]), fmaxf(pm8[6], pm8[7])));
+            const float mt = fmaxf(m, pm * p.scale_log2);  // base-2 units
             if (mt != -INFINITY) {
-                float sum = 0.f;
+                const float c2 = p.scale_log2;
+                float s8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    s8[e] = 0.f;
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
-                    sum += fast_exp2(sc[j] - mt);
+                    s8[j & 7] += fast_exp2(fmaf(sc[j], c2, -mt));
+                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                 l = l * fast_exp2(m - mt) + sum;
                 m = mt;
             }
