@@ -118,17 +118,28 @@ def aggregate(rank_bytes: int, rank_ms: float, world: int):
     return total / (ms_max * 1e-3) / 1e9, ms_max, int(total)
 
 
-def kernel_sources_sha256() -> str:
-    """Hash of the CUDA sources and the C header with comments and whitespace
+# The sources each kernel family is built from: a capture stays valid while
+# these are unchanged (comments and whitespace aside).
+KERNEL_SOURCES = {
+    "decode": ["pa_kernels.cuh", "pa_common.cuh", "pa_ptx.cuh", "pa_inst_f32.cu", "pa_inst_f16.cu",
+               "pa_inst_bf16.cu", "pa_host.cu", "../../include/pa_decode.h"],
+    "prefill_tc": ["pa_prefill_tc.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_common.cuh", "pa_host.cu"],
+    "vjp": ["pa_vjp.cu", "pa_vjp_tc.cu", "pa_vjp.cuh", "pa_tc.cuh", "pa_ptx.cuh",
+            "../../include/pa_attention_vjp.h"],
+}
+
+
+def kernel_sources_sha256(family: str = "decode") -> str:
+    """Hash of the sources of one kernel family with comments and whitespace
     removed, so that a comment edit does not retire a capture of the same code."""
     import hashlib
     import re
 
     token = re.compile(r'("(?:\\.|[^"\\\n])*")|(//[^\n]*)|(/\*.*?\*/)', re.S)
-    files = sorted((ROOT / "paged_kv_cache_182_gb300" / "csrc").glob("*.cu*"))
-    files.append(ROOT / "include" / "pa_decode.h")
+    csrc = ROOT / "paged_kv_cache_182_gb300" / "csrc"
     h = hashlib.sha256()
-    for f in files:
+    for name in KERNEL_SOURCES[family]:
+        f = (csrc / name).resolve()
         code = token.sub(lambda m: m.group(1) or " ", f.read_text())
         h.update(f.name.encode())
         h.update(" ".join(code.split()).encode())
@@ -144,7 +155,7 @@ def partition_kernel_name(spec):
     return "pa_mmat_kernel" if spec.group * spec.NQ <= 8 else "pa_mma_kernel"
 
 
-def captured_traffic(kernel: str, workload: str):
+def captured_traffic(kernel: str, workload: str, family: str = "decode"):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, or None when there is none or the kernel sources changed since."""
     path = ROOT / "profiles" / f"{kernel}_{workload}.md"
@@ -155,7 +166,7 @@ def captured_traffic(kernel: str, workload: str):
         key, sep, val = line.strip().partition(": ")
         if sep and key in ("csrc_sha256", "traffic_bytes_per_launch"):
             fields[key] = val.strip()
-    if fields.get("csrc_sha256") != kernel_sources_sha256():
+    if fields.get("csrc_sha256") != kernel_sources_sha256(family):
         return None
     v = fields.get("traffic_bytes_per_launch")
     return int(v) if v else None
@@ -475,6 +486,13 @@ def prefill_timing(device, steps=20, warmup=3):
             "us_per_call": round(us, 1), "new_tokens_per_s": round(s.B * s.NQ / (us * 1e-6), 1),
             "flops_per_call": flops, "TFLOP_per_s": round(tflops, 2),
             "frac_of_measured_tensor_peak": round(tflops / peak, 4),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": captured_traffic("pa_prefill_tc_kernel", "prefill_fp16",
+                                                     "prefill_tc"),
+                         "kernel": "pa_prefill_tc_kernel (and the store of the new rows)",
+                         "peak_kind": "bf16_tflops of MEASURED_PEAKS.json (burst); f16 has the "
+                                      "same nominal dense rate"},
             "launches_per_call": (binding.kernel_launches() - launches) // steps,
             "l2": f"{len(plans)} copies of the KV pools ({pool_bytes // 2**20} MiB) rotated"}
 
@@ -510,6 +528,11 @@ def vjp_timing(device, steps=10, warmup=3):
             "us_per_call": round(us, 1), "tokens_per_s": round(s.B * s.SQ / (us * 1e-6), 1),
             "flops_per_call": flops, "TFLOP_per_s": round(tflops, 2),
             "frac_of_measured_tensor_peak": round(tflops / peak, 4),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": captured_traffic("vjp_main_tc", "vjp_bf16", "vjp"),
+                         "kernel": "the whole call: vjp_stats_tc, vjp_main_tc, vjp_dq_round",
+                         "peak_kind": "bf16_tflops of MEASURED_PEAKS.json (burst)"},
             "launches_per_call": (binding.kernel_launches() - launches) // steps,
             "l2": "inputs and outputs (about 350 MB) larger than L2"}
 
