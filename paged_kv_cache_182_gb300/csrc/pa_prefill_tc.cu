@@ -125,9 +125,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.v_empty[s], 1);
             mbar_init(&bars.s_full[s], 1);
-            mbar_init(&bars.s_free[s], kTcSoftmax);
+            mbar_init(&bars.s_free[s], kTcSoftmax / 32);  // one arrival per softmax warp
         }
-        mbar_init(&bars.p_full, kTcSoftmax);
+        mbar_init(&bars.p_full, kTcSoftmax / 32);
         mbar_init(&bars.o_done, 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -324,7 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.s_free[s]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.s_free[s]);
             // the other half of the row's maximum
             bars.xchg[s][part][row] = pm;
             if (pair_bar_or(pair_bar, !got)) {
@@ -396,7 +398,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.p_full);
         }
         if (ok)
             ok = __all_sync(kFull, !fault && mbar_wait_bounded(&bars.o_done, (ntiles - 1) & 1, kWaitLimitNs));

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
             mbar_init(&bars.s_full[s], 1);
-            mbar_init(&bars.s_free[s], kSoftmax);
+            mbar_init(&bars.s_free[s], kSoftmax / 32);  // one arrival per softmax warp
         }
         bars.abort = 0;
         fence_mbar_init();
@@ -303,7 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.s_free[s]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.s_free[s]);
             const float pm = fmaxf(fmaxf(fmaxf(pm8[0], pm8[1]), fmaxf(pm8[2], pm8[3])),
                                    fmaxf(fmaxf(pm8[4], pm8[5]), fmaxf(pm8[6], pm8[7])));
             const float mt = fmaxf(m, pm * p.scale_log2);  // base-2 units
@@ -398,10 +400,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.p_ready, kMSoftmax);
-        mbar_init(&bars.ds_ready, kMSoftmax);
+        // the softmax warps arrive once each (lane 0, after the warp's fences and a __syncwarp)
+        mbar_init(&bars.p_ready, kMSoftmax / 32);
+        mbar_init(&bars.ds_ready, kMSoftmax / 32);
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_free, kMSoftmax);
+        mbar_init(&bars.dq_free, kMSoftmax / 32);
         mbar_init(&bars.mma_done, 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -621,7 +624,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
             tc_fence_before();
-            mbar_arrive(&bars.p_ready);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.p_ready);
             got = __all_sync(kAll, mbar_wait_bounded(&bars.dp_full, it & 1, wait_ns));
             if (!got) {
                 fault = true;
@@ -659,7 +664,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars.ds_ready);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.ds_ready);
             // dQ^T of the step (lane = d, columns = rows): read, hand the columns
             // back for the next dP^T, then add into the float32 accumulator
             got = __all_sync(kAll, mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
@@ -672,7 +679,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                 Cols32 x;
                 tmem_ld32(x, tP + lane_off + part * 32);
                 tc_fence_before();
-                mbar_arrive(&bars.dq_free);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars.dq_free);
                 float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + rb) * kD + ln;
                 const int rows = min(32, p.SQ - rb);
 #pragma unroll
