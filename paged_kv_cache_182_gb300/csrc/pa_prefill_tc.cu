@@ -59,9 +59,12 @@ constexpr int kTcHalf = 16384;      // one 64-column half of a 128-row tile, byt
 constexpr int kTcSoftmax = 256;     // softmax threads (warps 0-7)
 constexpr int kTcThreads = 352;     // warps 0-7 softmax, 8-9 TMA (K, V), 10 MMA
 constexpr uint32_t kTcCols = 512;   // tensor-memory columns: S0 | S1 | O | (unused)
-// Q 2, K 4, V 4, P 4 halves, then the barriers and the row-maximum exchange;
-// the dynamic shared-memory base must be 1024-aligned (checked at entry)
-constexpr int kTcSmem = 14 * kTcHalf + 3072;
+constexpr int kTcStages = 3;        // K and V rings
+// Q 2 halves, K and V rings (kTcStages x 2 halves each), then the barriers
+// and the row-maximum exchange; the dynamic shared-memory base must be
+// 1024-aligned (checked at entry)
+constexpr int kTcSmem = (2 + 4 * kTcStages) * kTcHalf + 3072;
+static_assert(kTcSmem <= 232448, "prefill shared memory");
 
 struct PrefillTcParams {
     const int32_t* table;     // [B][maxb]
@@ -73,7 +76,10 @@ struct PrefillTcParams {
 };
 
 struct TcBars {
-    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, o_done;
+    // s_full, p_full and o_done alternate by key-tile parity (the S buffer);
+    // the K and V rings have kTcStages stages
+    uint64_t q_full, k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages], s_full[2],
+        p_full[2], o_done[2];
     uint32_t tmem;
     int abort;
     float xchg[2][2][kTcTile];  // [tile parity][column half][row]: partial row maxima, then sums
@@ -93,11 +99,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     unsigned char* base = smem_raw;
-    unsigned char* sQ = base;                  // 2 halves
-    unsigned char* sK = base + 2 * kTcHalf;    // 2 stages x 2 halves
-    unsigned char* sV = base + 6 * kTcHalf;    // 2 stages x 2 halves
-    unsigned char* sP = base + 10 * kTcHalf;   // P_hi (2 token halves), P_lo (2 token halves)
-    TcBars& bars = *reinterpret_cast<TcBars*>(base + 14 * kTcHalf);
+    unsigned char* sQ = base;                                // 2 halves
+    unsigned char* sK = base + 2 * kTcHalf;                  // kTcStages x 2 halves
+    unsigned char* sV = base + (2 + 2 * kTcStages) * kTcHalf;  // kTcStages x 2 halves
+    TcBars& bars = *reinterpret_cast<TcBars*>(base + (2 + 4 * kTcStages) * kTcHalf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // the last row tiles see the most keys: they are launched first, so that
@@ -119,16 +124,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (tid == 0) {
         mbar_init(&bars.q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.v_empty[s], 1);
-            mbar_init(&bars.s_full[s], 1);
-            mbar_init(&bars.s_free[s], kTcSoftmax / 32);  // one arrival per softmax warp
         }
-        mbar_init(&bars.p_full, kTcSoftmax / 32);
-        mbar_init(&bars.o_done, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.s_full[s], 1);
+            mbar_init(&bars.p_full[s], kTcSoftmax / 32);  // one arrival per softmax warp
+            mbar_init(&bars.o_done[s], 1);
+        }
         bars.abort = 0;
         fence_mbar_init();
     }
@@ -142,7 +148,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS0 = bars.tmem, tO = bars.tmem + 2 * kTcTile;  // S(t) at tS0 + 128 (t & 1)
+    // S(t) at tS0 + 128 (t & 1); P(t) overwrites it as 16-bit pairs (see the softmax)
+    const uint32_t tS0 = bars.tmem, tO = bars.tmem + 2 * kTcTile;
     volatile int* abort_flag = &bars.abort;
     auto fail = [&]() {
         *abort_flag = 1;
@@ -185,10 +192,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int row_next = entry(0);
         int issued = 0;
         for (int t = 0; t < ntiles; ++t) {
-            const int s = t & 1;
+            const int s = t % kTcStages;
             const int row0 = row_next;
-            if (t >= 2) {
-                bool ok = !*abort_flag && mbar_wait_bounded(&empty[s], ((t >> 1) - 1) & 1, kWaitLimitNs);
+            if (t >= kTcStages) {
+                bool ok = !*abort_flag && mbar_wait_bounded(&empty[s], ((t / kTcStages) - 1) & 1, kWaitLimitNs);
                 ok = __all_sync(kFull, ok);
                 if (!ok) {
                     if (lane == 0)
@@ -209,64 +216,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // no copy may land after the CTA's memory is released: wait (bounded)
         // for the last tile issued on each stage (and for q)
         if (lane == 0) {
-            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-                mbar_wait_bounded(&full[t & 1], (t >> 1) & 1, kWaitLimitNs);
+            for (int t = issued > kTcStages ? issued - kTcStages : 0; t < issued; ++t)
+                mbar_wait_bounded(&full[t % kTcStages], (t / kTcStages) & 1, kWaitLimitNs);
             if (!is_v)
                 mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 10) {
         // -------------------------------------------------------------- MMA issuer
+        // S(t + 1) goes into the S buffer that held P(t - 1): P(t - 1).V was
+        // issued before it by this thread, and the MMAs of one thread run in
+        // order.  A commit of S(t + 1) thus also covers P(t - 1).V.
         if (lane == 0) {
             bool ok = mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
             const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
-            const uint32_t phi = smem_u32(sP), plo = smem_u32(sP + 2 * kTcHalf);
             const uint32_t id_s = idesc<kBf>(kTcTile, false), id_o = idesc<kBf>(kTcD, true);
             // S(u) = Q K(u)^T over the head dimension (K-steps of 16 columns, four
-            // per 64-column half) into S buffer u & 1, once K(u) has landed and
-            // the softmax has read S(u - 2) from that buffer; K's stage is
-            // released when these MMAs complete
+            // per 64-column half) into S buffer u & 1, once K(u) has landed; K's
+            // stage is released when these MMAs complete
             auto issue_s = [&](int u) {
-                const int su = u & 1;
-                bool good = !*abort_flag && mbar_wait_bounded(&bars.k_full[su], (u >> 1) & 1, kWaitLimitNs);
-                if (good && u >= 2)
-                    good = mbar_wait_bounded(&bars.s_free[su], ((u >> 1) - 1) & 1, kWaitLimitNs);
-                if (!good)
+                const int ku = u % kTcStages;
+                if (*abort_flag || !mbar_wait_bounded(&bars.k_full[ku], (u / kTcStages) & 1, kWaitLimitNs))
                     return false;
                 tc_fence_after();
                 for (int ks = 0; ks < kTcD / 16; ++ks) {
                     const uint32_t o = (ks >> 2) * kTcHalf + (ks & 3) * 32;
-                    umma(tS0 + su * kTcTile, smem_desc(qa + o, 16, 1024),
-                         smem_desc(ka + su * 2 * kTcHalf + o, 16, 1024), id_s, ks > 0);
+                    umma(tS0 + (u & 1) * kTcTile, smem_desc(qa + o, 16, 1024),
+                         smem_desc(ka + ku * 2 * kTcHalf + o, 16, 1024), id_s, ks > 0);
                 }
-                umma_commit(&bars.s_full[su]);
-                umma_commit(&bars.k_empty[su]);
+                umma_commit(&bars.s_full[u & 1]);
+                umma_commit(&bars.k_empty[ku]);
                 return true;
             };
             if (ok && ntiles > 0)
                 ok = issue_s(0);
             for (int t = 0; t < ntiles && ok; ++t) {
-                const int s = t & 1;
+                const int sb = t & 1, vs = t % kTcStages;
                 if (t + 1 < ntiles && !issue_s(t + 1)) {
                     ok = false;
                     break;
                 }
-                ok = mbar_wait_bounded(&bars.p_full, t & 1, kWaitLimitNs);
+                ok = mbar_wait_bounded(&bars.p_full[sb], (t >> 1) & 1, kWaitLimitNs);
                 if (ok)
-                    ok = mbar_wait_bounded(&bars.v_full[s], (t >> 1) & 1, kWaitLimitNs);
+                    ok = mbar_wait_bounded(&bars.v_full[vs], (t / kTcStages) & 1, kWaitLimitNs);
                 if (!ok)
                     break;
                 tc_fence_after();
-                // O += P_hi V + P_lo V over the tile's keys: V is MN-major (its
-                // rows are keys, 64 columns of D per half, the halves 16 KB apart)
+                // O += P_hi V + P_lo V over the tile's keys.  P from tensor memory:
+                // keys 64 h + 16 j + (0 .. 15) of the high part at column
+                // 64 h + 8 j of the S buffer, the remainder 32 columns further;
+                // V is MN-major (its rows are keys, 64 columns of D per half, the
+                // halves 16 KB apart)
+                const uint32_t tP = tS0 + sb * kTcTile;
                 for (int part = 0; part < 2; ++part)
                     for (int ks = 0; ks < kTcTile / 16; ++ks) {
-                        const uint32_t pa = (part ? plo : phi) + (ks >> 2) * kTcHalf + (ks & 3) * 32;
-                        umma(tO, smem_desc(pa, 16, 1024), smem_desc(va + s * 2 * kTcHalf + ks * 2048, kTcHalf, 1024),
-                             id_o, t > 0 || part > 0 || ks > 0);
+                        const uint32_t pcol = (ks >> 2) * 64 + part * 32 + (ks & 3) * 8;
+                        umma_ts(tO, tP + pcol, smem_desc(va + vs * 2 * kTcHalf + ks * 2048, kTcHalf, 1024), id_o,
+                                t > 0 || part > 0 || ks > 0);
                     }
-                umma_commit(&bars.o_done);
-                umma_commit(&bars.v_empty[s]);
+                umma_commit(&bars.o_done[sb]);
+                umma_commit(&bars.v_empty[vs]);
             }
             if (!ok)
                 fail();
@@ -275,7 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
         // ---------------------------------------------- softmax and epilogue (rows)
         const int row = (warp & 3) * 32 + lane;  // tile row = tensor-memory lane
-        const int part = warp >> 2;              // columns [64 part, 64 part + 64)
+        const int part = warp >> 2;              // key columns [64 part, 64 part + 64)
         const int hg = row / p.T, tt = row - hg * p.T;
         const int r = r_base + tt;
         const bool real = r < p.NQ;
@@ -323,10 +332,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars.s_free[s]);
             // the other half of the row's maximum
             bars.xchg[s][part][row] = pm;
             if (pair_bar_or(pair_bar, !got)) {
@@ -352,58 +357,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (t * kTcTile + kTcTile > end) {  // uniform over the CTA
                 // the V stage has landed; the wait orders these stores after the
                 // copy's writes (and they come before p_full, which P.V waits for)
-                const bool landed =
-                    __all_sync(kFull, mbar_wait_bounded(&bars.v_full[s], (t >> 1) & 1, kWaitLimitNs));
+                const int vs = t % kTcStages;
+                const bool landed = __all_sync(
+                    kFull, mbar_wait_bounded(&bars.v_full[vs], (t / kTcStages) & 1, kWaitLimitNs));
                 fault |= !landed;
                 if (landed && tok >= end) {
-                    uint4* vrow = reinterpret_cast<uint4*>(sV + s * 2 * kTcHalf + part * kTcHalf + row * 128);
+                    uint4* vrow = reinterpret_cast<uint4*>(sV + vs * 2 * kTcHalf + part * kTcHalf + row * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         vrow[c] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            if (t > 0) {
-                // the previous tile's P.V is complete: P may be overwritten and
-                // O rescaled (warp-uniform: tcgen05.ld/st are warp-wide)
+            // O is rescaled only when a row maximum moved (warp-uniform: tcgen05
+            // ld/st are warp-wide), after P(t - 1).V has completed
+            if (t > 0 && __any_sync(kFull, alpha != 1.f)) {
                 const bool done = __all_sync(
-                    kFull, !fault && mbar_wait_bounded(&bars.o_done, (t - 1) & 1, kWaitLimitNs));
+                    kFull, !fault && mbar_wait_bounded(&bars.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, kWaitLimitNs));
                 fault |= !done;
                 if (done) {
                     tc_fence_after();
-                    if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            Cols32 x;
-                            tmem_ld32(x, tO + lane_off + col0 + c * 32);
+                    for (int c = 0; c < 2; ++c) {
+                        Cols32 x;
+                        tmem_ld32(x, tO + lane_off + col0 + c * 32);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
-                            tmem_st32(x, tO + lane_off + col0 + c * 32);
-                        }
+                        for (int j = 0; j < 32; ++j)
+                            x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
+                        tmem_st32(x, tO + lane_off + col0 + c * 32);
                     }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
             }
-            // P as high part + remainder, K-major A operand (128-byte swizzle):
-            // row `row`, keys 64 part + 8c .. + 7 in chunk c of token half `part`
+            // P as high part + remainder, packed 16-bit pairs, over this thread's
+            // own S columns (it has read them): keys 64 part + 2 e, 2 e + 1 of the
+            // high part at column 64 part + e, of the remainder at 64 part + 32 + e.
+            // S(t) was committed after P(t - 2).V, so that product is complete.
+            {
+                Cols32 hi, lo;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    split_pair<T>(sc[c * 8 + 2 * k], sc[c * 8 + 2 * k + 1], hi[k], lo[k]);
-                const uint32_t off = part * kTcHalf + sw128(row, c);
-                *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sP + 2 * kTcHalf + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                for (int e = 0; e < 32; ++e)
+                    split_pair<T>(sc[2 * e], sc[2 * e + 1], hi.r[e], lo.r[e]);
+                tmem_st32(hi, tS0 + s * kTcTile + lane_off + col0);
+                tmem_st32(lo, tS0 + s * kTcTile + lane_off + col0 + 32);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            fence_proxy_async_smem();
+            fence_proxy_async_smem();  // the zeroed V rows
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars.p_full);
+                mbar_arrive(&bars.p_full[s]);
         }
-        if (ok)
-            ok = __all_sync(kFull, !fault && mbar_wait_bounded(&bars.o_done, (ntiles - 1) & 1, kWaitLimitNs));
+        if (ok && ntiles > 0)
+            ok = __all_sync(kFull, !fault && mbar_wait_bounded(&bars.o_done[(ntiles - 1) & 1],
+                                                               ((ntiles - 1) >> 1) & 1, kWaitLimitNs));
         // the row sum over both halves, through the exchange slots of tile
         // parity ntiles & 1: the partner's last read of them came before the
         // last tile's barrier
