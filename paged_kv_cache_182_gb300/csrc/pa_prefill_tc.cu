@@ -105,11 +105,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcBars& bars = *reinterpret_cast<TcBars*>(base + (2 + 4 * kTcStages) * kTcHalf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the last row tiles see the most keys: they are launched first, so that
-    // the short ones fill the last wave
-    const int rt = p.tiles - 1 - static_cast<int>(blockIdx.x % p.tiles);
-    const int kh = (blockIdx.x / p.tiles) % p.KV;
-    const int b = blockIdx.x / (p.tiles * p.KV);
+    // the last row tiles see the most keys: all of them are launched first
+    // (row tile slowest), so that the short ones fill the last wave
+    const int rt = p.tiles - 1 - static_cast<int>(blockIdx.x / (p.B * p.KV));
+    const int kh = static_cast<int>(blockIdx.x % (p.B * p.KV)) % p.KV;
+    const int b = static_cast<int>(blockIdx.x % (p.B * p.KV)) / p.KV;
     const int r_base = rt * p.T;
     const int r_last = min(r_base + p.T, p.NQ) - 1;  // last new row of the tile
     const int cap = p.maxb * p.BLOCK - p.NQ;         // largest past the table can hold

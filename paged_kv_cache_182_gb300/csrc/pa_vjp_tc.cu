@@ -122,8 +122,8 @@ __device__ __forceinline__ float2 unpack2(uint32_t w)
 }
 
 // ---------------------------------------------------------------------------
-// Row statistics.  grid = B * HQ * ceil(SQ / 128), the row tiles that see the
-// most keys (causal) first.
+// Row statistics.  grid = B * HQ * ceil(SQ / 128), row tile slowest: the row
+// tiles that see the most keys (causal) are launched first.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     vjp_stats_tc(const __grid_constant__ VjpParams p, const __grid_constant__ CUtensorMap qmap,
@@ -142,9 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tiles = (p.SQ + kSRows - 1) / kSRows;
-    const int rt = tiles - 1 - static_cast<int>(blockIdx.x % tiles);
-    const int h = (blockIdx.x / tiles) % p.HQ;
-    const int b = blockIdx.x / (tiles * p.HQ);
+    // row tile slowest: every CTA of a row tile goes before those of the next
+    const int rt = tiles - 1 - static_cast<int>(blockIdx.x / (p.B * p.HQ));
+    const int h = static_cast<int>(blockIdx.x % (p.B * p.HQ)) % p.HQ;
+    const int b = static_cast<int>(blockIdx.x % (p.B * p.HQ)) / p.HQ;
     const int kh = h / p.groups;
     const int i0 = rt * kSRows;
     const int nk = p.causal ? min(p.SK, i0 + kSRows) : p.SK;
