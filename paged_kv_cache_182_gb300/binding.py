@@ -267,8 +267,11 @@ class Plan:
 
     def run(self, stream=None):
         """Launch on ``stream`` (default: torch's current stream); returns ``out``."""
-        with torch.cuda.device(self.device):
+        if torch.cuda.current_device() == self.device.index:
             rc = LIB.pa_decode(*self._args, _stream_handle(stream))
+        else:
+            with torch.cuda.device(self.device):
+                rc = LIB.pa_decode(*self._args, _stream_handle(stream))
         if rc != 0:
             raise PagedAttentionError(rc)
         return self.out

@@ -286,6 +286,31 @@ int prepare_func(const void* fn, int threads, int smem, int* occ, int* sms)
     return PA_OK;
 }
 
+// The opt-in shared-memory limit per block of the current device, asked of the
+// runtime once per device.
+int device_smem_optin(int* out)
+{
+    constexpr int kDevices = 64;
+    static std::atomic<int> cached[kDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (dev >= 0 && dev < kDevices) {
+        const int v = cached[dev].load(std::memory_order_relaxed);
+        if (v > 0) {
+            *out = v;
+            return PA_OK;
+        }
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (dev >= 0 && dev < kDevices)
+        cached[dev].store(v, std::memory_order_relaxed);
+    *out = v;
+    return PA_OK;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
@@ -550,10 +575,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
         stage_end = vnew_off + NQ * D * es;
     }
     const int stage_bytes = static_cast<int>(align_up(stage_end, 1024));
-    int dev = 0, smem_optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-            cudaSuccess)
+    int smem_optin = 0;
+    if (device_smem_optin(&smem_optin) != PA_OK)
         return PA_ERR_CUDA;
     const int slack = 1024;  // alignment of the dynamic shared-memory base
     // consumer scratch: tensor-core path, (max, sum) tables, one merge round of
