@@ -1124,6 +1124,9 @@ struct PrefillAppendParams {
 __global__ void __launch_bounds__(256)
     pa_prefill_append_kernel(const __grid_constant__ PrefillAppendParams a)
 {
+    // the tensor-core prefill that follows may start its set-up now; it waits
+    // for this grid's completion before it reads the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long per = a.rows * a.vpr;
     if (i >= 2 * per)

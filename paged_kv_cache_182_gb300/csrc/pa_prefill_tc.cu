@@ -191,6 +191,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         int row_next = entry(0);
         int issued = 0;
+        // launched as a programmatic dependent of the store of the new rows:
+        // the cache is read only once that grid has completed
+        grid_dependency_wait();
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kTcStages;
             const int row0 = row_next;
@@ -528,8 +531,20 @@ int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, c
     const long long grid = static_cast<long long>(B) * KV * prm.tiles;
     if (grid >= (1ll << 31))
         return PA_ERR_BAD_DIMS;
-    fn<<<static_cast<unsigned>(grid), kTcThreads, kTcSmem, st>>>(prm, qmap, kmap, vmap);
-    if (cudaGetLastError() != cudaSuccess)
+    // programmatic dependent launch: the CTAs set up (barriers, tensor memory,
+    // the query tile) while the store of the new rows finishes; the TMA
+    // producers wait for it before reading the cache
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fn, prm, qmap, kmap, vmap) != cudaSuccess)
         return PA_ERR_CUDA;
     if (launches)
         ++*launches;
