@@ -120,6 +120,16 @@ typedef struct pa_opts {
      *                      undefined; zero the split counters again after it) */
     unsigned long long wait_limit_ns;
     int debug_withhold_stage;
+    /* inputs_unchanged = 1: the caller guarantees that the kernel enqueued on
+     * `stream` just before this call writes none of q, k_cache, v_cache,
+     * block_table, seq_lens, k_new, v_new (for example: the previous decode
+     * step of the same batch).  The partition kernel then reads them (the
+     * lengths, the schedule, the table, the first stages of K and V) before
+     * that kernel has completed; it still waits for it before writing out or
+     * the workspace.  0 (default): every input is read after it.  Ignored by
+     * pa_decode_positions, pa_decode_host and pa_prefill, which run their
+     * own kernels just before the decode. */
+    int inputs_unchanged;
 } pa_opts;
 
 /*

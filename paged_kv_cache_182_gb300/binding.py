@@ -54,6 +54,7 @@ class PaOpts(ctypes.Structure):
         ("merge_kernel", ctypes.c_int),
         ("wait_limit_ns", ctypes.c_ulonglong),
         ("debug_withhold_stage", ctypes.c_int),
+        ("inputs_unchanged", ctypes.c_int),
     ]
 
 
@@ -199,7 +200,7 @@ class Plan:
     def __init__(self, q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *,
                  scale: float, causal: bool = False, partitions: int = 0, out=None,
                  out_dtype=None, workspace=None, status=None, checked: bool = False,
-                 trace=None, merge_kernel: bool = False):
+                 trace=None, merge_kernel: bool = False, inputs_unchanged: bool = False):
         B, H, NQ, D = q.shape
         NB, BLOCK, KV, D2 = k_cache.shape
         if (D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape)
@@ -244,7 +245,7 @@ class Plan:
             status=None if status is None else status.data_ptr(),
             trace_begin=None if trace is None else trace[0].cuda_event,
             trace_split=None if trace is None else trace[1].cuda_event,
-            merge_kernel=int(bool(merge_kernel)))
+            merge_kernel=int(bool(merge_kernel)), inputs_unchanged=int(bool(inputs_unchanged)))
         self._args = [_ptr(t) for t in tensors] + [_ptr(out), ctypes.c_float(scale), H, KV, D,
                                                    BLOCK, NQ, int(bool(causal)),
                                                    ctypes.byref(self.opts)]

@@ -77,6 +77,7 @@ struct SplitParams {
     int stage_off;
     unsigned long long wait_ns;  // limit of every mbarrier wait
     int withhold;      // test switch: each CTA's V producer leaves its stage withhold - 1 out (0: off)
+    int early;         // 1: the inputs are read before the grid-dependency wait (see pa_opts)
 };
 
 struct CombineParams {

@@ -672,6 +672,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     p.stage_off = stage_off;
     p.wait_ns = opts->wait_limit_ns ? opts->wait_limit_ns : kWaitLimitNs;
     p.withhold = opts->debug_withhold_stage > 0 ? opts->debug_withhold_stage : 0;
+    // the slot-patched decode runs right after its own append kernel
+    p.early = opts->inputs_unchanged && !positions ? 1 : 0;
 
     if (!launch)
         return PA_OK;
@@ -1082,6 +1084,7 @@ int pa_decode_host(const void* q, const void* k_cache, const void* v_cache,
                 return PA_ERR_CUDA;
     }
     pa_opts dev = *opts;
+    dev.inputs_unchanged = 0;  // the gather kernel just before writes the inputs
     dev.workspace = split ? ws : nullptr;
     dev.workspace_bytes = split;
     // a registered output is written by the kernels in place (no copy back)
@@ -1314,6 +1317,7 @@ int pa_prefill(const void* q, void* k_cache, void* v_cache, const int32_t* block
     pa_opts dopts = *opts;
     dopts.trace_begin = nullptr;
     dopts.trace_split = nullptr;
+    dopts.inputs_unchanged = 0;  // the store of the new rows (and chunk copies) come just before
     unsigned char* ws = static_cast<unsigned char*>(opts->workspace);
     const bool direct = NQ <= PA_MAX_NQ;  // one chunk: the caller's buffers serve the decode
     PrefillLayout l{};

@@ -725,7 +725,11 @@ constexpr long long kTablePrefetchBytes = 512 * 1024;
 // previous kernel on the stream may still write: the tensor maps are fetched
 // (producer warps), the block table is prefetched into L2 (coherent: a later
 // write by the previous kernel still wins), the parameters are warmed, the
-// barriers initialised; then the grid-dependency wait.
+// barriers initialised; then the grid-dependency wait.  With p.early (the
+// caller guarantees that the previous kernel writes no input) the wait is
+// left to the consumer warps, before their first write of the output or the
+// workspace: the schedule, the table entries and the first stages are then
+// read while the previous kernel finishes.
 __device__ __forceinline__ void kernel_entry(const SplitParams& p, const CUtensorMap& kmap,
                                              const CUtensorMap& vmap, const Smem& sm)
 {
@@ -741,7 +745,8 @@ __device__ __forceinline__ void kernel_entry(const SplitParams& p, const CUtenso
     const int w0 = param_word(p), w1 = param_word(kmap), w2 = param_word(vmap);
     asm volatile("" ::"r"(w0), "r"(w1), "r"(w2));
     init_cta(p, sm);
-    grid_dependency_wait();
+    if (!p.early)
+        grid_dependency_wait();
     grid_dependents_launch();
 }
 
@@ -1316,6 +1321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         produce<T, D, false>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
+    // consumers: the previous kernel's writes of the output and the workspace
+    // are complete before any of ours (p.early: the inputs were read earlier)
+    if (p.early)
+        grid_dependency_wait();
 
     using Math = SimtMath<T, D, RG>;
     uint32_t gt = 0;
@@ -1605,6 +1614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
+    // consumers: the previous kernel's writes of the output and the workspace
+    // are complete before any of ours (p.early: the inputs were read earlier)
+    if (p.early)
+        grid_dependency_wait();
 
     const int g = lane >> 2, qd = lane & 3;
     const int rg = warp % MT;
@@ -1931,6 +1944,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
+    // consumers: the previous kernel's writes of the output and the workspace
+    // are complete before any of ours (p.early: the inputs were read earlier)
+    if (p.early)
+        grid_dependency_wait();
 
     // MMA fragment coordinates: g = lane / 4 (accumulator row: token; operand
     // column: query row), qd = lane % 4 (accumulator columns 2 qd, 2 qd + 1:

@@ -378,14 +378,18 @@ def test_choose_partitions_matches_its_definition(lib):
 
 def test_failure_test_switches_are_off_by_default(lib):
     """A zero-filled pa_opts (what the binding builds) leaves the wait limit at
-    its default and withholds no stage."""
+    its default, withholds no stage and reads no input early; the binding's
+    structure lists the header's members in the header's order."""
     o = lib.PaOpts()
-    assert o.wait_limit_ns == 0 and o.debug_withhold_stage == 0
+    assert o.wait_limit_ns == 0 and o.debug_withhold_stage == 0 and o.inputs_unchanged == 0
     header = (ROOT / "include" / "pa_decode.h").read_text()
+    body = header[header.index("typedef struct pa_opts {"):header.index("} pa_opts;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    members = re.findall(r"\b(\w+)\s*;", body)
+    assert members == [f[0] for f in lib.PaOpts._fields_]
     assert "unsigned long long wait_limit_ns;" in header
     assert "int debug_withhold_stage;" in header
-    names = [f[0] for f in lib.PaOpts._fields_]
-    assert names[-2:] == ["wait_limit_ns", "debug_withhold_stage"]
+    assert "int inputs_unchanged;" in header
 
 
 def test_host_register_rejects_memory_that_is_not_page_locked(lib):

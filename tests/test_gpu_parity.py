@@ -320,3 +320,31 @@ def test_host_entry_point_registered_buffers(name):
     torch.cuda.synchronize()
     assert torch.equal(out, want)
     pu.check(out, pu.run_oracle(w), s.dtype, "f32", f"{name} registered host buffers")
+
+
+@pytest.mark.parametrize("name,P", [("ragged_fp16", 0), ("long_bf16", 32), ("gqa_fp16", 0),
+                                    ("causal_append_fp16", 0), ("tiny_fp32", 0)])
+def test_inputs_unchanged_back_to_back(name, P):
+    """pa_opts.inputs_unchanged: two batches with different data share the output
+    and the workspace and run back to back with no sync, each reading its
+    inputs before the previous decode has completed.  The writes still wait,
+    so the last call's batch is what out holds, and it matches the oracle."""
+    from paged_kv_cache_182_gb300 import binding
+
+    wa = W.make(small(name), seed=21)
+    wb = W.make(small(name), seed=22)
+    dev = "cuda"
+    da, db = wa.to(dev), wb.to(dev)
+    out = torch.empty(da.q.shape, dtype=torch.float32, device=dev)
+    s = wa.spec
+    ws = binding.new_workspace(s.B, s.H, s.KV, s.D, s.NQ, P, dev)
+    plans = [binding.Plan(*d.tensors(), scale=s.scale, causal=s.causal, partitions=P, out=out,
+                          workspace=ws, out_dtype=torch.float32, inputs_unchanged=True)
+             for d in (da, db)]
+    want = [pu.run_oracle(w) for w in (wa, wb)]
+    for last in (1, 0):
+        n = 11
+        for i in range(n):  # alternating, ending on plan `last`
+            plans[last ^ ((n - 1 - i) & 1)].run()
+        torch.cuda.synchronize()
+        pu.check(out, want[last], s.dtype, "f32", f"{name} back to back, last = {'ab'[last]}")
