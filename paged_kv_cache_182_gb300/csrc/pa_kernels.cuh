@@ -1321,10 +1321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         produce<T, D, false>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
-    // consumers: the previous kernel's writes of the output and the workspace
-    // are complete before any of ours (p.early: the inputs were read earlier)
-    if (p.early)
-        grid_dependency_wait();
+    // consumers: with p.early (the inputs read before the previous kernel
+    // completed), the grid-dependency wait comes at the first piece end,
+    // before any write of the output or the workspace
+    bool dep_ok = !p.early;
 
     using Math = SimtMath<T, D, RG>;
     uint32_t gt = 0;
@@ -1367,6 +1367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // Merge the token subsets of each row and finish the item.
+        if (!dep_ok) {
+            grid_dependency_wait();
+            dep_ok = true;
+        }
         const int span = nrg * RG;
         consumer_bar_sync();  // the previous item's readers are done with the buffer
         mt.store(mb_o, mb_m, mb_l, ts * span + rg * RG);
@@ -1614,10 +1618,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
-    // consumers: the previous kernel's writes of the output and the workspace
-    // are complete before any of ours (p.early: the inputs were read earlier)
-    if (p.early)
-        grid_dependency_wait();
+    // consumers: with p.early (the inputs read before the previous kernel
+    // completed), the grid-dependency wait comes at the first piece end,
+    // before any write of the output or the workspace
+    bool dep_ok = !p.early;
 
     const int g = lane >> 2, qd = lane & 3;
     const int rg = warp % MT;
@@ -1841,6 +1845,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
             mbar_arrive(&sm.q_free[piece & 1]);
 
+        if (!dep_ok) {
+            grid_dependency_wait();
+            dep_ok = true;
+        }
         // ---- piece end: merge the TS warps of each row group.  Each warp
         // leaves its running (max, sum) and its unscaled accumulators in
         // shared memory; the summing threads apply the factors 2^(m_t - M).
@@ -1944,10 +1952,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
-    // consumers: the previous kernel's writes of the output and the workspace
-    // are complete before any of ours (p.early: the inputs were read earlier)
-    if (p.early)
-        grid_dependency_wait();
+    // consumers: with p.early (the inputs read before the previous kernel
+    // completed), the grid-dependency wait comes at the first piece end,
+    // before any write of the output or the workspace
+    bool dep_ok = !p.early;
 
     // MMA fragment coordinates: g = lane / 4 (accumulator row: token; operand
     // column: query row), qd = lane % 4 (accumulator columns 2 qd, 2 qd + 1:
@@ -2160,6 +2168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
             mbar_arrive(&sm.q_free[piece & 1]);
 
+        if (!dep_ok) {
+            grid_dependency_wait();
+            dep_ok = true;
+        }
         // ---- piece end: row sums over the lanes of a row, then the merge of
         // the eight warps through shared memory
 #pragma unroll
