@@ -130,6 +130,14 @@ typedef struct pa_opts {
      * pa_decode_positions, pa_decode_host and pa_prefill, which run their
      * own kernels just before the decode. */
     int inputs_unchanged;
+    /* kernel = 0 (default): 16-bit inputs with D = 128 and more than 16 query
+     * rows per KV head (H/KV * NQ > 16) run the tcgen05 partition kernel
+     * (S^T = K Q^T and O^T += V^T P^T on the tensor cores, accumulators in
+     * tensor memory), when its shared memory fits beside two pipeline stages;
+     * every other case runs the mma.sync kernels.  1: the mma.sync kernels
+     * for every 16-bit case (same results within the tolerance; for
+     * comparison).  Other values: PA_ERR_UNSUPPORTED. */
+    int kernel;
 } pa_opts;
 
 /*

@@ -55,6 +55,7 @@ class PaOpts(ctypes.Structure):
         ("wait_limit_ns", ctypes.c_ulonglong),
         ("debug_withhold_stage", ctypes.c_int),
         ("inputs_unchanged", ctypes.c_int),
+        ("kernel", ctypes.c_int),
     ]
 
 
@@ -200,7 +201,8 @@ class Plan:
     def __init__(self, q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *,
                  scale: float, causal: bool = False, partitions: int = 0, out=None,
                  out_dtype=None, workspace=None, status=None, checked: bool = False,
-                 trace=None, merge_kernel: bool = False, inputs_unchanged: bool = False):
+                 trace=None, merge_kernel: bool = False, inputs_unchanged: bool = False,
+                 kernel: int = 0):
         B, H, NQ, D = q.shape
         NB, BLOCK, KV, D2 = k_cache.shape
         if (D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape)
@@ -245,7 +247,8 @@ class Plan:
             status=None if status is None else status.data_ptr(),
             trace_begin=None if trace is None else trace[0].cuda_event,
             trace_split=None if trace is None else trace[1].cuda_event,
-            merge_kernel=int(bool(merge_kernel)), inputs_unchanged=int(bool(inputs_unchanged)))
+            merge_kernel=int(bool(merge_kernel)), inputs_unchanged=int(bool(inputs_unchanged)),
+            kernel=int(kernel))
         self._args = [_ptr(t) for t in tensors] + [_ptr(out), ctypes.c_float(scale), H, KV, D,
                                                    BLOCK, NQ, int(bool(causal)),
                                                    ctypes.byref(self.opts)]
@@ -280,14 +283,17 @@ class Plan:
 
 def decode(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, *, scale: float,
            causal: bool = False, partitions: int = 0, out=None, out_dtype=None, workspace=None,
-           status=None, checked: bool = False, stream=None, merge_kernel: bool = False):
+           status=None, checked: bool = False, stream=None, merge_kernel: bool = False,
+           kernel: int = 0):
     """Decode attention on device tensors (see the module docstring); returns ``out``.
 
     A caller-provided ``workspace`` must be zero-filled before its first use
-    (see pa_opts.workspace); ``new_workspace`` makes one."""
+    (see pa_opts.workspace); ``new_workspace`` makes one.  ``kernel`` is
+    pa_opts.kernel (0 automatic, 1 the mma.sync kernels only)."""
     plan = Plan(q, k_cache, v_cache, block_table, seq_lens, k_new, v_new, scale=scale,
                 causal=causal, partitions=partitions, out=out, out_dtype=out_dtype,
-                workspace=workspace, status=status, checked=checked, merge_kernel=merge_kernel)
+                workspace=workspace, status=status, checked=checked, merge_kernel=merge_kernel,
+                kernel=kernel)
     return plan.run(stream)
 
 

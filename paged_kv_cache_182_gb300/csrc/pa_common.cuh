@@ -78,6 +78,7 @@ struct SplitParams {
     unsigned long long wait_ns;  // limit of every mbarrier wait
     int withhold;      // test switch: each CTA's V producer leaves its stage withhold - 1 out (0: off)
     int early;         // 1: the inputs are read before the grid-dependency wait (see pa_opts)
+    int tc_off;        // tcgen05 kernel: byte offset of its region (P, Q, barriers) from the base
 };
 
 struct CombineParams {
@@ -119,6 +120,11 @@ int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, c
                       const int32_t* seq_lens, void* out, float scale, int B, int H, int KV, int BLOCK,
                       int NQ, int maxb, int num_blocks, int dtype, int out_dtype, int* status,
                       cudaStream_t st, uint64_t* launches);
+// tcgen05 partition kernel for 32 query rows per pass at D = 128
+// (pa_decode_tc.cu): its shared region's bytes and the kernel of a type pair.
+constexpr int kTcRegionBytes = 51200;
+constexpr int kUmmaThreads = kThreads + 32;  // one more warp: the MMA issuer
+SplitFn pick_split_tc(int dtype, bool f32_out);
 CombineFn pick_combine_f32(int D);
 CombineFn pick_combine_f16(int D);
 CombineFn pick_combine_bf16(int D);

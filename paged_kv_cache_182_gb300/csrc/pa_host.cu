@@ -134,11 +134,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
 struct MapKey {
     const void* ptr;
     long long rows;
-    int KV, D, BLOCK, dtype;
+    int KV, D, BLOCK, dtype, halves;
     bool operator==(const MapKey& o) const
     {
         return ptr == o.ptr && rows == o.rows && KV == o.KV && D == o.D && BLOCK == o.BLOCK &&
-               dtype == o.dtype;
+               dtype == o.dtype && halves == o.halves;
     }
 };
 
@@ -151,11 +151,11 @@ int g_map_count = 0, g_map_next = 0;
 // Cache pool [num_blocks * BLOCK rows][KV][D] as a 3-D tensor; one box is one
 // block of one KV head: {D, 1, BLOCK}.
 int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dtype, int box_rows,
-              CUtensorMap* out)
+              bool halves, CUtensorMap* out)
 {
-    // 16-bit caches feed the tensor-core kernel: 64-column boxes, 128-byte swizzle.
+    // 16-bit caches feed the tensor-core kernels: 64-column boxes, 128-byte swizzle.
     const bool swz = dtype != PA_F32;
-    const MapKey key{base, static_cast<long long>(num_blocks) * BLOCK, KV, D, box_rows, dtype};
+    const MapKey key{base, static_cast<long long>(num_blocks) * BLOCK, KV, D, box_rows, dtype, halves ? 1 : 0};
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_map_count; ++i)
         if (g_map_keys[i] == key) {
@@ -171,7 +171,9 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // float32 (CUDA-core path): 3-D {D, KV, rows}, box {D, 1, box_rows}, no swizzle.
     // 16-bit (tensor-core path): 4-D {64, D/64, KV, rows}, box {64, D/64, 1,
-    // box_rows} -- one box brings both 64-column halves of box_rows token rows.
+    // box_rows} -- one box brings both 64-column halves of box_rows token rows
+    // -- or, with `halves` (the tcgen05 kernel), box {64, 1, 1, box_rows}: one
+    // half, so that each half of a tile is a run of 128-byte rows.
     // L2 fills no wider than one token row of one KV head: with 128-byte rows
     // (D = 64, 16-bit) a 256-byte promotion would also fetch the neighbouring
     // head's row, which another CTA reads at another time
@@ -185,7 +187,7 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
                               static_cast<cuuint64_t>(key.rows)};
         cuuint64_t strides[3] = {128u, static_cast<cuuint64_t>(D) * es,
                                  static_cast<cuuint64_t>(KV) * D * es};
-        cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(D / 64), 1u,
+        cuuint32_t box[4] = {64u, halves ? 1u : static_cast<cuuint32_t>(D / 64), 1u,
                              static_cast<cuuint32_t>(box_rows)};
         cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
         rc = enc(&map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -506,6 +508,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
         return PA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale))
         return PA_ERR_BAD_DIMS;
+    if (opts->kernel != 0 && opts->kernel != 1)
+        return PA_ERR_UNSUPPORTED;
     if (B == 0)
         return PA_OK;
     if (B > kMaxBatch)
@@ -582,29 +586,46 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // consumer scratch: tensor-core path, (max, sum) tables, one merge round of
     // kObufFloats floats of merge rounds and two query-row buffers; CUDA-core
     // path, per-warp states
-    const int qbuf_off = 2048 + kObufFloats * 4;
+    int qbuf_off = 2048 + kObufFloats * 4;
     const int merge_bytes = mma ? qbuf_off + 2 * ROWS * q_row_bytes(D)
                                 : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4 +
                                       kConsumerWarps * RG * 8;
-    const int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));
+    int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));
+    // The tcgen05 kernel (32-row passes at D = 128): the (max, sum) tables,
+    // the two query-row buffers, then its own region (P and query tiles,
+    // barriers; the split merge's factors share the P tiles), when two stages
+    // still fit after it.
+    int tc_off = 0;
+    bool tc32 = false;
+    if (mma && MT == 2 && D == 128 && opts->kernel == 0) {
+        const int t_off = static_cast<int>(align_up(merge_off + 2048 + 2 * ROWS * q_row_bytes(D), 1024));
+        const int t_stage = static_cast<int>(align_up(t_off + kTcRegionBytes, 1024));
+        if ((smem_optin - slack - t_stage) / stage_bytes >= 2) {
+            tc32 = true;
+            qbuf_off = 2048;
+            tc_off = t_off;
+            stage_off = t_stage;
+        }
+    }
     int stages = (smem_optin - slack - stage_off) / stage_bytes;
-    if (stages > kMaxStages)
-        stages = kMaxStages;
+    if (stages > (tc32 ? kMaxStages / 2 : kMaxStages))  // tcgen05: K and V released apart
+        stages = tc32 ? kMaxStages / 2 : kMaxStages;
     if (stages < 2)
         return PA_ERR_UNSUPPORTED;
     const int smem = slack + stage_off + stages * stage_bytes;
 
     CUtensorMap kmap, vmap;
-    int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, &kmap);
+    int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, tc32, &kmap);
     if (rc == PA_OK)
-        rc = cache_map(v_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, &vmap);
+        rc = cache_map(v_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, tc32, &vmap);
     if (rc != PA_OK)
         return rc;
 
-    const SplitFn split =
-        pick_split(dtype, out_dtype == PA_F32 && dtype != PA_F32, D, mma ? MT : RG);
+    const bool f32_out = out_dtype == PA_F32 && dtype != PA_F32;
+    const SplitFn split = tc32 ? pick_split_tc(dtype, f32_out) : pick_split(dtype, f32_out, D, mma ? MT : RG);
     int occ = 1, sms = 1;
-    rc = prepare_func(reinterpret_cast<const void*>(split), kThreads, smem, &occ, &sms);
+    const int threads = tc32 ? kUmmaThreads : kThreads;
+    rc = prepare_func(reinterpret_cast<const void*>(split), threads, smem, &occ, &sms);
     if (rc != PA_OK)
         return rc;
 
@@ -650,7 +671,10 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
         grid = records;
     p.qbuf_off = qbuf_off;
     p.box_rows = box_rows;
-    p.empty_count = mma ? (TT / TPW) * row_groups(MT) : kConsumerWarps;
+    // warps that release a stage; the tcgen05 kernel's MMA commits release
+    // its K and V parts (one arrival each)
+    p.empty_count = tc32 ? 1 : mma ? (TT / TPW) * row_groups(MT) : kConsumerWarps;
+    p.tc_off = tc_off;
     p.checked = opts->checked ? 1 : 0;
     p.R = R;
     p.rows_per_cta = rows_per_cta;
@@ -696,7 +720,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;

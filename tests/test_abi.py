@@ -105,6 +105,8 @@ def test_rejects_invalid_arguments(lib):
     assert call(lib, q=ctypes.c_void_p(0x10008)) == -4
     assert call(lib, partitions=0) == -5
     assert call(lib, partitions=0, workspace=0x100010, workspace_bytes=1 << 30) == -4
+    assert call(lib, kernel=2) == -3
+    assert call(lib, kernel=-1, batch=0) == -3  # checked before the empty-batch return
 
 
 def test_batch_limit_is_unsupported_not_a_workspace_limit(lib):
@@ -390,6 +392,7 @@ def test_failure_test_switches_are_off_by_default(lib):
     assert "unsigned long long wait_limit_ns;" in header
     assert "int debug_withhold_stage;" in header
     assert "int inputs_unchanged;" in header
+    assert o.kernel == 0 and "int kernel;" in body
 
 
 def test_host_register_rejects_memory_that_is_not_page_locked(lib):
