@@ -256,8 +256,12 @@ size_t pa_host_workspace_bytes(int batch, int max_blocks, int H, int KV, int D, 
  * kernel here lays every (sequence, row group, KV head) segment end to end,
  * cut into stage-sized units, and gives each of its persistent CTAs an equal
  * share of the cost (units plus a fixed charge per segment); a segment is
- * split where a CTA's share ends inside it.  This call repeats that
- * arithmetic on the host for given lengths.
+ * split where a CTA's share ends inside it.  Splits are merged by the last
+ * CTA to finish a piece of the segment, which costs it about four stages, so
+ * when the segments are no more than those CTAs and the longest is at most a
+ * CTA's share of the stages plus four, every CTA takes one whole segment
+ * instead (none split; this assumes the default in-kernel merge).  This call
+ * repeats that arithmetic on the host for given lengths.
  *   host_seq_lens  HOST int32 [batch] cached tokens per sequence, or NULL: all
  *                  sequences hold max_len tokens
  *   max_len        the table's capacity in tokens (max_blocks * BLOCK): lengths

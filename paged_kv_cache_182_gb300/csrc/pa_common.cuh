@@ -23,6 +23,17 @@ constexpr int kMaxGrid = 1024;      // partition-kernel CTAs at most (sizes the 
 constexpr int kPieceStages = 1;   // automatic schedule: stages charged per segment
 constexpr int kPieceStages2 = 6;  // the same with two 16-row groups per CTA pass
 constexpr long long kMinCtaCost = 4;  // automatic schedule: stages of cost a CTA takes at least
+constexpr long long kMergeStages = 4;  // automatic schedule: what the in-kernel merge of a split
+                                       // segment costs its last CTA, in stages (measured)
+
+// Automatic schedule with the in-kernel merge: whole segments, one per CTA
+// (none split, nothing merged), when the S segments are no more than the G
+// CTAs the split would use and the longest, max_units stages, is at most a
+// CTA's share of the W real stages plus the merge that a split costs.
+__host__ __device__ inline bool whole_segments(long long S, long long G, long long W, long long max_units)
+{
+    return S <= G && max_units * G <= W + kMergeStages * G;
+}
 
 // CTAs of `grid` that the automatic schedule gives units to, for total cost C
 // over `segments` segments: every CTA at least kMinCtaCost stages of cost (a
@@ -79,6 +90,7 @@ struct SplitParams {
     int withhold;      // test switch: each CTA's V producer leaves its stage withhold - 1 out (0: off)
     int early;         // 1: the inputs are read before the grid-dependency wait (see pa_opts)
     int tc_off;        // tcgen05 kernel: byte offset of its region (P, Q, barriers) from the base
+    int stages_v;      // tcgen05 kernel: V ring depth (stages: the K ring's; stage_bytes: one tile)
 };
 
 struct CombineParams {
@@ -96,6 +108,7 @@ struct CombineParams {
 };
 
 using SplitFn = void (*)(SplitParams, CUtensorMap, CUtensorMap);
+using SplitTcFn = void (*)(SplitParams, CUtensorMap, CUtensorMap, CUtensorMap);  // + the query map
 using CombineFn = void (*)(CombineParams);
 
 // Kernel tables, one per input element type (pa_inst_*.cu).  float32 inputs
@@ -121,10 +134,13 @@ int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, c
                       int NQ, int maxb, int num_blocks, int dtype, int out_dtype, int* status,
                       cudaStream_t st, uint64_t* launches);
 // tcgen05 partition kernel for 32 query rows per pass at D = 128
-// (pa_decode_tc.cu): its shared region's bytes and the kernel of a type pair.
-constexpr int kTcRegionBytes = 51200;
+// (pa_decode_tc.cu): its shared region's bytes (P^T and query tiles,
+// barriers, reductions), one K or V tile's bytes, its threads, and the kernel
+// of a type pair.
+constexpr int kTcRegionBytes = 26624;
+constexpr int kTcTileBytes = 32768;
 constexpr int kUmmaThreads = kThreads + 32;  // one more warp: the MMA issuer
-SplitFn pick_split_tc(int dtype, bool f32_out);
+SplitTcFn pick_split_tc(int dtype, bool f32_out);
 CombineFn pick_combine_f32(int D);
 CombineFn pick_combine_f16(int D);
 CombineFn pick_combine_bf16(int D);

@@ -19,10 +19,17 @@
 // below 256 in P), so the cross-lane maximum and the rescale of O in tensor
 // memory are rare; the row sums stay per thread until the piece ends.
 //
+// The stream is latency-bound: a tile lands some 3 us after its copy is
+// issued, so throughput is the bytes in flight per SM.  K and V therefore
+// have rings of their own (three 32 KB tiles each where shared memory allows),
+// land and are released apart (K once its S MMAs complete, V once its PV MMAs
+// do), and everything else is kept small: one P^T tile, one query tile
+// (loaded by TMA straight into the swizzled operand layout once the previous
+// piece's S MMAs are done), the new rows written into the tiles from L2.
+//
 // Warps: 0-7 softmax (two per lane quarter, 16 rows each; also the split
-// merge's consumer warps), 8-9 the TMA producers of pa_kernels.cuh (K and V
-// released separately by the MMAs' commits), 10 the MMA issuer (it also
-// swizzles each piece's query rows and writes the new rows into the stage).
+// merge's consumer warps), 8-9 the TMA producers (K, V), 10 the MMA issuer
+// (it also writes the new rows into the tiles).
 #include "pa_kernels.cuh"
 #include "pa_tc.cuh"
 
@@ -39,19 +46,20 @@ constexpr int kMmaWarp = kConsumerWarps + kProducerWarps;  // after the producer
 constexpr float kGrowth = 8.f;        // log2 units a score may exceed m before m moves
 constexpr uint32_t kColO = 128;       // S buffers at columns 0 and 64, O buffers at 128 and 192
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kPBytes = kTcTT * 128;           // one P^T buffer: 128 tokens x (32 hi + 32 lo)
-constexpr uint32_t kQBytes = 2 * kTcRows * 128;     // one swizzled query tile: 2 halves x 32 rows
+constexpr uint32_t kPBytes = kTcTT * 128;           // P^T: 128 tokens x (32 hi + 32 lo) 16-bit
+constexpr uint32_t kQBytes = 2 * kTcRows * 128;     // the query tile: 2 halves x 32 rows
 constexpr uint32_t kHalfBytes = kTcTT * 128;        // one 64-column half of a K or V tile
+constexpr int kVRing = kMaxStages / 2;              // V ring barriers: full/empty[kVRing + s]
 
 // Layout of the kernel's own region (kTcRegionBytes from base + tc_off).
 struct TcSmem {
-    unsigned char* pbuf;  // [2][128 tokens][128 B]: P^T, columns 0-31 high, 32-63 remainder
-    unsigned char* qsw;   // [2][2 halves][32 rows][128 B]: query rows, 128-byte swizzle
+    unsigned char* pbuf;  // [128 tokens][128 B]: P^T, columns 0-31 high, 32-63 remainder
+    unsigned char* qsw;   // [2 halves][32 rows][128 B]: query rows, 128-byte swizzle
     uint64_t* s_full;     // [2] S^T of a stage is in tensor memory (MMA commit)
-    uint64_t* s_free;     // [2] the softmax warps have read it (4 arrivals)
-    uint64_t* p_full;     // [2] P^T of a stage is in shared memory (4 arrivals)
-    uint64_t* pv_done;    // [2] O^T += V^T P^T of a stage has completed (MMA commit)
-    uint64_t* o_free;     // [2] O of a piece has been read (4 arrivals)
+    uint64_t* s_free;     // [2] the softmax warps have read it (8 arrivals)
+    uint64_t* p_full;     // P^T of a stage is in shared memory (8 arrivals)
+    uint64_t* pv_done;    // O^T += V^T P^T of a stage has completed (MMA commit)
+    uint64_t* o_free;     // [2] O of a piece has been read (8 arrivals)
     uint64_t* fin;        // every MMA of the CTA has completed
     uint32_t* tmem_slot;
     float* red_max;       // [32 rows][4 lane quarters]
@@ -64,20 +72,21 @@ __device__ __forceinline__ TcSmem carve_tc(const SplitParams& p, unsigned char* 
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u) + p.tc_off;
     TcSmem t;
     t.pbuf = base;
-    t.qsw = base + 2 * kPBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * kPBytes + 2 * kQBytes);
+    t.qsw = base + kPBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kPBytes + kQBytes);
     t.s_full = bars;
     t.s_free = bars + 2;
     t.p_full = bars + 4;
-    t.pv_done = bars + 6;
-    t.o_free = bars + 8;
-    t.fin = bars + 10;
-    t.tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    t.pv_done = bars + 5;
+    t.o_free = bars + 6;
+    t.fin = bars + 8;
+    t.tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
     t.red_max = reinterpret_cast<float*>(bars + 16);
     t.red_sum = t.red_max + kTcRows * 4;
     t.red_fac = t.red_sum + kTcRows * 4;
     return t;
 }
+static_assert(kPBytes + kQBytes + 128 + 3 * 512 <= static_cast<uint32_t>(kTcRegionBytes), "tcgen05 region");
 
 // Named barrier `id` of the four softmax warps of a row half.
 __device__ __forceinline__ void soft_bar_sync(int id)
@@ -100,25 +109,10 @@ __device__ __forceinline__ bool soft_bar_or(int id, bool v)
     return r != 0;
 }
 
-__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
-}
-
 __device__ __forceinline__ void st_shared4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared4(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
 }
 
 // Byte offset of 16-byte chunk c (0-7) of token row `tok` in one 64-column
@@ -128,63 +122,204 @@ __device__ __forceinline__ uint32_t swz_row(int tok, int c)
     return static_cast<uint32_t>(tok) * 128 + ((static_cast<uint32_t>(c) ^ (tok & 7)) << 4);
 }
 
-// ------------------------------------------------------------------ MMA warp
-// The piece's query rows, from the producer's row buffer (rows padded to
-// q_row_bytes) into the swizzled K-major operand tile; rows past the pass
-// are zero.  All 32 lanes.
-__device__ __forceinline__ void swizzle_query(const SplitParams& p, const Smem& sm, const TcSmem& ts, int par,
-                                              int R_cta, int lane)
+// ------------------------------------------------------------------ producers
+// A producer warp (role 0: K, role 1: V): for every tile of this CTA's
+// pieces, wait for a free slot of its ring and issue, per cache block, one TMA
+// box per 64-column half (half h of the tile at h * kHalfBytes: the canonical
+// K-major / MN-major operand layout).  Role 0 also loads each piece's query
+// rows (two boxes into the swizzled query tile, once the MMA warp has
+// committed the previous piece's S) and, for a segment's last stage, both
+// roles prefetch its new rows into L2 for the MMA warp.  Table entries come
+// kTableAhead tiles ahead by cp.async (fetch_entries).
+template <typename T>
+__device__ void produce_tc(const SplitParams& p, const Sched& sc, const Smem& sm, const TcSmem& ts,
+                           const CUtensorMap* kmap, const CUtensorMap* vmap, const CUtensorMap* qmap, int role,
+                           int lane)
 {
-    const uint32_t src = smem_u32(sm.scratch + p.qbuf_off) + par * kTcRows * q_row_bytes(kTcD);
-    const uint32_t dst = smem_u32(ts.qsw) + par * kQBytes;
-#pragma unroll 4
-    for (int idx = lane; idx < kTcRows * 16; idx += 32) {
-        const int r = idx >> 4, ch = idx & 15, h = ch >> 3, c = ch & 7;
-        const uint4 v = r < R_cta ? ld_shared4(src + r * q_row_bytes(kTcD) + ch * 16) : make_uint4(0, 0, 0, 0);
-        st_shared4(dst + h * (kTcRows * 128) + swz_row(r, c), v.x, v.y, v.z, v.w);
+    const CUtensorMap* map = role == 0 ? kmap : vmap;
+    const int S = role == 0 ? p.stages : p.stages_v;
+    uint64_t* full = sm.full + (role ? kVRing : 0);
+    uint64_t* empty = sm.empty + (role ? kVRing : 0);
+    unsigned char* ring = sm.ring + static_cast<size_t>(role ? p.stages : 0) * p.stage_bytes;
+    const T* news = static_cast<const T*>(role == 0 ? p.k_new : p.v_new);
+    const uint32_t half_bytes = static_cast<uint32_t>(p.box_rows) * 128;  // one half of a box
+    int* entries = sm.entries + role * (kTableSlots * kSlotInts);
+    const int HB = p.box_rows;
+
+    TileIter cur, ahead;
+    cur.start(p, sc);
+    ahead = cur;
+    fetch_entries(p, ahead, entries, lane);
+    if (ahead.valid())
+        ahead.next(p, sc);
+    uint32_t gt = 0;  // tiles issued by this role
+    int s = 0;        // ring slot of tile gt
+    uint32_t ph = 0;  // completed passes over the ring
+    int piece = -1, q_issued = 0;
+    for (; cur.valid(); cur.next(p, sc), ++gt) {
+        if (gt == 0) {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        } else {
+            fetch_entries(p, ahead, entries + ((gt + kTableAhead) % kTableSlots) * kSlotInts, lane);
+            if (ahead.valid())
+                ahead.next(p, sc);
+            asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
+        }
+        if (ph > 0) {
+            bool ok = !*sm.abort_flag && mbar_wait_bounded(&empty[s], (ph - 1) & 1, p.wait_ns);
+            ok = __all_sync(kFull, ok);
+            if (!ok) {
+                if (lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+                break;
+            }
+        }
+        const Item& it = cur.pc.it;
+        if (cur.j == 0) {
+            ++piece;
+            if (role == 0) {
+                // the one query tile is free once the previous piece's S MMAs are done
+                if (piece >= 1) {
+                    bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.q_free[0], (piece - 1) & 1, p.wait_ns);
+                    ok = __all_sync(kFull, ok);
+                    if (!ok) {
+                        if (lane == 0)
+                            flag_timeout(p, sm.abort_flag);
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    const int row0 = (it.b * p.KV + it.kh) * p.R + it.rsg * kTcRows;
+                    mbar_arrive_expect_tx(&sm.q_full[0], kQBytes);
+                    tma_load_3d(ts.qsw, qmap, 0, 0, row0, &sm.q_full[0]);
+                    tma_load_3d(ts.qsw + kTcRows * 128, qmap, 0, 1, row0, &sm.q_full[0]);
+                }
+                ++q_issued;
+                // the next piece's query rows into L2 (its load waits for this
+                // piece's S MMAs): 64 lines of 128 bytes, two a lane
+                PieceIter nx = cur.pc;
+                nx.next(p, sc);
+                if (nx.ok) {
+                    const int rows = min(kTcRows, p.R - nx.it.rsg * kTcRows);
+                    const char* src = static_cast<const char*>(p.q) +
+                                      ((static_cast<size_t>(nx.it.b) * p.KV + nx.it.kh) * p.R +
+                                       static_cast<size_t>(nx.it.rsg) * kTcRows) * (kTcD * 2);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (lane + 32 * u < 2 * rows)
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(src + (lane + 32 * u) * 128));
+                }
+            }
+        }
+        const int t0 = it.start + (cur.j << p.lg_tt);
+        const int t1 = min(t0 + p.TT, it.end);
+        const int cache_end = min(t1, it.past);
+        const int nb = cache_end > t0 ? (cache_end - t0 + HB - 1) >> p.lg_box : 0;
+        const int* ent = entries + (gt % kTableSlots) * kSlotInts;
+        if (role == 0 && lane < nb && p.checked) {
+            const int phys = ent[lane];  // own cp.async
+            if ((phys < 0 || phys >= p.num_blocks) && p.status)
+                atomicOr(p.status, PA_STATUS_BAD_BLOCK);
+        }
+        unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
+        // test switch (pa_opts.debug_withhold_stage): every CTA's V producer
+        // leaves one stage out, so that the waits for it run out
+        const bool withheld = p.withhold > 0 && role == 1 && gt + 1 == static_cast<uint32_t>(p.withhold);
+        if (lane == 0 && !withheld)
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nb) * 2 * half_bytes);
+        __syncwarp();  // entries written by other lanes' cp.async are visible
+        if (lane < nb && !withheld) {
+            const int phys = ent[lane];
+            // out-of-pool coordinates read as zeros: the copy never faults
+            const int z = (phys << p.lg_block) + ((t0 + (lane << p.lg_box)) & (p.BLOCK - 1));
+#pragma unroll
+            for (int h = 0; h < kTcD / 64; ++h)
+                tma_load_4d(st + h * kHalfBytes + lane * half_bytes, map, 0, h, it.kh, z, &full[s]);
+        }
+        if (t1 > it.past && lane < 2 * p.NQ) {  // the new rows, 128 bytes a lane
+            const char* src = reinterpret_cast<const char*>(news + (static_cast<size_t>(it.b) * p.KV + it.kh) * p.NQ * kTcD);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(src + lane * 128));
+        }
+        if (++s == S) {
+            s = 0;
+            ++ph;
+        }
+        if (gt == 0)
+            for (int k = 1; k <= kTableAhead; ++k) {
+                fetch_entries(p, ahead, entries + (k % kTableSlots) * kSlotInts, lane);
+                if (ahead.valid())
+                    ahead.next(p, sc);
+            }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // no copy left in flight when the pipeline was abandoned
+    __syncwarp();
+    if (*sm.abort_flag && lane == 0) {
+        const uint32_t first = gt > static_cast<uint32_t>(S) ? gt - S : 0u;
+        for (uint32_t g = first; g < gt; ++g)
+            mbar_wait_bounded(&full[g % S], (g / S) & 1, p.wait_ns);
+        if (q_issued > 0)
+            mbar_wait_bounded(&sm.q_full[0], (q_issued - 1) & 1, p.wait_ns);
     }
 }
 
-// The stage's new rows (tokens past the cache, from the stage's new-row
-// area) written into the K and V tiles, and the V rows from the stage's end
-// up to the next multiple of 16 zeroed (the cache box may hold anything
-// there, and the last MMA of the stage reads them with P = 0).  All lanes.
-__device__ __forceinline__ void fix_stage(const SplitParams& p, uint32_t st, int t0, int n_tile, int past, int lane)
+// ------------------------------------------------------------------ MMA warp
+// A stage's new rows (tokens past the cache; `rows` = the segment's new rows
+// [NQ][D] in global memory, prefetched into L2 by the producer) written into
+// its K or V tile; with zero_tail also the rows from the stage's end up to the
+// next multiple of 16 zeroed (the cache box may hold anything there, and the
+// stage's last PV MMA reads them with P = 0).  All lanes; up to 16 new rows.
+template <typename T>
+__device__ __forceinline__ void fix_tile(uint32_t tile, const T* rows, int t0, int n_tile, int past, bool zero_tail,
+                                         int lane)
 {
     const int a0 = max(past - t0, 0);
-    const int nnew = n_tile - a0;
-    for (int idx = lane; idx < nnew * 32; idx += 32) {
-        const int row = idx >> 5, which = (idx >> 4) & 1, ch = idx & 15;
-        const int tok = a0 + row;
-        const uint32_t src = st + (which ? p.vnew_off : p.knew_off) + (t0 + tok - past) * (kTcD * 2) + ch * 16;
-        const uint32_t dst = st + (which ? p.v_off : 0) + (ch >> 3) * kHalfBytes + swz_row(tok, ch & 7);
-        const uint4 v = ld_shared4(src);
-        st_shared4(dst, v.x, v.y, v.z, v.w);
+    const int n = (n_tile - a0) * 16;  // 16-byte chunks of the stage's new rows
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = lane + 32 * u;
+        if (idx < n)
+            v[u] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<size_t>(t0 + a0 - past) * kTcD) + idx);
     }
-    const int z1 = (n_tile + 15) & ~15;
-    for (int idx = lane; idx < (z1 - n_tile) * 16; idx += 32) {
-        const int tok = n_tile + (idx >> 4), ch = idx & 15;
-        st_shared4(st + p.v_off + (ch >> 3) * kHalfBytes + swz_row(tok, ch & 7), 0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = lane + 32 * u;
+        if (idx < n) {
+            const int tok = a0 + (idx >> 4), ch = idx & 15;
+            st_shared4(tile + (ch >> 3) * kHalfBytes + swz_row(tok, ch & 7), v[u].x, v[u].y, v[u].z, v[u].w);
+        }
+    }
+    if (zero_tail) {
+        const int z1 = (n_tile + 15) & ~15;
+        for (int idx = lane; idx < (z1 - n_tile) * 16; idx += 32) {
+            const int tok = n_tile + (idx >> 4), ch = idx & 15;
+            st_shared4(tile + (ch >> 3) * kHalfBytes + swz_row(tok, ch & 7), 0, 0, 0, 0);
+        }
     }
 }
 
-// Issues, as the barriers allow, S^T of each stage (once its tiles have
-// landed and its S buffer is free) and O^T += V^T P^T (once the softmax has
-// written P), polling both, so that S of the next stage runs while the
-// softmax works on this one.  Lane 0 issues; the warp swizzles the query rows
-// and fixes the stages.  Gives up (abort flag, status) after wait_ns without
-// progress.
-template <bool kBf>
+// Issues, as the barriers allow, S^T of each stage (once its K tile has
+// landed and its S buffer is free) and O^T += V^T P^T (once its V tile has
+// landed and the softmax has written P), polling both, so that S of the next
+// stage runs while the softmax works on this one.  After the last S of a
+// piece it commits the query tile free.  Lane 0 issues; the warp writes the
+// new rows.  Gives up (abort flag, status) after wait_ns without progress.
+template <typename T>
 __device__ void mma_warp(const SplitParams& p, const Sched& sc, const Smem& sm, const TcSmem& ts, uint32_t tmem,
                          int lane)
 {
-    const int S = p.stages;
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    const int SK = p.stages, SV = p.stages_v;
     const uint32_t id_s = idesc<kBf>(kTcRows, false);      // S^T: N 32 rows, K and Q K-major
     const uint32_t id_o = idesc<kBf>(64, true, true);      // O^T: N 64 (hi | lo), V^T and P^T MN-major
-    const uint32_t ring = smem_u32(sm.ring);
-    const uint32_t pbuf = smem_u32(ts.pbuf), qsw = smem_u32(ts.qsw);
+    const uint32_t ring_k = smem_u32(sm.ring);
+    const uint32_t ring_v = ring_k + SK * p.stage_bytes;
+    const uint64_t dq = smem_desc(smem_u32(ts.qsw), 16, 1024);
+    const uint64_t dp = smem_desc(smem_u32(ts.pbuf), kPBytes, 1024);
     struct Pend {
-        int s, pc, first, nks;
+        int pc, first, nks, t0, n_tile, past;
+        size_t nrow;  // the segment's first new row in v_new
     } pend[4];
     TileIter ti;
     ti.start(p, sc);
@@ -195,37 +330,34 @@ __device__ void mma_warp(const SplitParams& p, const Sched& sc, const Smem& sm, 
         bool prog = false;
         if (ti.valid() && ns - npv < 3) {
             const Item& it = ti.pc.it;
-            const int s = static_cast<int>(ns % S), b = ns & 1;
+            const int sk = static_cast<int>(ns % SK), b = ns & 1;
             const bool first = ti.j == 0;
             const int pc = piece + (first ? 1 : 0);
             bool ready = true;
             if (lane == 0) {
-                ready = mbar_test_wait(&sm.full[s], (ns / S) & 1);
-                // S(ns - 2), and with it every earlier MMA (the query tile of
-                // piece pc - 2 included), has completed once its readers are done
-                if (ready && ns >= 2)
+                ready = mbar_test_wait(&sm.full[sk], (ns / SK) & 1);
+                if (ready && ns >= 2)  // the softmax has read S(ns - 2)
                     ready = mbar_test_wait(&ts.s_free[b], ((ns >> 1) - 1) & 1);
                 if (ready && first)
-                    ready = mbar_test_wait(&sm.q_full[pc & 1], (pc >> 1) & 1);
+                    ready = mbar_test_wait(&sm.q_full[0], pc & 1);
             }
             if (__shfl_sync(kFull, ready ? 1 : 0, 0)) {
                 const int t0 = it.start + (ti.j << 7);
                 const int n_tile = min(kTcTT, it.end - t0);
-                const uint32_t st = ring + s * p.stage_bytes;
-                if (first) {
-                    piece = pc;
-                    swizzle_query(p, sm, ts, pc & 1, min(kTcRows, p.R - it.rsg * kTcRows), lane);
+                const uint32_t st = ring_k + sk * p.stage_bytes;
+                const size_t nrow = (static_cast<size_t>(it.b) * p.KV + it.kh) * p.NQ;
+                if (t0 + n_tile > it.past) {
+                    fix_tile(st, static_cast<const T*>(p.k_new) + nrow * kTcD, t0, n_tile, it.past, false, lane);
+                    fence_proxy_async_smem();
                 }
-                if (t0 + n_tile > it.past || (n_tile & 15))
-                    fix_stage(p, st, t0, n_tile, it.past, lane);
-                fence_proxy_async_smem();
                 __syncwarp();
+                piece = pc;
+                pend[ns & 3] = Pend{pc, first ? 1 : 0, (n_tile + 15) >> 4, t0, n_tile, it.past, nrow};
+                ti.next(p, sc);
+                const bool piece_end = !ti.valid() || ti.j == 0;
                 if (lane == 0) {
-                    if (first)
-                        mbar_arrive_n(&sm.q_free[pc & 1], kConsumerWarps);
                     tc_fence_after();
                     const uint64_t dk = smem_desc(st, 16, 1024);
-                    const uint64_t dq = smem_desc(qsw + (pc & 1) * kQBytes, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < kTcD / 16; ++ks) {
                         const uint32_t ka = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
@@ -233,34 +365,41 @@ __device__ void mma_warp(const SplitParams& p, const Sched& sc, const Smem& sm, 
                         umma(tmem + b * 64, dk + (ka >> 4), dq + (qa >> 4), id_s, ks > 0);
                     }
                     umma_commit(&ts.s_full[b]);
-                    umma_commit(&sm.empty[s]);  // K part of the stage
+                    umma_commit(&sm.empty[sk]);  // the K slot
+                    if (piece_end)
+                        umma_commit(&sm.q_free[0]);  // the query tile
                 }
                 __syncwarp();
-                pend[ns & 3] = Pend{s, pc, first ? 1 : 0, (n_tile + 15) >> 4};
                 ++ns;
-                ti.next(p, sc);
                 prog = true;
             }
         }
         if (npv < ns) {
             const Pend pd = pend[npv & 3];
-            const int b = npv & 1;
+            const int sv = static_cast<int>(npv % SV);
             bool ready = true;
             if (lane == 0) {
-                ready = mbar_test_wait(&ts.p_full[b], (npv >> 1) & 1);
+                ready = mbar_test_wait(ts.p_full, npv & 1) &&
+                        mbar_test_wait(&sm.full[kVRing + sv], (npv / SV) & 1);
                 if (ready && pd.first && pd.pc >= 2)
                     ready = mbar_test_wait(&ts.o_free[pd.pc & 1], ((pd.pc >> 1) - 1) & 1);
             }
             if (__shfl_sync(kFull, ready ? 1 : 0, 0)) {
+                const uint32_t st = ring_v + sv * p.stage_bytes;
+                if (pd.t0 + pd.n_tile > pd.past || (pd.n_tile & 15)) {
+                    fix_tile(st, static_cast<const T*>(p.v_new) + pd.nrow * kTcD, pd.t0, pd.n_tile, pd.past, true,
+                             lane);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint64_t dv = smem_desc(ring + pd.s * p.stage_bytes + p.v_off, kHalfBytes, 1024);
-                    const uint64_t dp = smem_desc(pbuf + b * kPBytes, kPBytes, 1024);
+                    const uint64_t dv = smem_desc(st, kHalfBytes, 1024);
                     const uint32_t to = tmem + kColO + (pd.pc & 1) * 64;
                     for (int ks = 0; ks < pd.nks; ++ks)
                         umma(to, dv + ((ks * 2048) >> 4), dp + ((ks * 2048) >> 4), id_o, !(pd.first && ks == 0));
-                    umma_commit(&ts.pv_done[b]);
-                    umma_commit(&sm.empty[kMaxStages / 2 + pd.s]);  // V part
+                    umma_commit(ts.pv_done);
+                    umma_commit(&sm.empty[kVRing + sv]);  // the V slot
                 }
                 __syncwarp();
                 ++npv;
@@ -384,8 +523,8 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
 #pragma unroll
             for (int r = 0; r < kWarpRows; ++r)
                 need |= x[r] > m[r] + kGrowth;
-            if (ok && gt >= 2)  // PV of stage gt - 2 has read P buffer b
-                ok = !*sm.abort_flag && mbar_wait_bounded(&ts.pv_done[b], ((gt >> 1) - 1) & 1, p.wait_ns);
+            if (ok && gt >= 1)  // PV of stage gt - 1 has read the P^T tile (and O is current)
+                ok = !*sm.abort_flag && mbar_wait_bounded(ts.pv_done, (gt - 1) & 1, p.wait_ns);
             ok = __all_sync(kFull, ok);
             if (soft_bar_or(bar, need || !ok)) {
                 if (soft_bar_or(bar, !ok)) {
@@ -413,14 +552,7 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
                 }
                 __syncwarp();
                 if (j > 0 && shrink) {  // uniform over the row half: m is
-                    // O of the piece's stages so far, once the last one's PV is done
-                    const uint32_t gp = gt - 1;
-                    bool ok2 = !*sm.abort_flag && mbar_wait_bounded(&ts.pv_done[gp & 1], (gp >> 1) & 1, p.wait_ns);
-                    ok2 = __all_sync(kFull, ok2);
-                    if (soft_bar_or(bar, !ok2)) {
-                        give_up(ok2);
-                        break;
-                    }
+                    // O of the piece's stages so far (their PV has completed)
                     tc_fence_after();
                     const uint32_t to = tl + kColO + (piece & 1) * 64 + h * kWarpRows;
 #pragma unroll
@@ -436,8 +568,8 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
                 }
             }
             // P = 2^(x - m): the row sums, and P^T (high | remainder) of this
-            // warp's rows into buffer b (chunks 2h, 2h + 1 and 4 + 2h, 5 + 2h)
-            const uint32_t pr = prow + b * kPBytes;
+            // warp's rows (chunks 2h, 2h + 1 and 4 + 2h, 5 + 2h of its token row)
+            const uint32_t pr = prow;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t hi[4], lo[4];
@@ -457,7 +589,7 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&ts.p_full[b]);
+                mbar_arrive(ts.p_full);
         }
         if (dead)
             break;
@@ -468,7 +600,7 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
         if (lane < kWarpRows)
             ts.red_sum[(h * kWarpRows + lane) * 4 + qt] = ls;
         const uint32_t gl = gt - 1;
-        bool ok = !*sm.abort_flag && mbar_wait_bounded(&ts.pv_done[gl & 1], (gl >> 1) & 1, p.wait_ns);
+        bool ok = !*sm.abort_flag && mbar_wait_bounded(ts.pv_done, gl & 1, p.wait_ns);
         ok = __all_sync(kFull, ok);
         if (soft_bar_or(bar, !ok)) {  // also publishes red_sum
             give_up(ok);
@@ -535,26 +667,34 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
 template <typename T, typename TO>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
     pa_umma32_kernel(const __grid_constant__ SplitParams p, const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap)
+                     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap)
 {
-    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const Smem sm = carve(p, smem_raw);
     const TcSmem ts = carve_tc(p, smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    if (warp == kMmaWarp && lane == 0)
+        tma_prefetch_desc(&qmap);
     kernel_entry(p, kmap, vmap, sm);
     if (threadIdx.x == 0) {
+        // K and V rings apart, each slot landing and released by one arrival;
+        // one query tile, released by the MMA warp's commit
         for (int s = 0; s < p.stages; ++s)
-            mbar_init(&sm.empty[kMaxStages / 2 + s], 1);  // V parts (K parts: init_cta)
+            mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < p.stages_v; ++s) {
+            mbar_init(&sm.full[kVRing + s], 1);
+            mbar_init(&sm.empty[kVRing + s], 1);
+        }
+        mbar_init(&sm.q_free[0], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ts.s_full[i], 1);
             mbar_init(&ts.s_free[i], kSoftWarps);
-            mbar_init(&ts.p_full[i], kSoftWarps);
-            mbar_init(&ts.pv_done[i], 1);
             mbar_init(&ts.o_free[i], kSoftWarps);
         }
+        mbar_init(ts.p_full, kSoftWarps);
+        mbar_init(ts.pv_done, 1);
         mbar_init(ts.fin, 1);
         fence_mbar_init();
     }
@@ -571,7 +711,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const uint32_t tmem = *ts.tmem_slot;
 
     if (warp == kMmaWarp) {
-        mma_warp<kBf>(p, sc, sm, ts, tmem, lane);
+        mma_warp<T>(p, sc, sm, ts, tmem, lane);
         // tensor memory is freed once the softmax warps are done with it
         asm volatile("bar.sync 6, %0;" ::"n"((kSoftWarps + 1) * 32) : "memory");
         tc_fence_after();
@@ -580,7 +720,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         return;
     }
     if (warp >= kConsumerWarps) {
-        produce<T, kTcD, kHalvesSwizzled>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
+        produce_tc<T>(p, sc, sm, ts, &kmap, &vmap, &qmap, warp - kConsumerWarps, lane);
         return;
     }
     // the softmax warps are the consumer warps of the split merge
@@ -588,21 +728,22 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     int nsplit = 0;
     softmax_warps<T, TO>(p, sc, sm, ts, tmem, warp, lane, nsplit, dep_ok);
     // Without an abort every warp has seen every piece (nsplit is uniform);
-    // the last PV has completed, so the P buffers serve the merge.
+    // the last PV has completed, so the P^T tile and the reduction arrays
+    // serve the merge.
     tc_fence_before();
     const bool aborted = consumer_bar_or(*sm.abort_flag != 0);
     asm volatile("bar.arrive 6, %0;" ::"n"((kSoftWarps + 1) * 32) : "memory");
     if (nsplit > 0 && !aborted) {
         if (!dep_ok)
             grid_dependency_wait();
-        flush_split_pieces<kTcD, TO>(p, sc, sm.split_list, nsplit, reinterpret_cast<float2*>(sm.scratch + 1024),
+        flush_split_pieces<kTcD, TO>(p, sc, sm.split_list, nsplit, reinterpret_cast<float2*>(ts.red_max),
                                      2 * kTcRows, reinterpret_cast<float*>(ts.pbuf), kObufFloats);
     }
 }
 
 }  // namespace
 
-SplitFn pick_split_tc(int dtype, bool f32_out)
+SplitTcFn pick_split_tc(int dtype, bool f32_out)
 {
     if (dtype == PA_BF16)
         return f32_out ? pa_umma32_kernel<__nv_bfloat16, float> : pa_umma32_kernel<__nv_bfloat16, __nv_bfloat16>;

@@ -213,6 +213,40 @@ int cache_map(const void* base, int num_blocks, int BLOCK, int KV, int D, int dt
     return PA_OK;
 }
 
+// The query rows [rows][D] (16-bit) for the tcgen05 kernel: 3-D {64, D/64,
+// rows}, box {64, 1, 32} with the 128-byte swizzle -- one 64-column half of a
+// 32-row pass, in the canonical K-major operand layout; rows past the end
+// read as zeros.
+int query_map(const void* q, long long rows, int D, int dtype, CUtensorMap* out)
+{
+    const MapKey key{q, rows, 0, D, -1, dtype, 1};
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < g_map_count; ++i)
+        if (g_map_keys[i] == key) {
+            *out = g_maps[i];
+            return PA_OK;
+        }
+    auto enc = encoder();
+    if (!enc)
+        return PA_ERR_DRIVER;
+    const CUtensorMapDataType dt = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {128u, static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[3] = {64u, 1u, 32u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUtensorMap map;
+    if (enc(&map, dt, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+    const int slot = g_map_count < kMapCache ? g_map_count++ : (g_map_next++ % kMapCache);
+    g_map_keys[slot] = key;
+    g_maps[slot] = map;
+    *out = map;
+    return PA_OK;
+}
+
 // --- kernel table -----------------------------------------------------------------
 SplitFn pick_split(int dtype, bool f32_out, int D, int RG)
 {
@@ -441,6 +475,17 @@ int pa_choose_partitions(const int32_t* host_seq_lens, int max_len, int batch, i
         return PA_ERR_BAD_DIMS;
     const long long G = active_ctas(grid, C, static_cast<long long>(batch) * U);
     plan->active = static_cast<int>(G);
+    long long max_units = 0;
+    for (int b = 0; b < batch; ++b) {
+        const long long nu = (length(b) + NQ + TT - 1) / TT;
+        max_units = nu > max_units ? nu : max_units;
+    }
+    if (whole_segments(static_cast<long long>(batch) * U, G, W, max_units)) {
+        plan->active = batch * U;  // one whole segment per CTA
+        plan->pieces = batch * U;
+        plan->max_pieces = 1;
+        return 1;
+    }
     auto owner = [&](long long c) { return c * G / C < G - 1 ? c * G / C : G - 1; };
     long long x0 = 0, g = 0;
     int most = 1;
@@ -578,7 +623,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
         vnew_off = v_off + TT * D * es;
         stage_end = vnew_off + NQ * D * es;
     }
-    const int stage_bytes = static_cast<int>(align_up(stage_end, 1024));
+    int stage_bytes = static_cast<int>(align_up(stage_end, 1024));
     int smem_optin = 0;
     if (device_smem_optin(&smem_optin) != PA_OK)
         return PA_ERR_CUDA;
@@ -586,46 +631,53 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // consumer scratch: tensor-core path, (max, sum) tables, one merge round of
     // kObufFloats floats of merge rounds and two query-row buffers; CUDA-core
     // path, per-warp states
-    int qbuf_off = 2048 + kObufFloats * 4;
+    const int qbuf_off = 2048 + kObufFloats * 4;
     const int merge_bytes = mma ? qbuf_off + 2 * ROWS * q_row_bytes(D)
                                 : (kConsumerWarps * RG * D + 2 * kConsumerWarps * RG) * 4 +
                                       kConsumerWarps * RG * 8;
     int stage_off = static_cast<int>(align_up(merge_off + merge_bytes, 1024));
-    // The tcgen05 kernel (32-row passes at D = 128): the (max, sum) tables,
-    // the two query-row buffers, then its own region (P and query tiles,
-    // barriers; the split merge's factors share the P tiles), when two stages
-    // still fit after it.
-    int tc_off = 0;
+    // The tcgen05 kernel (32-row passes at D = 128): its region (P^T and
+    // query tiles, barriers, reductions) after the lengths, then a K ring and
+    // a V ring of 32 KB tiles, half of the remaining tiles each (the new rows
+    // stay in global memory), when each ring gets two tiles at least.
+    int tc_off = 0, stages_v = 0;
     bool tc32 = false;
     if (mma && MT == 2 && D == 128 && opts->kernel == 0) {
-        const int t_off = static_cast<int>(align_up(merge_off + 2048 + 2 * ROWS * q_row_bytes(D), 1024));
+        const int t_off = static_cast<int>(align_up(merge_off, 1024));
         const int t_stage = static_cast<int>(align_up(t_off + kTcRegionBytes, 1024));
-        if ((smem_optin - slack - t_stage) / stage_bytes >= 2) {
+        const int tiles = (smem_optin - slack - t_stage) / kTcTileBytes;
+        if (tiles >= 4) {
             tc32 = true;
-            qbuf_off = 2048;
             tc_off = t_off;
             stage_off = t_stage;
+            stage_bytes = kTcTileBytes;
+            stages_v = (tiles + 1) / 2 < kMaxStages / 2 ? (tiles + 1) / 2 : kMaxStages / 2;
         }
     }
     int stages = (smem_optin - slack - stage_off) / stage_bytes;
-    if (stages > (tc32 ? kMaxStages / 2 : kMaxStages))  // tcgen05: K and V released apart
+    if (tc32)
+        stages -= stages_v;  // the K ring: the tiles the V ring leaves
+    if (stages > (tc32 ? kMaxStages / 2 : kMaxStages))
         stages = tc32 ? kMaxStages / 2 : kMaxStages;
     if (stages < 2)
         return PA_ERR_UNSUPPORTED;
-    const int smem = slack + stage_off + stages * stage_bytes;
+    const int smem = slack + stage_off + (stages + stages_v) * stage_bytes;
 
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap, qmap;
     int rc = cache_map(k_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, tc32, &kmap);
     if (rc == PA_OK)
         rc = cache_map(v_cache, opts->num_blocks, BLOCK, KV, D, dtype, box_rows, tc32, &vmap);
+    if (rc == PA_OK && tc32)
+        rc = query_map(q, static_cast<long long>(B) * H * NQ, D, dtype, &qmap);
     if (rc != PA_OK)
         return rc;
 
     const bool f32_out = out_dtype == PA_F32 && dtype != PA_F32;
-    const SplitFn split = tc32 ? pick_split_tc(dtype, f32_out) : pick_split(dtype, f32_out, D, mma ? MT : RG);
+    const void* split = tc32 ? reinterpret_cast<const void*>(pick_split_tc(dtype, f32_out))
+                             : reinterpret_cast<const void*>(pick_split(dtype, f32_out, D, mma ? MT : RG));
     int occ = 1, sms = 1;
     const int threads = tc32 ? kUmmaThreads : kThreads;
-    rc = prepare_func(reinterpret_cast<const void*>(split), threads, smem, &occ, &sms);
+    rc = prepare_func(split, threads, smem, &occ, &sms);
     if (rc != PA_OK)
         return rc;
 
@@ -675,6 +727,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // its K and V parts (one arrival each)
     p.empty_count = tc32 ? 1 : mma ? (TT / TPW) * row_groups(MT) : kConsumerWarps;
     p.tc_off = tc_off;
+    p.stages_v = stages_v;
     p.checked = opts->checked ? 1 : 0;
     p.R = R;
     p.rows_per_cta = rows_per_cta;
@@ -725,8 +778,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache,
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void* args[3] = {&p, &kmap, &vmap};
-    if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(split), args) != cudaSuccess)
+    void* args[4] = {&p, &kmap, &vmap, &qmap};
+    if (cudaLaunchKernelExC(&cfg, split, args) != cudaSuccess)
         return PA_ERR_CUDA;
     g_launches.fetch_add(1);
 

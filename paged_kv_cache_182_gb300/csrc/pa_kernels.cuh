@@ -769,9 +769,24 @@ __device__ __forceinline__ Sched setup_cta(const SplitParams& p, const Smem& sm)
         if (p.partitions == 0) {
             // G <= C: every CTA inside a segment then holds a unit.  The starts
             // of this CTA's range and of the next CTA's.
-            const int G = active_ctas(gridDim.x, sc.cost, static_cast<long long>(p.B) * p.NRS * p.KV);
+            const long long S = static_cast<long long>(p.B) * p.NRS * p.KV;
+            const int G = active_ctas(gridDim.x, sc.cost, S);
             CostPos c0{0, 0, 0, 0}, c1{0, 0, 0, 0};
-            if (static_cast<int>(blockIdx.x) < G) {
+            int max_units = 0;  // the longest segment, in stages
+            for (int b = lane; b < p.B; b += 32)
+                max_units = max(max_units, (sm.lens[b] + p.NQ + p.TT - 1) >> p.lg_tt);
+            max_units = __reduce_max_sync(kFull, max_units);
+            if (p.counters && whole_segments(S, G, sc.total, max_units)) {
+                // segment k for CTA k (the range of its units), none for the rest
+                const int k = blockIdx.x, U = p.NRS * p.KV;
+                c0 = c1 = CostPos{sc.total, p.B, 0, 0};
+                if (k < S) {
+                    const int b = k / U, seg = k - b * U;
+                    const int nb = (sm.lens[b] + p.NQ + p.TT - 1) >> p.lg_tt;
+                    c0 = CostPos{sm.prefix[b] + seg * nb, b, seg, 0};
+                    c1.x = c0.x + nb;
+                }
+            } else if (static_cast<int>(blockIdx.x) < G) {
                 c0 = cost_start(p, sc, blockIdx.x, G, lane);
                 c1 = cost_start(p, sc, blockIdx.x + 1, G, lane);
             }
@@ -846,14 +861,6 @@ __device__ __forceinline__ void fetch_entries(const SplitParams& p, const TileIt
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Stage layouts of the producer: float32 rows unswizzled [tokens][D]
-// (kRowsPlain); 16-bit rows [tokens][D/64 halves][64 columns] with the
-// 128-byte swizzle, one box per block (kRowsSwizzled); or the halves apart,
-// [D/64 halves][tokens][64 columns], one box per block and half
-// (kHalvesSwizzled: the canonical operand layout of tcgen05, whose K and V
-// parts are released separately, K on empty[s], V on empty[kMaxStages/2 + s]).
-constexpr int kRowsPlain = 0, kRowsSwizzled = 1, kHalvesSwizzled = 2;
-
 // A producer warp: for every tile of every item of this CTA, wait for a free
 // stage and issue one TMA box per cache block (or per tile when a block spans
 // several tiles).  Role 0 issues the K boxes, the query rows of each piece
@@ -862,12 +869,10 @@ constexpr int kRowsPlain = 0, kRowsSwizzled = 1, kHalvesSwizzled = 2;
 // role counts its bytes on the stage's full barrier (two arrivals).  Table
 // entries are fetched kTableAhead tiles ahead with cp.async, so no dependent
 // global load sits on the issue path.
-template <typename T, int D, int kLayout>
+template <typename T, int D, bool kSwizzled>
 __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, const CUtensorMap* kmap,
                         const CUtensorMap* vmap, int role, int lane)
 {
-    constexpr bool kSwizzled = kLayout != kRowsPlain;
-    uint64_t* empty = sm.empty + (kLayout == kHalvesSwizzled && role == 1 ? kMaxStages / 2 : 0);
     const CUtensorMap* map = role == 0 ? kmap : vmap;  // fetched at kernel entry
     const int S = p.stages;
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows * D * sizeof(T));
@@ -898,7 +903,7 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
             asm volatile("cp.async.wait_group %0;" ::"n"(kTableAhead) : "memory");
         }
         if (ph > 0) {
-            bool ok = !*sm.abort_flag && mbar_wait_bounded(&empty[s], (ph - 1) & 1, p.wait_ns);
+            bool ok = !*sm.abort_flag && mbar_wait_bounded(&sm.empty[s], (ph - 1) & 1, p.wait_ns);
             ok = __all_sync(kFull, ok);
             if (!ok) {
                 if (lane == 0)
@@ -963,19 +968,11 @@ __device__ void produce(const SplitParams& p, const Sched& sc, const Smem& sm, c
             const int phys = ent[lane];
             // Out-of-pool coordinates read as zeros: the copy never faults.
             const int z = (phys << p.lg_block) + ((t0 + (lane << p.lg_box)) & (p.BLOCK - 1));
-            unsigned char* dst = st + (role == 0 ? 0 : p.v_off);
-            if constexpr (kLayout == kHalvesSwizzled) {
-                // per half a box [HB rows][64 columns]; half h of the tile at h * TT rows
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h)
-                    tma_load_4d(dst + (static_cast<size_t>(h) * p.TT + lane * HB) * 128, map, 0, h, it.kh, z,
-                                &sm.full[s]);
-            } else if constexpr (kSwizzled) {
+            unsigned char* dst = st + (role == 0 ? 0 : p.v_off) + static_cast<size_t>(lane) * HB * D * sizeof(T);
+            if constexpr (kSwizzled) {
                 // box [HB rows][D/64 halves][64 columns], 128-byte swizzle
-                tma_load_4d(dst + static_cast<size_t>(lane) * HB * D * sizeof(T), map, 0, 0, it.kh, z,
-                            &sm.full[s]);
+                tma_load_4d(dst, map, 0, 0, it.kh, z, &sm.full[s]);
             } else {
-                dst += static_cast<size_t>(lane) * HB * D * sizeof(T);
                 tma_load_3d(dst, map, 0, it.kh, z, &sm.full[s]);
             }
         }
@@ -1336,7 +1333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Sched sc = setup_cta(p, sm);
 
     if (warp >= kConsumerWarps) {
-        produce<T, D, kRowsPlain>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
+        produce<T, D, false>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
     // consumers: with p.early (the inputs read before the previous kernel
@@ -1633,7 +1630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Sched sc = setup_cta(p, sm);
 
     if (warp >= kConsumerWarps) {
-        produce<T, D, kRowsSwizzled>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
+        produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
     // consumers: with p.early (the inputs read before the previous kernel
@@ -1967,7 +1964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Sched sc = setup_cta(p, sm);
 
     if (warp >= kConsumerWarps) {
-        produce<T, D, kRowsSwizzled>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
+        produce<T, D, true>(p, sc, sm, &kmap, &vmap, warp - kConsumerWarps, lane);
         return;
     }
     // consumers: with p.early (the inputs read before the previous kernel

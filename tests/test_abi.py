@@ -320,11 +320,16 @@ def _brute_force_split(lens, max_len, U, TT, V, grid):
     segment; G CTAs take part (each at least 4 stages of cost unless there are
     more segments than that, at most C); CTA k of G owns the cost positions
     [ceil(k C / G), ceil((k + 1) C / G)); a segment's pieces are the CTAs its
-    real units fall in (NQ = 1 here)."""
+    real units fall in (NQ = 1 here).  When the segments are no more than G
+    and the longest is at most W / G + 4 stages (W: all real units; 4: what a
+    merge costs), every CTA takes one whole segment instead."""
     units = [(min(max(n, 0), max_len) + 1 + TT - 1) // TT for n in lens]
     C = sum(u * U for u in units) + V * len(lens) * U
     # every CTA at least 4 stages of cost, unless the segments are more; never more than C
     G = min(grid, min(C, max(len(units) * U, -(-C // 4))))
+    W = sum(u * U for u in units)
+    if len(units) * U <= G and max(units) * G <= W + 4 * G:
+        return [1] * (len(units) * U), len(units) * U
     starts = [-(-k * C // G) for k in range(G + 1)]  # ceil(k C / G)
 
     def owner(c):
@@ -353,6 +358,7 @@ def test_choose_partitions_matches_its_definition(lib):
     import torch
 
     rng = random.Random(5)
+    whole = 0
     for trial in range(40):
         B = rng.randint(1, 40)
         KV = rng.choice([1, 2, 8])
@@ -362,12 +368,17 @@ def test_choose_partitions_matches_its_definition(lib):
         plan = lib.choose_partitions(lens, max_len, 4 * KV, KV, 128, 16, 1, torch.float16, sms=sms)
         bound = B * KV * ((max_len + 1 + 127) // 128 + 1)  # pa_decode's launch: no idle CTAs
         counts, G = _brute_force_split(lens, max_len, KV, 128, 1, min(sms, 1024, bound))
+        whole += all(n == 1 for n in counts) and G == len(counts)
         assert plan.active == G and plan.grid == min(sms, 1024, bound)
         assert plan.segments == len(counts)
         assert plan.pieces == sum(counts)
         assert plan.split_segments == sum(1 for n in counts if n > 1)
         assert plan.records == sum(n for n in counts if n > 1)
         assert plan.max_pieces == max(counts)
+    assert whole > 0  # the whole-segment rule was taken
+    # 128 equal segments on 152 SMs (the causal-append shape): whole segments
+    eq = lib.choose_partitions([2048] * 16, 2048, 64, 8, 128, 32, 4, torch.float16, sms=152)
+    assert (eq.active, eq.pieces, eq.records, eq.max_pieces) == (128, 128, 0, 1)
     # no lengths: every sequence holds max_len tokens
     a = lib.choose_partitions(None, 32768, 32, 8, 128, 16, 1, torch.bfloat16, sms=152, batch=1)
     b = lib.choose_partitions([32768], 32768, 32, 8, 128, 16, 1, torch.bfloat16, sms=152)
