@@ -299,10 +299,11 @@ __device__ __forceinline__ void fix_tile(uint32_t tile, const T* rows, int t0, i
     }
 }
 
-// Issues, as the barriers allow, S^T of each stage (once its K tile has
-// landed and its S buffer is free) and O^T += V^T P^T (once its V tile has
-// landed and the softmax has written P), polling both, so that S of the next
-// stage runs while the softmax works on this one.  After the last S of a
+// Issues, as the barriers allow, O^T += V^T P^T of each stage (once its V
+// tile has landed and the softmax has written P; first, as the softmax of the
+// next stage waits for it) and S^T (once its K tile has landed and its S
+// buffer is free), polling both, so that S of the next stage runs while the
+// softmax works on this one.  After the last S of a
 // piece it commits the query tile free.  Lane 0 issues; the warp writes the
 // new rows.  Gives up (abort flag, status) after wait_ns without progress.
 template <typename T>
@@ -328,6 +329,38 @@ __device__ void mma_warp(const SplitParams& p, const Sched& sc, const Smem& sm, 
     uint64_t last = global_timer_ns();
     while (true) {
         bool prog = false;
+        if (npv < ns) {
+            const Pend pd = pend[npv & 3];
+            const int sv = static_cast<int>(npv % SV);
+            bool ready = true;
+            if (lane == 0) {
+                ready = mbar_test_wait(ts.p_full, npv & 1) &&
+                        mbar_test_wait(&sm.full[kVRing + sv], (npv / SV) & 1);
+                if (ready && pd.first && pd.pc >= 2)
+                    ready = mbar_test_wait(&ts.o_free[pd.pc & 1], ((pd.pc >> 1) - 1) & 1);
+            }
+            if (__shfl_sync(kFull, ready ? 1 : 0, 0)) {
+                const uint32_t st = ring_v + sv * p.stage_bytes;
+                if (pd.t0 + pd.n_tile > pd.past || (pd.n_tile & 15)) {
+                    fix_tile(st, static_cast<const T*>(p.v_new) + pd.nrow * kTcD, pd.t0, pd.n_tile, pd.past, true,
+                             lane);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint64_t dv = smem_desc(st, kHalfBytes, 1024);
+                    const uint32_t to = tmem + kColO + (pd.pc & 1) * 64;
+                    for (int ks = 0; ks < pd.nks; ++ks)
+                        umma(to, dv + ((ks * 2048) >> 4), dp + ((ks * 2048) >> 4), id_o, !(pd.first && ks == 0));
+                    umma_commit(ts.pv_done);
+                    umma_commit(&sm.empty[kVRing + sv]);  // the V slot
+                }
+                __syncwarp();
+                ++npv;
+                prog = true;
+            }
+        }
         if (ti.valid() && ns - npv < 3) {
             const Item& it = ti.pc.it;
             const int sk = static_cast<int>(ns % SK), b = ns & 1;
@@ -371,38 +404,6 @@ __device__ void mma_warp(const SplitParams& p, const Sched& sc, const Smem& sm, 
                 }
                 __syncwarp();
                 ++ns;
-                prog = true;
-            }
-        }
-        if (npv < ns) {
-            const Pend pd = pend[npv & 3];
-            const int sv = static_cast<int>(npv % SV);
-            bool ready = true;
-            if (lane == 0) {
-                ready = mbar_test_wait(ts.p_full, npv & 1) &&
-                        mbar_test_wait(&sm.full[kVRing + sv], (npv / SV) & 1);
-                if (ready && pd.first && pd.pc >= 2)
-                    ready = mbar_test_wait(&ts.o_free[pd.pc & 1], ((pd.pc >> 1) - 1) & 1);
-            }
-            if (__shfl_sync(kFull, ready ? 1 : 0, 0)) {
-                const uint32_t st = ring_v + sv * p.stage_bytes;
-                if (pd.t0 + pd.n_tile > pd.past || (pd.n_tile & 15)) {
-                    fix_tile(st, static_cast<const T*>(p.v_new) + pd.nrow * kTcD, pd.t0, pd.n_tile, pd.past, true,
-                             lane);
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint64_t dv = smem_desc(st, kHalfBytes, 1024);
-                    const uint32_t to = tmem + kColO + (pd.pc & 1) * 64;
-                    for (int ks = 0; ks < pd.nks; ++ks)
-                        umma(to, dv + ((ks * 2048) >> 4), dp + ((ks * 2048) >> 4), id_o, !(pd.first && ks == 0));
-                    umma_commit(ts.pv_done);
-                    umma_commit(&sm.empty[kVRing + sv]);  // the V slot
-                }
-                __syncwarp();
-                ++npv;
                 prog = true;
             }
         }
@@ -523,9 +524,6 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
 #pragma unroll
             for (int r = 0; r < kWarpRows; ++r)
                 need |= x[r] > m[r] + kGrowth;
-            if (ok && gt >= 1)  // PV of stage gt - 1 has read the P^T tile (and O is current)
-                ok = !*sm.abort_flag && mbar_wait_bounded(ts.pv_done, (gt - 1) & 1, p.wait_ns);
-            ok = __all_sync(kFull, ok);
             if (soft_bar_or(bar, need || !ok)) {
                 if (soft_bar_or(bar, !ok)) {
                     give_up(ok);
@@ -552,7 +550,13 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
                 }
                 __syncwarp();
                 if (j > 0 && shrink) {  // uniform over the row half: m is
-                    // O of the piece's stages so far (their PV has completed)
+                    // O of the piece's stages so far, once the last one's PV is done
+                    bool ok2 = !*sm.abort_flag && mbar_wait_bounded(ts.pv_done, (gt - 1) & 1, p.wait_ns);
+                    ok2 = __all_sync(kFull, ok2);
+                    if (soft_bar_or(bar, !ok2)) {
+                        give_up(ok2);
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t to = tl + kColO + (piece & 1) * 64 + h * kWarpRows;
 #pragma unroll
@@ -567,23 +571,34 @@ __device__ void softmax_warps(const SplitParams& p, const Sched& sc, const Smem&
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
             }
-            // P = 2^(x - m): the row sums, and P^T (high | remainder) of this
-            // warp's rows (chunks 2h, 2h + 1 and 4 + 2h, 5 + 2h of its token row)
-            const uint32_t pr = prow;
+            // P = 2^(x - m) into registers and the row sums; then, once PV of
+            // stage gt - 1 has read the P^T tile, P^T (high | remainder) of this
+            // warp's rows (chunks 2h, 2h + 1 and 4 + 2h, 5 + 2h of its token row).
+            // A wait that runs out skips the stage; the next barrier of the row
+            // half then gives up uniformly (the abort flag is set).
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float p0 = fast_exp2(x[2 * k] - m[2 * k]);
+                const float p1 = fast_exp2(x[2 * k + 1] - m[2 * k + 1]);
+                l[2 * k] += p0;
+                l[2 * k + 1] += p1;
+                split_pair<T>(p0, p1, hi[k], lo[k]);
+            }
+            bool pv_ok = true;
+            if (gt >= 1)
+                pv_ok = !*sm.abort_flag && mbar_wait_bounded(ts.pv_done, (gt - 1) & 1, p.wait_ns);
+            if (!__all_sync(kFull, pv_ok)) {
+                if (lane == 0)
+                    flag_timeout(p, sm.abort_flag);
+                continue;
+            }
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r0 = 8 * cc + 2 * k;
-                    const float p0 = fast_exp2(x[r0] - m[r0]);
-                    const float p1 = fast_exp2(x[r0 + 1] - m[r0 + 1]);
-                    l[r0] += p0;
-                    l[r0 + 1] += p1;
-                    split_pair<T>(p0, p1, hi[k], lo[k]);
-                }
-                st_shared4(pr + (((2 * h + cc) ^ swz) << 4), hi[0], hi[1], hi[2], hi[3]);
-                st_shared4(pr + (((4 + 2 * h + cc) ^ swz) << 4), lo[0], lo[1], lo[2], lo[3]);
+                st_shared4(prow + (((2 * h + cc) ^ swz) << 4), hi[4 * cc], hi[4 * cc + 1], hi[4 * cc + 2],
+                           hi[4 * cc + 3]);
+                st_shared4(prow + (((4 + 2 * h + cc) ^ swz) << 4), lo[4 * cc], lo[4 * cc + 1], lo[4 * cc + 2],
+                           lo[4 * cc + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
