@@ -122,7 +122,8 @@ def aggregate(rank_bytes: int, rank_ms: float, world: int):
 # these are unchanged (comments and whitespace aside).
 KERNEL_SOURCES = {
     "decode": ["pa_kernels.cuh", "pa_common.cuh", "pa_ptx.cuh", "pa_inst_f32.cu", "pa_inst_f16.cu",
-               "pa_inst_bf16.cu", "pa_host.cu", "../../include/pa_decode.h"],
+               "pa_inst_bf16.cu", "pa_decode_tc.cu", "pa_tc.cuh", "pa_host.cu",
+               "../../include/pa_decode.h"],
     "prefill_tc": ["pa_prefill_tc.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_common.cuh", "pa_host.cu"],
     "vjp": ["pa_vjp.cu", "pa_vjp_tc.cu", "pa_vjp.cuh", "pa_tc.cuh", "pa_ptx.cuh",
             "../../include/pa_attention_vjp.h"],
@@ -148,11 +149,15 @@ def kernel_sources_sha256(family: str = "decode") -> str:
 
 def partition_kernel_name(spec):
     """Which partition kernel runs a workload: float32 caches take the
-    CUDA-core kernel; 16-bit caches the transposed tensor-core kernel at 8 or
-    fewer query rows per KV head, else the 16-row one."""
+    CUDA-core kernel; 16-bit caches the transposed mma.sync kernel at 8 or
+    fewer query rows per KV head, the tcgen05 kernel above 16 rows at D = 128,
+    else the 16-row mma.sync one."""
     if spec.dtype == "f32":
         return "pa_split_kernel"
-    return "pa_mmat_kernel" if spec.group * spec.NQ <= 8 else "pa_mma_kernel"
+    rows = spec.group * spec.NQ
+    if rows <= 8:
+        return "pa_mmat_kernel"
+    return "pa_umma32_kernel" if rows > 16 and spec.D == 128 else "pa_mma_kernel"
 
 
 def captured_traffic(kernel: str, workload: str, family: str = "decode"):
