@@ -861,6 +861,9 @@ struct AppendParams {
 
 __global__ void __launch_bounds__(256) pa_append_kernel(const __grid_constant__ AppendParams a)
 {
+    // a decode launched after it may start (it waits for this grid before
+    // reading anything this kernel writes)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long per = a.rows * a.vpr;  // vectors of K (or V)
     if (i >= 2 * per)
@@ -902,6 +905,9 @@ struct GatherParams {
 
 __global__ void __launch_bounds__(256) pa_gather_kernel(const __grid_constant__ GatherParams g)
 {
+    // the decode launched next sets up while the inputs move (it waits for
+    // this grid before reading them)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int k = blockIdx.y;
     const int n = g.bytes[k];
     const int t = blockIdx.x * blockDim.x + threadIdx.x, nt = gridDim.x * blockDim.x;
