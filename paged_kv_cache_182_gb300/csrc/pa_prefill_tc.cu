@@ -73,18 +73,51 @@ struct PrefillTcParams {
     int* status;
     float qscale;             // scale * log2(e)
     int B, H, KV, NQ, BLOCK, maxb, num_blocks, g, T, tiles;  // tiles: row tiles per (b, kh)
+    int total;                // row tiles in all: B * KV * tiles
 };
 
 struct TcBars {
     // s_full, p_full and o_done alternate by key-tile parity (the S buffer);
-    // the K and V rings have kTcStages stages
-    uint64_t q_full, k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages], s_full[2],
-        p_full[2], o_done[2];
+    // the K and V rings have kTcStages stages; q_empty: the row tile's S MMAs
+    // are done with the query tile; o_free: its epilogue has read O
+    uint64_t q_full, q_empty, o_free, fin, k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages],
+        v_empty[kTcStages], s_full[2], p_full[2], o_done[2];
     uint32_t tmem;
     int abort;
     float xchg[2][2][kTcTile];  // [tile parity][column half][row]: partial row maxima, then sums
 };
 static_assert(sizeof(TcBars) <= 3072, "barrier area");
+
+// Row tile i of the grid's work: the last row tiles see the most keys and come
+// first (the row tile is the slowest index).  Persistent CTA c of G takes the
+// tiles c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... in turn (a snake over that
+// order, so that every CTA gets long and short tiles).
+__device__ __forceinline__ int tile_of(int k, int c, int G) { return (k & 1) ? (k + 1) * G - 1 - c : k * G + c; }
+
+struct RowTile {
+    int b, kh, r_base, r_last, past, end, ntiles;
+};
+
+__device__ __forceinline__ RowTile row_tile(const PrefillTcParams& p, int i, int tid)
+{
+    RowTile rt;
+    const int t = p.tiles - 1 - i / (p.B * p.KV);
+    rt.kh = (i % (p.B * p.KV)) % p.KV;
+    rt.b = (i % (p.B * p.KV)) / p.KV;
+    rt.r_base = t * p.T;
+    rt.r_last = min(rt.r_base + p.T, p.NQ) - 1;  // last new row of the tile
+    const int cap = p.maxb * p.BLOCK - p.NQ;      // largest past the table can hold
+    int past = p.seq_lens[rt.b];
+    if (past < 0 || past > cap) {
+        if (tid == 0 && t == 0 && rt.kh == 0 && p.status)
+            atomicOr(p.status, PA_STATUS_BAD_LENGTH);
+        past = past < 0 ? 0 : (cap < 0 ? 0 : cap);
+    }
+    rt.past = past;
+    rt.end = past + p.NQ;                                          // keys of the sequence
+    rt.ntiles = (past + rt.r_last + 1 + kTcTile - 1) / kTcTile;  // keys 0 .. past + r_last
+    return rt;
+}
 
 template <typename T, typename TO>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -105,25 +138,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcBars& bars = *reinterpret_cast<TcBars*>(base + (2 + 4 * kTcStages) * kTcHalf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the last row tiles see the most keys: all of them are launched first
-    // (row tile slowest), so that the short ones fill the last wave
-    const int rt = p.tiles - 1 - static_cast<int>(blockIdx.x / (p.B * p.KV));
-    const int kh = static_cast<int>(blockIdx.x % (p.B * p.KV)) % p.KV;
-    const int b = static_cast<int>(blockIdx.x % (p.B * p.KV)) / p.KV;
-    const int r_base = rt * p.T;
-    const int r_last = min(r_base + p.T, p.NQ) - 1;  // last new row of the tile
-    const int cap = p.maxb * p.BLOCK - p.NQ;         // largest past the table can hold
-    int past = p.seq_lens[b];
-    if (past < 0 || past > cap) {
-        if (tid == 0 && rt == 0 && kh == 0 && p.status)
-            atomicOr(p.status, PA_STATUS_BAD_LENGTH);
-        past = past < 0 ? 0 : (cap < 0 ? 0 : cap);
-    }
-    const int end = past + p.NQ;                                 // keys of the sequence
-    const int ntiles = (past + r_last + 1 + kTcTile - 1) / kTcTile;  // keys 0 .. past + r_last
+    const int C = blockIdx.x, G = gridDim.x;
 
     if (tid == 0) {
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
+        mbar_init(&bars.o_free, kTcSoftmax / 32);  // one arrival per softmax warp
+        mbar_init(&bars.fin, 1);
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
@@ -156,13 +177,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (p.status)
             atomicOr(p.status, PA_STATUS_TIMEOUT);
     };
+    // Key tiles are counted over all of this CTA's row tiles (g below): the
+    // rings, S buffers and their barriers run on across row tiles.
 
     if (warp == 8 || warp == 9) {
         // ----------------------------------------------------------- TMA producers
-        // Warp 8 issues the K boxes (and q), warp 9 the V boxes: lane k the
-        // boxes (both 64-column halves) of cache block k of each key tile; the
-        // table entries of the next tile are loaded while the current one is in
-        // flight.
+        // Warp 8 issues the K boxes (and each row tile's q, once the previous
+        // row tile's S MMAs are done with the query tile), warp 9 the V boxes:
+        // lane k the boxes (both 64-column halves) of cache block k of each
+        // key tile; the table entries of the next tile are loaded while the
+        // current one is in flight.
         const bool is_v = warp == 9;
         const CUtensorMap* map = is_v ? &vmap : &kmap;
         unsigned char* ring = is_v ? sV : sK;
@@ -171,262 +195,326 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int boxes = kTcTile / p.BLOCK;
         if (lane == 0) {
             tma_prefetch_desc(map);
-            if (!is_v) {
+            if (!is_v)
                 tma_prefetch_desc(&qmap);
-                mbar_arrive_expect_tx(&bars.q_full, 2 * kTcHalf);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_5d(sQ + h * kTcHalf, &qmap, 0, h, r_base, kh * p.g, b, &bars.q_full);
-            }
         }
-        auto entry = [&](int t) {  // cache row of this lane's block in tile t, or out of range
-            const int tok = t * kTcTile + lane * p.BLOCK;
-            const int blk = tok / p.BLOCK;
-            int row0 = p.num_blocks * p.BLOCK;  // past the pool: the box reads zeros
-            if (lane < boxes && t < ntiles && tok < end && blk < p.maxb) {
-                const int phys = p.table[static_cast<size_t>(b) * p.maxb + blk];
-                if (phys >= 0 && phys < p.num_blocks)
-                    row0 = phys * p.BLOCK;
-            }
-            return row0;
-        };
-        int row_next = entry(0);
-        int issued = 0;
-        // launched as a programmatic dependent of the store of the new rows:
-        // the cache is read only once that grid has completed
-        grid_dependency_wait();
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % kTcStages;
-            const int row0 = row_next;
-            if (t >= kTcStages) {
-                bool ok = !*abort_flag && mbar_wait_bounded(&empty[s], ((t / kTcStages) - 1) & 1, kWaitLimitNs);
-                ok = __all_sync(kFull, ok);
-                if (!ok) {
-                    if (lane == 0)
-                        fail();
-                    break;
+        int issued = 0, q_issued = 0;  // key tiles, query tiles
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int i = tile_of(k, C, G);
+            if (i >= p.total)
+                break;
+            const RowTile rt = row_tile(p, i, tid);
+            if (!is_v) {
+                if (q_issued > 0) {
+                    ok = !*abort_flag && mbar_wait_bounded(&bars.q_empty, (q_issued - 1) & 1, kWaitLimitNs);
+                    ok = __all_sync(kFull, ok);
+                    if (!ok) {
+                        if (lane == 0)
+                            fail();
+                        break;
+                    }
                 }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars.q_full, 2 * kTcHalf);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_5d(sQ + h * kTcHalf, &qmap, 0, h, rt.r_base, rt.kh * p.g, rt.b, &bars.q_full);
+                }
+                ++q_issued;
             }
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[s], 2 * kTcHalf);
-            __syncwarp();
-            if (lane < boxes)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(ring + s * 2 * kTcHalf + h * kTcHalf + lane * p.BLOCK * 128, map, 0, h, kh, row0,
-                                &full[s]);
-            issued = t + 1;
-            row_next = entry(t + 1);
+            auto entry = [&](int t) {  // cache row of this lane's block in tile t, or out of range
+                const int tok = t * kTcTile + lane * p.BLOCK;
+                const int blk = tok / p.BLOCK;
+                int row0 = p.num_blocks * p.BLOCK;  // past the pool: the box reads zeros
+                if (lane < boxes && t < rt.ntiles && tok < rt.end && blk < p.maxb) {
+                    const int phys = p.table[static_cast<size_t>(rt.b) * p.maxb + blk];
+                    if (phys >= 0 && phys < p.num_blocks)
+                        row0 = phys * p.BLOCK;
+                }
+                return row0;
+            };
+            int row_next = entry(0);
+            // launched as a programmatic dependent of the store of the new rows:
+            // the cache is read only once that grid has completed
+            if (k == 0)
+                grid_dependency_wait();
+            for (int t = 0; t < rt.ntiles; ++t) {
+                const int g = issued, s = g % kTcStages;
+                const int row0 = row_next;
+                if (g >= kTcStages) {
+                    ok = !*abort_flag && mbar_wait_bounded(&empty[s], ((g / kTcStages) - 1) & 1, kWaitLimitNs);
+                    ok = __all_sync(kFull, ok);
+                    if (!ok) {
+                        if (lane == 0)
+                            fail();
+                        break;
+                    }
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[s], 2 * kTcHalf);
+                __syncwarp();
+                if (lane < boxes)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(ring + s * 2 * kTcHalf + h * kTcHalf + lane * p.BLOCK * 128, map, 0, h, rt.kh,
+                                    row0, &full[s]);
+                issued = g + 1;
+                row_next = entry(t + 1);
+            }
         }
         // no copy may land after the CTA's memory is released: wait (bounded)
         // for the last tile issued on each stage (and for q)
         if (lane == 0) {
             for (int t = issued > kTcStages ? issued - kTcStages : 0; t < issued; ++t)
                 mbar_wait_bounded(&full[t % kTcStages], (t / kTcStages) & 1, kWaitLimitNs);
-            if (!is_v)
-                mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
+            if (!is_v && q_issued > 0)
+                mbar_wait_bounded(&bars.q_full, (q_issued - 1) & 1, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 10) {
         // -------------------------------------------------------------- MMA issuer
-        // S(t + 1) goes into the S buffer that held P(t - 1): P(t - 1).V was
-        // issued before it by this thread, and the MMAs of one thread run in
-        // order.  A commit of S(t + 1) thus also covers P(t - 1).V.
+        // Over the key tiles of all row tiles in order: S of key tile g + 1
+        // (possibly of the next row tile, once its query tile has landed), then
+        // P(g).V.  S(g + 1) goes into the S buffer that held P(g - 1): P(g - 1).V
+        // was issued before it by this thread, and the MMAs of one thread run in
+        // order, so a commit of S(g + 1) also covers P(g - 1).V.  After a row
+        // tile's last S the query tile is committed free; before its first P.V,
+        // the previous row tile's epilogue must have read O.
         if (lane == 0) {
-            bool ok = mbar_wait_bounded(&bars.q_full, 0, kWaitLimitNs);
             const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
             const uint32_t id_s = idesc<kBf>(kTcTile, false), id_o = idesc<kBf>(kTcD, true);
-            // S(u) = Q K(u)^T over the head dimension (K-steps of 16 columns, four
-            // per 64-column half) into S buffer u & 1, once K(u) has landed; K's
-            // stage is released when these MMAs complete
-            auto issue_s = [&](int u) {
-                const int ku = u % kTcStages;
-                if (*abort_flag || !mbar_wait_bounded(&bars.k_full[ku], (u / kTcStages) & 1, kWaitLimitNs))
+            // the S cursor (row tile k_s of this CTA, its key tile u_s, global g_s)
+            // runs one key tile ahead of the P.V cursor
+            int k_s = 0, u_s = 0, g_s = 0;
+            RowTile rt_s{};
+            bool s_valid = tile_of(0, C, G) < p.total;
+            if (s_valid)
+                rt_s = row_tile(p, tile_of(0, C, G), tid);
+            bool ok = true;
+            auto issue_s = [&]() {  // S(g_s) = Q K(g_s)^T, then the cursor moves on
+                const int ku = g_s % kTcStages;
+                if (u_s == 0 && (*abort_flag || !mbar_wait_bounded(&bars.q_full, k_s & 1, kWaitLimitNs)))
+                    return false;
+                if (*abort_flag || !mbar_wait_bounded(&bars.k_full[ku], (g_s / kTcStages) & 1, kWaitLimitNs))
                     return false;
                 tc_fence_after();
                 for (int ks = 0; ks < kTcD / 16; ++ks) {
                     const uint32_t o = (ks >> 2) * kTcHalf + (ks & 3) * 32;
-                    umma(tS0 + (u & 1) * kTcTile, smem_desc(qa + o, 16, 1024),
+                    umma(tS0 + (g_s & 1) * kTcTile, smem_desc(qa + o, 16, 1024),
                          smem_desc(ka + ku * 2 * kTcHalf + o, 16, 1024), id_s, ks > 0);
                 }
-                umma_commit(&bars.s_full[u & 1]);
+                umma_commit(&bars.s_full[g_s & 1]);
                 umma_commit(&bars.k_empty[ku]);
+                ++g_s;
+                if (++u_s == rt_s.ntiles) {
+                    umma_commit(&bars.q_empty);  // the query tile, once these S are done
+                    u_s = 0;
+                    ++k_s;
+                    const int i = tile_of(k_s, C, G);
+                    s_valid = i < p.total;
+                    if (s_valid)
+                        rt_s = row_tile(p, i, tid);
+                }
                 return true;
             };
-            if (ok && ntiles > 0)
-                ok = issue_s(0);
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int sb = t & 1, vs = t % kTcStages;
-                if (t + 1 < ntiles && !issue_s(t + 1)) {
-                    ok = false;
+            if (s_valid)
+                ok = issue_s();
+            int g = 0;
+            for (int k = 0; ok; ++k) {
+                const int i = tile_of(k, C, G);
+                if (i >= p.total)
                     break;
-                }
-                ok = mbar_wait_bounded(&bars.p_full[sb], (t >> 1) & 1, kWaitLimitNs);
-                if (ok)
-                    ok = mbar_wait_bounded(&bars.v_full[vs], (t / kTcStages) & 1, kWaitLimitNs);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                // O += P_hi V + P_lo V over the tile's keys.  P from tensor memory:
-                // keys 64 h + 16 j + (0 .. 15) of the high part at column
-                // 64 h + 8 j of the S buffer, the remainder 32 columns further;
-                // V is MN-major (its rows are keys, 64 columns of D per half, the
-                // halves 16 KB apart)
-                const uint32_t tP = tS0 + sb * kTcTile;
-                for (int part = 0; part < 2; ++part)
-                    for (int ks = 0; ks < kTcTile / 16; ++ks) {
-                        const uint32_t pcol = (ks >> 2) * 64 + part * 32 + (ks & 3) * 8;
-                        umma_ts(tO, tP + pcol, smem_desc(va + vs * 2 * kTcHalf + ks * 2048, kTcHalf, 1024), id_o,
-                                t > 0 || part > 0 || ks > 0);
+                const RowTile rt = row_tile(p, i, tid);
+                for (int t = 0; t < rt.ntiles && ok; ++t, ++g) {
+                    const int sb = g & 1, vs = g % kTcStages;
+                    if (s_valid && !issue_s()) {
+                        ok = false;
+                        break;
                     }
-                umma_commit(&bars.o_done[sb]);
-                umma_commit(&bars.v_empty[vs]);
+                    ok = mbar_wait_bounded(&bars.p_full[sb], (g >> 1) & 1, kWaitLimitNs);
+                    if (ok)
+                        ok = mbar_wait_bounded(&bars.v_full[vs], (g / kTcStages) & 1, kWaitLimitNs);
+                    if (ok && t == 0 && k > 0)
+                        ok = mbar_wait_bounded(&bars.o_free, (k - 1) & 1, kWaitLimitNs);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    // O += P_hi V + P_lo V over the tile's keys.  P from tensor memory:
+                    // keys 64 h + 16 j + (0 .. 15) of the high part at column
+                    // 64 h + 8 j of the S buffer, the remainder 32 columns further;
+                    // V is MN-major (its rows are keys, 64 columns of D per half, the
+                    // halves 16 KB apart)
+                    const uint32_t tP = tS0 + sb * kTcTile;
+                    for (int part = 0; part < 2; ++part)
+                        for (int ks = 0; ks < kTcTile / 16; ++ks) {
+                            const uint32_t pcol = (ks >> 2) * 64 + part * 32 + (ks & 3) * 8;
+                            umma_ts(tO, tP + pcol, smem_desc(va + vs * 2 * kTcHalf + ks * 2048, kTcHalf, 1024),
+                                    id_o, t > 0 || part > 0 || ks > 0);
+                        }
+                    umma_commit(&bars.o_done[sb]);
+                    umma_commit(&bars.v_empty[vs]);
+                }
             }
             if (!ok)
                 fail();
+            // every MMA complete before the tensor memory is freed
+            umma_commit(&bars.fin);
+            mbar_wait_bounded(&bars.fin, 0, kWaitLimitNs);
         }
         __syncwarp();
     } else {
         // ---------------------------------------------- softmax and epilogue (rows)
         const int row = (warp & 3) * 32 + lane;  // tile row = tensor-memory lane
         const int part = warp >> 2;              // key columns [64 part, 64 part + 64)
-        const int hg = row / p.T, tt = row - hg * p.T;
-        const int r = r_base + tt;
-        const bool real = r < p.NQ;
-        const int limit = past + r;  // last visible key
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t col0 = part * 64;
         const int pair_bar = 1 + (warp & 3);  // named barrier of warps w, w + 4
-        // m: the maximum the exponentials are taken against (the running
-        // maximum, moved only when the maximum grows by more than 2^8: P stays
-        // at most 256, and O / l is the same for any reference); l: this
-        // thread's share of the sum
-        float m = -INFINITY, l = 0.f;
-        const int vis = past + r_base;  // every row of the tile sees keys 0 .. vis
-        // The two warps of a row meet at one barrier per tile (the maximum
-        // exchange), and leave the loop only there, together: a wait that gave
-        // up (`fault`, warp-uniform) is OR-ed into that barrier.
+        const int hg = row / p.T, tt = row - hg * p.T;
+        int g0 = 0;  // key tiles of this CTA's earlier row tiles
         bool ok = true;
-        bool fault = false;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t & 1;
-            const bool got = __all_sync(
-                kFull, !fault && !*abort_flag && mbar_wait_bounded(&bars.s_full[s], (t >> 1) & 1, kWaitLimitNs));
-            float sc[64];
-            float pm = -INFINITY;
-            if (got) {
-                tc_fence_after();
-                const bool masked = t * kTcTile + kTcTile - 1 > vis;  // uniform over the CTA
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    Cols32 x;
-                    tmem_ld32(x, tS0 + s * kTcTile + lane_off + col0 + c * 32);
-                    if (masked) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int key = t * kTcTile + col0 + c * 32 + j;
-                            sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
-                            pm = fmaxf(pm, sc[c * 32 + j]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            sc[c * 32 + j] = __uint_as_float(x.r[j]) * p.qscale;
-                            pm = fmaxf(pm, sc[c * 32 + j]);
-                        }
-                    }
-                }
-            }
-            // the other half of the row's maximum
-            bars.xchg[s][part][row] = pm;
-            if (pair_bar_or(pair_bar, !got)) {
-                ok = false;
+        for (int k = 0; ok; ++k) {
+            const int i = tile_of(k, C, G);
+            if (i >= p.total)
                 break;
-            }
-            const float tile_max = fmaxf(pm, bars.xchg[s][part ^ 1][row]);
-            // both threads of the row take the same decision from the same values
-            const float mt = tile_max > m + 8.f ? tile_max : m;
-            const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf), else 1 or tiny
-            float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                sc[j] = fast_exp2(sc[j] - mt);
-                sum += sc[j];
-            }
-            l = l * alpha + sum;
-            m = mt;
-            // keys past the sequence end inside its last cache block hold other
-            // data (not finite for certain): their V rows are zeroed, since
-            // P = 0 does not cancel a non-finite value in the MMA
-            const int tok = t * kTcTile + row;
-            if (t * kTcTile + kTcTile > end) {  // uniform over the CTA
-                // the V stage has landed; the wait orders these stores after the
-                // copy's writes (and they come before p_full, which P.V waits for)
-                const int vs = t % kTcStages;
-                const bool landed = __all_sync(
-                    kFull, mbar_wait_bounded(&bars.v_full[vs], (t / kTcStages) & 1, kWaitLimitNs));
-                fault |= !landed;
-                if (landed && tok >= end) {
-                    uint4* vrow = reinterpret_cast<uint4*>(sV + vs * 2 * kTcHalf + part * kTcHalf + row * 128);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        vrow[c] = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            // O is rescaled only when a row maximum moved (warp-uniform: tcgen05
-            // ld/st are warp-wide), after P(t - 1).V has completed
-            if (t > 0 && __any_sync(kFull, alpha != 1.f)) {
-                const bool done = __all_sync(
-                    kFull, !fault && mbar_wait_bounded(&bars.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, kWaitLimitNs));
-                fault |= !done;
-                if (done) {
+            const RowTile rt = row_tile(p, i, tid);
+            const int r = rt.r_base + tt;
+            const bool real = r < p.NQ;
+            const int limit = rt.past + r;  // last visible key
+            // m: the maximum the exponentials are taken against (the running
+            // maximum, moved only when the maximum grows by more than 2^8: P stays
+            // at most 256, and O / l is the same for any reference); l: this
+            // thread's share of the sum
+            float m = -INFINITY, l = 0.f;
+            const int vis = rt.past + rt.r_base;  // every row of the tile sees keys 0 .. vis
+            // The two warps of a row meet at one barrier per tile (the maximum
+            // exchange), and leave the loop only there, together: a wait that gave
+            // up (`fault`, warp-uniform) is OR-ed into that barrier.
+            bool fault = false;
+            for (int t = 0; t < rt.ntiles; ++t) {
+                const int g = g0 + t, s = g & 1;
+                const bool got = __all_sync(kFull, !fault && !*abort_flag &&
+                                                       mbar_wait_bounded(&bars.s_full[s], (g >> 1) & 1, kWaitLimitNs));
+                float sc[64];
+                float pm = -INFINITY;
+                if (got) {
                     tc_fence_after();
+                    const bool masked = t * kTcTile + kTcTile - 1 > vis;  // uniform over the CTA
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         Cols32 x;
-                        tmem_ld32(x, tO + lane_off + col0 + c * 32);
+                        tmem_ld32(x, tS0 + s * kTcTile + lane_off + col0 + c * 32);
+                        if (masked) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
-                        tmem_st32(x, tO + lane_off + col0 + c * 32);
+                            for (int j = 0; j < 32; ++j) {
+                                const int key = t * kTcTile + col0 + c * 32 + j;
+                                sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
+                                pm = fmaxf(pm, sc[c * 32 + j]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                sc[c * 32 + j] = __uint_as_float(x.r[j]) * p.qscale;
+                                pm = fmaxf(pm, sc[c * 32 + j]);
+                            }
+                        }
                     }
                 }
-            }
-            // P as high part + remainder, packed 16-bit pairs, over this thread's
-            // own S columns (it has read them): keys 64 part + 2 e, 2 e + 1 of the
-            // high part at column 64 part + e, of the remainder at 64 part + 32 + e.
-            // S(t) was committed after P(t - 2).V, so that product is complete.
-            {
-                Cols32 hi, lo;
+                // the other half of the row's maximum
+                bars.xchg[s][part][row] = pm;
+                if (pair_bar_or(pair_bar, !got)) {
+                    ok = false;
+                    break;
+                }
+                const float tile_max = fmaxf(pm, bars.xchg[s][part ^ 1][row]);
+                // both threads of the row take the same decision from the same values
+                const float mt = tile_max > m + 8.f ? tile_max : m;
+                const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf), else 1 or tiny
+                float sum = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    split_pair<T>(sc[2 * e], sc[2 * e + 1], hi.r[e], lo.r[e]);
-                tmem_st32(hi, tS0 + s * kTcTile + lane_off + col0);
-                tmem_st32(lo, tS0 + s * kTcTile + lane_off + col0 + 32);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                for (int j = 0; j < 64; ++j) {
+                    sc[j] = fast_exp2(sc[j] - mt);
+                    sum += sc[j];
+                }
+                l = l * alpha + sum;
+                m = mt;
+                // keys past the sequence end inside its last cache block hold other
+                // data (not finite for certain): their V rows are zeroed, since
+                // P = 0 does not cancel a non-finite value in the MMA
+                const int tok = t * kTcTile + row;
+                if (t * kTcTile + kTcTile > rt.end) {  // uniform over the CTA
+                    // the V stage has landed; the wait orders these stores after the
+                    // copy's writes (and they come before p_full, which P.V waits for)
+                    const int vs = g % kTcStages;
+                    const bool landed = __all_sync(
+                        kFull, mbar_wait_bounded(&bars.v_full[vs], (g / kTcStages) & 1, kWaitLimitNs));
+                    fault |= !landed;
+                    if (landed && tok >= rt.end) {
+                        uint4* vrow = reinterpret_cast<uint4*>(sV + vs * 2 * kTcHalf + part * kTcHalf + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                // O is rescaled only when a row maximum moved (warp-uniform: tcgen05
+                // ld/st are warp-wide), after P(g - 1).V has completed
+                if (t > 0 && __any_sync(kFull, alpha != 1.f)) {
+                    const bool done = __all_sync(
+                        kFull, !fault && mbar_wait_bounded(&bars.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1,
+                                                           kWaitLimitNs));
+                    fault |= !done;
+                    if (done) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            Cols32 x;
+                            tmem_ld32(x, tO + lane_off + col0 + c * 32);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                x.r[j] = __float_as_uint(__uint_as_float(x.r[j]) * alpha);
+                            tmem_st32(x, tO + lane_off + col0 + c * 32);
+                        }
+                    }
+                }
+                // P as high part + remainder, packed 16-bit pairs, over this thread's
+                // own S columns (it has read them): keys 64 part + 2 e, 2 e + 1 of the
+                // high part at column 64 part + e, of the remainder at 64 part + 32 + e.
+                // S(g) was committed after P(g - 2).V, so that product is complete.
+                {
+                    Cols32 hi, lo;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        split_pair<T>(sc[2 * e], sc[2 * e + 1], hi.r[e], lo.r[e]);
+                    tmem_st32(hi, tS0 + s * kTcTile + lane_off + col0);
+                    tmem_st32(lo, tS0 + s * kTcTile + lane_off + col0 + 32);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+                fence_proxy_async_smem();  // the zeroed V rows
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars.p_full[s]);
             }
-            fence_proxy_async_smem();  // the zeroed V rows
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars.p_full[s]);
-        }
-        if (ok && ntiles > 0)
-            ok = __all_sync(kFull, !fault && mbar_wait_bounded(&bars.o_done[(ntiles - 1) & 1],
-                                                               ((ntiles - 1) >> 1) & 1, kWaitLimitNs));
-        // the row sum over both halves, through the exchange slots of tile
-        // parity ntiles & 1: the partner's last read of them came before the
-        // last tile's barrier
-        const int sl = ntiles & 1;
-        if (ok)
-            bars.xchg[sl][part][row] = l;
-        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-        if (!ok) {
-            if (lane == 0)
-                fail();
-        } else {
+            const int gl = g0 + rt.ntiles - 1;  // the row tile's last key tile
+            if (ok)
+                ok = __all_sync(kFull, !fault && mbar_wait_bounded(&bars.o_done[gl & 1], (gl >> 1) & 1,
+                                                                   kWaitLimitNs));
+            // the row sum over both halves, through the exchange slots of parity
+            // gl + 1: the partner's last read of them came before the last tile's
+            // barrier; a second barrier after the reads keeps the next row tile's
+            // first maximum exchange (the same slots) behind them.  Both warps of
+            // the row take the decision to go on together (the OR of a failure).
+            const int sl = (gl + 1) & 1;
+            if (ok)
+                bars.xchg[sl][part][row] = l;
+            if (pair_bar_or(pair_bar, !ok)) {
+                if (!ok && lane == 0)
+                    fail();
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const float L = l + bars.xchg[sl][part ^ 1][row];
-            const int h = kh * p.g + hg;
-            TO* o = static_cast<TO*>(p.out) + ((static_cast<size_t>(b) * p.H + h) * p.NQ + r) * kTcD + col0;
+            const int h = rt.kh * p.g + hg;
+            TO* o = static_cast<TO*>(p.out) + ((static_cast<size_t>(rt.b) * p.H + h) * p.NQ + r) * kTcD + col0;
             const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -439,6 +527,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (real)
                     store_row<TO>(o + c * 32, v);
             }
+            // O is free for the next row tile's first P.V
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.o_free);
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            g0 += rt.ntiles;
         }
     }
     tc_fence_before();
@@ -528,9 +623,19 @@ int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, c
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTcSmem) != cudaSuccess)
         return PA_ERR_CUDA;
-    const long long grid = static_cast<long long>(B) * KV * prm.tiles;
-    if (grid >= (1ll << 31))
+    const long long total = static_cast<long long>(B) * KV * prm.tiles;
+    if (total >= (1ll << 31) / 4)
         return PA_ERR_BAD_DIMS;
+    prm.total = static_cast<int>(total);
+    // persistent: one CTA per SM (shared and tensor memory allow no more)
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            return PA_ERR_CUDA;
+    }
+    const long long grid = total < sms ? total : sms;
     // programmatic dependent launch: the CTAs set up (barriers, tensor memory,
     // the query tile) while the store of the new rows finishes; the TMA
     // producers wait for it before reading the cache

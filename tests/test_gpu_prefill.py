@@ -64,6 +64,7 @@ CASES = [
     ("bf16", 16, 16, 128, 32, 45, [0, 130]),     # one head per tile: 128 rows, partial
     ("bf16", 64, 4, 128, 64, 70, [9, 1000]),     # 16 heads x 8 rows a tile, BLOCK 64
     ("f16", 16, 2, 128, 8, 130, [250, 3]),       # 8 heads x 16 rows, 16 blocks a key tile
+    ("f16", 32, 8, 128, 16, 630, [0, 300]),      # 320 row tiles: several per persistent CTA, ragged last
 ]
 
 
