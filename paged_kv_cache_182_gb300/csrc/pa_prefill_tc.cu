@@ -67,6 +67,7 @@ constexpr int kTcSmem = (2 + 4 * kTcStages) * kTcHalf + 3072;
 static_assert(kTcSmem <= 232448, "prefill shared memory");
 
 struct PrefillTcParams {
+    const void* q;            // [B][H][NQ][D] (for L2 prefetches; the tiles come by TMA)
     const int32_t* table;     // [B][maxb]
     const int32_t* seq_lens;  // [B] cached tokens before the new rows
     void* out;                // [B][H][NQ][D]
@@ -221,6 +222,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tma_load_5d(sQ + h * kTcHalf, &qmap, 0, h, rt.r_base, rt.kh * p.g, rt.b, &bars.q_full);
                 }
                 ++q_issued;
+                // the next row tile's query rows into L2 (its load waits for
+                // this tile's S MMAs): g heads x T rows of 256 bytes, 128-byte lines
+                const int i_next = tile_of(k + 1, C, G);
+                if (i_next < p.total) {
+                    const int t_n = p.tiles - 1 - i_next / (p.B * p.KV);
+                    const int kh_n = (i_next % (p.B * p.KV)) % p.KV, b_n = (i_next % (p.B * p.KV)) / p.KV;
+                    const int rows = min(p.T, p.NQ - t_n * p.T);
+                    const char* q0 = static_cast<const char*>(p.q) +
+                                     ((static_cast<size_t>(b_n) * p.H + kh_n * p.g) * p.NQ + t_n * p.T) * (kTcD * 2);
+                    for (int idx = lane; idx < p.g * rows * 2; idx += 32) {
+                        const int hh = idx / (rows * 2), w = idx - hh * rows * 2;
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(q0 + static_cast<size_t>(hh) * p.NQ * (kTcD * 2) +
+                                                                      w * 128));
+                    }
+                }
             }
             auto entry = [&](int t) {  // cache row of this lane's block in tile t, or out of range
                 const int tok = t * kTcTile + lane * p.BLOCK;
@@ -604,6 +620,7 @@ int launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, c
             return PA_ERR_CUDA;
     }
     PrefillTcParams prm{};
+    prm.q = q;
     prm.table = table;
     prm.seq_lens = seq_lens;
     prm.out = out;
