@@ -27,6 +27,8 @@ CASES = [
     ("bf16", 32, 1, 8, 1, False, [4096], False),           # MQA: 32 rows, 8-token blocks
     ("f16", 64, 8, 32, 4, True, [3000, 2500], True),       # the maximum moves mid-piece
     ("bf16", 16, 2, 16, 3, False, [1500, 9, 300], True),   # 24 rows, non-causal
+    ("f16", 16, 8, 64, 16, True, [40, 700], False),        # 2 heads x 16 new rows, 64-token blocks
+    ("bf16", 32, 1, 32, 1, False, [2049, 1, 128], True),   # 32 heads on one KV head
 ]
 
 
