@@ -142,9 +142,10 @@ typedef struct pa_opts {
 
 /*
  * Decode attention for `opts->batch` sequences (see the definition above).
- * Launches the partition kernel (one CTA per KV head and key range of a
- * sequence; every CTA serves all H/KV * NQ query rows of its KV head so each
- * K/V row is read from memory once) and, unless partitions == 1, the
+ * Launches the partition kernel (persistent CTAs, one per SM, each taking
+ * (sequence, KV head) segments or key ranges of them; a CTA serves all
+ * H/KV * NQ query rows of its KV head, so each K/V row is read from memory
+ * once) and, with fixed partitions (partitions >= 2) or merge_kernel = 1, the
  * log-sum-exp merge kernel for sequences that were split.
  *   scale     multiplies q . k, applied in float32 exactly as given
  *   H, KV     query heads and KV heads, H % KV == 0

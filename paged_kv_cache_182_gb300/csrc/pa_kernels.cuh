@@ -27,7 +27,9 @@
 //   * eight consumer warps: 16-bit caches on tensor cores (mma.sync
 //     m16n8k16, float32 accumulators) -- pa_mmat_kernel with the tokens on the
 //     MMA's 16-row side for at most 8 query rows per KV head, pa_mma_kernel
-//     with the query rows there otherwise; float32 caches on CUDA cores
+//     with the query rows there otherwise (more than 16 rows at D = 128 run
+//     on tcgen05 instead: pa_umma32_kernel, pa_decode_tc.cu, on the same
+//     schedule, pieces and merge); float32 caches on CUDA cores
 //     (pa_split_kernel: 16-byte shared-memory reads, FMAs, warp-shuffle dot
 //     reductions); an online base-2 softmax throughout;
 //   * a piece that covers a whole segment writes the normalised output;

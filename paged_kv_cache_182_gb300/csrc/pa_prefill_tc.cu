@@ -9,9 +9,10 @@
 // which pa_prefill stores into the cache first; the engine page
 // (src/engine.rs) keeps a prefill configuration next to the decode one.
 //
-// How: one CTA per (sequence, KV head, tile of 128 query rows); a tile's rows
-// are the g = H / KV query heads of the KV head times T = 128 / g consecutive
-// new rows (head-major), so that one K/V tile serves all of them.  Per key
+// How: persistent CTAs, one per SM, each walking row tiles (sequence, KV
+// head, 128 query rows) in turn; a tile's rows are the g = H / KV query heads
+// of the KV head times T = 128 / g consecutive new rows (head-major), so that
+// one K/V tile serves all of them.  Per key
 // tile of 128 tokens, fetched by TMA one cache block at a time through the
 // block table:
 //   S  = Q K^T            M 128 (rows), N 128 (keys), K = D; A and B K-major
@@ -25,7 +26,7 @@
 // Warps 0-7: softmax and epilogue, two threads a row (warps w and w + 4 take
 // the low and the high 64 columns of tensor-memory lanes 32 (w % 4) ..; they
 // exchange the row maximum of each key tile through shared memory); warps 8
-// and 9: TMA producers of K and of V (two stages each; a K stage is free again
+// and 9: TMA producers of K and of V (three stages each; a K stage is free again
 // once its S is computed, a V stage once its P.V is); warp 10: MMA issuer (one
 // thread).  S
 // is double-buffered in tensor memory, so that the MMA of key tile t + 1 runs
