@@ -559,6 +559,7 @@ def vjp_timing(device, steps=10, warmup=3):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "traffic": captured_traffic("vjp_main_tc", "vjp_bf16", "vjp"),
+                         "traffic_kernel": "vjp_main_tc, per launch (the call's largest)",
                          "kernel": "the whole call: vjp_stats_tc, vjp_main_tc, vjp_dq_round",
                          "peak_kind": "bf16_tflops of MEASURED_PEAKS.json (burst)"},
             "launches_per_call": (binding.kernel_launches() - launches) // steps,

@@ -10,14 +10,17 @@
 //
 // Two kernels:
 //
-// vjp_stats_tc -- one CTA per (batch, query head, 128 query rows):
+// vjp_stats_tc -- persistent (one CTA per SM), over items of (batch, query
+//   head, 128 query rows) dealt longest first in a snake order:
 //   S = Q K^T per 128-key tile (M 128 rows, N 128 keys, K = D; both operands
 //   K-major), double-buffered in tensor memory; two threads a row (64 key
 //   columns each) keep a running maximum and sum in base 2 over all tiles
 //   and merge them at the end: lse2 = max + log2(sum), +inf for a row that
-//   sees no key.  The same threads compute delta = rowsum(y g) and zero the
-//   float32 dq accumulator rows.  Warp 8 loads Q once and K tiles into a
-//   two-stage ring; warp 9 issues the MMAs.
+//   sees no key.  Warp 8 loads Q (two buffers: the next item's tile lands
+//   while the current one is in use) and K tiles into a four-stage ring
+//   that runs on across items; warp 9 issues the MMAs.  Warps 10-13 compute
+//   delta = rowsum(y g) and zero the float32 dq accumulator rows of the same
+//   items, with no wait on the others (plain coalesced loads and stores).
 //
 // vjp_main_tc -- one CTA per (batch, key/value head, 128 keys): K and V of
 //   the tile stay in shared memory; dK and dV accumulate in tensor memory
@@ -64,21 +67,43 @@ constexpr unsigned kAll = 0xffffffffu;
 constexpr int kD = 128;         // head size of this path
 constexpr int kKeys = 128;      // keys per tile (both kernels)
 constexpr int kSRows = 128;     // query rows per CTA of the statistics kernel
-constexpr int kRows = 64;       // query rows per step of the backward kernel
-constexpr int kThreads = 320;   // warps 0-7 softmax, 8 TMA, 9 MMA
-constexpr int kSoftmax = 256;
+constexpr int kSoftmax = 256;   // statistics kernel: warps 0-7 softmax, 8 TMA, 9 MMA,
+constexpr int kDeltaWarps = 4;  // 10-13 delta and dq zeroing
+constexpr int kStatsThreads = kSoftmax + 64 + kDeltaWarps * 32;
+constexpr int kKStages = 4;     // statistics kernel: K ring depth
 constexpr int kHalf128 = 16384;  // one 64-column half of a 128-row tile, bytes
-constexpr int kHalf64 = 8192;    // one 64-column half of a 64-row tile, bytes
 
 struct StatsBars {
-    uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_free[2];
+    uint64_t q_full[2], q_empty[2], k_full[kKStages], k_empty[kKStages], s_full[2], s_free[2], fin;
     uint32_t tmem;
     int abort;
-    float xm[kSRows], xl[kSRows], xd[kSRows];  // the high-half thread's max, sum, delta part
+    float xm[2][kSRows], xl[2][kSRows];  // the high-half thread's max and sum, by item parity
 };
-// Q (2 halves), K ring (2 stages x 2 halves), then the barriers
-constexpr int kStatsSmem = 6 * kHalf128 + 2048;
-static_assert(sizeof(StatsBars) <= 2048, "statistics barrier area");
+// Q (2 buffers x 2 halves), K ring (kKStages stages x 2 halves), then the barriers
+constexpr int kStatsBarBytes = 4096;
+constexpr int kStatsSmem = (4 + 2 * kKStages) * kHalf128 + kStatsBarBytes;
+static_assert(sizeof(StatsBars) <= kStatsBarBytes, "statistics barrier area");
+static_assert(kStatsSmem <= 232448, "statistics shared memory");
+
+// Item k of CTA c among G: longest first, the direction reversed every round
+// (snake), so that every CTA's share of the tiles is about the same.
+__device__ __forceinline__ int stats_item(int k, int c, int G) { return (k & 1) ? (k + 1) * G - 1 - c : k * G + c; }
+
+struct StatsItem {
+    int b, h, i0, nk, ntiles;
+};
+
+__device__ __forceinline__ StatsItem stats_item_at(const VjpParams& p, int n, int tiles)
+{
+    StatsItem it;
+    const int bh = n % (p.B * p.HQ);
+    it.b = bh / p.HQ;
+    it.h = bh % p.HQ;
+    it.i0 = (tiles - 1 - n / (p.B * p.HQ)) * kSRows;
+    it.nk = p.causal ? min(p.SK, it.i0 + kSRows) : p.SK;
+    it.ntiles = (it.nk + kKeys - 1) / kKeys;
+    return it;
+}
 
 struct MainBars {
     uint64_t kv_full, qd_full[2], qd_empty[2], s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, mma_done;
@@ -98,6 +123,36 @@ static_assert(kMainSmem <= 232448, "backward shared memory");
 __device__ __forceinline__ void red_add(float* addr, float v)
 {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// 32 columns of this warp's 32 tensor-memory lanes, issued without waiting
+// (tmem_ld_wait completes it), so that two loads are in flight together.
+__device__ __forceinline__ void tmem_ld32_issue(Cols32& c, uint32_t taddr)
+{
+    uint32_t* r = c.r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Waits for this thread's tensor-memory loads; the registers of `c` are
+// tied to the wait so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait(Cols32& c)
+{
+    uint32_t* r = c.r;
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
 }
 
 template <typename T>
@@ -122,10 +177,11 @@ __device__ __forceinline__ float2 unpack2(uint32_t w)
 }
 
 // ---------------------------------------------------------------------------
-// Row statistics.  grid = B * HQ * ceil(SQ / 128), row tile slowest: the row
-// tiles that see the most keys (causal) are launched first.
+// Row statistics.  grid = min(items, SMs); items = B * HQ * ceil(SQ / 128),
+// numbered row tile slowest, the row tiles that see the most keys (causal)
+// first.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kStatsThreads, 1)
     vjp_stats_tc(const __grid_constant__ VjpParams p, const __grid_constant__ CUtensorMap qmap,
                  const __grid_constant__ CUtensorMap kmap)
 {
@@ -136,30 +192,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(p.status, PA_STATUS_TIMEOUT);
         return;
     }
-    unsigned char* sQ = smem_raw;
-    unsigned char* sK = smem_raw + 2 * kHalf128;
-    StatsBars& bars = *reinterpret_cast<StatsBars*>(smem_raw + 6 * kHalf128);
+    unsigned char* sQ = smem_raw;                  // buffer u at u * 2 * kHalf128
+    unsigned char* sK = smem_raw + 4 * kHalf128;   // stage s at s * 2 * kHalf128
+    StatsBars& bars = *reinterpret_cast<StatsBars*>(smem_raw + (4 + 2 * kKStages) * kHalf128);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tiles = (p.SQ + kSRows - 1) / kSRows;
-    // row tile slowest: every CTA of a row tile goes before those of the next
-    const int rt = tiles - 1 - static_cast<int>(blockIdx.x / (p.B * p.HQ));
-    const int h = static_cast<int>(blockIdx.x % (p.B * p.HQ)) % p.HQ;
-    const int b = static_cast<int>(blockIdx.x % (p.B * p.HQ)) / p.HQ;
-    const int kh = h / p.groups;
-    const int i0 = rt * kSRows;
-    const int nk = p.causal ? min(p.SK, i0 + kSRows) : p.SK;
-    const int ntiles = (nk + kKeys - 1) / kKeys;
+    const int total = p.B * p.HQ * tiles;
+    const int C = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
     const uint64_t wait_ns = p.wait_ns;
 
     if (tid == 0) {
-        mbar_init(&bars.q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&bars.q_full[u], 1);
+            mbar_init(&bars.q_empty[u], 1);
+            mbar_init(&bars.s_full[u], 1);
+            mbar_init(&bars.s_free[u], kSoftmax / 32);  // one arrival per softmax warp
+        }
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
-            mbar_init(&bars.s_full[s], 1);
-            mbar_init(&bars.s_free[s], kSoftmax / 32);  // one arrival per softmax warp
         }
+        mbar_init(&bars.fin, 1);
         bars.abort = 0;
         fence_mbar_init();
     }
@@ -173,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = bars.tmem;  // S(t) at tS + 128 (t & 1)
+    const uint32_t tS = bars.tmem;  // S of key tile g (counted over the CTA's items) at tS + 128 (g & 1)
     volatile int* abort_flag = &bars.abort;
     auto fail = [&]() {
         *abort_flag = 1;
@@ -183,172 +237,253 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 8) {
         // --------------------------------------------------------------- TMA
-        if (lane == 0 && ntiles > 0) {
+        if (lane == 0) {
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
-            mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf128);
-            for (int hh = 0; hh < 2; ++hh)
-                tma_load_4d(sQ + hh * kHalf128, &qmap, 0, hh, i0, b * p.HQ + h, &bars.q_full);
-            int issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t & 1;
-                if (t >= 2 && (*abort_flag || !mbar_wait_bounded(&bars.k_empty[s], ((t >> 1) - 1) & 1, wait_ns))) {
-                    fail();
+            int qn = 0, g = 0;  // Q tiles and K tiles issued
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int n = stats_item(k, C, G);
+                if (n >= total)
+                    break;
+                const StatsItem it = stats_item_at(p, n, tiles);
+                if (it.ntiles == 0)
+                    continue;
+                const int u = qn & 1;
+                if (qn >= 2 && (*abort_flag || !mbar_wait_bounded(&bars.q_empty[u], ((qn >> 1) - 1) & 1, wait_ns))) {
+                    ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&bars.k_full[s], 2 * kHalf128);
+                mbar_arrive_expect_tx(&bars.q_full[u], 2 * kHalf128);
                 for (int hh = 0; hh < 2; ++hh)
-                    tma_load_4d(sK + s * 2 * kHalf128 + hh * kHalf128, &kmap, 0, hh, t * kKeys, b * p.HK + kh,
-                                &bars.k_full[s]);
-                issued = t + 1;
+                    tma_load_4d(sQ + u * 2 * kHalf128 + hh * kHalf128, &qmap, 0, hh, it.i0, it.b * p.HQ + it.h,
+                                &bars.q_full[u]);
+                ++qn;
+                const int kh = it.h / p.groups;
+                for (int t = 0; t < it.ntiles; ++t, ++g) {
+                    const int s = g % kKStages;
+                    if (g >= kKStages &&
+                        (*abort_flag || !mbar_wait_bounded(&bars.k_empty[s], ((g / kKStages) - 1) & 1, wait_ns))) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars.k_full[s], 2 * kHalf128);
+                    for (int hh = 0; hh < 2; ++hh)
+                        tma_load_4d(sK + s * 2 * kHalf128 + hh * kHalf128, &kmap, 0, hh, t * kKeys, it.b * p.HK + kh,
+                                    &bars.k_full[s]);
+                }
             }
+            if (!ok)
+                fail();
             // no copy may land after the CTA's memory is released
-            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-                mbar_wait_bounded(&bars.k_full[t & 1], (t >> 1) & 1, wait_ns);
-            mbar_wait_bounded(&bars.q_full, 0, wait_ns);
+            for (int t = g > kKStages ? g - kKStages : 0; t < g; ++t)
+                mbar_wait_bounded(&bars.k_full[t % kKStages], (t / kKStages) & 1, wait_ns);
+            for (int q = qn > 2 ? qn - 2 : 0; q < qn; ++q)
+                mbar_wait_bounded(&bars.q_full[q & 1], (q >> 1) & 1, wait_ns);
         }
         __syncwarp();
     } else if (warp == 9) {
         // --------------------------------------------------------------- MMA
-        if (lane == 0 && ntiles > 0) {
-            bool ok = mbar_wait_bounded(&bars.q_full, 0, wait_ns);
-            const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK);
+        if (lane == 0) {
+            const uint32_t ka = smem_u32(sK);
             const uint32_t id = idesc<kBf>(kKeys, false);
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int s = t & 1;
-                ok = !*abort_flag && mbar_wait_bounded(&bars.k_full[s], (t >> 1) & 1, wait_ns);
-                if (ok && t >= 2)
-                    ok = mbar_wait_bounded(&bars.s_free[s], ((t >> 1) - 1) & 1, wait_ns);
+            int qn = 0, g = 0;
+            bool ok = true, issued = false;
+            for (int k = 0; ok; ++k) {
+                const int n = stats_item(k, C, G);
+                if (n >= total)
+                    break;
+                const StatsItem it = stats_item_at(p, n, tiles);
+                if (it.ntiles == 0)
+                    continue;
+                const int u = qn & 1;
+                const uint32_t qa = smem_u32(sQ + u * 2 * kHalf128);
+                ok = !*abort_flag && mbar_wait_bounded(&bars.q_full[u], (qn >> 1) & 1, wait_ns);
+                for (int t = 0; t < it.ntiles && ok; ++t, ++g) {
+                    const int s = g & 1, ks = g % kKStages;
+                    ok = !*abort_flag && mbar_wait_bounded(&bars.k_full[ks], (g / kKStages) & 1, wait_ns);
+                    if (ok && g >= 2)
+                        ok = mbar_wait_bounded(&bars.s_free[s], ((g >> 1) - 1) & 1, wait_ns);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t kb = ka + ks * 2 * kHalf128;
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * kHalf128 + (kk & 3) * 32;
+                        umma(tS + s * kKeys, smem_desc(qa + o, 16, 1024), smem_desc(kb + o, 16, 1024), id, kk > 0);
+                    }
+                    issued = true;
+                    umma_commit(&bars.s_full[s]);
+                    umma_commit(&bars.k_empty[ks]);
+                }
                 if (!ok)
                     break;
-                tc_fence_after();
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t o = (ks >> 2) * kHalf128 + (ks & 3) * 32;
-                    umma(tS + s * kKeys, smem_desc(qa + o, 16, 1024),
-                         smem_desc(ka + s * 2 * kHalf128 + o, 16, 1024), id, ks > 0);
-                }
-                umma_commit(&bars.s_full[s]);
-                umma_commit(&bars.k_empty[s]);
+                umma_commit(&bars.q_empty[u]);  // this Q buffer is free once the item's MMAs complete
+                ++qn;
             }
             if (!ok)
                 fail();
+            // every MMA completes before the tensor memory is released
+            if (issued) {
+                umma_commit(&bars.fin);
+                mbar_wait_bounded(&bars.fin, 0, wait_ns);
+            }
         }
         __syncwarp();
-    } else {
+    } else if (warp < kSoftmax / 32) {
         // ------------------------------------------ statistics (two threads a row)
         const int row = (warp & 3) * 32 + lane;
-        const int part = warp >> 2;  // key columns [64 part, 64 part + 64), d columns likewise
-        const int i = i0 + row;
-        const bool real = i < p.SQ;
+        const int part = warp >> 2;  // key columns [64 part, 64 part + 64)
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        // delta share and the accumulator rows (while the first tiles load)
-        float dpart = 0.f;
-        if (real) {
-            const int64_t r = (static_cast<int64_t>(b) * p.HQ + h) * p.SQ + i;
-            const uint4* y = reinterpret_cast<const uint4*>(static_cast<const T*>(p.y) + r * kD + part * 64);
-            const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.g) + r * kD + part * 64);
-            float d8[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 yv = y[c], gv = g[c];
-                const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
-                float acc = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 a = unpack2<T>(ya[e]), bb = unpack2<T>(ga[e]);
-                    acc = fmaf(a.x, bb.x, acc);
-                    acc = fmaf(a.y, bb.y, acc);
-                }
-                d8[c] = acc;
-            }
-            dpart = ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
-            float4* acc = reinterpret_cast<float4*>(p.dq_sum + r * kD + part * 64);
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float m = -INFINITY, l = 0.f;
         bool fault = false;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t & 1;
-            const bool got =
-                __all_sync(kAll, !fault && !*abort_flag && mbar_wait_bounded(&bars.s_full[s], (t >> 1) & 1, wait_ns));
-            if (!got) {
-                fault = true;
+        int g = 0;
+        for (int k = 0;; ++k) {
+            const int n = stats_item(k, C, G);
+            if (n >= total)
                 break;
-            }
-            tc_fence_after();
-            // raw scores (scale > 0 commutes with the maximum); eight
-            // independent partial maxima and sums keep the dependency chains short
-            float sc[64];
-            float pm8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                pm8[e] = -INFINITY;
-            const int kbase = t * kKeys + part * 64;
-            const bool edge = kbase + 63 >= nk || (p.causal && kbase + 63 > i0);  // warp-uniform
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                Cols32 x;
-                tmem_ld32(x, tS + s * kKeys + lane_off + part * 64 + c * 32);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float v = __uint_as_float(x.r[j]);
-                    if (edge) {
-                        const int key = kbase + c * 32 + j;
-                        if (key >= p.SK || (p.causal && key > i))
-                            v = -INFINITY;
-                    }
-                    sc[c * 32 + j] = v;
-                    pm8[j & 7] = fmaxf(pm8[j & 7], v);
+            const StatsItem it = stats_item_at(p, n, tiles);
+            const int i = it.i0 + row;
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < it.ntiles && !fault; ++t, ++g) {
+                const int s = g & 1;
+                const bool got = __all_sync(
+                    kAll, !*abort_flag && mbar_wait_bounded(&bars.s_full[s], (g >> 1) & 1, wait_ns));
+                if (!got) {
+                    fault = true;
+                    if (lane == 0)
+                        fail();  // the other roles stop at their next wait
+                    break;
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bars.s_free[s]);
-            const float pm = fmaxf(fmaxf(fmaxf(pm8[0], pm8[1]), fmaxf(pm8[2], pm8[3])),
-                                   fmaxf(fmaxf(pm8[4], pm8[5]), fmaxf(pm8[6], pm8[7])));
-            const float mt = fmaxf(m, pm * p.scale_log2);  // base-2 units
-            if (mt != -INFINITY) {
-                const float c2 = p.scale_log2;
-                float s8[8];
+                tc_fence_after();
+                // raw scores (scale > 0 commutes with the maximum); eight
+                // independent partial maxima and sums keep the dependency chains short
+                float sc[64];
+                float pm8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    s8[e] = 0.f;
+                    pm8[e] = -INFINITY;
+                const int kbase = t * kKeys + part * 64;
+                Cols32 xs[2];
+                tmem_ld32_issue(xs[0], tS + s * kKeys + lane_off + part * 64);
+                tmem_ld32_issue(xs[1], tS + s * kKeys + lane_off + part * 64 + 32);
+                tmem_ld_wait(xs[1]);
+                tmem_ld_wait(xs[0]);
+                // the mask test is taken once per tile (warp-uniform), never per
+                // score: a branch per score cost more than the rest of the tile
+                if (kbase + 63 >= it.nk || (p.causal && kbase + 63 > it.i0)) {
+                    // keys kbase + jj with jj < lim are visible to row i
+                    const int lim = min(p.SK, p.causal ? i + 1 : p.SK) - kbase;
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    s8[j & 7] += fast_exp2(fmaf(sc[j], c2, -mt));
-                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-                l = l * fast_exp2(m - mt) + sum;
-                m = mt;
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float v = c * 32 + j < lim ? __uint_as_float(xs[c].r[j]) : -INFINITY;
+                            sc[c * 32 + j] = v;
+                            pm8[j & 7] = fmaxf(pm8[j & 7], v);
+                        }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float v = __uint_as_float(xs[c].r[j]);
+                            sc[c * 32 + j] = v;
+                            pm8[j & 7] = fmaxf(pm8[j & 7], v);
+                        }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars.s_free[s]);
+                const float pm = fmaxf(fmaxf(fmaxf(pm8[0], pm8[1]), fmaxf(pm8[2], pm8[3])),
+                                       fmaxf(fmaxf(pm8[4], pm8[5]), fmaxf(pm8[6], pm8[7])));
+                const float mt = fmaxf(m, pm * p.scale_log2);  // base-2 units
+                if (mt != -INFINITY) {
+                    const float c2 = p.scale_log2;
+                    float s8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        s8[e] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        s8[j & 7] += fast_exp2(fmaf(sc[j], c2, -mt));
+                    const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+                    l = l * fast_exp2(m - mt) + sum;
+                    m = mt;
+                }
+            }
+            // merge the two halves of every row (both warps of a pair pass
+            // this barrier once per item, faulted or not)
+            if (part == 1) {
+                bars.xm[k & 1][row] = m;
+                bars.xl[k & 1][row] = l;
+            }
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+            if (part == 0 && !fault) {
+                const float m1 = bars.xm[k & 1][row], l1 = bars.xl[k & 1][row];
+                const float mt = fmaxf(m, m1);
+                const int64_t srow = (static_cast<int64_t>(it.b) * p.HQ + it.h) * p.sqp + i;
+                if (i >= p.SQ || mt == -INFINITY) {  // padding rows up to sqp, rows that see no key
+                    p.lse[srow] = INFINITY;
+                } else {
+                    const float lt = l * exp2f(m - mt) + l1 * exp2f(m1 - mt);
+                    p.lse[srow] = mt + log2f(lt);
+                }
             }
         }
-        // merge the two halves of every row
-        if (part == 1) {
-            bars.xm[row] = m;
-            bars.xl[row] = l;
-            bars.xd[row] = dpart;
-        }
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-        if (fault) {
-            if (lane == 0)
-                fail();
-        } else if (part == 0) {
-            const float m1 = bars.xm[row], l1 = bars.xl[row];
-            const float mt = fmaxf(m, m1);
-            const int64_t srow = (static_cast<int64_t>(b) * p.HQ + h) * p.sqp + i;
-            if (!real) {  // padding rows up to sqp: no key, no gradient
-                p.lse[srow] = INFINITY;
-                p.delta[srow] = 0.f;
-            } else if (mt == -INFINITY) {
-                p.lse[srow] = INFINITY;
-            } else {
-                const float lt = l * exp2f(m - mt) + l1 * exp2f(m1 - mt);
-                p.lse[srow] = mt + log2f(lt);
+    } else {
+        // ------------------------------- delta = rowsum(y g), dq accumulator rows zeroed
+        // warp dw takes rows 32 dw .. 32 dw + 31 of each item, two rows per
+        // load (16 lanes x 16 bytes a row), eight row pairs in flight
+        const int dw = warp - (kSoftmax / 32 + 2);
+        const int half = lane >> 4, c16 = lane & 15;
+        for (int k = 0;; ++k) {
+            const int n = stats_item(k, C, G);
+            if (n >= total)
+                break;
+            const StatsItem it = stats_item_at(p, n, tiles);
+            const int64_t r0 = (static_cast<int64_t>(it.b) * p.HQ + it.h) * p.SQ;
+            const int64_t s0 = (static_cast<int64_t>(it.b) * p.HQ + it.h) * p.sqp;
+#pragma unroll 1
+            for (int rb = 0; rb < 32; rb += 16) {
+                uint4 yv[8], gv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = it.i0 + dw * 32 + rb + 2 * e + half;
+                    if (i < p.SQ) {
+                        const int64_t off = (r0 + i) * kD + c16 * 8;
+                        yv[e] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.y) + off));
+                        gv[e] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.g) + off));
+                    } else {
+                        yv[e] = make_uint4(0u, 0u, 0u, 0u);
+                        gv[e] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t ya[4] = {yv[e].x, yv[e].y, yv[e].z, yv[e].w};
+                    const uint32_t ga[4] = {gv[e].x, gv[e].y, gv[e].z, gv[e].w};
+                    float acc[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float2 a = unpack2<T>(ya[w]), bb = unpack2<T>(ga[w]);
+                        acc[w] = fmaf(a.y, bb.y, a.x * bb.x);
+                    }
+                    float d = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+                    for (int sh = 8; sh >= 1; sh >>= 1)
+                        d += __shfl_xor_sync(kAll, d, sh);
+                    const int i = it.i0 + dw * 32 + rb + 2 * e + half;
+                    if (c16 == 0)
+                        p.delta[s0 + i] = i < p.SQ ? d : 0.f;  // padding rows up to sqp: no gradient
+                }
             }
-            if (real)
-                p.delta[srow] = dpart + bars.xd[row];
+            // the item's real rows of the accumulator: contiguous, 512 bytes a row
+            const int nreal = min(kSRows, p.SQ - it.i0);
+            float4* acc = reinterpret_cast<float4*>(p.dq_sum + (r0 + it.i0) * kD);
+            const int nvec = nreal * (kD / 4);
+            for (int v = dw * 32 + lane; v < nvec; v += kDeltaWarps * 32)
+                acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     tc_fence_before();
@@ -778,10 +913,16 @@ int launch_vjp_tc(const VjpParams& p, int dtype, bool f32_out, cudaStream_t st, 
         if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kStatsSmem) != cudaSuccess)
             return PA_ERR_CUDA;
-        const long long grid = static_cast<long long>(p.B) * p.HQ * ((p.SQ + kSRows - 1) / kSRows);
-        if (grid >= (1ll << 31))
+        const long long items = static_cast<long long>(p.B) * p.HQ * ((p.SQ + kSRows - 1) / kSRows);
+        if (items >= (1ll << 31) / 4)
             return PA_ERR_BAD_DIMS;
-        fn<<<static_cast<unsigned>(grid), kThreads, kStatsSmem, st>>>(p, qmap, kmap);
+        // persistent: one CTA per SM (its shared memory allows no more)
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            return PA_ERR_CUDA;
+        const long long grid = items < sms ? items : sms;
+        fn<<<static_cast<unsigned>(grid), kStatsThreads, kStatsSmem, st>>>(p, qmap, kmap);
         if (cudaGetLastError() != cudaSuccess)
             return PA_ERR_CUDA;
         ++*launches;

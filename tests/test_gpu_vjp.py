@@ -173,6 +173,11 @@ TC_CASES = {
     "wide_causal_mha": (2, 3, 3, 70, 333, True),
     "single": (1, 2, 2, 1, 1, False),
     "gqa8_square": (1, 16, 2, 256, 256, True),
+    # more row tiles than SMs: every CTA of the persistent statistics kernel
+    # takes several items of different lengths (snake order), the K ring and
+    # the two Q buffers run on across them
+    "persistent_causal": (1, 40, 10, 1000, 1000, True),
+    "persistent_wide": (1, 64, 16, 700, 300, False),
 }
 
 
