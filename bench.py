@@ -124,8 +124,9 @@ KERNEL_SOURCES = {
     "decode": ["pa_kernels.cuh", "pa_common.cuh", "pa_ptx.cuh", "pa_inst_f32.cu", "pa_inst_f16.cu",
                "pa_inst_bf16.cu", "pa_decode_tc.cu", "pa_tc.cuh", "pa_host.cu",
                "../../include/pa_decode.h"],
-    "prefill_tc": ["pa_prefill_tc.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_common.cuh", "pa_host.cu"],
-    "vjp": ["pa_vjp.cu", "pa_vjp_tc.cu", "pa_vjp.cuh", "pa_tc.cuh", "pa_ptx.cuh",
+    "prefill_tc": ["pa_prefill_tc.cu", "pa_tc.cuh", "pa_tmem.cuh", "pa_ptx.cuh", "pa_common.cuh",
+                   "pa_host.cu"],
+    "vjp": ["pa_vjp.cu", "pa_vjp_tc.cu", "pa_vjp.cuh", "pa_tc.cuh", "pa_tmem.cuh", "pa_ptx.cuh",
             "../../include/pa_attention_vjp.h"],
 }
 

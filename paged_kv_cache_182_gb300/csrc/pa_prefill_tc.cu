@@ -47,6 +47,7 @@
 #include "pa_decode.h"
 #include "pa_ptx.cuh"
 #include "pa_tc.cuh"
+#include "pa_tmem.cuh"
 
 namespace pa {
 namespace {
@@ -414,26 +415,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float pm = -INFINITY;
                 if (got) {
                     tc_fence_after();
-                    const bool masked = t * kTcTile + kTcTile - 1 > vis;  // uniform over the CTA
+                    // both halves of this thread's score columns in flight together;
+                    // eight independent partial maxima keep the chains short
+                    Cols32 xs[2];
+                    tmem_ld32_issue(xs[0], tS0 + s * kTcTile + lane_off + col0);
+                    tmem_ld32_issue(xs[1], tS0 + s * kTcTile + lane_off + col0 + 32);
+                    tmem_ld_wait(xs[1]);
+                    tmem_ld_wait(xs[0]);
+                    float pm8[8];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        Cols32 x;
-                        tmem_ld32(x, tS0 + s * kTcTile + lane_off + col0 + c * 32);
-                        if (masked) {
+                    for (int e = 0; e < 8; ++e)
+                        pm8[e] = -INFINITY;
+                    if (t * kTcTile + kTcTile - 1 > vis) {  // masked tile, uniform over the CTA
+                        const int lim = limit - (t * kTcTile + col0);  // columns 0 .. lim visible
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
-                                const int key = t * kTcTile + col0 + c * 32 + j;
-                                sc[c * 32 + j] = key <= limit ? __uint_as_float(x.r[j]) * p.qscale : -INFINITY;
-                                pm = fmaxf(pm, sc[c * 32 + j]);
+                                const float v = c * 32 + j <= lim ? __uint_as_float(xs[c].r[j]) * p.qscale : -INFINITY;
+                                sc[c * 32 + j] = v;
+                                pm8[j & 7] = fmaxf(pm8[j & 7], v);
                             }
-                        } else {
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
-                                sc[c * 32 + j] = __uint_as_float(x.r[j]) * p.qscale;
-                                pm = fmaxf(pm, sc[c * 32 + j]);
+                                const float v = __uint_as_float(xs[c].r[j]) * p.qscale;
+                                sc[c * 32 + j] = v;
+                                pm8[j & 7] = fmaxf(pm8[j & 7], v);
                             }
-                        }
                     }
+                    pm = fmaxf(fmaxf(fmaxf(pm8[0], pm8[1]), fmaxf(pm8[2], pm8[3])),
+                               fmaxf(fmaxf(pm8[4], pm8[5]), fmaxf(pm8[6], pm8[7])));
                 }
                 // the other half of the row's maximum
                 bars.xchg[s][part][row] = pm;
@@ -445,12 +459,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // both threads of the row take the same decision from the same values
                 const float mt = tile_max > m + 8.f ? tile_max : m;
                 const float alpha = fast_exp2(m - mt);  // 0 at the first tile (m = -inf), else 1 or tiny
-                float sum = 0.f;
+                float s8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    s8[e] = 0.f;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     sc[j] = fast_exp2(sc[j] - mt);
-                    sum += sc[j];
+                    s8[j & 7] += sc[j];
                 }
+                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                 l = l * alpha + sum;
                 m = mt;
                 // keys past the sequence end inside its last cache block hold other
