@@ -681,6 +681,25 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const bool key_ok = key < p.SK;
         const bool keys_all = k0 + kKeys <= p.SK;  // every key of the tile is real
         bool fault = false;
+        // the dQ^T reductions of a step are issued in two halves: rows 0-15 of
+        // this thread's 32 as soon as they are read, rows 16-31 held in
+        // registers and issued in the next step while the dP^T products run,
+        // so that the reductions drain under the MMAs rather than after them
+        float held[16];
+        float* held_dst = nullptr;
+        int held_rows = 0;
+        auto reduce_half = [&](float* dst, const float* v, int rows) {  // rows of this half present
+            if (rows >= 16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    red_add(dst + static_cast<int64_t>(j) * kD, v[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < rows)
+                        red_add(dst + static_cast<int64_t>(j) * kD, v[j]);
+            }
+        };
         for (int it = 0; it < n; ++it) {
             const int st = it & 1;
             int h, i0;
@@ -734,6 +753,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars.p_ready);
+            if (held_dst) {
+                reduce_half(held_dst, held, held_rows);
+                held_dst = nullptr;
+            }
             got = __all_sync(kAll, mbar_wait_bounded(&bars.dp_full, it & 1, wait_ns));
             if (!got) {
                 fault = true;
@@ -791,12 +814,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                     mbar_arrive(&bars.dq_free);
                 float* dst = p.dq_sum + ((static_cast<int64_t>(b) * p.HQ + h) * p.SQ + rb) * kD + ln;
                 const int rows = min(32, p.SQ - rb);
+                float v[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j < rows)
-                        red_add(dst + static_cast<int64_t>(j) * kD, __uint_as_float(x.r[j]));
+                for (int j = 0; j < 16; ++j) {
+                    v[j] = __uint_as_float(x.r[j]);
+                    held[j] = __uint_as_float(x.r[16 + j]);
+                }
+                reduce_half(dst, v, rows);
+                if (rows > 16) {
+                    held_dst = dst + static_cast<int64_t>(16) * kD;
+                    held_rows = rows - 16;
+                }
             }
         }
+        if (held_dst)  // the last step's held rows
+            reduce_half(held_dst, held, held_rows);
         if (!fault && n > 0)
             fault = !__all_sync(kAll, !*abort_flag && mbar_wait_bounded(&bars.mma_done, 0, wait_ns));
         if (fault) {
