@@ -36,7 +36,9 @@
 //     dQ^T = K^T dS^T       M = D, N 128 rows, K 128 keys     (both MN-major),
 //                           into the dP^T columns the softmax has read
 //   and the same threads read dQ^T back and add it into the float32
-//   accumulator (one reduction per element, coalesced over D).  Every MMA
+//   accumulator (one reduction per element, coalesced over D; half of a
+//   thread's rows at once, the other half in the next step, under its dP^T
+//   products).  Every MMA
 //   has N = 128: a tcgen05 MMA of M = 128 costs at least as much as N = 64
 //   does.  Warp 16 loads K, V once and Q, dO, lse2, delta per step into a
 //   two-stage ring; warp 17 issues the MMAs (one thread).  Tensor memory
