@@ -37,8 +37,8 @@
 //                           into the dP^T columns the softmax has read
 //   and the same threads read dQ^T back and add it into the float32
 //   accumulator (one reduction per element, coalesced over D; half of a
-//   thread's rows at once, the other half in the next step, under its dP^T
-//   products).  Every MMA
+//   thread's rows at once, the other half in the next step, under its dK
+//   and dQ^T products).  Every MMA
 //   has N = 128: a tcgen05 MMA of M = 128 costs at least as much as N = 64
 //   does.  Warp 16 loads K, V once and Q, dO, lse2, delta per step into a
 //   two-stage ring; warp 17 issues the MMAs (one thread).  Tensor memory
@@ -685,8 +685,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         bool fault = false;
         // the dQ^T reductions of a step are issued in two halves: rows 0-15 of
         // this thread's 32 as soon as they are read, rows 16-31 held in
-        // registers and issued in the next step while the dP^T products run,
-        // so that the reductions drain under the MMAs rather than after them
+        // registers and issued in the next step once its dS^T is handed over,
+        // while the MMA warp computes dK and dQ^T (the softmax warps would
+        // otherwise wait for dQ^T), so that the reductions drain under the MMAs
         float held[16];
         float* held_dst = nullptr;
         int held_rows = 0;
@@ -755,10 +756,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars.p_ready);
-            if (held_dst) {
-                reduce_half(held_dst, held, held_rows);
-                held_dst = nullptr;
-            }
             got = __all_sync(kAll, mbar_wait_bounded(&bars.dp_full, it & 1, wait_ns));
             if (!got) {
                 fault = true;
@@ -799,6 +796,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars.ds_ready);
+            if (held_dst) {
+                reduce_half(held_dst, held, held_rows);
+                held_dst = nullptr;
+            }
             // dQ^T of the step (lane = d, columns = rows): read, hand the columns
             // back for the next dP^T, then add into the float32 accumulator
             got = __all_sync(kAll, mbar_wait_bounded(&bars.dq_full, it & 1, wait_ns));
